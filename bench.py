@@ -1,0 +1,323 @@
+"""Benchmark: ERI quartets/s and FP64 GFLOP/s per angular class on one GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload homogeneous|high_l] [--scale S]
+
+A step is one pass of the hot path over the workload's batch: for every class
+of the workload, the class kernel evaluates all its quartets (Gaussian-pair
+parameters, Boys function, VRR, contraction, HRR with the stepwise spherical
+transform, block store).  ``value`` is the whole job's shell quartets per second
+with inputs resident in HBM; ``e2e`` is the same metric through the C ABI with
+host buffers (plan creation from host shells, pinned host->device copy of the
+quartet lists, device->host copy of every block).
+
+Default workload (N=1): the homogeneous class batch, 1,048,576 (pp|pp) and
+1,048,576 (dd|dd) quartets, centers uniform in a 10 bohr cube, exponents
+log-uniform in [0.05, 100], contraction degree 1, spherical output.
+
+Under torchrun each rank runs the same per-GPU batch on its own GPU (replicas:
+quartets are independent, there is no data-path collective); ``value`` is the
+total quartets of all ranks over the slowest rank's time ("scaling": "weak").
+
+``--impl reference`` times the CPU oracle (oracle/, McMurchie-Davidson in
+C++/OpenMP) on the host cores on a bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "ERI quartets/s and FP64 GFLOP/s per angular class (fraction of GB300 FP64 peak)"
+# FP64 pipe peak from unit counts and clock: 152 SMs x 2 DFMA/clk x 2 flop x 2.070 GHz
+FP64_PEAK_TFLOPS = 152 * 2 * 2 * 2.070e9 / 1e12
+
+WORKLOADS = {
+    "homogeneous": {"desc": "homogeneous class batch: (pp|pp) x 1,048,576 + (dd|dd) x 1,048,576 quartets, "
+                            "centers U[0,10]^3 bohr, exponents log-U[0.05,100], degree 1, spherical",
+                    "classes": [((1, 1, 1, 1), 1 << 20, 1, 1), ((2, 2, 2, 2), 1 << 20, 1, 101)]},
+    "high_l": {"desc": "high-L batch: (ff|ff) x 131,072 + (fd|fd) x 262,144 quartets, degree 2, spherical",
+               "classes": [((3, 3, 3, 3), 131072, 2, 2), ((3, 2, 3, 2), 262144, 2, 102)]},
+}
+
+
+def env_int(k, d):
+    try:
+        return int(os.environ.get(k, d))
+    except ValueError:
+        return d
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_oracle_rate(wl, budget_s=20.0, nthreads=None):
+    """Oracle time per quartet for each class of the workload from a bounded
+    sample; returns (quartets/s for the whole step mix, description, cores)."""
+    import oracle
+    from electron_repulsion_integrals_gb300 import workloads as W
+    nthreads = nthreads or oracle.default_threads()
+    per_class = {}
+    total_time = 0.0
+    total_q = 0
+    parts = []
+    share = budget_s / len(wl["classes"])
+    for cls, n, deg, seed in wl["classes"]:
+        m = 64
+        spent = 0.0
+        done = 0
+        while spent < share:
+            s, q = W.homogeneous(cls, m, deg, seed_index=seed + 7000 + done)
+            S = oracle.ShellSet(s.centers, s.L, s.nprim, s.exps, s.coefs)
+            t0 = time.perf_counter()
+            oracle.eri_blocks(S, q, spherical=True, nthreads=nthreads)
+            dt = time.perf_counter() - t0
+            spent += dt
+            done += m
+            if dt < share / 8:
+                m *= 2
+        tq = spent / done
+        per_class[cls] = tq
+        total_time += tq * n
+        total_q += n
+        parts.append(f"{done} {cls} quartets")
+    return total_q / total_time, "oracle on " + " + ".join(parts), nthreads, per_class
+
+
+def run_reference(a, rank, world):
+    wl = WORKLOADS[a.workload]
+    if rank != 0:
+        return
+    rates = []
+    desc = ""
+    cores = 0
+    for _ in range(a.warmup):
+        cpu_oracle_rate(wl, budget_s=2.0)
+    t_all = time.perf_counter()
+    for _ in range(a.steps):
+        r, desc, cores, _ = cpu_oracle_rate(wl, budget_s=a.ref_budget)
+        rates.append(r)
+    elapsed = time.perf_counter() - t_all
+    value = statistics.median(rates)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "quartets/s", "n_gpus": world,
+            "steps": a.steps, "warmup": a.warmup, "ms_per_step": elapsed / a.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl["desc"]},
+            "cpu_baseline": {"value": value, "unit": "quartets/s", "cores": cores, "kind": "oracle",
+                             "sample": desc + " per step, projected to the full step mix"},
+            "e2e": {"value": value, "unit": "quartets/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(a, rank, world, local_rank):
+    import torch
+    import electron_repulsion_integrals_gb300 as eri
+    from electron_repulsion_integrals_gb300 import workloads as W
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    eri.lib()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    wl = WORKLOADS[a.workload]
+    stream = torch.cuda.current_stream()
+
+    # inputs resident in HBM: one plan per class batch and its quartet list
+    batches = []
+    for cls, n, deg, seed in wl["classes"]:
+        n = max(1, int(n * a.scale))
+        s, q = W.homogeneous(cls, n, deg, seed_index=seed)
+        plan = eri.Plan(s, spherical=True)
+        qd = torch.as_tensor(q, device=dev)
+        out = torch.empty(n * eri.block_size(cls), dtype=torch.float64, device=dev)
+        st = eri.eri_class_info(cls)
+        flops_q = st["vrr_flops"] * deg ** 4 + st["hrr_flops"]
+        batches.append(dict(cls=cls, n=n, deg=deg, shells=s, q=q, plan=plan, qd=qd, out=out, flops=flops_q,
+                            stats=st))
+    torch.cuda.synchronize()
+
+    def step(record=None):
+        for b in batches:
+            if record is not None:
+                record[b["cls"]][0].record(stream)
+            eri.eri_compute_class(b["plan"].handle, b["cls"], b["qd"], b["out"], stream)
+            if record is not None:
+                record[b["cls"]][1].record(stream)
+
+    for _ in range(max(a.warmup, 0)):
+        step()
+    torch.cuda.synchronize()
+    # timed region
+    evs = {b["cls"]: [] for b in batches}
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(a.steps):
+        rec = {b["cls"]: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for b in batches}
+        step(rec)
+        for k, v in rec.items():
+            evs[k].append(v)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    ms = t0.elapsed_time(t1)
+    if dist:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    total_q = sum(b["n"] for b in batches) * world
+    value = total_q * a.steps / (ms / 1e3)
+
+    per_class = {}
+    for b in batches:
+        kms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs[b["cls"]])
+        tf = b["flops"] * b["n"] / (kms / 1e3) / 1e12
+        per_class["({}{}|{}{})".format(*b["cls"])] = {
+            "quartets_per_s": b["n"] / (kms / 1e3), "primitive_quartets_per_s": b["n"] * b["deg"] ** 4 / (kms / 1e3),
+            "ms_per_launch": kms, "fp64_gflops": tf * 1e3, "frac_fp64_peak": tf / FP64_PEAK_TFLOPS,
+            "flops_per_quartet": b["flops"], "tier": "staged" if b["stats"]["staged"] else "reg"}
+    dom = max(batches, key=lambda b: b["flops"] * b["n"])
+    dname = "({}{}|{}{})".format(*dom["cls"])
+    ach = per_class[dname]["fp64_gflops"] / 1e3
+
+    # end to end through the C ABI with host buffers
+    e2e = None
+    if a.e2e:
+        host_q = [torch.from_numpy(b["q"]).pin_memory() for b in batches]
+        host_o = [torch.empty(b["out"].numel(), dtype=torch.float64).pin_memory() for b in batches]
+        h2d = sum(hq.numel() * 4 for hq in host_q) + sum(b["shells"].n * 48 + b["shells"].exps.size * 16
+                                                         for b in batches)
+        d2h = sum(ho.numel() * 8 for ho in host_o)
+        e_steps = max(1, min(a.steps, 3))
+        torch.cuda.synchronize()
+        te = time.perf_counter()
+        for _ in range(e_steps):
+            for b, hq, ho in zip(batches, host_q, host_o):
+                plan = eri.Plan(b["shells"], spherical=True, stream=stream)
+                qd = hq.to(dev, non_blocking=True)
+                eri.eri_compute_class(plan.handle, b["cls"], qd, b["out"], stream)
+                ho.copy_(b["out"], non_blocking=True)
+                torch.cuda.synchronize()
+                plan.close()
+        te = time.perf_counter() - te
+        e2e = {"value": sum(b["n"] for b in batches) * world * e_steps / te, "unit": "quartets/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    cpu = None
+    if rank == 0 and a.cpu_baseline:
+        rate, desc, cores, _ = cpu_oracle_rate(wl, budget_s=a.ref_budget)
+        cpu = {"value": rate, "unit": "quartets/s", "cores": cores, "kind": "oracle",
+               "sample": desc + ", projected to the full step mix"}
+
+    line = {"metric": METRIC, "value": value, "unit": "quartets/s", "n_gpus": world, "steps": a.steps,
+            "warmup": a.warmup, "ms_per_step": ms / a.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl["desc"] + ("" if a.scale == 1 else f" (scaled x{a.scale})"),
+                       "l2": "no flush: inputs and outputs of a step exceed the 126 MB L2",
+                       "parallelism": f"replicas x{world}"},
+            "per_class": per_class,
+            "roofline": {"bound": "alu", "kernel": dname, "achieved": ach, "peak": FP64_PEAK_TFLOPS,
+                         "unit": "TFLOP/s", "frac": ach / FP64_PEAK_TFLOPS, "traffic": None,
+                         "peak_source": "FP64 pipe: 152 SMs x 2 DFMA/clk x 2 flop x 2.07 GHz"},
+            "clocks": clk, "e2e": e2e, "cpu_baseline": cpu,
+            "gpu_launches": len(batches) * a.steps}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    for b in batches:
+        b["plan"].close()
+    if dist:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="homogeneous", choices=sorted(WORKLOADS))
+    ap.add_argument("--scale", type=float, default=1.0, help="fraction of the workload's quartets (profiling)")
+    ap.add_argument("--no-e2e", dest="e2e", action="store_false")
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--ref-budget", type=float, default=12.0, help="seconds of oracle work per sample")
+    a = ap.parse_args()
+    rank = env_int("RANK", 0)
+    world = env_int("WORLD_SIZE", 1)
+    local_rank = env_int("LOCAL_RANK", 0)
+    if a.impl == "reference":
+        run_reference(a, rank, world)
+    else:
+        run_ours(a, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

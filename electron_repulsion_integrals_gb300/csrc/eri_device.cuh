@@ -1,0 +1,285 @@
+// Device-side building blocks shared by the generated per-class ERI kernels.
+//
+// The method is that of FusionRCG ("FusionRCG: Orchestrating Recursive
+// Computation Graphs across GPU Memory Hierarchies"): Algorithm 2 (section
+// III-C) evaluates a shell quartet as
+//   for each primitive quartet: GAUSSIANPAIRS -> BOYS -> VRR -> H += c V
+//   HRR bra -> T x T -> HRR ket -> T x T -> scatter.
+// This header holds the parts that do not depend on the angular class: the
+// Gaussian-pair and quartet parameters (the zeta, eta, rho, P, Q, W, T of
+// section II-A), the Boys function F_m(T) = [00|00]^(m), the primitive loops
+// and the three output modes.  The class-specific straight-line VRR/HRR code is
+// generated (gen/emit.py) and includes this file.
+//
+// Every FP64 instruction here is on the critical resource of the GB300 (its
+// FP64 pipe runs at 1/64 of the FP32 rate), so the formulas are arranged to
+// use few FP64 operations: one reciprocal per primitive pair, one reciprocal
+// square root per primitive quartet, integer bit tricks for table indices.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace eri {
+
+constexpr int kThreads = 128;
+
+// ---------------------------------------------------------------- Boys table
+// Grid T_k = k / 8, k = 0..kBoysNgrid-1, covering [0, kBoysTmax].  Row k holds
+// exp(-T_k) followed by F_0(T_k) .. F_{kBoysMaxOrder}(T_k).  Below kBoysTmax the
+// top order is a kBoysTerms-term Taylor series around the nearest grid point
+// (|T - T_k| <= 1/16, truncation < 1e-18 relative) and lower orders follow from
+// the stable downward recursion F_m = (2T F_{m+1} + e^{-T}) / (2m+1).  At and
+// above kBoysTmax, F_0 = sqrt(pi/T)/2 and F_{m+1} = (2m+1) F_m / (2T): the
+// neglected e^{-T} and erfc terms are below 1e-18 relative for m <= 12.
+constexpr int kBoysTerms = 10;
+constexpr int kBoysMaxL = 16;
+constexpr int kBoysMaxOrder = kBoysMaxL + kBoysTerms;
+constexpr int kBoysCols = kBoysMaxOrder + 2;
+constexpr double kBoysTmax = 80.0;
+constexpr int kBoysNgrid = 641;  // 80 * 8 + 1
+
+// F'_m = pref * F_m(T), m = 0..L
+template <int L>
+__device__ __forceinline__ void boys_scaled(double T, double pref, const double* __restrict__ tab, double* F) {
+  if (T < kBoysTmax) {
+    // nearest grid index by the 1.5*2^52 rounding trick (no int<->double conversion)
+    const double magic = 6755399441055744.0;
+    const double x = fma(T, 8.0, magic);
+    const int k = __double2loint(x);
+    const double y = fma(x - magic, 0.125, -T);  // T_k - T
+    const double* __restrict__ row = tab + k * kBoysCols;
+    // y_j = y / j for the Horner form of sum_j c_j y^j / j!
+    double yj[kBoysTerms];
+    yj[1] = y;
+#pragma unroll
+    for (int j = 2; j < kBoysTerms; ++j) yj[j] = y * (1.0 / j);
+    double f = __ldg(row + 1 + L + kBoysTerms - 1);
+#pragma unroll
+    for (int j = kBoysTerms - 1; j >= 1; --j) f = fma(f, yj[j], __ldg(row + 1 + L + j - 1));
+    F[L] = pref * f;
+    if (L > 0) {
+      double ex = 1.0;
+#pragma unroll
+      for (int j = kBoysTerms - 1; j >= 1; --j) ex = fma(ex, yj[j], 1.0);
+      const double eT = (pref * __ldg(row)) * ex;
+      const double t2 = T + T;
+#pragma unroll
+      for (int m = L - 1; m >= 0; --m) F[m] = fma(t2, F[m + 1], eT) * (1.0 / (2 * m + 1));
+    }
+  } else {
+    const double r = rsqrt(T);
+    F[0] = (pref * 0.88622692545275801365) * r;  // sqrt(pi)/2
+    if (L > 0) {
+      const double h = 0.5 * r * r;  // 1/(2T)
+#pragma unroll
+      for (int m = 1; m <= L; ++m) F[m] = F[m - 1] * ((2 * m - 1) * h);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- launch data
+enum OutputMode { kStore = 0, kSchwarz = 1, kCoulomb = 2 };
+
+struct ShellsDev {
+  const double* cen;    // [nshell][3]
+  const int* L;         // [nshell]
+  const int* nprim;     // [nshell]
+  const int* poff;      // [nshell] offset into exps/coef
+  const double* exps;   // primitive exponents
+  const double* coef;   // normalised contraction coefficients times (sqrt(2) pi^{5/4})^{1/2}
+};
+
+struct EriLaunch {
+  ShellsDev sh;
+  const int* quartets;  // [n][4] shell indices in the requested order (store / Schwarz modes)
+  long long n;          // number of quartets
+  int canon[4];         // canonical shell k is requested position canon[k]
+  // store mode
+  double* out;
+  long long out_stride;  // doubles per block
+  int ostr[4];           // stride of canonical axis k in the requested block layout
+  // Schwarz mode: q_out[i] = sqrt(max diag |(ab|ab)|) of quartet i
+  double* q_out;
+  // Coulomb mode
+  const double* D;
+  double* J;
+  const int* fo;        // first basis function of each shell
+  int nbf;
+  // scratch for staged classes: slot s of thread t at scratch[s * nthreads + t]
+  double* scratch;
+  const double* boys;
+};
+
+struct Quartet {
+  int s[4];           // canonical shells A, B, C, D
+  double A[3], B[3], C[3], D[3];
+  double AB[3], CD[3];
+  double rAB2, rCD2;
+  int pa, pb, pc, pd, na, nb, nc, nd;
+};
+
+__device__ __forceinline__ void load_shell_center(const ShellsDev& sh, int s, double* c) {
+  c[0] = __ldg(sh.cen + 3 * s);
+  c[1] = __ldg(sh.cen + 3 * s + 1);
+  c[2] = __ldg(sh.cen + 3 * s + 2);
+}
+
+__device__ __forceinline__ void load_quartet(const EriLaunch& P, long long q, Quartet& Q) {
+  const int4 r = __ldg(reinterpret_cast<const int4*>(P.quartets) + q);
+  const int req[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int c = P.canon[k];
+    Q.s[k] = c == 0 ? req[0] : c == 1 ? req[1] : c == 2 ? req[2] : req[3];
+  }
+  load_shell_center(P.sh, Q.s[0], Q.A);
+  load_shell_center(P.sh, Q.s[1], Q.B);
+  load_shell_center(P.sh, Q.s[2], Q.C);
+  load_shell_center(P.sh, Q.s[3], Q.D);
+#pragma unroll
+  for (int x = 0; x < 3; ++x) {
+    Q.AB[x] = Q.A[x] - Q.B[x];
+    Q.CD[x] = Q.C[x] - Q.D[x];
+  }
+  Q.rAB2 = fma(Q.AB[2], Q.AB[2], fma(Q.AB[1], Q.AB[1], Q.AB[0] * Q.AB[0]));
+  Q.rCD2 = fma(Q.CD[2], Q.CD[2], fma(Q.CD[1], Q.CD[1], Q.CD[0] * Q.CD[0]));
+  Q.pa = __ldg(P.sh.poff + Q.s[0]);
+  Q.pb = __ldg(P.sh.poff + Q.s[1]);
+  Q.pc = __ldg(P.sh.poff + Q.s[2]);
+  Q.pd = __ldg(P.sh.poff + Q.s[3]);
+  Q.na = __ldg(P.sh.nprim + Q.s[0]);
+  Q.nb = __ldg(P.sh.nprim + Q.s[1]);
+  Q.nc = __ldg(P.sh.nprim + Q.s[2]);
+  Q.nd = __ldg(P.sh.nprim + Q.s[3]);
+}
+
+// Gaussian product of two primitives (alpha at A, beta at B):
+//   zeta = alpha + beta, P = (alpha A + beta B)/zeta, P - A = -beta/zeta (A - B),
+//   K = c_a c_b exp(-alpha beta/zeta |AB|^2) / zeta
+// (the sqrt(2) pi^{5/4} per side is carried by the coefficients, so that
+// K_ab K_cd / sqrt(zeta + eta) is the full prefactor 2 pi^{5/2}/(zeta eta
+// sqrt(zeta+eta)) K_AB K_CD of [00|00]^(m)).
+struct PrimPair {
+  double zeta, o2z, P[3], PA[3], K;
+};
+
+__device__ __forceinline__ void make_pair(double a, double ca, double b, double cb, const double* A, const double* AB,
+                                          double rAB2, PrimPair& p) {
+  p.zeta = a + b;
+  const double iz = __drcp_rn(p.zeta);
+  p.o2z = 0.5 * iz;
+  const double bz = b * iz;
+#pragma unroll
+  for (int x = 0; x < 3; ++x) {
+    p.PA[x] = -bz * AB[x];
+    p.P[x] = A[x] + p.PA[x];
+  }
+  p.K = (ca * cb * iz) * exp(-(a * bz) * rAB2);
+}
+
+// Quartet parameters of section II-A: rho = zeta eta/(zeta+eta),
+// rho/zeta = eta/(zeta+eta), rho/eta = zeta/(zeta+eta), 1/(2(zeta+eta)),
+// W - P = rho/zeta (Q - P), W - Q = -rho/eta (Q - P), T = rho |PQ|^2.
+struct QuartetSetup {
+  double roz, roe, o2ze, PQ[3];
+};
+
+template <int L>
+__device__ __forceinline__ void quartet_setup(const PrimPair& pb, const PrimPair& pk, const double* __restrict__ boys,
+                                              QuartetSetup& qs, double* F) {
+  const double rs = rsqrt(pb.zeta + pk.zeta);
+  const double inv = rs * rs;
+  qs.roz = pk.zeta * inv;
+  qs.roe = pb.zeta * inv;
+  qs.o2ze = 0.5 * inv;
+#pragma unroll
+  for (int x = 0; x < 3; ++x) qs.PQ[x] = pk.P[x] - pb.P[x];
+  const double r2 = fma(qs.PQ[2], qs.PQ[2], fma(qs.PQ[1], qs.PQ[1], qs.PQ[0] * qs.PQ[0]));
+  const double T = (pb.zeta * qs.roz) * r2;
+  boys_scaled<L>(T, (pb.K * pk.K) * rs, boys, F);
+}
+
+// Primitive loops of Algorithm 2: bra pair data once per bra primitive pair,
+// ket pair data per primitive quartet.  With CONTRACTED == false every shell
+// has exactly one primitive and the loops disappear.
+#define PRIM_LOOP_BEGIN(P, Q)                                                                              \
+  {                                                                                                        \
+    const int nab_ = CONTRACTED ? Q.na * Q.nb : 1;                                                         \
+    const int ncd_ = CONTRACTED ? Q.nc * Q.nd : 1;                                                         \
+    for (int iab_ = 0; iab_ < nab_; ++iab_) {                                                              \
+      const int i_ = CONTRACTED ? iab_ / Q.nb : 0, j_ = CONTRACTED ? iab_ - i_ * Q.nb : 0;                \
+      PrimPair pb;                                                                                         \
+      make_pair(__ldg(P.sh.exps + Q.pa + i_), __ldg(P.sh.coef + Q.pa + i_), __ldg(P.sh.exps + Q.pb + j_), \
+                __ldg(P.sh.coef + Q.pb + j_), Q.A, Q.AB, Q.rAB2, pb);                                      \
+      for (int icd_ = 0; icd_ < ncd_; ++icd_) {                                                            \
+        const int k_ = CONTRACTED ? icd_ / Q.nd : 0, l_ = CONTRACTED ? icd_ - k_ * Q.nd : 0;              \
+        PrimPair pk;                                                                                       \
+        make_pair(__ldg(P.sh.exps + Q.pc + k_), __ldg(P.sh.coef + Q.pc + k_), __ldg(P.sh.exps + Q.pd + l_), \
+                  __ldg(P.sh.coef + Q.pd + l_), Q.C, Q.CD, Q.rCD2, pk);                                    \
+        QuartetSetup qs;
+
+#define PRIM_LOOP_END \
+  }                   \
+  }                   \
+  }
+
+// ---------------------------------------------------------------- outputs
+// OUTPUT_ROW(r, ia, ib)            start of bra row (ia, ib) of the final block
+// OUTPUT_VAL(ia, ib, ic, id, v)    one final integral (ab|cd) in canonical order
+// OUTPUT_ROW_END()                 end of the row
+// OUTPUT_QUARTET_END()             end of the quartet
+#define OUTPUT_ROW(r, ia, ib)                                       \
+  {                                                                 \
+  double* __restrict__ orow_ = nullptr;                             \
+  if constexpr (MODE == kStore) {                                   \
+    orow_ = P.out + q * P.out_stride + (ia) * P.ostr[0] + (ib) * P.ostr[1]; \
+  }
+
+#define OUTPUT_VAL(ia, ib, ic, id, v)                               \
+  if constexpr (MODE == kStore) {                                   \
+    orow_[(ic) * P.ostr[2] + (id) * P.ostr[3]] = (v);              \
+  } else if constexpr (MODE == kSchwarz) {                          \
+    if ((ia) == (ic) && (ib) == (id)) smax_ = fmax(smax_, fabs(v)); \
+  }
+
+#define OUTPUT_ROW_END() \
+  (void)orow_;             \
+  }
+
+#define OUTPUT_QUARTET_END()                                        \
+  if constexpr (MODE == kSchwarz) {                                 \
+    P.q_out[q] = sqrt(smax_);                                       \
+  }
+
+}  // namespace eri
+
+// Per-class entry: instantiates the kernel for every mode and contraction flag
+// and exports the generator's per-class statistics.
+#define ERI_LAUNCH_MODE_(KERNEL, M)                                                    \
+  if (contracted)                                                                      \
+    KERNEL<M, true><<<blocks, kThreads, 0, st>>>(*P);                                  \
+  else                                                                                 \
+    KERNEL<M, false><<<blocks, kThreads, 0, st>>>(*P);
+
+#define ERI_DEFINE_CLASS_LAUNCHER(LA, LB, LC, LD, KERNEL, SLOTS, VOPS, VFLOPS, HOPS, HFLOPS)               \
+  extern "C" int eri_launch_c##LA##LB##LC##LD(const EriLaunch* P, int mode, int contracted, int blocks,    \
+                                               cudaStream_t st) {                                         \
+    if (mode == kStore) {                                                                                 \
+      ERI_LAUNCH_MODE_(KERNEL, kStore)                                                                    \
+    } else if (mode == kSchwarz) {                                                                        \
+      ERI_LAUNCH_MODE_(KERNEL, kSchwarz)                                                                  \
+    } else {                                                                                              \
+      return -1;                                                                                          \
+    }                                                                                                     \
+    return (int)cudaGetLastError();                                                                       \
+  }                                                                                                       \
+  extern "C" int eri_slots_c##LA##LB##LC##LD() { return SLOTS; }                                          \
+  extern "C" void eri_stats_c##LA##LB##LC##LD(long long* v) {                                             \
+    v[0] = VOPS;                                                                                          \
+    v[1] = VFLOPS;                                                                                        \
+    v[2] = HOPS;                                                                                          \
+    v[3] = HFLOPS;                                                                                        \
+    v[4] = SLOTS;                                                                                         \
+    v[5] = (SLOTS) > 0;                                                                                   \
+  }

@@ -1,0 +1,34 @@
+// Host-side interfaces shared by the runtime translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "eri_device.cuh"
+
+struct eri_plan;
+
+namespace eri {
+namespace screen {
+struct Screen;
+// Builds the plan-level Schwarz screen (pair data, Q factors, per-class
+// quartet sets) for eri_build_J; returns an eri_status.
+int build(eri_plan* p, cudaStream_t st);
+void destroy(Screen* s);
+}  // namespace screen
+
+namespace host {
+int launch_class(eri_plan* p, const int l[4], EriLaunch& P, int mode, cudaStream_t st);
+void canonical_order(const int l[4], int canon[4]);
+bool plan_spherical(const eri_plan* p);
+int plan_nshell(const eri_plan* p);
+const int* plan_L(const eri_plan* p);
+const int* plan_nprim(const eri_plan* p);
+const int* plan_fo(const eri_plan* p);
+const int* plan_poff(const eri_plan* p);
+const double* plan_centers(const eri_plan* p);
+const double* plan_exps(const eri_plan* p);
+int plan_nsm(const eri_plan* p);
+int* plan_dfo(const eri_plan* p);
+screen::Screen*& plan_screen(eri_plan* p);
+}  // namespace host
+}  // namespace eri

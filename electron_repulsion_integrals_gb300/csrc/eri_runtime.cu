@@ -1,0 +1,489 @@
+// Host runtime of the ERI library: plans, shell normalisation, the Boys table,
+// the class registry and kernel dispatch behind the C ABI of include/eri.h.
+//
+// Method: FusionRCG ("FusionRCG: Orchestrating Recursive Computation Graphs
+// across GPU Memory Hierarchies"), Algorithm 2 of section III-C, evaluated by
+// one generated kernel per canonical angular class (csrc/generated/).
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "../../include/eri.h"
+#include "eri_device.cuh"
+#include "eri_host.h"
+
+using namespace eri;
+
+// ------------------------------------------------------------------ registry
+#define ERI_CLASS(a, b, c, d)                                                                   \
+  extern "C" int eri_launch_c##a##b##c##d(const EriLaunch*, int, int, int, cudaStream_t);       \
+  extern "C" int eri_slots_c##a##b##c##d();                                                     \
+  extern "C" void eri_stats_c##a##b##c##d(long long*);
+#include "generated/registry.inc"
+#undef ERI_CLASS
+
+namespace {
+
+struct ClassEntry {
+  int l[4];
+  int (*launch)(const EriLaunch*, int, int, int, cudaStream_t);
+  int (*slots)();
+  void (*stats)(long long*);
+};
+
+const ClassEntry kClasses[] = {
+#define ERI_CLASS(a, b, c, d) {{a, b, c, d}, eri_launch_c##a##b##c##d, eri_slots_c##a##b##c##d, eri_stats_c##a##b##c##d},
+#include "generated/registry.inc"
+#undef ERI_CLASS
+};
+
+const ClassEntry* find_class(int la, int lb, int lc, int ld) {
+  for (const auto& c : kClasses)
+    if (c.l[0] == la && c.l[1] == lb && c.l[2] == lc && c.l[3] == ld) return &c;
+  return nullptr;
+}
+
+int built_lmax() {
+  int m = 0;
+  for (const auto& c : kClasses) m = std::max(m, c.l[0]);
+  return m;
+}
+
+inline int ncart(int l) { return (l + 1) * (l + 2) / 2; }
+inline int nfunc(int l, bool sph) { return (sph && l >= 2) ? 2 * l + 1 : ncart(l); }
+inline int pair_index(int l1, int l2) { return l1 * (l1 + 1) / 2 + l2; }
+
+#define CUDA_TRY(x)                          \
+  do {                                       \
+    cudaError_t e_ = (x);                    \
+    if (e_ != cudaSuccess) {                 \
+      (void)cudaGetLastError();              \
+      return e_ == cudaErrorMemoryAllocation ? ERI_ERR_OOM : ERI_ERR_CUDA; \
+    }                                        \
+  } while (0)
+
+// ------------------------------------------------------------------ Boys table
+// F_m(T_k) at T_k = k/8 for m = 0..kBoysMaxOrder and exp(-T_k), in long
+// double: the highest order from its power series
+//   F_M(T) = e^{-T} sum_i (2T)^i / ((2M+1)(2M+3)...(2M+2i+1)),
+// the others by the downward recursion F_m = (2T F_{m+1} + e^{-T})/(2m+1).
+std::vector<double> make_boys_table() {
+  std::vector<double> tab((size_t)kBoysNgrid * kBoysCols);
+  const int M = kBoysMaxOrder + 8;
+  std::vector<long double> F(M + 1);
+  for (int k = 0; k < kBoysNgrid; ++k) {
+    const long double T = (long double)k / 8.0L;
+    const long double eT = expl(-T);
+    long double term = 1.0L / (2 * M + 1), sum = term;
+    for (int i = 1; i < 100000; ++i) {
+      term *= 2.0L * T / (long double)(2 * M + 2 * i + 1);
+      sum += term;
+      if (term < 1e-24L * sum) break;
+    }
+    F[M] = eT * sum;
+    for (int m = M - 1; m >= 0; --m) F[m] = (2.0L * T * F[m + 1] + eT) / (long double)(2 * m + 1);
+    double* row = &tab[(size_t)k * kBoysCols];
+    row[0] = (double)eT;
+    for (int m = 0; m <= kBoysMaxOrder; ++m) row[1 + m] = (double)F[m];
+  }
+  return tab;
+}
+
+std::mutex g_boys_mu;
+double* g_boys_dev[64] = {nullptr};
+
+int boys_table_for_device(int dev, const double** out) {
+  if (dev < 0 || dev >= 64) return ERI_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_boys_mu);
+  if (!g_boys_dev[dev]) {
+    static std::vector<double> host = make_boys_table();
+    double* d = nullptr;
+    CUDA_TRY(cudaMalloc(&d, host.size() * sizeof(double)));
+    cudaError_t e = cudaMemcpy(d, host.data(), host.size() * sizeof(double), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) {
+      cudaFree(d);
+      return ERI_ERR_CUDA;
+    }
+    g_boys_dev[dev] = d;
+  }
+  *out = g_boys_dev[dev];
+  return ERI_OK;
+}
+
+// ------------------------------------------------------------------ normalisation
+// One thread per shell: coefficients of the normalised contracted shell (x^l
+// component of unit norm), each multiplied by sqrt(sqrt(2) pi^{5/4}) so that
+// the kernels' pair factor c_a c_b exp(..)/zeta carries half of the [00|00]
+// prefactor 2 pi^{5/2} / (zeta eta sqrt(zeta + eta)).
+//   N(alpha, l) = (2 alpha/pi)^{3/4} (4 alpha)^{l/2} / sqrt((2l-1)!!)
+//   S = sum_{k,k'} c_k c_k' N_k N_k' (2l-1)!! / (2 p)^l (pi/p)^{3/2},  p = alpha_k + alpha_k'
+__global__ void normalise_shells_kernel(int nshell, const int* __restrict__ L, const int* __restrict__ nprim,
+                                        const int* __restrict__ poff, const double* __restrict__ ex,
+                                        const double* __restrict__ raw, double* __restrict__ out,
+                                        int* __restrict__ bad) {
+  const int s = blockIdx.x * blockDim.x + threadIdx.x;
+  if (s >= nshell) return;
+  const int l = L[s], np = nprim[s], o = poff[s];
+  const double pi = 3.14159265358979323846;
+  double dl = 1.0;
+  for (int k = 2 * l - 1; k > 1; k -= 2) dl *= k;
+  double S = 0.0;
+  for (int i = 0; i < np; ++i) {
+    const double ai = ex[o + i];
+    const double ti = 2.0 * ai / pi;
+    double fi = 1.0;
+    for (int k = 0; k < l; ++k) fi *= 4.0 * ai;
+    const double Ni = sqrt(sqrt(ti * ti * ti) * fi / dl);
+    for (int j = 0; j < np; ++j) {
+      const double aj = ex[o + j];
+      const double tj = 2.0 * aj / pi;
+      double fj = 1.0;
+      for (int k = 0; k < l; ++k) fj *= 4.0 * aj;
+      const double Nj = sqrt(sqrt(tj * tj * tj) * fj / dl);
+      const double p = ai + aj;
+      double tp = 1.0;
+      for (int k = 0; k < l; ++k) tp *= 2.0 * p;
+      const double q = pi / p;
+      S += raw[o + i] * raw[o + j] * Ni * Nj * dl / tp * q * sqrt(q);
+    }
+  }
+  const double half_pref = 2.4320705525941497402;  // (2 pi^{5/2})^{1/4}
+  const double inv = half_pref / sqrt(S);
+  for (int i = 0; i < np; ++i) {
+    const double ai = ex[o + i];
+    const double ti = 2.0 * ai / pi;
+    double fi = 1.0;
+    for (int k = 0; k < l; ++k) fi *= 4.0 * ai;
+    const double c = raw[o + i] * sqrt(sqrt(ti * ti * ti) * fi / dl) * inv;
+    out[o + i] = c;
+    if (!isfinite(c)) atomicExch(bad, 1);
+  }
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ plan
+struct eri_plan {
+  int device = 0;
+  int nsm = 152;
+  int nshell = 0;
+  bool spherical = true;
+  bool contracted = false;
+  double tau = 0;
+  int lmax = 0;
+  std::vector<int> hL, hnprim, hpoff, hfo;
+  std::vector<double> hcen, hexps, hcoef;  // hcoef: the caller's raw coefficients
+  int nbf = 0;
+  // device copies
+  double* dcen = nullptr;
+  int* dL = nullptr;
+  int* dnprim = nullptr;
+  int* dpoff = nullptr;
+  int* dfo = nullptr;
+  double* dexps = nullptr;
+  double* dcoef = nullptr;
+  const double* dboys = nullptr;
+  // scratch
+  double* scratch = nullptr;
+  size_t scratch_len = 0;
+  int* qbuf = nullptr;  // device int4 quartet staging
+  size_t qbuf_len = 0;
+  eri::screen::Screen* screen = nullptr;
+};
+
+namespace {
+
+template <class T>
+int upload(T** dst, const std::vector<T>& src) {
+  size_t bytes = std::max<size_t>(src.size(), 1) * sizeof(T);
+  CUDA_TRY(cudaMalloc(dst, bytes));
+  if (!src.empty()) CUDA_TRY(cudaMemcpy(*dst, src.data(), src.size() * sizeof(T), cudaMemcpyHostToDevice));
+  return ERI_OK;
+}
+
+int ensure_scratch(eri_plan* p, size_t doubles) {
+  if (doubles <= p->scratch_len) return ERI_OK;
+  if (p->scratch) {
+    cudaFree(p->scratch);
+    p->scratch = nullptr;
+    p->scratch_len = 0;
+  }
+  CUDA_TRY(cudaMalloc(&p->scratch, doubles * sizeof(double)));
+  CUDA_TRY(cudaMemset(p->scratch, 0, doubles * sizeof(double)));
+  p->scratch_len = doubles;
+  return ERI_OK;
+}
+
+void fill_shells(const eri_plan* p, ShellsDev& sh) {
+  sh.cen = p->dcen;
+  sh.L = p->dL;
+  sh.nprim = p->dnprim;
+  sh.poff = p->dpoff;
+  sh.exps = p->dexps;
+  sh.coef = p->dcoef;
+}
+
+int normalise_on_device(eri_plan* p, cudaStream_t st) {
+  double* raw = nullptr;
+  int* bad = nullptr;
+  int rc = upload(&raw, p->hcoef);
+  if (rc) return rc;
+  cudaError_t e = cudaMalloc(&p->dcoef, std::max<size_t>(p->hcoef.size(), 1) * sizeof(double));
+  if (e == cudaSuccess) e = cudaMalloc(&bad, sizeof(int));
+  if (e == cudaSuccess) e = cudaMemsetAsync(bad, 0, sizeof(int), st);
+  if (e == cudaSuccess) {
+    normalise_shells_kernel<<<(p->nshell + 255) / 256, 256, 0, st>>>(p->nshell, p->dL, p->dnprim, p->dpoff, p->dexps,
+                                                                     raw, p->dcoef, bad);
+    e = cudaGetLastError();
+  }
+  int hbad = 0;
+  if (e == cudaSuccess) e = cudaMemcpyAsync(&hbad, bad, sizeof(int), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  cudaFree(raw);
+  cudaFree(bad);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return e == cudaErrorMemoryAllocation ? ERI_ERR_OOM : ERI_ERR_CUDA;
+  }
+  return hbad ? ERI_ERR_NOT_FINITE : ERI_OK;
+}
+
+}  // namespace
+
+// Launch helper shared with the screening / Coulomb code (eri_host.h).
+int eri::host::launch_class(eri_plan* p, const int l[4], EriLaunch& P, int mode, cudaStream_t st) {
+  const ClassEntry* ce = find_class(l[0], l[1], l[2], l[3]);
+  if (!ce) return ERI_ERR_UNSUPPORTED_L;
+  if (P.n <= 0) return ERI_OK;
+  fill_shells(p, P.sh);
+  P.boys = p->dboys;
+  const int slots = ce->slots();
+  long long blocks;
+  if (slots > 0) {
+    blocks = (long long)p->nsm * 2;
+    const long long nt = blocks * kThreads;
+    int rc = ensure_scratch(p, (size_t)slots * nt);
+    if (rc) return rc;
+    P.scratch = p->scratch;
+  } else {
+    blocks = std::min<long long>((P.n + kThreads - 1) / kThreads, (long long)p->nsm * 32);
+    P.scratch = nullptr;
+  }
+  int rc = ce->launch(&P, mode, p->contracted ? 1 : 0, (int)blocks, st);
+  if (rc == -1) return ERI_ERR_NOT_IMPLEMENTED;
+  return rc == 0 ? ERI_OK : ERI_ERR_CUDA;
+}
+
+// Requested class order -> canonical order (la >= lb, lc >= ld, pair(ab) >= pair(cd)).
+void eri::host::canonical_order(const int l[4], int canon[4]) {
+  int b0 = 0, b1 = 1, k0 = 2, k1 = 3;
+  if (l[b0] < l[b1]) std::swap(b0, b1);
+  if (l[k0] < l[k1]) std::swap(k0, k1);
+  if (pair_index(l[b0], l[b1]) < pair_index(l[k0], l[k1])) {
+    std::swap(b0, k0);
+    std::swap(b1, k1);
+  }
+  canon[0] = b0;
+  canon[1] = b1;
+  canon[2] = k0;
+  canon[3] = k1;
+}
+
+bool eri::host::plan_spherical(const eri_plan* p) { return p->spherical; }
+int eri::host::plan_nshell(const eri_plan* p) { return p->nshell; }
+const int* eri::host::plan_L(const eri_plan* p) { return p->hL.data(); }
+const int* eri::host::plan_nprim(const eri_plan* p) { return p->hnprim.data(); }
+const int* eri::host::plan_fo(const eri_plan* p) { return p->hfo.data(); }
+const double* eri::host::plan_centers(const eri_plan* p) { return p->hcen.data(); }
+const double* eri::host::plan_exps(const eri_plan* p) { return p->hexps.data(); }
+const int* eri::host::plan_poff(const eri_plan* p) { return p->hpoff.data(); }
+int eri::host::plan_nsm(const eri_plan* p) { return p->nsm; }
+int* eri::host::plan_dfo(const eri_plan* p) { return p->dfo; }
+eri::screen::Screen*& eri::host::plan_screen(eri_plan* p) { return p->screen; }
+
+extern "C" {
+
+const char* eri_status_string(int s) {
+  switch (s) {
+    case ERI_OK: return "ok";
+    case ERI_ERR_INVALID_ARG: return "invalid argument";
+    case ERI_ERR_UNSUPPORTED_L: return "unsupported angular momentum or basis";
+    case ERI_ERR_BUFFER_TOO_SMALL: return "output buffer too small";
+    case ERI_ERR_CUDA: return "CUDA error";
+    case ERI_ERR_OOM: return "out of memory";
+    case ERI_ERR_NOT_FINITE: return "non-finite or non-positive shell data";
+    case ERI_ERR_NOT_IMPLEMENTED: return "not implemented";
+  }
+  return "unknown status";
+}
+
+int eri_plan_destroy(eri_plan* p) {
+  if (!p) return ERI_OK;
+  eri::screen::destroy(p->screen);
+  cudaFree(p->dcen);
+  cudaFree(p->dL);
+  cudaFree(p->dnprim);
+  cudaFree(p->dpoff);
+  cudaFree(p->dfo);
+  cudaFree(p->dexps);
+  cudaFree(p->dcoef);
+  cudaFree(p->scratch);
+  cudaFree(p->qbuf);
+  delete p;
+  return ERI_OK;
+}
+
+int eri_plan_create(const eri_shell* shells, int nshell, const eri_options* opt, void* stream, eri_plan** out) {
+  if (!out) return ERI_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!shells || nshell <= 0 || !opt || opt->flags != 0) return ERI_ERR_INVALID_ARG;
+  const int lmax_built = built_lmax();
+  eri_plan* p = new (std::nothrow) eri_plan();
+  if (!p) return ERI_ERR_OOM;
+  p->nshell = nshell;
+  p->spherical = opt->spherical != 0;
+  p->tau = opt->schwarz_tau;
+  p->hL.resize(nshell);
+  p->hnprim.resize(nshell);
+  p->hpoff.resize(nshell);
+  p->hfo.resize(nshell + 1);
+  p->hcen.resize(3 * (size_t)nshell);
+  int rc = ERI_OK;
+  size_t np_total = 0;
+  for (int s = 0; s < nshell && rc == ERI_OK; ++s) {
+    const eri_shell& sh = shells[s];
+    if (sh.nprim <= 0 || sh.L < 0 || !sh.exps || !sh.coefs) rc = ERI_ERR_INVALID_ARG;
+    else if (sh.L > lmax_built) rc = ERI_ERR_UNSUPPORTED_L;
+    else {
+      for (int x = 0; x < 3; ++x)
+        if (!std::isfinite(sh.center[x])) rc = ERI_ERR_NOT_FINITE;
+      for (int k = 0; k < sh.nprim; ++k)
+        if (!(std::isfinite(sh.exps[k]) && sh.exps[k] > 0) || !std::isfinite(sh.coefs[k])) rc = ERI_ERR_NOT_FINITE;
+    }
+    if (rc) break;
+    p->hL[s] = sh.L;
+    p->hnprim[s] = sh.nprim;
+    p->hpoff[s] = (int)np_total;
+    np_total += sh.nprim;
+    if (np_total > (size_t)1 << 30) rc = ERI_ERR_INVALID_ARG;
+    for (int x = 0; x < 3; ++x) p->hcen[3 * (size_t)s + x] = sh.center[x];
+    p->lmax = std::max(p->lmax, sh.L);
+    if (sh.nprim > 1) p->contracted = true;
+  }
+  if (rc) {
+    delete p;
+    return rc;
+  }
+  p->hexps.resize(np_total);
+  p->hcoef.resize(np_total);
+  p->hfo[0] = 0;
+  for (int s = 0; s < nshell; ++s) {
+    const eri_shell& sh = shells[s];
+    std::memcpy(&p->hexps[p->hpoff[s]], sh.exps, sh.nprim * sizeof(double));
+    std::memcpy(&p->hcoef[p->hpoff[s]], sh.coefs, sh.nprim * sizeof(double));
+    p->hfo[s + 1] = p->hfo[s] + nfunc(sh.L, p->spherical);
+  }
+  p->nbf = p->hfo[nshell];
+  if (rc) {
+    delete p;
+    return rc;
+  }
+  cudaError_t e = cudaGetDevice(&p->device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&p->nsm, cudaDevAttrMultiProcessorCount, p->device);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    delete p;
+    return ERI_ERR_CUDA;
+  }
+  if ((rc = upload(&p->dcen, p->hcen)) || (rc = upload(&p->dL, p->hL)) || (rc = upload(&p->dnprim, p->hnprim)) ||
+      (rc = upload(&p->dpoff, p->hpoff)) || (rc = upload(&p->dfo, p->hfo)) || (rc = upload(&p->dexps, p->hexps)) ||
+      (rc = boys_table_for_device(p->device, &p->dboys))) {
+    eri_plan_destroy(p);
+    return rc;
+  }
+  rc = normalise_on_device(p, (cudaStream_t)stream);
+  if (rc) {
+    eri_plan_destroy(p);
+    return rc;
+  }
+  if (p->tau > 0) {
+    rc = eri::screen::build(p, (cudaStream_t)stream);
+    if (rc) {
+      eri_plan_destroy(p);
+      return rc;
+    }
+  }
+  *out = p;
+  return ERI_OK;
+}
+
+int eri_plan_nbf(const eri_plan* p, int* nbf) {
+  if (!p || !nbf) return ERI_ERR_INVALID_ARG;
+  *nbf = p->nbf;
+  return ERI_OK;
+}
+
+int eri_plan_shell_info(const eri_plan* p, int s, int* nf, int* first) {
+  if (!p || s < 0 || s >= p->nshell) return ERI_ERR_INVALID_ARG;
+  if (nf) *nf = p->hfo[s + 1] - p->hfo[s];
+  if (first) *first = p->hfo[s];
+  return ERI_OK;
+}
+
+int eri_compute_class(eri_plan* p, int la, int lb, int lc, int ld, const int* quartets_dev, long long n,
+                      double* out_dev, long long out_len, void* stream) {
+  if (!p || n < 0 || (n > 0 && (!quartets_dev || !out_dev))) return ERI_ERR_INVALID_ARG;
+  const int l[4] = {la, lb, lc, ld};
+  for (int k = 0; k < 4; ++k) {
+    if (l[k] < 0) return ERI_ERR_INVALID_ARG;
+    if (l[k] > built_lmax()) return ERI_ERR_UNSUPPORTED_L;
+    if (!p->spherical && l[k] >= 2) return ERI_ERR_UNSUPPORTED_L;
+  }
+  if (reinterpret_cast<uintptr_t>(quartets_dev) % 16 != 0) return ERI_ERR_INVALID_ARG;
+  int canon[4];
+  eri::host::canonical_order(l, canon);
+  const int cl[4] = {l[canon[0]], l[canon[1]], l[canon[2]], l[canon[3]]};
+  int nf[4], st[4];
+  for (int k = 0; k < 4; ++k) nf[k] = nfunc(l[k], p->spherical);
+  st[3] = 1;
+  st[2] = nf[3];
+  st[1] = nf[2] * nf[3];
+  st[0] = nf[1] * nf[2] * nf[3];
+  const long long blk = (long long)nf[0] * nf[1] * nf[2] * nf[3];
+  if (n > 0 && out_len / blk < n) return ERI_ERR_BUFFER_TOO_SMALL;
+  if (n == 0) return ERI_OK;
+  EriLaunch P;
+  std::memset(&P, 0, sizeof(P));
+  P.quartets = quartets_dev;
+  P.n = n;
+  for (int k = 0; k < 4; ++k) {
+    P.canon[k] = canon[k];
+    P.ostr[k] = st[canon[k]];
+  }
+  P.out = out_dev;
+  P.out_stride = blk;
+  return eri::host::launch_class(p, cl, P, kStore, (cudaStream_t)stream);
+}
+
+int eri_class_info(int la, int lb, int lc, int ld, eri_class_stats* out) {
+  if (!out) return ERI_ERR_INVALID_ARG;
+  const ClassEntry* ce = find_class(la, lb, lc, ld);
+  if (!ce) return ERI_ERR_UNSUPPORTED_L;
+  long long v[6];
+  ce->stats(v);
+  out->vrr_ops = v[0];
+  out->vrr_flops = v[1];
+  out->hrr_ops = v[2];
+  out->hrr_flops = v[3];
+  out->scratch_slots = (int)v[4];
+  out->staged = (int)v[5];
+  return ERI_OK;
+}
+
+}  // extern "C"

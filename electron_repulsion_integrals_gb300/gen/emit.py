@@ -1,0 +1,390 @@
+"""Emit one sm_103a CUDA kernel per canonical angular class.
+
+The emitted kernel evaluates a batch of contracted shell quartets, one quartet
+per thread, following FusionRCG Algorithm 2 (section III-C):
+
+  for each primitive quartet:            pair/quartet parameters, Boys F_0..F_L,
+                                         VRR (straight-line, scheduled), H += V
+  HRR bra -> T(la) x T(lb) -> HRR ket -> T(lc) x T(ld)   (stepwise fusion, Eq. (16))
+  store the block, digest it into J, or reduce it to a Schwarz factor
+
+Two storage shapes are emitted ("tiers"):
+  * "reg":     every intermediate is a local value; ptxas keeps them in
+               registers.  Used while the working set is small.
+  * "staged":  the VRR targets H[e][f] and the half-transformed G[a'b'][f] live
+               in a per-thread global scratch area, laid out slot-major so that
+               a warp's accesses to one slot are contiguous; HRR runs as loops
+               over columns (bra) and rows (ket) with straight-line bodies.
+
+The generated source is deterministic; ``eri_gen.py`` writes it under
+``csrc/generated``.
+"""
+
+from __future__ import annotations
+
+from . import graph as G
+from .sph import cart2sph, cart_list, nsph
+
+
+def _fmt(c):
+    r = repr(float(c))
+    if "e" not in r and "." not in r:
+        r += ".0"
+    return r
+
+
+class Emitter:
+    def __init__(self):
+        self.lines = []
+        self.ops = 0      # FP64 instructions
+        self.flops = 0    # FMA = 2, MUL/ADD = 1
+
+    def w(self, s):
+        self.lines.append(s)
+
+    def mul(self, a, b):
+        self.ops += 1
+        self.flops += 1
+        return f"{a} * {b}"
+
+    def fma(self, a, b, c):
+        self.ops += 1
+        self.flops += 2
+        return f"fma({a}, {b}, {c})"
+
+    def add(self, a, b):
+        self.ops += 1
+        self.flops += 1
+        return f"{a} + {b}"
+
+
+def lin_comb(em, terms, name, decl="const double"):
+    """name = sum c_k * x_k for constant coefficients c_k (zeros dropped).
+    Returns the expression name or a literal for an empty sum."""
+    terms = [(c, x) for c, x in terms if c != 0.0]
+    if not terms:
+        em.w(f"{decl} {name} = 0.0;")
+        return name
+    c0, x0 = terms[0]
+    if c0 == 1.0:
+        expr = x0
+    elif c0 == -1.0:
+        expr = f"-{x0}"
+    else:
+        expr = em.mul(_fmt(c0), x0)
+    if len(terms) == 1:
+        em.w(f"{decl} {name} = {expr};")
+        return name
+    em.w(f"double {name} = {expr};")
+    for c, x in terms[1:]:
+        if c == 1.0:
+            em.w(f"{name} = {em.add(name, x)};")
+        elif c == -1.0:
+            em.ops += 1
+            em.flops += 1
+            em.w(f"{name} = {name} - {x};")
+        else:
+            em.w(f"{name} = {em.fma(_fmt(c), x, name)};")
+    return name
+
+
+# ----------------------------------------------------------------------------- VRR
+
+
+def emit_vrr(em, g, order, sink):
+    """Straight-line VRR over the scheduled order.  sink(target_index, var)
+    is called right after a target value is produced."""
+    L = g.L
+    tpos = {t: k for k, t in enumerate(g.targets)}
+    name = {}
+    for v in order:
+        nd = g.nodes[v]
+        e, f, m = nd.key
+        var = f"v{v}"
+        name[v] = var
+        if nd.side == "base":
+            em.w(f"const double {var} = F[{m}];")
+        else:
+            ax = "xyz"[nd.axis]
+            if nd.side == "bra":
+                c0, c1, cy, cr = f"PA{ax}", f"WP{ax}", f"k{nd.ky}_o2z", "roz"
+            else:
+                c0, c1, cy, cr = f"QC{ax}", f"WQ{ax}", f"k{nd.ky}_o2e", "roe"
+            expr = em.mul(c0, name[nd.x0])
+            em.w(f"double {var} = {expr};")
+            em.w(f"{var} = {em.fma(c1, name[nd.x1], var)};")
+            if nd.y0 >= 0:
+                em.w(f"{var} = {em.fma(cy, em.fma('-' + cr, name[nd.y1], name[nd.y0]), var)};")
+            if nd.z1 >= 0:
+                em.w(f"{var} = {em.fma(f'k{nd.kz}_o2ze', name[nd.z1], var)};")
+        if v in tpos:
+            sink(tpos[v], name[v])
+    return name
+
+
+def vrr_coef_needs(g):
+    need = {"PA": set(), "WP": set(), "QC": set(), "WQ": set(), "o2z": set(), "o2e": set(), "o2ze": set(),
+            "roz": False, "roe": False}
+    for nd in g.nodes:
+        if nd.side == "bra":
+            need["PA"].add(nd.axis)
+            need["WP"].add(nd.axis)
+            if nd.y0 >= 0:
+                need["o2z"].add(nd.ky)
+                need["roz"] = True
+            if nd.z1 >= 0:
+                need["o2ze"].add(nd.kz)
+        elif nd.side == "ket":
+            need["QC"].add(nd.axis)
+            need["WQ"].add(nd.axis)
+            if nd.y0 >= 0:
+                need["o2e"].add(nd.ky)
+                need["roe"] = True
+            if nd.z1 >= 0:
+                need["o2ze"].add(nd.kz)
+    return need
+
+
+def emit_vrr_coefs(em, need):
+    """Per primitive quartet coefficient set used by the VRR (from the quartet
+    setup values pb/pk/qs); only what the graph uses is emitted."""
+    for ax in sorted(need["PA"]):
+        em.w(f"const double PA{'xyz'[ax]} = pb.PA[{ax}];")
+    for ax in sorted(need["QC"]):
+        em.w(f"const double QC{'xyz'[ax]} = pk.PA[{ax}];")
+    for ax in sorted(need["WP"]):
+        em.w(f"const double WP{'xyz'[ax]} = {em.mul('qs.roz', f'qs.PQ[{ax}]')};")
+    for ax in sorted(need["WQ"]):
+        em.w(f"const double WQ{'xyz'[ax]} = {em.mul('-qs.roe', f'qs.PQ[{ax}]')};")
+    if need["roz"]:
+        em.w("const double roz = qs.roz;")
+    if need["roe"]:
+        em.w("const double roe = qs.roe;")
+    for k in sorted(need["o2z"]):
+        em.w(f"const double k{k}_o2z = {'pb.o2z' if k == 1 else em.mul(_fmt(k), 'pb.o2z')};")
+    for k in sorted(need["o2e"]):
+        em.w(f"const double k{k}_o2e = {'pk.o2z' if k == 1 else em.mul(_fmt(k), 'pk.o2z')};")
+    for k in sorted(need["o2ze"]):
+        em.w(f"const double k{k}_o2ze = {'qs.o2ze' if k == 1 else em.mul(_fmt(k), 'qs.o2ze')};")
+
+
+# ----------------------------------------------------------------------------- HRR + sph
+
+
+def emit_hrr_column(em, la, lb, get_input, prefix, AB):
+    """One HRR sweep (Eq. (3)/(13)) for one column; returns {(a,b): var}."""
+    steps, inputs, targets = G.hrr_plan(la, lb)
+    val = {}
+    for key in inputs:
+        val[key] = get_input(key[0])
+    cnt = 0
+    for out, p1, p2, ax in steps:
+        var = f"{prefix}{cnt}"
+        cnt += 1
+        em.w(f"const double {var} = {em.fma(AB[ax], val[p2], val[p1])};")
+        val[out] = var
+    return {t: val[t] for t in targets}
+
+
+def emit_sph_pair(em, la, lb, cart_vals, prefix):
+    """Apply T(la) x T(lb) to a Cartesian (a,b) block: index a first, then b
+    (section III-B, Eq. (12)).  Returns list of vars in (a', b') row-major."""
+    ca, cb = cart_list(la), cart_list(lb)
+    Ta, Tb = cart2sph(la), cart2sph(lb)
+    na, nb = len(Ta), len(Tb)
+    # transform a for each Cartesian b
+    if la <= 1:
+        half = {(i, b): cart_vals[(ca[i], b)] for i in range(na) for b in cb}
+    else:
+        half = {}
+        for i in range(na):
+            for b in cb:
+                nm = f"{prefix}a{i}_{cb.index(b)}"
+                half[(i, b)] = lin_comb(em, [(Ta[i][k], cart_vals[(ca[k], b)]) for k in range(len(ca))], nm)
+    out = []
+    for i in range(na):
+        for j in range(nb):
+            if lb <= 1:
+                out.append(half[(i, cb[j])])
+            else:
+                nm = f"{prefix}s{i}_{j}"
+                out.append(lin_comb(em, [(Tb[j][k], half[(i, cb[k])]) for k in range(len(cb))], nm))
+    return out
+
+
+# ----------------------------------------------------------------------------- kernel
+
+
+HEADER = """// Generated by electron_repulsion_integrals_gb300/gen/eri_gen.py -- do not edit.
+// Class ({la}{lb}|{lc}{ld}): L = {L}, VRR nodes = {nv} (axis rule {rule}, {sched} order,
+// PeakLive {pl}), targets = {nt}, shape = {shape}.
+// FP64 work per primitive quartet (VRR + contraction): {vops} instructions;
+// per contracted quartet (HRR + spherical transform): {hops} instructions.
+#include "../eri_device.cuh"
+
+namespace eri {{
+namespace gen {{
+"""
+
+
+def BOYS_SETUP_OPS(L):
+    """FP64 instructions of quartet_setup + boys_scaled (table branch) in
+    eri_device.cuh, counting each library call (rsqrt) as one."""
+    quartet = 1 + 1 + 1 + 3 + 3 + 3 + 2 + 2
+    boys = 3 + 8 + 9 + 1 + (0 if L == 0 else 9 + 2 + 1 + 2 * L)
+    return quartet + boys
+
+
+def BOYS_SETUP_FLOPS(L):
+    quartet = 1 + 1 + 1 + 3 + 3 + 5 + 2 + 2
+    boys = 5 + 8 + 18 + 1 + (0 if L == 0 else 18 + 2 + 1 + 3 * L)
+    return quartet + boys
+
+
+def class_name(cls):
+    return "c{}{}{}{}".format(*cls)
+
+
+def choose_shape(g, peak, cls):
+    nacc = len(g.targets)
+    return "reg" if (nacc + peak) <= 150 else "staged"
+
+
+def emit_class(cls, spherical_out=True):
+    la, lb, lc, ld = cls
+    La, Lc = la + lb, lc + ld
+    L = La + Lc
+    g, order, info = G.best_vrr(cls)
+    shape = choose_shape(g, info["peak_live"], cls)
+    E = [e for k in range(la, La + 1) for e in cart_list(k)]
+    Fc = [f for k in range(lc, Lc + 1) for f in cart_list(k)]
+    NE, NF = len(E), len(Fc)
+    eidx = {e: i for i, e in enumerate(E)}
+    fidx = {f: i for i, f in enumerate(Fc)}
+    cname = class_name(cls)
+    nsa, nsb, nsc, nsd = (len(cart2sph(l)) for l in cls)
+    nca, ncb, ncc, ncd = (len(cart_list(l)) for l in cls)
+    NR = nsa * nsb
+
+    body = Emitter()
+    w = body.w
+
+    # ---- primitive quartet part (VRR + contraction) ----
+    vem = Emitter()
+    vem.w(f"double F[{L + 1}];")
+    vem.w(f"quartet_setup<{L}>(pb, pk, P.boys, qs, F);")
+    emit_vrr_coefs(vem, vrr_coef_needs(g))
+    tvars = [None] * len(g.targets)
+
+    if shape == "reg":
+        def sink(ti, var):
+            tvars[ti] = var
+            vem.w(f"if (CONTRACTED) {{ h{ti} += {var}; }} else {{ h{ti} = {var}; }}")
+    else:
+        def sink(ti, var):
+            e, f = g.target_ef[ti]
+            slot = eidx[e] * NF + fidx[f]
+            vem.w(f"if (CONTRACTED) {{ S[{slot} * nt] += {var}; }} else {{ S[{slot} * nt] = {var}; }}")
+    emit_vrr(vem, g, order, sink)
+    vops, vflops = vem.ops, vem.flops
+
+    # ---- kernel text ----
+    w(f"template <int MODE, bool CONTRACTED>")
+    w(f"__global__ void __launch_bounds__(kThreads) k_{cname}(const EriLaunch P) {{")
+    w("  const long long nt = (long long)gridDim.x * blockDim.x;")
+    w("  const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;")
+    if shape == "staged":
+        w("  double* __restrict__ S = P.scratch + gid;")
+    w("  for (long long q = gid; q < P.n; q += nt) {")
+    w("    Quartet Q;")
+    w("    load_quartet(P, q, Q);")
+    w("    double smax_ = 0.0;")
+    w("    (void)smax_;")
+    if shape == "reg":
+        w(f"    double h[{len(g.targets)}];")
+        for ti in range(len(g.targets)):
+            w(f"    double& h{ti} = h[{ti}];")
+        w("    if (CONTRACTED) {")
+        for ti in range(len(g.targets)):
+            w(f"      h{ti} = 0.0;")
+        w("    }")
+    else:
+        w("    if (CONTRACTED) {")
+        w(f"      for (int s = 0; s < {len(g.targets)}; ++s) S[s * nt] = 0.0;")
+        w("    }")
+    w("    PRIM_LOOP_BEGIN(P, Q)")
+    for ln in vem.lines:
+        w("      " + ln)
+    w("    PRIM_LOOP_END")
+
+    # ---- HRR + sph ----
+    hem = Emitter()
+    if shape == "reg":
+        # G[r][f] for every ket column f
+        gvals = {}
+        for f in Fc:
+            cart = emit_hrr_column(hem, la, lb, lambda e, f=f: f"h{g.target_ef.index((e, f))}", f"b{fidx[f]}_",
+                                   ["Q.AB[0]", "Q.AB[1]", "Q.AB[2]"])
+            rows = emit_sph_pair(hem, la, lb, cart, f"t{fidx[f]}_")
+            for r, var in enumerate(rows):
+                gvals[(r, f)] = var
+        for r in range(NR):
+            cart = emit_hrr_column(hem, lc, ld, lambda f, r=r: gvals[(r, f)], f"k{r}_",
+                                   ["Q.CD[0]", "Q.CD[1]", "Q.CD[2]"])
+            outs = emit_sph_pair(hem, lc, ld, cart, f"u{r}_")
+            hem.w(f"OUTPUT_ROW({r}, {r // nsb}, {r % nsb});")
+            for cdi, var in enumerate(outs):
+                hem.w(f"OUTPUT_VAL({r // nsb}, {r % nsb}, {cdi // nsd}, {cdi % nsd}, {var});")
+            hem.w("OUTPUT_ROW_END();")
+        hops = hem.ops
+        for ln in hem.lines:
+            w("    " + ln)
+    else:
+        # bra: loop over ket columns
+        bem = Emitter()
+        bem.w(f"const double* __restrict__ Hc = S + (long long)fi * nt;")
+        cart = emit_hrr_column(bem, la, lb, lambda e: f"Hc[{eidx[e] * NF} * nt]", "b", ["Q.AB[0]", "Q.AB[1]", "Q.AB[2]"])
+        rows = emit_sph_pair(bem, la, lb, cart, "t")
+        bem.w(f"double* __restrict__ Gc = S + (long long)({NE * NF} + fi) * nt;")
+        for r, var in enumerate(rows):
+            bem.w(f"Gc[{r * NF} * nt] = {var};")
+        w(f"    for (int fi = 0; fi < {NF}; ++fi) {{")
+        for ln in bem.lines:
+            w("      " + ln)
+        w("    }")
+        kem = Emitter()
+        kem.w(f"const double* __restrict__ Gr = S + (long long)({NE * NF} + r * {NF}) * nt;")
+        cart = emit_hrr_column(kem, lc, ld, lambda f: f"Gr[{fidx[f]} * nt]", "k", ["Q.CD[0]", "Q.CD[1]", "Q.CD[2]"])
+        outs = emit_sph_pair(kem, lc, ld, cart, "u")
+        kem.w(f"OUTPUT_ROW(r, r / {nsb}, r % {nsb});")
+        for cdi, var in enumerate(outs):
+            kem.w(f"OUTPUT_VAL(r / {nsb}, r % {nsb}, {cdi // nsd}, {cdi % nsd}, {var});")
+        kem.w("OUTPUT_ROW_END();")
+        w(f"    for (int r = 0; r < {NR}; ++r) {{")
+        for ln in kem.lines:
+            w("      " + ln)
+        w("    }")
+        hops = bem.ops * NF + kem.ops * NR
+        hem.flops = bem.flops * NF + kem.flops * NR
+    w("    OUTPUT_QUARTET_END();")
+    w("  }")
+    w("}")
+
+    scratch_slots = (NE * NF + NR * NF) if shape == "staged" else 0
+    meta = dict(cls=cls, L=L, shape=shape, nvrr=len(g.nodes), ntargets=len(g.targets), vrr_ops=vops,
+                vrr_flops=vflops, hrr_ops=hops, hrr_flops=hem.flops, scratch_slots=scratch_slots,
+                nfunc=(nsa, nsb, nsc, nsd), ncart=(nca, ncb, ncc, ncd), **info)
+    head = HEADER.format(la=la, lb=lb, lc=lc, ld=ld, L=L, nv=len(g.nodes), rule=g.rule, sched=info["schedule"],
+                         pl=info["peak_live"], nt=len(g.targets), shape=shape, vops=vops, hops=hops)
+    vops_all, vflops_all = vops + BOYS_SETUP_OPS(L), vflops + BOYS_SETUP_FLOPS(L)
+    meta["vrr_ops_total"], meta["vrr_flops_total"] = vops_all, vflops_all
+    vops, vflops = vops_all, vflops_all
+    hflops = hem.flops
+    tail = f"""
+}}  // namespace gen
+
+ERI_DEFINE_CLASS_LAUNCHER({la}, {lb}, {lc}, {ld}, gen::k_{cname}, {scratch_slots}, {vops}LL, {vflops}LL, {hops}LL, {hflops}LL)
+
+}}  // namespace eri
+"""
+    return head + "\n".join(body.lines) + "\n" + tail, meta

@@ -1,0 +1,150 @@
+/*
+ * eri.h -- C ABI of the GB300 electron-repulsion-integral library (liberi.so).
+ *
+ * The library evaluates batches of contracted Gaussian electron repulsion
+ * integrals
+ *     (ab|cd) = \iint phi_a(r1) phi_b(r1) phi_c(r2) phi_d(r2) / |r1 - r2|
+ * (FusionRCG: "Orchestrating Recursive Computation Graphs across GPU Memory
+ * Hierarchies", section II-A, Eq. (1)) with the Head-Gordon-Pople scheme of
+ * that page: Boys function base values, the vertical recurrence Eq. (2), the
+ * horizontal recurrence Eq. (3) / Eq. (13), and the stepwise Cartesian-to-
+ * spherical transform of section III-B (Eqs. (8), (16)), one generated CUDA
+ * kernel per angular-momentum class.  It digests the integrals into the
+ * Coulomb matrix, the "J += SCATTER(G, D)" step of Algorithm 2.
+ *
+ * Conventions (the page leaves them open; these are the library's readings):
+ *   - primitive g = x_A^i y_A^j z_A^k exp(-alpha r_A^2) times
+ *     N(alpha, l) = (2 alpha/pi)^{3/4} (4 alpha)^{l/2} / sqrt((2l-1)!!);
+ *     the caller's coefficients multiply these normalised primitives and the
+ *     contracted shell is rescaled so that its x^l component has unit norm;
+ *   - Cartesian component order: x exponent descending, then y descending;
+ *   - spherical components (l >= 2): real solid harmonics m = -l..l without the
+ *     Condon-Shortley phase, unit normalised; l = 1 keeps (x, y, z);
+ *   - an integral block is stored row-major [a][b][c][d] in the order the
+ *     caller names the shells.
+ *
+ * Threading and streams: a plan may be used from one host thread at a time.
+ * Every entry point that takes `stream` (a cudaStream_t, NULL = legacy default
+ * stream) only enqueues work on it and returns; results are ready when the
+ * stream has been synchronised.  Asynchronous CUDA errors surface as
+ * ERI_ERR_CUDA from a later call.
+ *
+ * Errors: every int-returning function returns ERI_OK (0) or a negative
+ * eri_status.  No call aborts, traps or throws across the ABI; a failed call
+ * leaves the plan usable and the output buffers' contents unspecified.
+ */
+#ifndef ERI_GB300_H
+#define ERI_GB300_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ERI_OK = 0,
+  ERI_ERR_INVALID_ARG = -1,      /* NULL pointer, negative count, bad shell data, mismatched class */
+  ERI_ERR_UNSUPPORTED_L = -2,    /* angular momentum above the built maximum (3) or Cartesian d/f output */
+  ERI_ERR_BUFFER_TOO_SMALL = -3, /* output length smaller than the batch needs */
+  ERI_ERR_CUDA = -4,             /* a CUDA runtime call failed (also reports earlier asynchronous faults) */
+  ERI_ERR_OOM = -5,              /* device or host allocation failed */
+  ERI_ERR_NOT_FINITE = -6,       /* non-finite or non-positive exponent, non-finite coefficient or center */
+  ERI_ERR_NOT_IMPLEMENTED = -7   /* option not built in this library */
+} eri_status;
+
+/* One contracted shell as the caller describes it (host memory, read during
+ * eri_plan_create only).  exps/coefs hold nprim values each; coefs multiply
+ * normalised primitives (see above). */
+typedef struct {
+  double center[3]; /* bohr */
+  int L;            /* 0..3 */
+  int nprim;        /* >= 1 */
+  const double* exps;
+  const double* coefs;
+} eri_shell;
+
+typedef struct {
+  int spherical;      /* 1: spherical functions for l >= 2 (required for d and f shells); 0: Cartesian */
+  double schwarz_tau; /* Schwarz threshold for eri_build_J / eri_plan_quartet_count; <= 0 keeps every quartet */
+  int flags;          /* reserved, must be 0 */
+} eri_options;
+
+typedef struct eri_plan eri_plan;
+
+/* Create a plan over `nshell` shells (FusionRCG Algorithm 2 input "shell
+ * quartet (a,b,c,d) with primitives {(alpha_i, c_i)}").  The plan deep-copies
+ * and normalises the shells on the current CUDA device, uploads the Boys
+ * tables (once per device) and, when opt->schwarz_tau > 0, builds the
+ * primitive-pair data, the Schwarz factors Q_ab = sqrt(max |(ab|ab)|) on the
+ * GPU and the per-class screened quartet sets used by eri_build_J.  Work is
+ * enqueued on `stream` and the call synchronises it before returning.
+ * Ownership: *out is owned by the caller and released with eri_plan_destroy.
+ * Errors: INVALID_ARG (NULL, nshell <= 0, nprim <= 0, L < 0), UNSUPPORTED_L
+ * (L > 3), NOT_FINITE, OOM, CUDA. */
+int eri_plan_create(const eri_shell* shells, int nshell, const eri_options* opt, void* stream, eri_plan** out);
+
+/* Release every device and host resource of the plan (NULL is allowed). */
+int eri_plan_destroy(eri_plan* plan);
+
+/* Number of basis functions of the plan (spherical or Cartesian as chosen). */
+int eri_plan_nbf(const eri_plan* plan, int* nbf);
+
+/* Number of basis functions of shell `s` and the index of its first function. */
+int eri_plan_shell_info(const eri_plan* plan, int s, int* nfunc, int* first);
+
+/* Evaluate `n` shell quartets of class (la lb|lc ld) and store their blocks.
+ *   quartets_dev: device int32 array [n][4] of shell indices in the caller's
+ *                 order; shell quartets[i][k] must have angular momentum
+ *                 (la, lb, lc, ld)[k] (not checked on the device).
+ *   out_dev:      device double array; block i starts at out_dev + i*B where
+ *                 B = nf(la) nf(lb) nf(lc) nf(ld) and is row-major [a][b][c][d];
+ *   out_len:      number of doubles available at out_dev (>= n*B).
+ * The kernel for the canonical class (la >= lb, lc >= ld, pair(la,lb) >=
+ * pair(lc,ld)) is used for every ordering through the permutational symmetry
+ * of the integral; no screening is applied.  Errors: INVALID_ARG,
+ * UNSUPPORTED_L, BUFFER_TOO_SMALL, CUDA, OOM (scratch for large classes). */
+int eri_compute_class(eri_plan* plan, int la, int lb, int lc, int ld, const int* quartets_dev, long long n,
+                      double* out_dev, long long out_len, void* stream);
+
+/* Schwarz factors of `n` shell pairs of class (la, lb): q_out_dev[i] =
+ * sqrt(max_{mu in a, nu in b} |(mu nu|mu nu)|) for pairs_dev[i] = (a, b)
+ * (device int32 [n][2], shell a of angular momentum la, b of lb), computed on
+ * the GPU from the diagonal blocks (ab|ab) in the plan's basis.  This is the
+ * screening quantity of the Schwarz inequality |(ab|cd)| <= Q_ab Q_cd. */
+int eri_schwarz(eri_plan* plan, int la, int lb, const int* pairs_dev, long long n, double* q_out_dev, void* stream);
+
+/* Coulomb matrix J_{mu nu} = sum_{lambda sigma} (mu nu|lambda sigma) D_{lambda sigma}
+ * over every unique shell quartet that passes Q_ab Q_cd >= schwarz_tau
+ * (all of them when tau <= 0).  D_dev and J_dev are device nbf x nbf row-major
+ * double matrices; D must be symmetric; J is overwritten (not accumulated) and
+ * comes out symmetric.  The class kernels digest each block as soon as it is
+ * formed (no integral is written to memory); J is accumulated with FP64
+ * atomics, so its last bits depend on scheduling.  Errors: INVALID_ARG,
+ * CUDA, OOM. */
+int eri_build_J(eri_plan* plan, const double* D_dev, double* J_dev, void* stream);
+
+/* Number of unique shell quartets of canonical class (la lb|lc ld) that
+ * eri_build_J evaluates (after screening). */
+int eri_plan_quartet_count(const eri_plan* plan, int la, int lb, int lc, int ld, long long* n);
+
+/* Per-class statistics of the generated kernel (canonical class): FP64
+ * instructions and flops (FMA = 2) per primitive quartet (pair setup excluded,
+ * Boys and VRR included) and per contracted quartet (HRR + spherical
+ * transform), scratch slots per thread, and whether the class uses the
+ * register or the staged tier (0 / 1). */
+typedef struct {
+  long long vrr_ops, vrr_flops, hrr_ops, hrr_flops;
+  int scratch_slots;
+  int staged;
+} eri_class_stats;
+int eri_class_info(int la, int lb, int lc, int ld, eri_class_stats* out);
+
+/* Human-readable text for a status code (static storage). */
+const char* eri_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ERI_GB300_H */

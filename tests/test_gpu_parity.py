@@ -1,0 +1,184 @@
+"""GPU parity: the CUDA library against the CPU oracle, element by element.
+
+Every comparison goes through the C ABI (via the thin binding) and uses the
+per-integral tolerance |gpu - oracle| <= max(1e-12, 1e-10 |oracle|).
+"""
+
+import itertools
+
+import numpy as np
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+import oracle  # noqa: E402
+import electron_repulsion_integrals_gb300 as eri  # noqa: E402
+from electron_repulsion_integrals_gb300 import workloads as W  # noqa: E402
+
+ATOL, RTOL = 1e-12, 1e-10
+
+
+def built_lmax():
+    lm = 0
+    for l in range(5):
+        try:
+            eri.eri_class_info((l, 0, 0, 0))
+            lm = l
+        except eri.EriError:
+            break
+    return lm
+
+
+def oshells(s):
+    return oracle.ShellSet(s.centers, s.L, s.nprim, s.exps, s.coefs)
+
+
+def check(got, ref, what=""):
+    got = np.asarray(got, dtype=np.float64).ravel()
+    ref = np.asarray(ref, dtype=np.float64).ravel()
+    assert got.shape == ref.shape
+    bad = np.abs(got - ref) > np.maximum(ATOL, RTOL * np.abs(ref))
+    if bad.any():
+        i = int(np.argmax(np.abs(got - ref) - np.maximum(ATOL, RTOL * np.abs(ref))))
+        raise AssertionError(f"{what}: {int(bad.sum())}/{bad.size} outside tolerance; worst at {i}: "
+                             f"gpu={got[i]!r} oracle={ref[i]!r}")
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    eri.lib()
+    return torch.device("cuda", 0)
+
+
+def run_class(plan, cls, quartets, dev):
+    q = torch.as_tensor(np.ascontiguousarray(quartets, dtype=np.int32), device=dev)
+    out = plan.compute_class(cls, q)
+    torch.cuda.synchronize()
+    return out.cpu().numpy()
+
+
+def test_tiny_cartesian_tensor(dev):
+    """Full Cartesian (20)^4 tensor of the tiny set over all ordered quartets."""
+    s = W.tiny()
+    plan = eri.Plan(s, spherical=False)
+    n = s.n
+    nf = [eri.nfunc(l, False) for l in s.L]
+    fo = np.concatenate([[0], np.cumsum(nf)])
+    nbf = int(fo[-1])
+    T = np.zeros((nbf,) * 4)
+    by_class = {}
+    for a, b, c, d in itertools.product(range(n), repeat=4):
+        by_class.setdefault((s.L[a], s.L[b], s.L[c], s.L[d]), []).append((a, b, c, d))
+    for cls, qs in by_class.items():
+        out = run_class(plan, cls, qs, dev)
+        bs = int(np.prod([eri.nfunc(l, False) for l in cls]))
+        for i, (a, b, c, d) in enumerate(qs):
+            T[fo[a]:fo[a + 1], fo[b]:fo[b + 1], fo[c]:fo[c + 1], fo[d]:fo[d + 1]] = \
+                out[i * bs:(i + 1) * bs].reshape(nf[a], nf[b], nf[c], nf[d])
+    ref = oracle.eri_tensor(oshells(s), spherical=False)
+    check(T, ref, "tiny tensor")
+    plan.close()
+
+
+def _homogeneous_check(dev, cls, n, degree, seed_index, sample=None):
+    s, quartets = W.homogeneous(cls, n, degree, seed_index=seed_index)
+    plan = eri.Plan(s, spherical=True)
+    out = run_class(plan, cls, quartets, dev)
+    bs = eri.block_size(cls)
+    idx = np.arange(n) if sample is None else np.sort(np.random.default_rng(5).choice(n, sample, replace=False))
+    ref = oracle.eri_blocks(oshells(s), quartets[idx], spherical=True)
+    got = out.reshape(n, bs)[idx].ravel()
+    check(got, ref, f"class {cls} n={n}")
+    plan.close()
+
+
+@pytest.mark.parametrize("cls", [(1, 1, 1, 1), (2, 2, 2, 2)])
+def test_homogeneous_small_full(dev, cls):
+    # several thread blocks plus a ragged tail
+    _homogeneous_check(dev, cls, 3 * 128 + 77, 1, seed_index=50)
+
+
+@pytest.mark.parametrize("cls", [(1, 1, 1, 1), (2, 2, 2, 2)])
+def test_homogeneous_full_size_sampled(dev, cls):
+    # the benchmark's launch configuration (2^20 quartets), sampled outputs
+    _homogeneous_check(dev, cls, 1 << 20, 1, seed_index=1 if cls == (1, 1, 1, 1) else 101, sample=600)
+
+
+def all_classes(lmax):
+    from electron_repulsion_integrals_gb300.gen.eri_gen import canonical_classes
+    return canonical_classes(lmax)
+
+
+@pytest.mark.parametrize("degree", [1, 2])
+def test_every_canonical_class(dev, degree):
+    lmax = built_lmax()
+    for cls in all_classes(lmax):
+        n = 131 if sum(cls) <= 8 else 37
+        _homogeneous_check(dev, cls, n, degree, seed_index=200 + sum(cls) + 10 * degree)
+
+
+def test_non_canonical_orderings(dev):
+    """Every ordering of a (d p | s d)-type quartet goes through the canonical kernel."""
+    rng = np.random.default_rng(3)
+    base = (2, 1, 0, 2)
+    for perm in set(itertools.permutations(range(4))):
+        cls = tuple(base[p] for p in perm)
+        s, quartets = W.homogeneous(cls, 53, 2, seed_index=300)
+        plan = eri.Plan(s, spherical=True)
+        out = run_class(plan, cls, quartets, dev)
+        ref = oracle.eri_blocks(oshells(s), quartets, spherical=True)
+        check(out, ref, f"ordering {cls}")
+        plan.close()
+
+
+def test_edge_cases(dev):
+    # coincident centers (T = 0, AB = CD = 0), far-apart pairs (large T), tiny and huge exponents
+    cases = []
+    for cls in [(1, 1, 1, 1), (2, 1, 2, 0), (2, 2, 2, 2)]:
+        s, q = W.homogeneous(cls, 8, 1, seed_index=400)
+        s.centers[:] = s.centers[0]
+        cases.append((cls, s, q))
+        s2, q2 = W.homogeneous(cls, 8, 1, seed_index=401, box=60.0)
+        cases.append((cls, s2, q2))
+        s3, q3 = W.homogeneous(cls, 8, 2, seed_index=402, exp_range=(0.05, 5000.0))
+        cases.append((cls, s3, q3))
+    for cls, s, q in cases:
+        plan = eri.Plan(s, spherical=True)
+        out = run_class(plan, cls, q, dev)
+        check(out, oracle.eri_blocks(oshells(s), q, spherical=True), f"edge {cls}")
+        plan.close()
+
+
+def test_empty_and_errors(dev):
+    s, q = W.homogeneous((1, 1, 1, 1), 4, 1, seed_index=500)
+    plan = eri.Plan(s, spherical=True)
+    qt = torch.as_tensor(q, device=dev)
+    empty = torch.zeros((0, 4), dtype=torch.int32, device=dev)
+    eri.eri_compute_class(plan.handle, (1, 1, 1, 1), empty, torch.zeros(1, dtype=torch.float64, device=dev))
+    small = torch.zeros(10, dtype=torch.float64, device=dev)
+    with pytest.raises(eri.EriError) as ei:
+        eri.eri_compute_class(plan.handle, (1, 1, 1, 1), qt, small)
+    assert ei.value.code == -3
+    with pytest.raises(eri.EriError) as ei:
+        eri.eri_compute_class(plan.handle, (9, 1, 1, 1), qt, small)
+    assert ei.value.code == -2
+    plan.close()
+
+
+def test_schwarz_factors(dev):
+    s = W.cluster(5, seed_index=600, radius=4.0)
+    plan = eri.Plan(s, spherical=True)
+    Qref = oracle.schwarz(oshells(s), spherical=True)
+    for la in range(3):
+        for lb in range(la + 1):
+            pairs = [(a, b) for a in range(s.n) for b in range(s.n) if s.L[a] == la and s.L[b] == lb]
+            if not pairs:
+                continue
+            pt = torch.as_tensor(np.asarray(pairs, dtype=np.int32), device=dev)
+            q = plan.schwarz(la, lb, pt).cpu().numpy()
+            check(q, [Qref[a, b] for a, b in pairs], f"Schwarz ({la},{lb})")
+    plan.close()
