@@ -24,7 +24,8 @@ LIB_PATH = os.path.join(HERE, "_build", "liberi.so")
 
 ERI_OK = 0
 STATUS = {0: "ok", -1: "invalid argument", -2: "unsupported angular momentum or basis", -3: "output buffer too small",
-          -4: "CUDA error", -5: "out of memory", -6: "non-finite or non-positive shell data", -7: "not implemented"}
+          -4: "CUDA error", -5: "out of memory", -6: "non-finite or non-positive shell data", -7: "not implemented",
+          -8: "class needs more scratch than the static no-allocation array holds"}
 
 _lib = None
 
@@ -62,6 +63,8 @@ def lib():
         L.eri_plan_nbf.argtypes = [vp, ip]
         L.eri_plan_shell_info.argtypes = [vp, ctypes.c_int, ip, ip]
         L.eri_compute_class.argtypes = [vp] + [ctypes.c_int] * 4 + [vp, ctypes.c_longlong, dp, ctypes.c_longlong, vp]
+        L.eri_compute_class_noalloc.argtypes = [vp] + [ctypes.c_int] * 4 + [vp, ctypes.c_longlong, dp,
+                                                                             ctypes.c_longlong, vp]
         L.eri_schwarz.argtypes = [vp, ctypes.c_int, ctypes.c_int, vp, ctypes.c_longlong, dp, vp]
         L.eri_build_J.argtypes = [vp, dp, dp, vp]
         L.eri_plan_quartet_count.argtypes = [vp] + [ctypes.c_int] * 4 + [ctypes.POINTER(ctypes.c_longlong)]
@@ -136,6 +139,14 @@ def eri_compute_class(plan, cls, quartets, out, stream=None):
     rc = lib().eri_compute_class(plan, *[int(x) for x in cls], _ptr(quartets), int(n), _ptr(out), int(out.numel()),
                                  ctypes.c_void_p(_stream_handle(stream)))
     _check("eri_compute_class", rc)
+
+
+def eri_compute_class_noalloc(plan, cls, quartets, out, stream=None):
+    """eri_compute_class without device allocation (static scratch array; see include/eri.h)."""
+    n = quartets.shape[0] if quartets is not None else 0
+    rc = lib().eri_compute_class_noalloc(plan, *[int(x) for x in cls], _ptr(quartets), int(n), _ptr(out),
+                                         int(out.numel()), ctypes.c_void_p(_stream_handle(stream)))
+    _check("eri_compute_class_noalloc", rc)
 
 
 def eri_schwarz(plan, la, lb, pairs, q_out, stream=None):

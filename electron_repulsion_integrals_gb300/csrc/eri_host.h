@@ -30,5 +30,10 @@ const double* plan_exps(const eri_plan* p);
 int plan_nsm(const eri_plan* p);
 int* plan_dfo(const eri_plan* p);
 screen::Screen*& plan_screen(eri_plan* p);
+int class_launcher(const int l[4], int (**launch)(const EriLaunch*, int, int, int, cudaStream_t), int* slots);
+void fill_plan_inputs(const eri_plan* p, EriLaunch& P);
+bool plan_contracted(const eri_plan* p);
+int plan_device(const eri_plan* p);
+int built_lmax();
 }  // namespace host
 }  // namespace eri

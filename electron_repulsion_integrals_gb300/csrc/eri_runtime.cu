@@ -295,6 +295,23 @@ void eri::host::canonical_order(const int l[4], int canon[4]) {
   canon[3] = k1;
 }
 
+// Accessors for the allocation-free entry point (eri_noalloc.cu).
+int eri::host::class_launcher(const int l[4], int (**launch)(const EriLaunch*, int, int, int, cudaStream_t),
+                              int* slots) {
+  const ClassEntry* ce = find_class(l[0], l[1], l[2], l[3]);
+  if (!ce) return ERI_ERR_UNSUPPORTED_L;
+  *launch = ce->launch;
+  *slots = ce->slots();
+  return ERI_OK;
+}
+void eri::host::fill_plan_inputs(const eri_plan* p, EriLaunch& P) {
+  fill_shells(p, P.sh);
+  P.boys = p->dboys;
+}
+bool eri::host::plan_contracted(const eri_plan* p) { return p->contracted; }
+int eri::host::plan_device(const eri_plan* p) { return p->device; }
+int eri::host::built_lmax() { return ::built_lmax(); }
+
 bool eri::host::plan_spherical(const eri_plan* p) { return p->spherical; }
 int eri::host::plan_nshell(const eri_plan* p) { return p->nshell; }
 const int* eri::host::plan_L(const eri_plan* p) { return p->hL.data(); }
@@ -319,6 +336,7 @@ const char* eri_status_string(int s) {
     case ERI_ERR_OOM: return "out of memory";
     case ERI_ERR_NOT_FINITE: return "non-finite or non-positive shell data";
     case ERI_ERR_NOT_IMPLEMENTED: return "not implemented";
+    case ERI_ERR_SCRATCH_LIMIT: return "class needs more scratch than the static no-allocation array holds";
   }
   return "unknown status";
 }

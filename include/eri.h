@@ -50,7 +50,8 @@ typedef enum {
   ERI_ERR_CUDA = -4,             /* a CUDA runtime call failed (also reports earlier asynchronous faults) */
   ERI_ERR_OOM = -5,              /* device or host allocation failed */
   ERI_ERR_NOT_FINITE = -6,       /* non-finite or non-positive exponent, non-finite coefficient or center */
-  ERI_ERR_NOT_IMPLEMENTED = -7   /* option not built in this library */
+  ERI_ERR_NOT_IMPLEMENTED = -7, /* option not built in this library */
+  ERI_ERR_SCRATCH_LIMIT = -8     /* eri_compute_class_noalloc: the class needs more scratch than the static array */
 } eri_status;
 
 /* One contracted shell as the caller describes it (host memory, read during
@@ -106,6 +107,38 @@ int eri_plan_shell_info(const eri_plan* plan, int s, int* nfunc, int* first);
  * UNSUPPORTED_L, BUFFER_TOO_SMALL, CUDA, OOM (scratch for large classes). */
 int eri_compute_class(eri_plan* plan, int la, int lb, int lc, int ld, const int* quartets_dev, long long n,
                       double* out_dev, long long out_len, void* stream);
+
+/* Allocation-free variant of eri_compute_class.  (The page has no
+ * counterpart: this entry exists for callers of this library, not for the
+ * method.)
+ *
+ * Some callers cannot allocate device memory at call time: a framework whose
+ * caching allocator already holds (nearly) all of the GPU's memory, where a
+ * cudaMalloc would fail or fragment it, or a latency-sensitive pipeline that
+ * cannot afford the device-wide synchronisation cudaMalloc/cudaFree imply.
+ * eri_compute_class may allocate on its first use of a large class (the
+ * staging scratch of the "staged" tier); this entry never does.  It computes
+ * exactly what eri_compute_class computes, with the same arguments, layout and
+ * errors, but takes the staging scratch of staged classes from one file-scope
+ * device array of ERI_NOALLOC_SCRATCH_BYTES (64 MiB) that every GPU which
+ * loads the library holds until the process exits.  The launch grid is sized
+ * so that all its threads' scratch fits in that array (fewer threads than
+ * eri_compute_class uses for the same class, hence lower throughput).
+ *   - No cudaMalloc, cudaFree or allocating library routine is called.
+ *     The plan must already exist (eri_plan_create allocates).
+ *   - The first call on a device (with that device current) looks up the
+ *     array's device address with cudaGetSymbolAddress; make that first call
+ *     before any stream capture.
+ *   - Every call shares the one array per device and leaves its last contents
+ *     in it; the kernels initialise every scratch slot they read within a
+ *     call, so nothing needs clearing between calls.  Calls whose kernels
+ *     overlap on the GPU (different streams, or different host threads) race
+ *     on the array and give wrong results: serialise them.
+ * Errors: those of eri_compute_class, plus ERI_ERR_SCRATCH_LIMIT when one
+ * thread block's scratch for the class exceeds the array. */
+#define ERI_NOALLOC_SCRATCH_BYTES (64ull << 20)
+int eri_compute_class_noalloc(eri_plan* plan, int la, int lb, int lc, int ld, const int* quartets_dev, long long n,
+                              double* out_dev, long long out_len, void* stream);
 
 /* Schwarz factors of `n` shell pairs of class (la, lb): q_out_dev[i] =
  * sqrt(max_{mu in a, nu in b} |(mu nu|mu nu)|) for pairs_dev[i] = (a, b)
