@@ -49,6 +49,12 @@ WORKLOADS = {
                     "classes": [((1, 1, 1, 1), 1 << 20, 1, 1), ((2, 2, 2, 2), 1 << 20, 1, 101)]},
     "high_l": {"desc": "high-L batch: (ff|ff) x 131,072 + (fd|fd) x 262,144 quartets, degree 2, spherical",
                "classes": [((3, 3, 3, 3), 131072, 2, 2), ((3, 2, 3, 2), 262144, 2, 102)]},
+    "cluster64": {"desc": "64-atom synthetic cluster (radius 12 bohr, 32 heavy 3s2p1d + 32 light 2s1p, 1-6 "
+                          "primitives, exponents log-U[0.1,5000]): Coulomb J over all unique quartets surviving "
+                          "Schwarz 1e-10, spherical, D = C C^T", "cluster": (64, 3)},
+    "cluster200": {"desc": "200-atom synthetic cluster (same composition), Coulomb J over all unique quartets "
+                           "surviving Schwarz 1e-10, spherical, D = C C^T (C: N x N/4, N(0,1)/sqrt(N))",
+                   "cluster": (200, 4)},
 }
 
 
@@ -166,6 +172,147 @@ def run_reference(a, rank, world):
                              "sample": desc + " per step, projected to the full step mix"},
             "e2e": {"value": value, "unit": "quartets/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def run_coulomb(a, rank, world, local_rank):
+    """Cluster workloads: one step = eri_build_J over every surviving unique quartet."""
+    import torch
+    import electron_repulsion_integrals_gb300 as eri
+    from electron_repulsion_integrals_gb300 import workloads as W
+    from electron_repulsion_integrals_gb300.gen.eri_gen import canonical_classes
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    eri.lib()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    wl = WORKLOADS[a.workload]
+    natom, idx = wl["cluster"]
+    s = W.cluster(natom, seed_index=idx)
+    nbf = W.nbf(s)
+    D = W.density(nbf, idx)
+    stream = torch.cuda.current_stream()
+    t = time.perf_counter()
+    plan = eri.Plan(s, spherical=True, schwarz_tau=1e-10, stream=stream)
+    plan_s = time.perf_counter() - t
+    counts = {c: plan.quartet_count(c) for c in canonical_classes(int(s.L.max()))}
+    nq = sum(counts.values())
+    Dd = torch.as_tensor(D, device=dev)
+    J = torch.empty_like(Dd)
+    for _ in range(a.warmup):
+        plan.build_J(Dd, J, stream)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(a.steps):
+        plan.build_J(Dd, J, stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    ms = t0.elapsed_time(t1)
+    if dist:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    value = nq * world * a.steps / (ms / 1e3)
+    # algorithmic flops: per class, quartets x (primitive quartets x VRR + HRR) + 4 per digested integral
+    prim_q = 0.0
+    flops = 0.0
+    for c, n in counts.items():
+        if n == 0:
+            continue
+        st = eri.eri_class_info(c)
+        kavg = plan_avg_primitive_quartets(s, c)
+        prim_q += n * kavg
+        flops += n * (kavg * st["vrr_flops"] + st["hrr_flops"] + 4 * eri.block_size(c))
+    ach = flops / (ms / a.steps / 1e3) / 1e12
+    e2e = None
+    if a.e2e:
+        hD = torch.from_numpy(D).pin_memory()
+        hJ = torch.empty_like(hD).pin_memory()
+        torch.cuda.synchronize()
+        te = time.perf_counter()
+        p2 = eri.Plan(s, spherical=True, schwarz_tau=1e-10, stream=stream)
+        dd = hD.to(dev, non_blocking=True)
+        Jd = p2.build_J(dd, None, stream)
+        hJ.copy_(Jd, non_blocking=True)
+        torch.cuda.synchronize()
+        te = time.perf_counter() - te
+        p2.close()
+        e2e = {"value": nq * world / te, "unit": "quartets/s", "h2d_bytes_per_step": hD.numel() * 8 + s.n * 48 +
+               s.exps.size * 16, "d2h_bytes_per_step": hJ.numel() * 8}
+    cpu = None
+    if rank == 0 and a.cpu_baseline:
+        rate, desc, cores = cpu_oracle_rate_cluster(s, counts, budget_s=a.ref_budget)
+        cpu = {"value": rate, "unit": "quartets/s", "cores": cores, "kind": "oracle", "sample": desc}
+    line = {"metric": METRIC, "value": value, "unit": "quartets/s", "n_gpus": world, "steps": a.steps,
+            "warmup": a.warmup, "ms_per_step": ms / a.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl["desc"], "unique_quartets": nq, "primitive_quartets": prim_q, "nbf": nbf,
+                       "plan_create_s": plan_s, "l2": "no flush: J digestion re-reads D; kernels are FP64-bound",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "alu", "kernel": "all class kernels of eri_build_J", "achieved": ach,
+                         "peak": FP64_PEAK_TFLOPS, "unit": "TFLOP/s", "frac": ach / FP64_PEAK_TFLOPS,
+                         "traffic": None, "peak_source": "FP64 pipe: 152 SMs x 2 DFMA/clk x 2 flop x 2.07 GHz"},
+            "clocks": clk, "e2e": e2e, "cpu_baseline": cpu,
+            "gpu_launches": a.steps * (sum(1 for n in counts.values() if n) + 1)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    plan.close()
+    if dist:
+        dist.destroy_process_group()
+
+
+def plan_avg_primitive_quartets(s, cls):
+    """Mean primitive-quartet count of quartets of a class (from the shell
+    contraction degrees; every shell pair of the class weighted equally)."""
+    by_l = {}
+    for L, n in zip(s.L, s.nprim):
+        by_l.setdefault(int(L), []).append(int(n))
+    m = [np.mean(by_l[l]) for l in cls]
+    return float(np.prod(m))
+
+
+def cpu_oracle_rate_cluster(s, counts, budget_s=12.0):
+    """Oracle quartets/s on random unique quartets of the cluster, per class,
+    projected to the class mix of the screened set."""
+    import oracle
+    S = oracle.ShellSet(s.centers, s.L, s.nprim, s.exps, s.coefs)
+    rng = np.random.default_rng(5)
+    by_l = {}
+    for i, L in enumerate(s.L):
+        by_l.setdefault(int(L), []).append(i)
+    tot_q = sum(counts.values())
+    classes = [c for c, n in counts.items() if n]
+    share = budget_s / len(classes)
+    total_time = 0.0
+    done_all = 0
+    for c in classes:
+        spent, done, m = 0.0, 0, 16
+        while spent < share:
+            q = np.array([[rng.choice(by_l[l]) for l in c] for _ in range(m)], dtype=np.int32)
+            t = time.perf_counter()
+            oracle.eri_blocks(S, q, spherical=True)
+            dt = time.perf_counter() - t
+            spent += dt
+            done += m
+            if dt < share / 8:
+                m *= 2
+        total_time += spent / done * counts[c]
+        done_all += done
+    return tot_q / total_time, f"oracle on {done_all} random quartets over {len(classes)} classes, projected to the " \
+        f"screened class mix", oracle.default_threads()
 
 
 def run_ours(a, rank, world, local_rank):
@@ -315,6 +462,8 @@ def main():
     local_rank = env_int("LOCAL_RANK", 0)
     if a.impl == "reference":
         run_reference(a, rank, world)
+    elif "cluster" in WORKLOADS[a.workload]:
+        run_coulomb(a, rank, world, local_rank)
     else:
         run_ours(a, rank, world, local_rank)
 

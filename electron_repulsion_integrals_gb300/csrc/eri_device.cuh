@@ -101,15 +101,31 @@ struct EriLaunch {
   int ostr[4];           // stride of canonical axis k in the requested block layout
   // Schwarz mode: q_out[i] = sqrt(max diag |(ab|ab)|) of quartet i
   double* q_out;
-  // Coulomb mode
-  const double* D;
-  double* J;
-  const int* fo;        // first basis function of each shell
+  // Coulomb mode: quartet t of the class is found through the segment list;
+  // segment k covers work items [seg_start[k], seg_start[k+1]) = bra pair
+  // segs[k].x with ket pairs segs[k].y .. segs[k].y + segs[k].z - 1.
+  const double* D;       // density, nbf x nbf row-major
+  double* J;             // accumulator, nbf x nbf row-major (pair-oriented blocks)
+  const int* fo;         // first basis function of each shell
   int nbf;
+  const struct PairMeta* pairs;
+  const double* prims;   // primitive-pair records, kPrimRec doubles each
+  const int4* segs;
+  const long long* seg_start;
+  int nseg;
   // scratch for staged classes: slot s of thread t at scratch[s * nthreads + t]
   double* scratch;
   const double* boys;
 };
+
+// A screened shell pair of the plan (L_a >= L_b) and its primitive pairs.
+struct PairMeta {
+  int a, b;       // shells
+  int poff, np;   // primitive-pair records [poff, poff + np)
+  double AB[3];   // A - B
+  double rAB2;
+};
+constexpr int kPrimRec = 10;  // zeta, 1/(2 zeta), P[3], P-A[3], K, (pad)
 
 struct Quartet {
   int s[4];           // canonical shells A, B, C, D
@@ -117,6 +133,11 @@ struct Quartet {
   double AB[3], CD[3];
   double rAB2, rCD2;
   int pa, pb, pc, pd, na, nb, nc, nd;
+  // Coulomb mode
+  int bra, ket;       // pair ids
+  int pab, nab, pcd, ncd;
+  int fa, fb, fc, fd;  // first basis functions of the four shells
+  double fab, fcd;     // 2 for a pair of distinct shells, else 1
 };
 
 __device__ __forceinline__ void load_shell_center(const ShellsDev& sh, int s, double* c) {
@@ -154,6 +175,41 @@ __device__ __forceinline__ void load_quartet(const EriLaunch& P, long long q, Qu
   Q.nd = __ldg(P.sh.nprim + Q.s[3]);
 }
 
+// Coulomb mode: work item t -> (bra pair, ket pair) by binary search over the
+// segment starts, then the pair records.
+__device__ __forceinline__ void load_quartet_coulomb(const EriLaunch& P, long long t, Quartet& Q) {
+  int lo = 0, hi = P.nseg - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(P.seg_start + mid) <= t) lo = mid;
+    else hi = mid - 1;
+  }
+  const int4 sg = __ldg(P.segs + lo);
+  Q.bra = sg.x;
+  Q.ket = sg.y + (int)(t - __ldg(P.seg_start + lo));
+  const PairMeta* mb = P.pairs + Q.bra;
+  const PairMeta* mk = P.pairs + Q.ket;
+  Q.s[0] = __ldg(&mb->a);
+  Q.s[1] = __ldg(&mb->b);
+  Q.s[2] = __ldg(&mk->a);
+  Q.s[3] = __ldg(&mk->b);
+  Q.pab = __ldg(&mb->poff);
+  Q.nab = __ldg(&mb->np);
+  Q.pcd = __ldg(&mk->poff);
+  Q.ncd = __ldg(&mk->np);
+#pragma unroll
+  for (int x = 0; x < 3; ++x) {
+    Q.AB[x] = __ldg(&mb->AB[x]);
+    Q.CD[x] = __ldg(&mk->AB[x]);
+  }
+  Q.fa = __ldg(P.fo + Q.s[0]);
+  Q.fb = __ldg(P.fo + Q.s[1]);
+  Q.fc = __ldg(P.fo + Q.s[2]);
+  Q.fd = __ldg(P.fo + Q.s[3]);
+  Q.fab = Q.s[0] != Q.s[1] ? 2.0 : 1.0;
+  Q.fcd = Q.s[2] != Q.s[3] ? 2.0 : 1.0;
+}
+
 // Gaussian product of two primitives (alpha at A, beta at B):
 //   zeta = alpha + beta, P = (alpha A + beta B)/zeta, P - A = -beta/zeta (A - B),
 //   K = c_a c_b exp(-alpha beta/zeta |AB|^2) / zeta
@@ -176,6 +232,24 @@ __device__ __forceinline__ void make_pair(double a, double ca, double b, double 
     p.P[x] = A[x] + p.PA[x];
   }
   p.K = (ca * cb * iz) * exp(-(a * bz) * rAB2);
+}
+
+__device__ __forceinline__ void load_prim(const double* __restrict__ prims, int k, PrimPair& p) {
+  const double* r = prims + (size_t)k * kPrimRec;
+  const double2 z = __ldg(reinterpret_cast<const double2*>(r));
+  const double2 p01 = __ldg(reinterpret_cast<const double2*>(r + 2));
+  const double2 p2a0 = __ldg(reinterpret_cast<const double2*>(r + 4));
+  const double2 a12 = __ldg(reinterpret_cast<const double2*>(r + 6));
+  const double2 kk = __ldg(reinterpret_cast<const double2*>(r + 8));
+  p.zeta = z.x;
+  p.o2z = z.y;
+  p.P[0] = p01.x;
+  p.P[1] = p01.y;
+  p.P[2] = p2a0.x;
+  p.PA[0] = p2a0.y;
+  p.PA[1] = a12.x;
+  p.PA[2] = a12.y;
+  p.K = kk.x;
 }
 
 // Quartet parameters of section II-A: rho = zeta eta/(zeta+eta),
@@ -205,18 +279,26 @@ __device__ __forceinline__ void quartet_setup(const PrimPair& pb, const PrimPair
 // has exactly one primitive and the loops disappear.
 #define PRIM_LOOP_BEGIN(P, Q)                                                                              \
   {                                                                                                        \
-    const int nab_ = CONTRACTED ? Q.na * Q.nb : 1;                                                         \
-    const int ncd_ = CONTRACTED ? Q.nc * Q.nd : 1;                                                         \
+    const int nab_ = MODE == kCoulomb ? Q.nab : CONTRACTED ? Q.na * Q.nb : 1;                              \
+    const int ncd_ = MODE == kCoulomb ? Q.ncd : CONTRACTED ? Q.nc * Q.nd : 1;                              \
     for (int iab_ = 0; iab_ < nab_; ++iab_) {                                                              \
-      const int i_ = CONTRACTED ? iab_ / Q.nb : 0, j_ = CONTRACTED ? iab_ - i_ * Q.nb : 0;                \
       PrimPair pb;                                                                                         \
-      make_pair(__ldg(P.sh.exps + Q.pa + i_), __ldg(P.sh.coef + Q.pa + i_), __ldg(P.sh.exps + Q.pb + j_), \
-                __ldg(P.sh.coef + Q.pb + j_), Q.A, Q.AB, Q.rAB2, pb);                                      \
+      if constexpr (MODE == kCoulomb) {                                                                    \
+        load_prim(P.prims, Q.pab + iab_, pb);                                                              \
+      } else {                                                                                             \
+        const int i_ = CONTRACTED ? iab_ / Q.nb : 0, j_ = CONTRACTED ? iab_ - i_ * Q.nb : 0;              \
+        make_pair(__ldg(P.sh.exps + Q.pa + i_), __ldg(P.sh.coef + Q.pa + i_), __ldg(P.sh.exps + Q.pb + j_), \
+                  __ldg(P.sh.coef + Q.pb + j_), Q.A, Q.AB, Q.rAB2, pb);                                    \
+      }                                                                                                    \
       for (int icd_ = 0; icd_ < ncd_; ++icd_) {                                                            \
-        const int k_ = CONTRACTED ? icd_ / Q.nd : 0, l_ = CONTRACTED ? icd_ - k_ * Q.nd : 0;              \
         PrimPair pk;                                                                                       \
-        make_pair(__ldg(P.sh.exps + Q.pc + k_), __ldg(P.sh.coef + Q.pc + k_), __ldg(P.sh.exps + Q.pd + l_), \
-                  __ldg(P.sh.coef + Q.pd + l_), Q.C, Q.CD, Q.rCD2, pk);                                    \
+        if constexpr (MODE == kCoulomb) {                                                                  \
+          load_prim(P.prims, Q.pcd + icd_, pk);                                                            \
+        } else {                                                                                           \
+          const int k_ = CONTRACTED ? icd_ / Q.nd : 0, l_ = CONTRACTED ? icd_ - k_ * Q.nd : 0;            \
+          make_pair(__ldg(P.sh.exps + Q.pc + k_), __ldg(P.sh.coef + Q.pc + k_), __ldg(P.sh.exps + Q.pd + l_), \
+                    __ldg(P.sh.coef + Q.pd + l_), Q.C, Q.CD, Q.rCD2, pk);                                  \
+        }                                                                                                  \
         QuartetSetup qs;
 
 #define PRIM_LOOP_END \
@@ -229,27 +311,48 @@ __device__ __forceinline__ void quartet_setup(const PrimPair& pb, const PrimPair
 // OUTPUT_VAL(ia, ib, ic, id, v)    one final integral (ab|cd) in canonical order
 // OUTPUT_ROW_END()                 end of the row
 // OUTPUT_QUARTET_END()             end of the quartet
-#define OUTPUT_ROW(r, ia, ib)                                       \
-  {                                                                 \
-  double* __restrict__ orow_ = nullptr;                             \
-  if constexpr (MODE == kStore) {                                   \
-    orow_ = P.out + q * P.out_stride + (ia) * P.ostr[0] + (ib) * P.ostr[1]; \
+#define OUTPUT_ROW(r, ia, ib)                                               \
+  {                                                                         \
+    double* __restrict__ orow_ = nullptr;                                   \
+    double jrow_ = 0.0, dab_ = 0.0;                                         \
+    double* jdst_ = nullptr;                                                \
+    if constexpr (MODE == kStore) {                                         \
+      orow_ = P.out + q * P.out_stride + (ia) * P.ostr[0] + (ib) * P.ostr[1]; \
+    } else if constexpr (MODE == kCoulomb) {                                \
+      const size_t rowoff_ = (size_t)(Q.fa + (ia)) * P.nbf + Q.fb + (ib);   \
+      dab_ = Q.fab * __ldg(P.D + rowoff_);                                  \
+      jdst_ = P.J + rowoff_;                                                \
+    }
+
+#define OUTPUT_VAL(ia, ib, ic, id, v)                                          \
+  if constexpr (MODE == kStore) {                                              \
+    orow_[(ic) * P.ostr[2] + (id) * P.ostr[3]] = (v);                          \
+  } else if constexpr (MODE == kSchwarz) {                                     \
+    if ((ia) == (ic) && (ib) == (id)) smax_ = fmax(smax_, fabs(v));            \
+  } else {                                                                     \
+    jrow_ = fma((v), __ldg(P.D + (size_t)(Q.fc + (ic)) * P.nbf + Q.fd + (id)), jrow_); \
+    jcd_[(ic) * kNSD_ + (id)] = fma((v), dab_, jcd_[(ic) * kNSD_ + (id)]);   \
   }
 
-#define OUTPUT_VAL(ia, ib, ic, id, v)                               \
-  if constexpr (MODE == kStore) {                                   \
-    orow_[(ic) * P.ostr[2] + (id) * P.ostr[3]] = (v);              \
-  } else if constexpr (MODE == kSchwarz) {                          \
-    if ((ia) == (ic) && (ib) == (id)) smax_ = fmax(smax_, fabs(v)); \
+#define OUTPUT_ROW_END()                                    \
+  if constexpr (MODE == kCoulomb) {                         \
+    atomicAdd(jdst_, Q.fcd * jrow_);                        \
+  }                                                         \
+  (void)orow_;                                              \
+  (void)jrow_;                                              \
+  (void)dab_;                                               \
+  (void)jdst_;                                              \
   }
 
-#define OUTPUT_ROW_END() \
-  (void)orow_;             \
-  }
-
-#define OUTPUT_QUARTET_END()                                        \
-  if constexpr (MODE == kSchwarz) {                                 \
-    P.q_out[q] = sqrt(smax_);                                       \
+#define OUTPUT_QUARTET_END()                                                             \
+  if constexpr (MODE == kSchwarz) {                                                      \
+    P.q_out[q] = sqrt(smax_);                                                            \
+  } else if constexpr (MODE == kCoulomb) {                                               \
+    if (Q.bra != Q.ket) {                                                                \
+      _Pragma("unroll") for (int k_ = 0; k_ < kNCD_; ++k_) {                             \
+        atomicAdd(P.J + (size_t)(Q.fc + k_ / kNSD_) * P.nbf + Q.fd + k_ % kNSD_, jcd_[k_]); \
+      }                                                                                  \
+    }                                                                                    \
   }
 
 }  // namespace eri
@@ -269,6 +372,8 @@ __device__ __forceinline__ void quartet_setup(const PrimPair& pb, const PrimPair
       ERI_LAUNCH_MODE_(KERNEL, kStore)                                                                    \
     } else if (mode == kSchwarz) {                                                                        \
       ERI_LAUNCH_MODE_(KERNEL, kSchwarz)                                                                  \
+    } else if (mode == kCoulomb) {                                                                        \
+      KERNEL<kCoulomb, true><<<blocks, kThreads, 0, st>>>(*P);                                            \
     } else {                                                                                              \
       return -1;                                                                                          \
     }                                                                                                     \

@@ -35,5 +35,6 @@ void fill_plan_inputs(const eri_plan* p, EriLaunch& P);
 bool plan_contracted(const eri_plan* p);
 int plan_device(const eri_plan* p);
 int built_lmax();
+double plan_tau(const eri_plan* p);
 }  // namespace host
 }  // namespace eri

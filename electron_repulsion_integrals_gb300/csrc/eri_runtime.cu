@@ -309,6 +309,7 @@ void eri::host::fill_plan_inputs(const eri_plan* p, EriLaunch& P) {
   P.boys = p->dboys;
 }
 bool eri::host::plan_contracted(const eri_plan* p) { return p->contracted; }
+double eri::host::plan_tau(const eri_plan* p) { return p->tau; }
 int eri::host::plan_device(const eri_plan* p) { return p->device; }
 int eri::host::built_lmax() { return ::built_lmax(); }
 

@@ -1,12 +1,33 @@
-// Schwarz factors on the GPU, the plan-level screen and the Coulomb build.
+// Schwarz factors on the GPU, the plan-level screened quartet sets and the
+// Coulomb build J = sum (ab|cd) D_cd.
 //
-// FusionRCG (section V-C) batches shell quartets by angular class; the page
-// does not describe screening.  This library screens with the Schwarz bound
-// |(ab|cd)| <= Q_ab Q_cd, Q_ab = sqrt(max |(ab|ab)|), keeping a unique quartet
-// when Q_ab Q_cd >= tau.
+// FusionRCG batches shell quartets by angular class (section V-C) and ends
+// Algorithm 2 with "J, K += SCATTER(G, D)"; it does not describe screening.
+// This library screens with the Schwarz bound |(ab|cd)| <= Q_ab Q_cd,
+// Q_ab = sqrt(max |(ab|ab)|), and keeps a unique quartet when Q_ab Q_cd >= tau.
+//
+// Layout of the screen:
+//  * shell pairs are oriented (L_a >= L_b; a >= b when L_a = L_b), grouped by
+//    pair class (la, lb), and inside a class by their primitive-pair count K
+//    (K descending) and then by Q (descending);
+//  * a pair survives if Q_ab * max Q >= tau;
+//  * for a canonical quartet class (P_bra, P_ket) the quartets of bra pair i
+//    with one K-group of ket pairs are a prefix of that group (the ket pairs
+//    with Q >= tau / Q_i), stored as one segment (bra, first ket, count); for
+//    P_bra == P_ket only ket pairs at or before i in the pair order are kept,
+//    so each unordered pair of pairs is evaluated once;
+//  * segments are ordered by K_bra * K_ket (descending), so that the threads of
+//    a warp run the same number of primitive iterations.
+// The class kernels locate work item t by binary search over the segment
+// starts, read the precomputed primitive-pair records, and digest each block
+// into J with FP64 atomics as soon as it is formed.
 #include <cuda_runtime.h>
 
+#include <algorithm>
+#include <cmath>
 #include <cstring>
+#include <numeric>
+#include <vector>
 
 #include "../../include/eri.h"
 #include "eri_device.cuh"
@@ -16,6 +37,17 @@ using namespace eri;
 
 namespace {
 
+#define CUDA_TRY(x)                                                        \
+  do {                                                                     \
+    cudaError_t e_ = (x);                                                  \
+    if (e_ != cudaSuccess) {                                               \
+      (void)cudaGetLastError();                                            \
+      return e_ == cudaErrorMemoryAllocation ? ERI_ERR_OOM : ERI_ERR_CUDA; \
+    }                                                                      \
+  } while (0)
+
+inline int pair_index(int l1, int l2) { return l1 * (l1 + 1) / 2 + l2; }
+
 __global__ void pairs_to_diag_quartets(const int2* __restrict__ pairs, long long n, int4* __restrict__ q) {
   long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i < n) {
@@ -24,64 +56,342 @@ __global__ void pairs_to_diag_quartets(const int2* __restrict__ pairs, long long
   }
 }
 
-}  // namespace
+// One thread per screened shell pair: its primitive-pair records (the
+// GAUSSIANPAIRS step of Algorithm 2, done once per pair instead of once per
+// quartet).
+__global__ void build_prim_pairs(int npairs, const PairMeta* __restrict__ pairs, ShellsDev sh,
+                                 double* __restrict__ prims) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= npairs) return;
+  const PairMeta m = pairs[i];
+  double A[3];
+  load_shell_center(sh, m.a, A);
+  const int pa = sh.poff[m.a], pb = sh.poff[m.b], na = sh.nprim[m.a], nb = sh.nprim[m.b];
+  int k = 0;
+  for (int u = 0; u < na; ++u)
+    for (int v = 0; v < nb; ++v, ++k) {
+      PrimPair p;
+      make_pair(sh.exps[pa + u], sh.coef[pa + u], sh.exps[pb + v], sh.coef[pb + v], A, m.AB, m.rAB2, p);
+      double* r = prims + (size_t)(m.poff + k) * kPrimRec;
+      r[0] = p.zeta;
+      r[1] = p.o2z;
+      r[2] = p.P[0];
+      r[3] = p.P[1];
+      r[4] = p.P[2];
+      r[5] = p.PA[0];
+      r[6] = p.PA[1];
+      r[7] = p.PA[2];
+      r[8] = p.K;
+      r[9] = 0.0;
+    }
+}
 
-namespace eri {
-namespace screen {
-struct Screen {};
-int build(eri_plan*, cudaStream_t) { return ERI_ERR_NOT_IMPLEMENTED; }
-void destroy(Screen* s) { delete s; }
-}  // namespace screen
-}  // namespace eri
+// J_out[i][j] = J_acc[i][j] + J_acc[j][i] for functions of different shells
+// (each unique pair was accumulated in one orientation only), J_acc[i][j]
+// inside a diagonal shell block.
+__global__ void symmetrise(int nbf, const int* __restrict__ shell_of, const double* __restrict__ Jacc,
+                           double* __restrict__ J) {
+  const int j = blockIdx.x * blockDim.x + threadIdx.x;
+  const int i = blockIdx.y;
+  if (j >= nbf) return;
+  double v = Jacc[(size_t)i * nbf + j];
+  if (shell_of[i] != shell_of[j]) v += Jacc[(size_t)j * nbf + i];
+  J[(size_t)i * nbf + j] = v;
+}
 
-namespace {
 struct DevBuf {
   void* p = nullptr;
   ~DevBuf() { cudaFree(p); }
 };
+
+struct ClassWork {
+  int l[4];
+  int nseg = 0;
+  long long total = 0;
+  int4* dsegs = nullptr;
+  long long* dstart = nullptr;
+};
+
 }  // namespace
 
-extern "C" {
+namespace eri {
+namespace screen {
 
-int eri_schwarz(eri_plan* p, int la, int lb, const int* pairs_dev, long long n, double* q_out_dev, void* stream) {
-  if (!p || n < 0 || (n > 0 && (!pairs_dev || !q_out_dev)) || la < 0 || lb < 0) return ERI_ERR_INVALID_ARG;
+struct Screen {
+  int npairs = 0;
+  PairMeta* dpairs = nullptr;
+  double* dprims = nullptr;
+  int* dshell_of = nullptr;
+  double* Jacc = nullptr;
+  std::vector<ClassWork> classes;
+  ~Screen() {
+    cudaFree(dpairs);
+    cudaFree(dprims);
+    cudaFree(dshell_of);
+    cudaFree(Jacc);
+    for (auto& c : classes) {
+      cudaFree(c.dsegs);
+      cudaFree(c.dstart);
+    }
+  }
+};
+
+void destroy(Screen* s) { delete s; }
+
+namespace {
+
+// Schwarz factors of n pairs of class (la, lb) on the GPU (device in / out).
+int schwarz_dev(eri_plan* p, int la, int lb, const int2* pairs, long long n, double* q, cudaStream_t st) {
   if (n == 0) return ERI_OK;
-  if (reinterpret_cast<uintptr_t>(pairs_dev) % 8 != 0) return ERI_ERR_INVALID_ARG;
   const int l[4] = {la, lb, la, lb};
   int canon[4];
   eri::host::canonical_order(l, canon);
   const int cl[4] = {l[canon[0]], l[canon[1]], l[canon[2]], l[canon[3]]};
-  cudaStream_t st = (cudaStream_t)stream;
   DevBuf qb;
-  if (cudaMalloc(&qb.p, (size_t)n * sizeof(int4)) != cudaSuccess) {
-    (void)cudaGetLastError();
-    return ERI_ERR_OOM;
-  }
-  const int nb = (int)((n + 255) / 256);
-  pairs_to_diag_quartets<<<nb, 256, 0, st>>>(reinterpret_cast<const int2*>(pairs_dev), n,
-                                              reinterpret_cast<int4*>(qb.p));
-  if (cudaGetLastError() != cudaSuccess) return ERI_ERR_CUDA;
+  CUDA_TRY(cudaMalloc(&qb.p, (size_t)n * sizeof(int4)));
+  pairs_to_diag_quartets<<<(int)((n + 255) / 256), 256, 0, st>>>(pairs, n, reinterpret_cast<int4*>(qb.p));
+  CUDA_TRY(cudaGetLastError());
   EriLaunch P;
   std::memset(&P, 0, sizeof(P));
   P.quartets = reinterpret_cast<const int*>(qb.p);
   P.n = n;
   for (int k = 0; k < 4; ++k) P.canon[k] = canon[k];
-  P.q_out = q_out_dev;
+  P.q_out = q;
   int rc = eri::host::launch_class(p, cl, P, kSchwarz, st);
   if (rc) return rc;
-  // the temporary quartet buffer is freed by DevBuf after the stream drains
-  if (cudaStreamSynchronize(st) != cudaSuccess) return ERI_ERR_CUDA;
+  CUDA_TRY(cudaStreamSynchronize(st));
   return ERI_OK;
 }
 
-int eri_build_J(eri_plan* p, const double* D, double* J, void*) {
-  if (!p || !D || !J) return ERI_ERR_INVALID_ARG;
-  return ERI_ERR_NOT_IMPLEMENTED;
+}  // namespace
+
+int build(eri_plan* p, cudaStream_t st) {
+  const int ns = eri::host::plan_nshell(p);
+  const int* L = eri::host::plan_L(p);
+  const int* np = eri::host::plan_nprim(p);
+  const double* cen = eri::host::plan_centers(p);
+  const double tau = eri::host::plan_tau(p);
+  int lmax = 0;
+  for (int s = 0; s < ns; ++s) lmax = std::max(lmax, L[s]);
+  Screen* S = new (std::nothrow) Screen();
+  if (!S) return ERI_ERR_OOM;
+  eri::host::plan_screen(p) = S;
+
+  // 1. pairs per pair class, oriented L_a >= L_b (a >= b for equal L)
+  const int npc = (lmax + 1) * (lmax + 2) / 2;
+  std::vector<std::vector<int2>> pc(npc);
+  for (int a = 0; a < ns; ++a)
+    for (int b = 0; b < ns; ++b) {
+      if (L[a] < L[b] || (L[a] == L[b] && a < b)) continue;
+      pc[pair_index(L[a], L[b])].push_back(make_int2(a, b));
+    }
+  // 2. Schwarz factors on the GPU
+  std::vector<std::vector<double>> qv(npc);
+  double qmax = 0;
+  for (int la = 0; la <= lmax; ++la)
+    for (int lb = 0; lb <= la; ++lb) {
+      auto& v = pc[pair_index(la, lb)];
+      auto& q = qv[pair_index(la, lb)];
+      q.assign(v.size(), 0.0);
+      if (v.empty()) continue;
+      DevBuf dp, dq;
+      CUDA_TRY(cudaMalloc(&dp.p, v.size() * sizeof(int2)));
+      CUDA_TRY(cudaMalloc(&dq.p, v.size() * sizeof(double)));
+      CUDA_TRY(cudaMemcpyAsync(dp.p, v.data(), v.size() * sizeof(int2), cudaMemcpyHostToDevice, st));
+      int rc = schwarz_dev(p, la, lb, (const int2*)dp.p, (long long)v.size(), (double*)dq.p, st);
+      if (rc) return rc;
+      CUDA_TRY(cudaMemcpyAsync(q.data(), dq.p, v.size() * sizeof(double), cudaMemcpyDeviceToHost, st));
+      CUDA_TRY(cudaStreamSynchronize(st));
+      for (double x : q) qmax = std::max(qmax, x);
+    }
+  // 3. survivors, grouped by K (descending) then Q (descending); global pair order
+  std::vector<PairMeta> meta;
+  std::vector<double> qglob;
+  std::vector<int> kglob;
+  struct Group {
+    int first, count, K;
+  };
+  std::vector<std::vector<Group>> groups(npc);
+  int prim_total = 0;
+  for (int c = 0; c < npc; ++c) {
+    std::vector<int> idx;
+    for (int i = 0; i < (int)pc[c].size(); ++i)
+      if (qv[c][i] * qmax >= tau) idx.push_back(i);
+    std::sort(idx.begin(), idx.end(), [&](int x, int y) {
+      const int kx = np[pc[c][x].x] * np[pc[c][x].y], ky = np[pc[c][y].x] * np[pc[c][y].y];
+      if (kx != ky) return kx > ky;
+      if (qv[c][x] != qv[c][y]) return qv[c][x] > qv[c][y];
+      return x < y;
+    });
+    for (int i : idx) {
+      const int2 pr = pc[c][i];
+      const int K = np[pr.x] * np[pr.y];
+      if (groups[c].empty() || groups[c].back().K != K) groups[c].push_back({(int)meta.size(), 0, K});
+      groups[c].back().count++;
+      PairMeta m;
+      m.a = pr.x;
+      m.b = pr.y;
+      m.poff = prim_total;
+      m.np = K;
+      double r2 = 0;
+      for (int x = 0; x < 3; ++x) {
+        m.AB[x] = cen[3 * (size_t)pr.x + x] - cen[3 * (size_t)pr.y + x];
+        r2 += m.AB[x] * m.AB[x];
+      }
+      m.rAB2 = r2;
+      prim_total += K;
+      meta.push_back(m);
+      qglob.push_back(qv[c][i]);
+      kglob.push_back(K);
+    }
+  }
+  S->npairs = (int)meta.size();
+  // 4. pair table + primitive-pair records on the device
+  CUDA_TRY(cudaMalloc(&S->dpairs, std::max<size_t>(meta.size(), 1) * sizeof(PairMeta)));
+  CUDA_TRY(cudaMalloc(&S->dprims, std::max<size_t>(prim_total, 1) * kPrimRec * sizeof(double)));
+  if (!meta.empty()) {
+    CUDA_TRY(cudaMemcpyAsync(S->dpairs, meta.data(), meta.size() * sizeof(PairMeta), cudaMemcpyHostToDevice, st));
+    EriLaunch P;
+    std::memset(&P, 0, sizeof(P));
+    eri::host::fill_plan_inputs(p, P);
+    build_prim_pairs<<<(S->npairs + 127) / 128, 128, 0, st>>>(S->npairs, S->dpairs, P.sh, S->dprims);
+    CUDA_TRY(cudaGetLastError());
+  }
+  // 5. segments per canonical class
+  for (int la = 0; la <= lmax; ++la)
+    for (int lb = 0; lb <= la; ++lb)
+      for (int lc = 0; lc <= lmax; ++lc)
+        for (int ld = 0; ld <= lc; ++ld) {
+          const int cb = pair_index(la, lb), ck = pair_index(lc, ld);
+          if (cb < ck) continue;
+          ClassWork W;
+          W.l[0] = la;
+          W.l[1] = lb;
+          W.l[2] = lc;
+          W.l[3] = ld;
+          std::vector<int4> segs;
+          std::vector<long long> cost;
+          for (const Group& gb : groups[cb])
+            for (int i = gb.first; i < gb.first + gb.count; ++i) {
+              const double qi = qglob[i];
+              if (!(qi > 0)) continue;
+              const double need = tau / qi;
+              for (const Group& gk : groups[ck]) {
+                if (cb == ck && gk.first > i) break;  // only ket pairs at or before i
+                // ket pairs of the group with Q >= need form a prefix
+                const double* q0 = &qglob[gk.first];
+                int cnt = (int)(std::upper_bound(q0, q0 + gk.count, need, [](double v, double x) { return v > x; }) - q0);
+                // upper_bound with "v > x": first element with !(need > x) ... i.e. x <= need is not strict;
+                // recount exactly: number of x with x >= need
+                cnt = 0;
+                {
+                  int lo = 0, hi = gk.count;
+                  while (lo < hi) {
+                    const int mid = (lo + hi) / 2;
+                    if (q0[mid] >= need) lo = mid + 1;
+                    else hi = mid;
+                  }
+                  cnt = lo;
+                }
+                if (cb == ck && gk.first <= i && i < gk.first + gk.count) cnt = std::min(cnt, i - gk.first + 1);
+                if (cnt <= 0) continue;
+                segs.push_back(make_int4(i, gk.first, cnt, 0));
+                cost.push_back((long long)gb.K * gk.K);
+              }
+            }
+          if (segs.empty()) {
+            S->classes.push_back(W);
+            continue;
+          }
+          std::vector<int> ord(segs.size());
+          std::iota(ord.begin(), ord.end(), 0);
+          std::stable_sort(ord.begin(), ord.end(), [&](int x, int y) { return cost[x] > cost[y]; });
+          std::vector<int4> so(segs.size());
+          std::vector<long long> start(segs.size() + 1);
+          long long t = 0;
+          for (size_t k = 0; k < ord.size(); ++k) {
+            so[k] = segs[ord[k]];
+            start[k] = t;
+            t += so[k].z;
+          }
+          start[segs.size()] = t;
+          W.nseg = (int)segs.size();
+          W.total = t;
+          CUDA_TRY(cudaMalloc(&W.dsegs, so.size() * sizeof(int4)));
+          CUDA_TRY(cudaMalloc(&W.dstart, start.size() * sizeof(long long)));
+          CUDA_TRY(cudaMemcpyAsync(W.dsegs, so.data(), so.size() * sizeof(int4), cudaMemcpyHostToDevice, st));
+          CUDA_TRY(cudaMemcpyAsync(W.dstart, start.data(), start.size() * sizeof(long long), cudaMemcpyHostToDevice,
+                                   st));
+          CUDA_TRY(cudaStreamSynchronize(st));
+          S->classes.push_back(W);
+        }
+  // 6. J accumulator and the shell of every basis function
+  const int nbf = eri::host::plan_fo(p)[ns];
+  std::vector<int> shell_of(nbf);
+  for (int s = 0; s < ns; ++s)
+    for (int f = eri::host::plan_fo(p)[s]; f < eri::host::plan_fo(p)[s + 1]; ++f) shell_of[f] = s;
+  CUDA_TRY(cudaMalloc(&S->dshell_of, std::max(nbf, 1) * sizeof(int)));
+  CUDA_TRY(cudaMemcpyAsync(S->dshell_of, shell_of.data(), nbf * sizeof(int), cudaMemcpyHostToDevice, st));
+  CUDA_TRY(cudaMalloc(&S->Jacc, std::max<size_t>((size_t)nbf * nbf, 1) * sizeof(double)));
+  CUDA_TRY(cudaStreamSynchronize(st));
+  return ERI_OK;
 }
 
-int eri_plan_quartet_count(const eri_plan* p, int, int, int, int, long long* n) {
+}  // namespace screen
+}  // namespace eri
+
+extern "C" {
+
+int eri_schwarz(eri_plan* p, int la, int lb, const int* pairs_dev, long long n, double* q_out_dev, void* stream) {
+  if (!p || n < 0 || (n > 0 && (!pairs_dev || !q_out_dev)) || la < 0 || lb < 0) return ERI_ERR_INVALID_ARG;
+  if (la > eri::host::built_lmax() || lb > eri::host::built_lmax()) return ERI_ERR_UNSUPPORTED_L;
+  if (n == 0) return ERI_OK;
+  if (reinterpret_cast<uintptr_t>(pairs_dev) % 8 != 0) return ERI_ERR_INVALID_ARG;
+  return eri::screen::schwarz_dev(p, la, lb, reinterpret_cast<const int2*>(pairs_dev), n, q_out_dev,
+                                  (cudaStream_t)stream);
+}
+
+int eri_build_J(eri_plan* p, const double* D, double* J, void* stream) {
+  if (!p || !D || !J) return ERI_ERR_INVALID_ARG;
+  eri::screen::Screen* S = eri::host::plan_screen(p);
+  if (!S) return ERI_ERR_INVALID_ARG;  // plan created with schwarz_tau <= 0 has no screen
+  cudaStream_t st = (cudaStream_t)stream;
+  const int ns = eri::host::plan_nshell(p);
+  const int nbf = eri::host::plan_fo(p)[ns];
+  CUDA_TRY(cudaMemsetAsync(S->Jacc, 0, (size_t)nbf * nbf * sizeof(double), st));
+  for (const ClassWork& W : S->classes) {
+    if (W.total == 0) continue;
+    EriLaunch P;
+    std::memset(&P, 0, sizeof(P));
+    P.n = W.total;
+    P.D = D;
+    P.J = S->Jacc;
+    P.fo = eri::host::plan_dfo(p);
+    P.nbf = nbf;
+    P.pairs = S->dpairs;
+    P.prims = S->dprims;
+    P.segs = W.dsegs;
+    P.seg_start = W.dstart;
+    P.nseg = W.nseg;
+    int rc = eri::host::launch_class(p, W.l, P, kCoulomb, st);
+    if (rc) return rc;
+  }
+  dim3 grid((nbf + 127) / 128, nbf);
+  symmetrise<<<grid, 128, 0, st>>>(nbf, S->dshell_of, S->Jacc, J);
+  CUDA_TRY(cudaGetLastError());
+  return ERI_OK;
+}
+
+int eri_plan_quartet_count(const eri_plan* p, int la, int lb, int lc, int ld, long long* n) {
   if (!p || !n) return ERI_ERR_INVALID_ARG;
-  return ERI_ERR_NOT_IMPLEMENTED;
+  eri::screen::Screen* S = eri::host::plan_screen(const_cast<eri_plan*>(p));
+  if (!S) return ERI_ERR_INVALID_ARG;
+  for (const ClassWork& W : S->classes)
+    if (W.l[0] == la && W.l[1] == lb && W.l[2] == lc && W.l[3] == ld) {
+      *n = W.total;
+      return ERI_OK;
+    }
+  return ERI_ERR_UNSUPPORTED_L;
 }
 
 }  // extern "C"

@@ -297,9 +297,20 @@ def emit_class(cls, spherical_out=True):
         w("  double* __restrict__ S = P.scratch + gid;")
     w("  for (long long q = gid; q < P.n; q += nt) {")
     w("    Quartet Q;")
-    w("    load_quartet(P, q, Q);")
+    w("    if constexpr (MODE == kCoulomb) {")
+    w("      load_quartet_coulomb(P, q, Q);")
+    w("    } else {")
+    w("      load_quartet(P, q, Q);")
+    w("    }")
     w("    double smax_ = 0.0;")
     w("    (void)smax_;")
+    w(f"    constexpr int kNSD_ = {nsd};")
+    w(f"    constexpr int kNCD_ = {nsc * nsd};")
+    w("    double jcd_[kNCD_];")
+    w("    if constexpr (MODE == kCoulomb) {")
+    w("      _Pragma(\"unroll\") for (int k_ = 0; k_ < kNCD_; ++k_) jcd_[k_] = 0.0;")
+    w("    }")
+    w("    (void)jcd_;")
     if shape == "reg":
         w(f"    double h[{len(g.targets)}];")
         for ti in range(len(g.targets)):

@@ -63,6 +63,8 @@ def _load():
             lib.ora_eri_blocks.argtypes = shell_args + [ip, ctypes.c_longlong, ctypes.c_int, ctypes.c_int, lp, dp,
                                                         ctypes.c_int]
             lib.ora_schwarz.argtypes = shell_args + [ctypes.c_int, dp, ctypes.c_int]
+            lib.ora_J_blocks.argtypes = shell_args + [ctypes.c_int, ctypes.c_double, dp, dp, ip, ctypes.c_longlong,
+                                                      lp, dp, ctypes.c_int]
             lib.ora_build_J.argtypes = shell_args + [ctypes.c_int, ctypes.c_double, dp, dp, dp, lp, ctypes.c_int]
             _lib = lib
     return _lib
@@ -206,3 +208,25 @@ def build_J(S: ShellSet, D, spherical=True, tau=1e-10, Q=None, nthreads=None):
     if rc:
         raise ValueError("ora_build_J: bad arguments")
     return J, int(kept[0])
+
+
+def J_blocks(S: ShellSet, D, pairs, spherical=True, tau=1e-10, Q=None, nthreads=None):
+    """Blocks J[a][b] for the requested shell pairs, from the definition (see oracle.cpp)."""
+    pairs = np.ascontiguousarray(pairs, dtype=np.int32).reshape(-1, 2)
+    D = np.ascontiguousarray(D, dtype=np.float64)
+    if tau > 0 and Q is None:
+        Q = schwarz(S, spherical, nthreads)
+    Qp = _dp(np.ascontiguousarray(Q, dtype=np.float64)) if Q is not None else None
+    sizes = np.array([nfunc(S.L[a], spherical) * nfunc(S.L[b], spherical) for a, b in pairs], dtype=np.int64)
+    off = np.zeros(len(pairs), dtype=np.int64)
+    if len(pairs) > 1:
+        off[1:] = np.cumsum(sizes)[:-1]
+    out = np.zeros(int(sizes.sum()))
+    Qkeep = Q
+    rc = _load().ora_J_blocks(*S.args(), int(bool(spherical)), float(tau), Qp, _dp(D), _ip(pairs), len(pairs),
+                              _lp(off), _dp(out), int(nthreads or default_threads()))
+    del Qkeep
+    if rc:
+        raise ValueError("ora_J_blocks: bad arguments")
+    return [out[o:o + sz].reshape(nfunc(S.L[a], spherical), nfunc(S.L[b], spherical))
+            for (a, b), o, sz in zip(pairs, off, sizes)]

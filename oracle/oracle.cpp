@@ -631,4 +631,57 @@ int ora_build_J(int nshell, const double* centers, const int* L, const int* npri
   return 0;
 }
 
+// Selected blocks of the Coulomb matrix straight from its definition:
+//   J[a-block][b-block] = sum over all ordered shell pairs (c, d) with
+//   Q_ab Q_cd >= tau (every pair when tau <= 0) of (ab|cd) . D_cd,
+// for the n requested shell pairs ab_pairs[i] = (a, b).  Block i is written
+// row-major (nf(a) x nf(b)) at out + out_off[i].  Q (nshell x nshell) is
+// required when tau > 0.  Used to check sampled parts of J on systems whose
+// full J is too costly here.
+int ora_J_blocks(int nshell, const double* centers, const int* L, const int* nprim, const int* off,
+                 const double* exps, const double* coefs, int spherical, double tau, const double* Q,
+                 const double* D, const int* ab_pairs, long long n, const long long* out_off, double* out,
+                 int nthreads) {
+  Shells S{nshell, centers, L, nprim, off, exps, coefs};
+  if (!shells_ok(S) || !D || !ab_pairs || !out || !out_off || n < 0 || (tau > 0 && !Q)) return -1;
+  std::vector<int> fo(nshell + 1, 0);
+  for (int i = 0; i < nshell; ++i) fo[i + 1] = fo[i] + nfunc(S.L[i], spherical);
+  const int nbf = fo[nshell];
+  for (long long r = 0; r < n; ++r) {
+    const int a = ab_pairs[2 * r], b = ab_pairs[2 * r + 1];
+    if (a < 0 || a >= nshell || b < 0 || b >= nshell) return -1;
+    const int na = nfunc(S.L[a], spherical), nb = nfunc(S.L[b], spherical);
+    std::vector<double> acc((size_t)na * nb, 0.0);
+    int nt = nthreads > 0 ? nthreads : 1;
+    std::vector<std::vector<double>> part(nt, std::vector<double>((size_t)na * nb, 0.0));
+#pragma omp parallel num_threads(nt)
+    {
+      int tid = 0;
+#ifdef _OPENMP
+      tid = omp_get_thread_num();
+#endif
+      std::vector<double> blk;
+#pragma omp for schedule(dynamic, 8)
+      for (long long cd = 0; cd < (long long)nshell * nshell; ++cd) {
+        const int c = (int)(cd / nshell), d = (int)(cd % nshell);
+        if (tau > 0 && Q[(size_t)a * nshell + b] * Q[(size_t)c * nshell + d] < tau) continue;
+        eri_block<double>(S, a, b, c, d, spherical, blk);
+        const int nc = nfunc(S.L[c], spherical), nd = nfunc(S.L[d], spherical);
+        for (int i = 0; i < na; ++i)
+          for (int j = 0; j < nb; ++j) {
+            double sum = 0;
+            for (int k = 0; k < nc; ++k)
+              for (int l = 0; l < nd; ++l)
+                sum += blk[(((size_t)i * nb + j) * nc + k) * nd + l] * D[(size_t)(fo[c] + k) * nbf + fo[d] + l];
+            part[tid][(size_t)i * nb + j] += sum;
+          }
+      }
+    }
+    for (int t = 0; t < nt; ++t)
+      for (size_t k = 0; k < acc.size(); ++k) acc[k] += part[t][k];
+    std::memcpy(out + out_off[r], acc.data(), acc.size() * sizeof(double));
+  }
+  return 0;
+}
+
 }  // extern "C"

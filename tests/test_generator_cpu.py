@@ -31,7 +31,7 @@ def fma(a, b, c):
 
 def translate(src):
     """Python source of the kernel body between the quartet load and the end."""
-    body = src[src.index("load_quartet(P, q, Q);") + len("load_quartet(P, q, Q);"):src.index("OUTPUT_QUARTET_END();")]
+    body = src[src.index("(void)jcd_;") + len("(void)jcd_;"):src.index("OUTPUT_QUARTET_END();")]
     out = []
     ind = 0
     for raw in body.splitlines():
