@@ -391,7 +391,7 @@ def run_ours(a, rank, world, local_rank):
         per_class["({}{}|{}{})".format(*b["cls"])] = {
             "quartets_per_s": b["n"] / (kms / 1e3), "primitive_quartets_per_s": b["n"] * b["deg"] ** 4 / (kms / 1e3),
             "ms_per_launch": kms, "fp64_gflops": tf * 1e3, "frac_fp64_peak": tf / FP64_PEAK_TFLOPS,
-            "flops_per_quartet": b["flops"], "tier": "staged" if b["stats"]["staged"] else "reg"}
+            "flops_per_quartet": b["flops"], "tier": ["reg", "staged", "coop"][b["stats"]["staged"]]}
     dom = max(batches, key=lambda b: b["flops"] * b["n"])
     dname = "({}{}|{}{})".format(*dom["cls"])
     ach = per_class[dname]["fp64_gflops"] / 1e3

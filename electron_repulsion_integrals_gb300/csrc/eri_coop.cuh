@@ -1,0 +1,276 @@
+// Warp-cooperative evaluation of high angular momentum classes.
+//
+// One warp evaluates one contracted shell quartet (FusionRCG Algorithm 2):
+//   * the lanes compute the pair/quartet parameters and Boys values of up to
+//     32 primitive quartets at once (one each) into shared memory;
+//   * for each primitive quartet the VRR (Eq. (2) and its ket form) runs as a
+//     sequence of steps over a per-warp shared-memory arena: the bra part
+//     (column 0, [e|0]^(m)) level by level, then the ket columns
+//     [e|g]^(m) in depth-first order; inside a step the lanes take the nodes
+//     (m, e) in turn, every node performing the same operation;
+//   * targets [e|g]^(0) are added to per-warp accumulators H[g][e] in global
+//     memory (a small, L2-resident region) when column g is complete;
+//   * HRR bra + T x T runs with one lane per ket column, HRR ket + T x T with
+//     one lane per bra row (straight-line generated code).
+// The per-class tables and the HRR code are generated (gen/coop.py,
+// gen/emit.py); the class traits struct C provides the sizes and tables.
+#pragma once
+
+#include "eri_device.cuh"
+
+namespace eri {
+
+constexpr int kCoopWarps = 2;                 // warps per block
+constexpr int kCoopThreads = 32 * kCoopWarps;
+constexpr int kCoopBatch = 16;                // primitive quartets set up at once
+
+// Layout of one primitive quartet's parameters in shared memory (doubles):
+//   0..2 P-A, 3..5 W-P, 6..8 Q-C, 9..11 W-Q, 12 rho/zeta, 13 rho/eta,
+//   14.. k/(2 zeta) for k = 1..La, then k/(2 eta) for k = 1..Lc, then
+//   k/(2(zeta+eta)) for k = 0..max(La, Lc), then F'_0..F'_L.
+template <int La, int Lc>
+struct CoopSetup {
+  static constexpr int L = La + Lc;
+  static constexpr int KO2Z = 14;
+  static constexpr int KO2E = KO2Z + La;
+  static constexpr int KO2ZE = KO2E + Lc;
+  static constexpr int F = KO2ZE + (La > Lc ? La : Lc) + 1;
+  static constexpr int SIZE = F + L + 1;
+  static constexpr int STRIDE = SIZE | 1;  // odd stride: lanes hit different banks
+};
+
+struct CoopCol {
+  int out, x, y, axis, ky, level, target, pad;
+};
+
+// Parameters of primitive quartet (iab, icd) of quartet Q into s[] (one lane).
+template <int MODE, int La, int Lc>
+__device__ __forceinline__ void coop_setup_one(const EriLaunch& P, const Quartet& Q, int iab, int icd, double* s) {
+  using S = CoopSetup<La, Lc>;
+  PrimPair pb, pk;
+  if constexpr (MODE == kCoulomb) {
+    load_prim(P.prims, Q.pab + iab, pb);
+    load_prim(P.prims, Q.pcd + icd, pk);
+  } else {
+    const int i = iab / Q.nb, j = iab - i * Q.nb;
+    const int k = icd / Q.nd, l = icd - k * Q.nd;
+    make_pair(__ldg(P.sh.exps + Q.pa + i), __ldg(P.sh.coef + Q.pa + i), __ldg(P.sh.exps + Q.pb + j),
+              __ldg(P.sh.coef + Q.pb + j), Q.A, Q.AB, Q.rAB2, pb);
+    make_pair(__ldg(P.sh.exps + Q.pc + k), __ldg(P.sh.coef + Q.pc + k), __ldg(P.sh.exps + Q.pd + l),
+              __ldg(P.sh.coef + Q.pd + l), Q.C, Q.CD, Q.rCD2, pk);
+  }
+  QuartetSetup qs;
+  double F[S::L + 1];
+  quartet_setup<S::L>(pb, pk, P.boys, qs, F);
+#pragma unroll
+  for (int x = 0; x < 3; ++x) {
+    s[x] = pb.PA[x];
+    s[3 + x] = qs.roz * qs.PQ[x];
+    s[6 + x] = pk.PA[x];
+    s[9 + x] = -qs.roe * qs.PQ[x];
+  }
+  s[12] = qs.roz;
+  s[13] = qs.roe;
+#pragma unroll
+  for (int k = 1; k <= La; ++k) s[S::KO2Z + k - 1] = k * pb.o2z;
+#pragma unroll
+  for (int k = 1; k <= Lc; ++k) s[S::KO2E + k - 1] = k * pk.o2z;
+  s[S::KO2ZE] = 0.0;
+#pragma unroll
+  for (int k = 1; k <= (La > Lc ? La : Lc); ++k) s[S::KO2ZE + k] = k * qs.o2ze;
+#pragma unroll
+  for (int m = 0; m <= S::L; ++m) s[S::F + m] = F[m];
+}
+
+// VRR of one primitive quartet with parameters s[] into the arena; targets
+// accumulated into H (global, [target column][e - e_la]).
+template <class C>
+__device__ __forceinline__ void coop_vrr(double* __restrict__ arena, const double* __restrict__ s,
+                                         double* __restrict__ H, int lane, bool first) {
+  using S = CoopSetup<C::La, C::Lc>;
+  constexpr int NE = C::NE;
+  double* bra = arena + C::BRA_COL;
+  // column 0: Boys values [00|00]^(m)
+  if (lane <= C::L) bra[lane * NE] = s[S::F + lane];
+  __syncwarp();
+  const double roz = s[12], roe = s[13];
+  // bra levels
+#pragma unroll 1
+  for (int k = 0; k < C::La; ++k) {
+    const int y0 = C::bra_y_start()[k], y1 = C::bra_y_start()[k + 1];
+#pragma unroll 2
+    for (int t = y0 + lane; t < y1; t += 32) {
+      const int4 nd = __ldg(C::bra_y() + t);
+      const int ax = nd.w & 3, ky = nd.w >> 2;
+      double v = s[ax] * bra[nd.y];
+      v = fma(s[3 + ax], bra[nd.y + NE], v);
+      v = fma(s[S::KO2Z + ky - 1], fma(-roz, bra[nd.z + NE], bra[nd.z]), v);
+      bra[nd.x] = v;
+    }
+    const int n0 = C::bra_n_start()[k], n1 = C::bra_n_start()[k + 1];
+#pragma unroll 2
+    for (int t = n0 + lane; t < n1; t += 32) {
+      const int4 nd = __ldg(C::bra_n() + t);
+      const int ax = nd.z;
+      double v = s[ax] * bra[nd.y];
+      v = fma(s[3 + ax], bra[nd.y + NE], v);
+      bra[nd.x] = v;
+    }
+    __syncwarp();
+  }
+  if constexpr (C::lc == 0) {
+    // column 0 is a target column (ket component (0,0,0))
+    for (int k = lane; k < C::NET; k += 32) {
+      const double v = bra[C::IE_LA + k];
+      H[k] = first ? v : H[k] + v;
+    }
+  }
+  // ket columns
+#pragma unroll 1
+  for (int c = 0; c < C::NCOL; ++c) {
+    const CoopCol st = C::cols()[c];
+    const double* X = arena + st.x;
+    const double* Y = arena + (st.y >= 0 ? st.y : st.x);
+    double* O = arena + st.out;
+    const double qc = s[6 + st.axis], wq = s[9 + st.axis];
+    const bool hy = st.y >= 0;
+    const double kyo2e = hy ? s[S::KO2E + st.ky - 1] : 0.0;
+    const int rows = C::Lc - st.level + 1;
+    // nodes with e_i > 0 (cross term [e - 1_i | f]^(m+1))
+    {
+      const int nz = C::nz(st.axis);
+      const int4* zl = C::zlist(st.axis);
+      const int total = rows * nz;
+      const float inv = 1.0f / (float)nz;
+#pragma unroll 2
+      for (int t = lane; t < total; t += 32) {
+        const int m = (int)(((float)t + 0.5f) * inv);
+        const int4 z = __ldg(zl + (t - m * nz));
+        const int o = m * NE + z.x;
+        double v = qc * X[o];
+        v = fma(wq, X[o + NE], v);
+        if (hy) v = fma(kyo2e, fma(-roe, Y[o + NE], Y[o]), v);
+        v = fma(s[S::KO2ZE + z.z], X[(m + 1) * NE + z.y], v);
+        O[o] = v;
+      }
+    }
+    // nodes with e_i = 0
+    {
+      const int nn = C::nn(st.axis);
+      const int* nl = C::nlist(st.axis);
+      const int total = rows * nn;
+      const float inv = 1.0f / (float)nn;
+#pragma unroll 2
+      for (int t = lane; t < total; t += 32) {
+        const int m = (int)(((float)t + 0.5f) * inv);
+        const int o = m * NE + __ldg(nl + (t - m * nn));
+        double v = qc * X[o];
+        v = fma(wq, X[o + NE], v);
+        if (hy) v = fma(kyo2e, fma(-roe, Y[o + NE], Y[o]), v);
+        O[o] = v;
+      }
+    }
+    __syncwarp();
+    if (st.target >= 0) {
+      double* Ht = H + (size_t)st.target * C::NET;
+      for (int k = lane; k < C::NET; k += 32) {
+        const double v = O[C::IE_LA + k];
+        Ht[k] = first ? v : Ht[k] + v;
+      }
+    }
+  }
+  __syncwarp();
+}
+
+}  // namespace eri
+
+// Kernel body shared by every cooperative class.  C: traits; BRA_HRR(fi, Hc, G)
+// and KET_HRR(r, Gr) are the generated per-column / per-row HRR functions.
+#define ERI_COOP_KERNEL(NAME, C, BRA_FN, KET_FN)                                                          \
+  template <int MODE, bool CONTRACTED>                                                                    \
+  __global__ void __launch_bounds__(kCoopThreads) NAME(const EriLaunch P) {                               \
+    extern __shared__ double smem_[];                                                                     \
+    using S_ = CoopSetup<C::La, C::Lc>;                                                                   \
+    const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;                                            \
+    double* arena = smem_ + (size_t)wib * C::WARP_SMEM;                                                   \
+    double* setup = arena + C::ARENA;                                                                     \
+    const long long nw = (long long)gridDim.x * kCoopWarps;                                               \
+    const long long wid = (long long)blockIdx.x * kCoopWarps + wib;                                       \
+    double* H = P.scratch + (size_t)wid * C::NH;                                                          \
+    for (long long q = wid; q < P.n; q += nw) {                                                           \
+      Quartet Q;                                                                                          \
+      if constexpr (MODE == kCoulomb) {                                                                   \
+        load_quartet_coulomb(P, q, Q);                                                                    \
+      } else {                                                                                            \
+        load_quartet<C::la == C::lb, C::lc == C::ld>(P, q, Q);                                            \
+      }                                                                                                   \
+      const int nab = MODE == kCoulomb ? Q.nab : Q.na * Q.nb;                                             \
+      const int ncd = MODE == kCoulomb ? Q.ncd : Q.nc * Q.nd;                                             \
+      const int nprim = nab * ncd;                                                                        \
+      for (int base = 0; base < nprim; base += kCoopBatch) {                                              \
+        const int p = base + lane;                                                                        \
+        if (p < nprim) coop_setup_one<MODE, C::La, C::Lc>(P, Q, p / ncd, p - (p / ncd) * ncd,             \
+                                                          setup + lane * S_::STRIDE);                     \
+        __syncwarp();                                                                                     \
+        const int cnt = nprim - base < kCoopBatch ? nprim - base : kCoopBatch;                            \
+        for (int pp = 0; pp < cnt; ++pp) coop_vrr<C>(arena, setup + pp * S_::STRIDE, H, lane, base + pp == 0); \
+        __syncwarp();                                                                                     \
+      }                                                                                                   \
+      /* HRR bra + T x T: one lane per ket column; G[r][f] in the arena */                               \
+      double* G = arena;                                                                                  \
+      for (int fi = lane; fi < C::NF; fi += 32) BRA_FN(Q, H, fi, G);                                      \
+      __syncwarp();                                                                                       \
+      double smax_ = 0.0;                                                                                 \
+      for (int r = lane; r < C::NR; r += 32) KET_FN<MODE>(P, Q, q, r, G, smax_);                          \
+      if constexpr (MODE == kSchwarz) {                                                                   \
+        _Pragma("unroll") for (int o = 16; o > 0; o >>= 1) smax_ = fmax(smax_, __shfl_xor_sync(0xffffffffu, smax_, o)); \
+        if (lane == 0) P.q_out[q] = sqrt(smax_);                                                          \
+      }                                                                                                   \
+      __syncwarp();                                                                                       \
+    }                                                                                                     \
+  }
+
+// Per-class entry points of a cooperative class (same interface as
+// ERI_DEFINE_CLASS_LAUNCHER): launch, grid/scratch sizing, statistics.
+#define ERI_COOP_SMEM_(T) ((size_t)kCoopWarps * (T::WARP_SMEM) * sizeof(double))
+#define ERI_COOP_LAUNCH_(KERNEL, T, M, C)                                                                \
+  {                                                                                                      \
+    cudaFuncSetAttribute(KERNEL<M, C>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ERI_COOP_SMEM_(T)); \
+    KERNEL<M, C><<<blocks, kCoopThreads, ERI_COOP_SMEM_(T), st>>>(*P);                                   \
+  }
+
+#define ERI_DEFINE_COOP_LAUNCHER(LA, LB, LC, LD, KERNEL, T, VOPS, VFLOPS, HOPS, HFLOPS)                  \
+  extern "C" int eri_launch_c##LA##LB##LC##LD(const EriLaunch* P, int mode, int contracted, int blocks,   \
+                                               cudaStream_t st) {                                        \
+    (void)contracted;                                                                                    \
+    if (mode == kStore) ERI_COOP_LAUNCH_(KERNEL, T, kStore, true)                                        \
+    else if (mode == kSchwarz) ERI_COOP_LAUNCH_(KERNEL, T, kSchwarz, true)                               \
+    else return -1;                                                                                      \
+    return (int)cudaGetLastError();                                                                      \
+  }                                                                                                      \
+  extern "C" int eri_grid_c##LA##LB##LC##LD(int nsm, long long n, long long* blocks, long long* scratch) { \
+    int occ = 0;                                                                                         \
+    cudaFuncSetAttribute(KERNEL<kStore, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,              \
+                         (int)ERI_COOP_SMEM_(T));                                                        \
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, KERNEL<kStore, true>, kCoopThreads,          \
+                                                      ERI_COOP_SMEM_(T)) != cudaSuccess || occ < 1) {    \
+      (void)cudaGetLastError();                                                                          \
+      occ = 1;                                                                                           \
+    }                                                                                                    \
+    long long b = (long long)nsm * occ;                                                                  \
+    const long long need = (n + kCoopWarps - 1) / kCoopWarps;                                            \
+    if (b > need) b = need;                                                                              \
+    if (b < 1) b = 1;                                                                                    \
+    *blocks = b;                                                                                         \
+    *scratch = b * kCoopWarps * (long long)T::NH;                                                        \
+    return 0;                                                                                            \
+  }                                                                                                      \
+  extern "C" int eri_slots_c##LA##LB##LC##LD() { return 0; }                                             \
+  extern "C" void eri_stats_c##LA##LB##LC##LD(long long* v) {                                            \
+    v[0] = VOPS;                                                                                         \
+    v[1] = VFLOPS;                                                                                       \
+    v[2] = HOPS;                                                                                         \
+    v[3] = HFLOPS;                                                                                       \
+    v[4] = T::NH;                                                                                        \
+    v[5] = 2;                                                                                            \
+  }

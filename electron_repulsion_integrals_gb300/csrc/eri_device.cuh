@@ -138,7 +138,34 @@ struct Quartet {
   int pab, nab, pcd, ncd;
   int fa, fb, fc, fd;  // first basis functions of the four shells
   double fab, fcd;     // 2 for a pair of distinct shells, else 1
+  int ost[4];          // store mode: output stride of canonical axes a, b, c, d
 };
+
+// Which shell of a pair of equal angular momentum should carry the VRR.  The
+// HRR of Eq. (3) rebuilds (ab| from [e0| functions of x_A; when A's Gaussians
+// are diffuse and B's tight and the centers far apart, the product center P
+// lies near B, the [e0| grow like |P-A|^(la+lb) and the HRR cancels them back
+// down, losing many digits.  Building on the center P lies closest to keeps
+// the intermediates at the size of the result.  Over all primitive pairs,
+// |P - A| / |AB| is at most beta_max/(alpha_min + beta_max) and |P - B| / |AB|
+// at most alpha_max/(alpha_max + beta_min); returns true when B is the better
+// VRR center.  (A heuristic decision: FP32 is enough.)
+__device__ __forceinline__ bool second_is_better_center(const ShellsDev& sh, int a, int b) {
+  const int pa = __ldg(sh.poff + a), na = __ldg(sh.nprim + a);
+  const int pb = __ldg(sh.poff + b), nb = __ldg(sh.nprim + b);
+  float amin = 3.0e38f, amax = 0.0f, bmin = 3.0e38f, bmax = 0.0f;
+  for (int i = 0; i < na; ++i) {
+    const float x = (float)__ldg(sh.exps + pa + i);
+    amin = fminf(amin, x);
+    amax = fmaxf(amax, x);
+  }
+  for (int i = 0; i < nb; ++i) {
+    const float x = (float)__ldg(sh.exps + pb + i);
+    bmin = fminf(bmin, x);
+    bmax = fmaxf(bmax, x);
+  }
+  return amax / (amax + bmin) < bmax / (amin + bmax);
+}
 
 __device__ __forceinline__ void load_shell_center(const ShellsDev& sh, int s, double* c) {
   c[0] = __ldg(sh.cen + 3 * s);
@@ -146,6 +173,10 @@ __device__ __forceinline__ void load_shell_center(const ShellsDev& sh, int s, do
   c[2] = __ldg(sh.cen + 3 * s + 2);
 }
 
+// SYM_AB / SYM_CD: the class has la == lb / lc == ld, so the two shells of that
+// pair may be exchanged (with their output strides) to put the VRR on the
+// better-conditioned center.
+template <bool SYM_AB, bool SYM_CD>
 __device__ __forceinline__ void load_quartet(const EriLaunch& P, long long q, Quartet& Q) {
   const int4 r = __ldg(reinterpret_cast<const int4*>(P.quartets) + q);
   const int req[4] = {r.x, r.y, r.z, r.w};
@@ -153,6 +184,23 @@ __device__ __forceinline__ void load_quartet(const EriLaunch& P, long long q, Qu
   for (int k = 0; k < 4; ++k) {
     const int c = P.canon[k];
     Q.s[k] = c == 0 ? req[0] : c == 1 ? req[1] : c == 2 ? req[2] : req[3];
+    Q.ost[k] = P.ostr[k];
+  }
+  if (SYM_AB && Q.s[0] != Q.s[1] && second_is_better_center(P.sh, Q.s[0], Q.s[1])) {
+    const int t = Q.s[0];
+    Q.s[0] = Q.s[1];
+    Q.s[1] = t;
+    const int u = Q.ost[0];
+    Q.ost[0] = Q.ost[1];
+    Q.ost[1] = u;
+  }
+  if (SYM_CD && Q.s[2] != Q.s[3] && second_is_better_center(P.sh, Q.s[2], Q.s[3])) {
+    const int t = Q.s[2];
+    Q.s[2] = Q.s[3];
+    Q.s[3] = t;
+    const int u = Q.ost[2];
+    Q.ost[2] = Q.ost[3];
+    Q.ost[3] = u;
   }
   load_shell_center(P.sh, Q.s[0], Q.A);
   load_shell_center(P.sh, Q.s[1], Q.B);
@@ -317,7 +365,7 @@ __device__ __forceinline__ void quartet_setup(const PrimPair& pb, const PrimPair
     double jrow_ = 0.0, dab_ = 0.0;                                         \
     double* jdst_ = nullptr;                                                \
     if constexpr (MODE == kStore) {                                         \
-      orow_ = P.out + q * P.out_stride + (ia) * P.ostr[0] + (ib) * P.ostr[1]; \
+      orow_ = P.out + q * P.out_stride + (ia) * Q.ost[0] + (ib) * Q.ost[1]; \
     } else if constexpr (MODE == kCoulomb) {                                \
       const size_t rowoff_ = (size_t)(Q.fa + (ia)) * P.nbf + Q.fb + (ib);   \
       dab_ = Q.fab * __ldg(P.D + rowoff_);                                  \
@@ -326,7 +374,7 @@ __device__ __forceinline__ void quartet_setup(const PrimPair& pb, const PrimPair
 
 #define OUTPUT_VAL(ia, ib, ic, id, v)                                          \
   if constexpr (MODE == kStore) {                                              \
-    orow_[(ic) * P.ostr[2] + (id) * P.ostr[3]] = (v);                          \
+    orow_[(ic) * Q.ost[2] + (id) * Q.ost[3]] = (v);                            \
   } else if constexpr (MODE == kSchwarz) {                                     \
     if ((ia) == (ic) && (ib) == (id)) smax_ = fmax(smax_, fabs(v));            \
   } else {                                                                     \
@@ -380,6 +428,18 @@ __device__ __forceinline__ void quartet_setup(const PrimPair& pb, const PrimPair
     return (int)cudaGetLastError();                                                                       \
   }                                                                                                       \
   extern "C" int eri_slots_c##LA##LB##LC##LD() { return SLOTS; }                                          \
+  extern "C" int eri_grid_c##LA##LB##LC##LD(int nsm, long long n, long long* blocks, long long* scratch) {  \
+    if ((SLOTS) > 0) {                                                                                    \
+      *blocks = (long long)nsm * 2;                                                                       \
+      *scratch = (long long)(SLOTS) * *blocks * kThreads;                                                 \
+    } else {                                                                                              \
+      long long b = (n + kThreads - 1) / kThreads;                                                        \
+      if (b > (long long)nsm * 32) b = (long long)nsm * 32;                                               \
+      *blocks = b < 1 ? 1 : b;                                                                            \
+      *scratch = 0;                                                                                       \
+    }                                                                                                     \
+    return 0;                                                                                             \
+  }                                                                                                       \
   extern "C" void eri_stats_c##LA##LB##LC##LD(long long* v) {                                             \
     v[0] = VOPS;                                                                                          \
     v[1] = VFLOPS;                                                                                        \

@@ -36,5 +36,6 @@ bool plan_contracted(const eri_plan* p);
 int plan_device(const eri_plan* p);
 int built_lmax();
 double plan_tau(const eri_plan* p);
+int class_grid(const int l[4], int nsm, long long n, long long* blocks, long long* scratch);
 }  // namespace host
 }  // namespace eri

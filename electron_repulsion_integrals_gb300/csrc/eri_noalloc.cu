@@ -79,19 +79,20 @@ extern "C" int eri_compute_class_noalloc(eri_plan* p, int la, int lb, int lc, in
   int slots = 0;
   int rc = eri::host::class_launcher(cl, &launch, &slots);
   if (rc) return rc;
-  // grid: as many 128-thread blocks as the array holds, at most the usual two per SM
-  long long blocks;
+  // grid: the class's usual grid, shrunk until every block's scratch fits the array
+  long long blocks = 0, need = 0;
+  rc = eri::host::class_grid(cl, eri::host::plan_nsm(p), n, &blocks, &need);
+  if (rc) return rc;
   double* scratch = nullptr;
-  if (slots > 0) {
-    const unsigned long long per_block = (unsigned long long)slots * kThreads;
-    blocks = (long long)std::min<unsigned long long>(kNoallocDoubles / per_block,
-                                                     (unsigned long long)eri::host::plan_nsm(p) * 2);
-    if (blocks < 1) return ERI_ERR_SCRATCH_LIMIT;
-  } else {
-    blocks = std::min<long long>((n + kThreads - 1) / kThreads, (long long)eri::host::plan_nsm(p) * 32);
+  if (need > 0) {
+    const unsigned long long per_block = (unsigned long long)((need + blocks - 1) / blocks);
+    const long long fit = (long long)(kNoallocDoubles / per_block);
+    if (fit < 1) return ERI_ERR_SCRATCH_LIMIT;
+    if (blocks > fit) blocks = fit;
   }
+  (void)slots;
   if (n == 0) return ERI_OK;
-  if (slots > 0) {
+  if (need > 0) {
     rc = scratch_address(eri::host::plan_device(p), &scratch);
     if (rc) return rc;
   }

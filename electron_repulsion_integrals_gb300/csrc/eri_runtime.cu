@@ -24,6 +24,7 @@ using namespace eri;
 #define ERI_CLASS(a, b, c, d)                                                                   \
   extern "C" int eri_launch_c##a##b##c##d(const EriLaunch*, int, int, int, cudaStream_t);       \
   extern "C" int eri_slots_c##a##b##c##d();                                                     \
+  extern "C" int eri_grid_c##a##b##c##d(int, long long, long long*, long long*);                \
   extern "C" void eri_stats_c##a##b##c##d(long long*);
 #include "generated/registry.inc"
 #undef ERI_CLASS
@@ -35,10 +36,12 @@ struct ClassEntry {
   int (*launch)(const EriLaunch*, int, int, int, cudaStream_t);
   int (*slots)();
   void (*stats)(long long*);
+  int (*grid)(int, long long, long long*, long long*);
 };
 
 const ClassEntry kClasses[] = {
-#define ERI_CLASS(a, b, c, d) {{a, b, c, d}, eri_launch_c##a##b##c##d, eri_slots_c##a##b##c##d, eri_stats_c##a##b##c##d},
+#define ERI_CLASS(a, b, c, d) \
+  {{a, b, c, d}, eri_launch_c##a##b##c##d, eri_slots_c##a##b##c##d, eri_stats_c##a##b##c##d, eri_grid_c##a##b##c##d},
 #include "generated/registry.inc"
 #undef ERI_CLASS
 };
@@ -263,16 +266,13 @@ int eri::host::launch_class(eri_plan* p, const int l[4], EriLaunch& P, int mode,
   if (P.n <= 0) return ERI_OK;
   fill_shells(p, P.sh);
   P.boys = p->dboys;
-  const int slots = ce->slots();
-  long long blocks;
-  if (slots > 0) {
-    blocks = (long long)p->nsm * 2;
-    const long long nt = blocks * kThreads;
-    int rc = ensure_scratch(p, (size_t)slots * nt);
+  long long blocks = 0, scratch = 0;
+  ce->grid(p->nsm, P.n, &blocks, &scratch);
+  if (scratch > 0) {
+    int rc = ensure_scratch(p, (size_t)scratch);
     if (rc) return rc;
     P.scratch = p->scratch;
   } else {
-    blocks = std::min<long long>((P.n + kThreads - 1) / kThreads, (long long)p->nsm * 32);
     P.scratch = nullptr;
   }
   int rc = ce->launch(&P, mode, p->contracted ? 1 : 0, (int)blocks, st);
@@ -303,6 +303,11 @@ int eri::host::class_launcher(const int l[4], int (**launch)(const EriLaunch*, i
   *launch = ce->launch;
   *slots = ce->slots();
   return ERI_OK;
+}
+int eri::host::class_grid(const int l[4], int nsm, long long n, long long* blocks, long long* scratch) {
+  const ClassEntry* ce = find_class(l[0], l[1], l[2], l[3]);
+  if (!ce) return ERI_ERR_UNSUPPORTED_L;
+  return ce->grid(nsm, n, blocks, scratch);
 }
 void eri::host::fill_plan_inputs(const eri_plan* p, EriLaunch& P) {
   fill_shells(p, P.sh);

@@ -180,10 +180,29 @@ int build(eri_plan* p, cudaStream_t st) {
   // 1. pairs per pair class, oriented L_a >= L_b (a >= b for equal L)
   const int npc = (lmax + 1) * (lmax + 2) / 2;
   std::vector<std::vector<int2>> pc(npc);
+  const double* ex = eri::host::plan_exps(p);
+  const int* po = eri::host::plan_poff(p);
+  // equal-L pairs carry the VRR on the center the Gaussian products lie
+  // closest to (see second_is_better_center in eri_device.cuh)
+  auto second_better = [&](int a, int b) {
+    double amin = 1e300, amax = 0, bmin = 1e300, bmax = 0;
+    for (int i = 0; i < np[a]; ++i) {
+      amin = std::min(amin, ex[po[a] + i]);
+      amax = std::max(amax, ex[po[a] + i]);
+    }
+    for (int i = 0; i < np[b]; ++i) {
+      bmin = std::min(bmin, ex[po[b] + i]);
+      bmax = std::max(bmax, ex[po[b] + i]);
+    }
+    return amax / (amax + bmin) < bmax / (amin + bmax);
+  };
   for (int a = 0; a < ns; ++a)
     for (int b = 0; b < ns; ++b) {
       if (L[a] < L[b] || (L[a] == L[b] && a < b)) continue;
-      pc[pair_index(L[a], L[b])].push_back(make_int2(a, b));
+      if (L[a] == L[b] && a != b && second_better(a, b))
+        pc[pair_index(L[a], L[b])].push_back(make_int2(b, a));
+      else
+        pc[pair_index(L[a], L[b])].push_back(make_int2(a, b));
     }
   // 2. Schwarz factors on the GPU
   std::vector<std::vector<double>> qv(npc);

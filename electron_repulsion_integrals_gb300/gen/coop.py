@@ -1,0 +1,329 @@
+"""Warp-cooperative tier for high angular momentum classes.
+
+For classes whose straight-line code would be too large to compile (and whose
+working set exceeds the register file), one warp evaluates one contracted
+quartet.  The VRR of FusionRCG Eq. (2) is organised by ket component
+("columns"):
+
+  column g (a ket Cartesian component f with |f| = j) holds [e|g]^(m) for every
+  bra component e with |e| <= la+lb and m = 0 .. (lc+ld) - j (column 0, the
+  bra part, holds m = 0 .. L);
+
+  column 0 is built by bra steps (e = e' + 1_i) level by level in |e|;
+  column g = f + 1_i (i chosen by the ket-first z -> y -> x axis rule) is built
+  from column f (terms [e|f]^m, [e|f]^(m+1), [e-1_i|f]^(m+1)) and, when
+  f_i > 0, column f - 1_i -- the ket form of the Obara-Saika step.
+
+Inside one column step every node has the same operation, only the bra
+component e (and so e_i and the index of e - 1_i) differs: the 32 lanes take
+nodes (m, e) in turn, so the warp runs the step as SIMT code with no
+divergence.  Columns live in a per-warp shared-memory arena; the order of the
+column steps (depth first along the axis chains) and a first-fit allocator
+keep the live arena small, e.g. 29 KB for (ff|ff).
+
+Targets [e|g]^(0), |e| >= la, |g| >= lc, are added to per-warp accumulators in
+global memory (L2-resident) as soon as column g is complete.  After the
+primitive loop the bra HRR + spherical transform runs with one lane per ket
+column and the ket HRR + transform with one lane per bra row (straight-line
+code from the register-tier emitter).
+"""
+
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+from .sph import cart_list
+
+
+def ncart(l):
+    return (l + 1) * (l + 2) // 2
+
+
+def _dec(v, i, k=1):
+    v = list(v)
+    v[i] -= k
+    return tuple(v)
+
+
+def _axis(v):
+    for i in (2, 1, 0):
+        if v[i] > 0:
+            return i
+    return None
+
+
+@dataclass
+class ColStep:
+    g: tuple
+    level: int
+    axis: int
+    ky: int           # f_i of the X source column f = g - 1_i (Y term when > 0)
+    out: int          # arena offset (doubles) of column g
+    x: int            # arena offset of column f
+    y: int            # arena offset of column f - 1_i, or -1
+    target: int       # index of g among the target columns, or -1
+
+
+@dataclass
+class CoopPlan:
+    cls: tuple
+    La: int
+    Lc: int
+    L: int
+    NE: int                    # bra components |e| <= La
+    e_list: list
+    ie_la: int                 # first e with |e| >= la (targets)
+    f_targets: list            # ket components with |f| in [lc, Lc]
+    bra_nodes_y: list = field(default_factory=list)    # per level: list of (out, x, y, axis, ky)
+    bra_nodes_n: list = field(default_factory=list)    # per level: list of (out, x, axis)
+    cols: list = field(default_factory=list)
+    zlist: list = field(default_factory=list)          # per axis: [(ie, ie_m1, e_i)] with e_i > 0
+    nlist: list = field(default_factory=list)          # per axis: [ie] with e_i = 0
+    arena: int = 0             # doubles per warp
+    bra_col: int = 0           # arena offset of column 0
+    fp64_ops: int = 0          # FP64 instructions per primitive quartet in the VRR (lane-summed)
+    nodes: int = 0             # VRR nodes per primitive quartet (one DMUL each, the rest FMAs)
+
+
+def plan(cls):
+    la, lb, lc, ld = cls
+    La, Lc = la + lb, lc + ld
+    L = La + Lc
+    e_list = [e for k in range(La + 1) for e in cart_list(k)]
+    eidx = {e: i for i, e in enumerate(e_list)}
+    NE = len(e_list)
+    ie_la = sum(ncart(k) for k in range(la))
+    f_targets = [f for j in range(lc, Lc + 1) for f in cart_list(j)]
+    fidx = {f: i for i, f in enumerate(f_targets)}
+    P = CoopPlan(tuple(cls), La, Lc, L, NE, e_list, ie_la, f_targets)
+    ops = 0
+    # ---- bra part (column 0): level k nodes (m, e), |e| = k, m <= L - k
+    for k in range(1, La + 1):
+        ly, ln = [], []
+        for e in cart_list(k):
+            i = _axis(e)
+            e1 = _dec(e, i)
+            for m in range(0, L - k + 1):
+                out = m * NE + eidx[e]
+                x = m * NE + eidx[e1]
+                if e1[i] > 0:
+                    y = m * NE + eidx[_dec(e1, i)]
+                    ly.append((out, x, y, i, e1[i]))
+                    ops += 4
+                    P.nodes += 1
+                else:
+                    ln.append((out, x, i))
+                    ops += 2
+                    P.nodes += 1
+        P.bra_nodes_y.append(ly)
+        P.bra_nodes_n.append(ln)
+    # ---- per-axis e lists for the ket steps
+    for i in range(3):
+        P.zlist.append([(eidx[e], eidx[_dec(e, i)], e[i]) for e in e_list if e[i] > 0])
+        P.nlist.append([eidx[e] for e in e_list if e[i] == 0])
+    # ---- ket columns, depth-first order, first-fit arena
+    cols = [f for j in range(Lc + 1) for f in cart_list(j)]
+    src = {}
+    for g in cols:
+        if sum(g) == 0:
+            continue
+        i = _axis(g)
+        f = _dec(g, i)
+        src[g] = (i, f, _dec(f, i) if f[i] > 0 else None)
+    order, seen = [], set()
+
+    def visit(g):
+        if g in seen:
+            return
+        if g in src:
+            i, f, h = src[g]
+            visit(f)
+            if h is not None:
+                visit(h)
+        seen.add(g)
+        order.append(g)
+
+    for g in sorted(cols, key=lambda g: (g[0] + g[1], -g[0], g[2])):
+        visit(g)
+    cons = {g: [] for g in cols}
+    for g, (i, f, h) in src.items():
+        cons[f].append(g)
+        if h is not None:
+            cons[h].append(g)
+    pos = {g: k for k, g in enumerate(order)}
+    last = {g: max([pos[c] for c in cons[g]], default=pos[g]) for g in cols}
+
+    def size(g):
+        return (L + 1) * NE if sum(g) == 0 else (Lc - sum(g) + 1) * NE
+
+    free = [(0, 1 << 30)]  # (start, length) of free arena ranges
+    where = {}
+    peak = 0
+
+    def alloc(n):
+        nonlocal peak
+        for k, (s, ln) in enumerate(free):
+            if ln >= n:
+                free[k] = (s + n, ln - n)
+                peak = max(peak, s + n)
+                return s
+        raise RuntimeError("arena")
+
+    def release(s, n):
+        free.append((s, n))
+        free.sort()
+        merged = []
+        for a, b in free:
+            if merged and merged[-1][0] + merged[-1][1] == a:
+                merged[-1] = (merged[-1][0], merged[-1][1] + b)
+            else:
+                merged.append((a, b))
+        free[:] = merged
+
+    for t, g in enumerate(order):
+        where[g] = alloc(size(g))
+        if sum(g) == 0:
+            P.bra_col = where[g]
+        else:
+            i, f, h = src[g]
+            j = sum(g)
+            st = ColStep(g, j, i, f[i], where[g], where[f], where[h] if h is not None else -1,
+                         fidx.get(g, -1) if j >= lc else -1)
+            P.cols.append(st)
+            rows = Lc - j + 1
+            nz = len(P.zlist[i])
+            nn = len(P.nlist[i])
+            per = 2 + (2 if st.y >= 0 else 0)
+            ops += rows * (nz * (per + 1) + nn * per)
+            P.nodes += rows * (nz + nn)
+        # free columns whose last consumer is this step
+        for c in list(where):
+            if c != g and last[c] == t and c in where:
+                release(where[c], size(c))
+                del where[c]
+        if not cons[g]:
+            # columns nobody consumes (the top level) are released right after accumulation
+            release(where[g], size(g))
+            del where[g]
+    P.arena = peak
+    P.fp64_ops = ops
+    return P
+
+
+# --------------------------------------------------------------------------- emission
+
+def _arr(name, ctype, items, fmt):
+    body = ",".join(fmt(x) for x in items) if items else fmt(None)
+    return f"__device__ const {ctype} {name}[] = {{{body}}};"
+
+
+def emit_coop_class(cls):
+    """CUDA source of the cooperative-tier kernel for canonical class cls."""
+    from . import emit as E
+    from .sph import cart2sph
+
+    P = plan(cls)
+    la, lb, lc, ld = cls
+    cname = E.class_name(cls)
+    NE, La, Lc, L = P.NE, P.La, P.Lc, P.L
+    NET = NE - P.ie_la
+    NF = len(P.f_targets)
+    nsa, nsb, nsc, nsd = (len(cart2sph(l)) for l in cls)
+    NR = nsa * nsb
+    GS = NF | 1
+    arena = max(P.arena, NR * GS)
+    # tables
+    by = [x for lev in P.bra_nodes_y for x in lev]
+    bys = [0]
+    for lev in P.bra_nodes_y:
+        bys.append(bys[-1] + len(lev))
+    bn = [x for lev in P.bra_nodes_n for x in lev]
+    bns = [0]
+    for lev in P.bra_nodes_n:
+        bns.append(bns[-1] + len(lev))
+    bc = P.bra_col
+    i4 = lambda t: "{0,0,0,0}" if t is None else "{%d,%d,%d,%d}" % t
+    lines = []
+    w = lines.append
+    w(f"// Generated by electron_repulsion_integrals_gb300/gen/eri_gen.py -- do not edit.")
+    w(f"// Class ({la}{lb}|{lc}{ld}): L = {L}, warp-cooperative tier; {len(P.cols)} ket column steps, "
+      f"{len(by) + len(bn)} bra nodes, arena {arena} doubles per warp, VRR {P.fp64_ops} FP64 instructions "
+      f"per primitive quartet.")
+    w('#include "../eri_coop.cuh"')
+    w("")
+    w("namespace eri {")
+    w("namespace gen {")
+    w(_arr(f"kBraY_{cname}", "int4", [(bc + o, bc + x, bc + y, ax | (ky << 2)) for o, x, y, ax, ky in by], i4))
+    w(_arr(f"kBraYS_{cname}", "int", bys, lambda v: "0" if v is None else str(v)))
+    w(_arr(f"kBraN_{cname}", "int4", [(bc + o, bc + x, ax, 0) for o, x, ax in bn], i4))
+    w(_arr(f"kBraNS_{cname}", "int", bns, lambda v: "0" if v is None else str(v)))
+    zall = [t for ax in range(3) for t in P.zlist[ax]]
+    w(_arr(f"kZ_{cname}", "int4", [(a, b, c, 0) for a, b, c in zall], i4))
+    nall = [t for ax in range(3) for t in P.nlist[ax]]
+    w(_arr(f"kN_{cname}", "int", nall, lambda v: "0" if v is None else str(v)))
+    w(_arr(f"kCols_{cname}", "CoopCol", [(c.out, c.x, c.y, c.axis, c.ky, c.level, c.target, 0) for c in P.cols],
+           lambda t: "{0,0,0,0,0,0,0,0}" if t is None else "{%d,%d,%d,%d,%d,%d,%d,%d}" % t))
+    nz = [len(P.zlist[a]) for a in range(3)]
+    nn = [len(P.nlist[a]) for a in range(3)]
+    T = f"Traits_{cname}"
+    w(f"struct {T} {{")
+    w(f"  static constexpr int la = {la}, lb = {lb}, lc = {lc}, ld = {ld}, La = {La}, Lc = {Lc}, L = {L};")
+    w(f"  static constexpr int NE = {NE}, NET = {NET}, IE_LA = {P.ie_la}, NF = {NF}, NR = {NR}, GS = {GS};")
+    w(f"  static constexpr int NCOL = {len(P.cols)}, BRA_COL = {bc}, ARENA = {arena}, NH = {NF * NET};")
+    w(f"  static constexpr int WARP_SMEM = ARENA + kCoopBatch * CoopSetup<La, Lc>::STRIDE;")
+    w(f"  static __device__ __forceinline__ const int4* bra_y() {{ return kBraY_{cname}; }}")
+    w(f"  static __device__ __forceinline__ const int* bra_y_start() {{ return kBraYS_{cname}; }}")
+    w(f"  static __device__ __forceinline__ const int4* bra_n() {{ return kBraN_{cname}; }}")
+    w(f"  static __device__ __forceinline__ const int* bra_n_start() {{ return kBraNS_{cname}; }}")
+    w(f"  static __device__ __forceinline__ const CoopCol* cols() {{ return kCols_{cname}; }}")
+    w(f"  static __device__ __forceinline__ int nz(int a) {{ return a == 0 ? {nz[0]} : a == 1 ? {nz[1]} : {nz[2]}; }}")
+    w(f"  static __device__ __forceinline__ int nn(int a) {{ return a == 0 ? {nn[0]} : a == 1 ? {nn[1]} : {nn[2]}; }}")
+    w(f"  static __device__ __forceinline__ const int4* zlist(int a) {{ return kZ_{cname} + (a == 0 ? 0 : a == 1 ? "
+      f"{nz[0]} : {nz[0] + nz[1]}); }}")
+    w(f"  static __device__ __forceinline__ const int* nlist(int a) {{ return kN_{cname} + (a == 0 ? 0 : a == 1 ? "
+      f"{nn[0]} : {nn[0] + nn[1]}); }}")
+    w("};")
+    # bra HRR + sph for one ket column
+    E_targets = [e for k in range(la, La + 1) for e in cart_list(k)]
+    eidx = {e: i for i, e in enumerate(E_targets)}
+    fidx = {f: i for i, f in enumerate(P.f_targets)}
+    bem = E.Emitter()
+    cart = E.emit_hrr_column(bem, la, lb, lambda e: f"Hc[{eidx[e]}]", "b", ["Q.AB[0]", "Q.AB[1]", "Q.AB[2]"])
+    rows = E.emit_sph_pair(bem, la, lb, cart, "t")
+    w(f"__device__ __forceinline__ void bra_hrr_{cname}(const Quartet& Q, const double* __restrict__ H, int fi, "
+      f"double* __restrict__ G) {{")
+    w(f"  const double* __restrict__ Hc = H + (size_t)fi * {NET};")
+    for ln in bem.lines:
+        w("  " + ln)
+    for r, var in enumerate(rows):
+        w(f"  G[{r * GS} + fi] = {var};")
+    w("}")
+    kem = E.Emitter()
+    cart = E.emit_hrr_column(kem, lc, ld, lambda f: f"Gr[{fidx[f]}]", "k", ["Q.CD[0]", "Q.CD[1]", "Q.CD[2]"])
+    outs = E.emit_sph_pair(kem, lc, ld, cart, "u")
+    w("template <int MODE>")
+    w(f"__device__ __forceinline__ void ket_hrr_{cname}(const EriLaunch& P, const Quartet& Q, long long q, int r, "
+      f"const double* __restrict__ G, double& smax_) {{")
+    w(f"  const double* __restrict__ Gr = G + r * {GS};")
+    w("  constexpr int kNSD_ = 1;")
+    w("  double jcd_[1];")
+    w("  (void)jcd_;")
+    for ln in kem.lines:
+        w("  " + ln)
+    w(f"  OUTPUT_ROW(r, r / {nsb}, r % {nsb});")
+    for cdi, var in enumerate(outs):
+        w(f"  OUTPUT_VAL(r / {nsb}, r % {nsb}, {cdi // nsd}, {cdi % nsd}, {var});")
+    w("  OUTPUT_ROW_END();")
+    w("}")
+    w(f"ERI_COOP_KERNEL(k_{cname}, {T}, bra_hrr_{cname}, ket_hrr_{cname})")
+    w("}  // namespace gen")
+    vops = P.fp64_ops + E.BOYS_SETUP_OPS(L)
+    vflops = 2 * P.fp64_ops - P.nodes + E.BOYS_SETUP_FLOPS(L)
+    hops = bem.ops * NF + kem.ops * NR
+    hflops = bem.flops * NF + kem.flops * NR
+    w(f"ERI_DEFINE_COOP_LAUNCHER({la}, {lb}, {lc}, {ld}, gen::k_{cname}, gen::{T}, {vops}LL, {vflops}LL, {hops}LL, "
+      f"{hflops}LL)")
+    w("}  // namespace eri")
+    meta = dict(cls=cls, L=L, shape="coop", arena=arena, ncol=len(P.cols), vrr_ops=P.fp64_ops, vrr_ops_total=vops,
+                vrr_flops_total=vflops, hrr_ops=hops, hrr_flops=hflops, nfunc=(nsa, nsb, nsc, nsd), scratch_slots=0)
+    return "\n".join(lines) + "\n", meta

@@ -300,7 +300,7 @@ def emit_class(cls, spherical_out=True):
     w("    if constexpr (MODE == kCoulomb) {")
     w("      load_quartet_coulomb(P, q, Q);")
     w("    } else {")
-    w("      load_quartet(P, q, Q);")
+    w(f"      load_quartet<{'true' if la == lb else 'false'}, {'true' if lc == ld else 'false'}>(P, q, Q);")
     w("    }")
     w("    double smax_ = 0.0;")
     w("    (void)smax_;")

@@ -170,3 +170,75 @@ def test_both_tiers_agree(shape, monkeypatch):
     got, _ = run_generated(src, cls, prims, Qns, True, shape, meta)
     ref = oracle.eri_block(S, 0, 1, 2, 3, spherical=True)
     assert np.allclose(got, ref, rtol=1e-10, atol=1e-13)
+
+
+def emulate_coop(cls, prims):
+    """Run the cooperative tier's VRR plan (tables as the kernel reads them) on
+    the CPU; returns the accumulators H[target column][e - e_la]."""
+    from electron_repulsion_integrals_gb300.gen import coop
+    P = coop.plan(cls)
+    NE, L, La, Lc = P.NE, P.L, P.La, P.Lc
+    NET = NE - P.ie_la
+    H = np.zeros((len(P.f_targets), NET))
+    for pb, pk, qs, F in prims:
+        A = np.zeros(max(P.arena, 1) + 4 * NE)
+        PA, QC = pb.PA, pk.PA
+        WP = [qs.roz * x for x in qs.PQ]
+        WQ = [-qs.roe * x for x in qs.PQ]
+        o2z, o2e, o2ze = pb.o2z, pk.o2z, qs.o2ze
+        bc = P.bra_col
+        for m in range(L + 1):
+            A[bc + m * NE] = F[m]
+        for k in range(La):
+            for out, x, y, ax, ky in P.bra_nodes_y[k]:
+                A[bc + out] = PA[ax] * A[bc + x] + WP[ax] * A[bc + x + NE] + ky * o2z * (A[bc + y] - qs.roz * A[bc + y + NE])
+            for out, x, ax in P.bra_nodes_n[k]:
+                A[bc + out] = PA[ax] * A[bc + x] + WP[ax] * A[bc + x + NE]
+        if cls[2] == 0:
+            H[0] += A[bc + P.ie_la:bc + NE]
+        for st in P.cols:
+            rows = Lc - st.level + 1
+            for m in range(rows):
+                for ie, iem1, ei in P.zlist[st.axis]:
+                    o = m * NE + ie
+                    v = QC[st.axis] * A[st.x + o] + WQ[st.axis] * A[st.x + o + NE]
+                    if st.y >= 0:
+                        v += st.ky * o2e * (A[st.y + o] - qs.roe * A[st.y + o + NE])
+                    v += ei * o2ze * A[st.x + (m + 1) * NE + iem1]
+                    A[st.out + o] = v
+                for ie in P.nlist[st.axis]:
+                    o = m * NE + ie
+                    v = QC[st.axis] * A[st.x + o] + WQ[st.axis] * A[st.x + o + NE]
+                    if st.y >= 0:
+                        v += st.ky * o2e * (A[st.y + o] - qs.roe * A[st.y + o + NE])
+                    A[st.out + o] = v
+            if st.target >= 0:
+                H[st.target] += A[st.out + P.ie_la:st.out + NE]
+    return H, P
+
+
+@pytest.mark.parametrize("cls", [(1, 1, 1, 1), (2, 1, 2, 0), (2, 2, 1, 1), (3, 2, 2, 2), (2, 0, 0, 0), (2, 2, 0, 0)],
+                         ids=lambda c: "".join(map(str, c)))
+def test_coop_plan_reproduces_vrr_targets(cls):
+    """The cooperative tier's column schedule yields the same VRR targets as the
+    straight-line VRR (itself checked against the oracle above)."""
+    rng = np.random.default_rng(7)
+    src, meta = E.emit_class(cls)
+    S, prims, Qns = harness(cls, rng, nprim=2)
+    code = translate(src)
+    # run only the primitive loop of the straight-line kernel to get h
+    ns = {"fma": fma, "prims": prims, "Q": Qns, "CONTRACTED": True, "OUT": {}, "h": [0.0] * meta["ntargets"], "S": {}}
+    exec(compile(code, "<vrr>", "exec"), ns)
+    from electron_repulsion_integrals_gb300.gen.graph import best_vrr
+    g, _, _ = best_vrr(cls)
+    H, P = emulate_coop(cls, prims)
+    eidx = {e: i for i, e in enumerate(P.e_list)}
+    fidx = {f: i for i, f in enumerate(P.f_targets)}
+    for ti, (e, f) in enumerate(g.target_ef):
+        if meta["shape"] == "reg":
+            ref = ns["h"][ti]
+        else:
+            slot = (eidx[e] - P.ie_la) * len(P.f_targets) + fidx[f]
+            ref = ns["S"][slot]
+        got = H[fidx[f], eidx[e] - P.ie_la]
+        assert abs(got - ref) <= 1e-12 * max(1.0, abs(ref)), (e, f, got, ref)
