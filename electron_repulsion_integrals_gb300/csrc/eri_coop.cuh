@@ -136,38 +136,51 @@ __device__ __forceinline__ void coop_vrr(double* __restrict__ arena, const doubl
     const bool hy = st.y >= 0;
     const double kyo2e = hy ? s[S::KO2E + st.ky - 1] : 0.0;
     const int rows = C::Lc - st.level + 1;
-    // nodes with e_i > 0 (cross term [e - 1_i | f]^(m+1))
+    // nodes with e_i > 0 (cross term [e - 1_i | f]^(m+1)); lane walks (m, k)
+    // over the rows x list rectangle in steps of 32 with integer arithmetic only
     {
       const int nz = C::nz(st.axis);
       const int4* zl = C::zlist(st.axis);
-      const int total = rows * nz;
-      const float inv = 1.0f / (float)nz;
-#pragma unroll 2
-      for (int t = lane; t < total; t += 32) {
-        const int m = (int)(((float)t + 0.5f) * inv);
-        const int4 z = __ldg(zl + (t - m * nz));
+      int m = 0, k = lane;
+      while (k >= nz) {
+        k -= nz;
+        ++m;
+      }
+      while (m < rows) {
+        const int4 z = __ldg(zl + k);
         const int o = m * NE + z.x;
         double v = qc * X[o];
         v = fma(wq, X[o + NE], v);
         if (hy) v = fma(kyo2e, fma(-roe, Y[o + NE], Y[o]), v);
         v = fma(s[S::KO2ZE + z.z], X[(m + 1) * NE + z.y], v);
         O[o] = v;
+        k += 32;
+        while (k >= nz) {
+          k -= nz;
+          ++m;
+        }
       }
     }
     // nodes with e_i = 0
     {
       const int nn = C::nn(st.axis);
       const int* nl = C::nlist(st.axis);
-      const int total = rows * nn;
-      const float inv = 1.0f / (float)nn;
-#pragma unroll 2
-      for (int t = lane; t < total; t += 32) {
-        const int m = (int)(((float)t + 0.5f) * inv);
-        const int o = m * NE + __ldg(nl + (t - m * nn));
+      int m = 0, k = lane;
+      while (k >= nn) {
+        k -= nn;
+        ++m;
+      }
+      while (m < rows) {
+        const int o = m * NE + __ldg(nl + k);
         double v = qc * X[o];
         v = fma(wq, X[o + NE], v);
         if (hy) v = fma(kyo2e, fma(-roe, Y[o + NE], Y[o]), v);
         O[o] = v;
+        k += 32;
+        while (k >= nn) {
+          k -= nn;
+          ++m;
+        }
       }
     }
     __syncwarp();

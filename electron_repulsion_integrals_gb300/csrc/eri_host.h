@@ -36,6 +36,8 @@ bool plan_contracted(const eri_plan* p);
 int plan_device(const eri_plan* p);
 int built_lmax();
 double plan_tau(const eri_plan* p);
+size_t plan_nprim_total(const eri_plan* p);
+const double* plan_dcoef(const eri_plan* p);
 int class_grid(const int l[4], int nsm, long long n, long long* blocks, long long* scratch);
 }  // namespace host
 }  // namespace eri

@@ -315,6 +315,8 @@ void eri::host::fill_plan_inputs(const eri_plan* p, EriLaunch& P) {
 }
 bool eri::host::plan_contracted(const eri_plan* p) { return p->contracted; }
 double eri::host::plan_tau(const eri_plan* p) { return p->tau; }
+size_t eri::host::plan_nprim_total(const eri_plan* p) { return p->hexps.size(); }
+const double* eri::host::plan_dcoef(const eri_plan* p) { return p->dcoef; }
 int eri::host::plan_device(const eri_plan* p) { return p->device; }
 int eri::host::built_lmax() { return ::built_lmax(); }
 

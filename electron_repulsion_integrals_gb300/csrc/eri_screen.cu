@@ -10,7 +10,8 @@
 //  * shell pairs are oriented (L_a >= L_b; a >= b when L_a = L_b), grouped by
 //    pair class (la, lb), and inside a class by their primitive-pair count K
 //    (K descending) and then by Q (descending);
-//  * a pair survives if Q_ab * max Q >= tau;
+//  * a pair survives if Q_ab * max Q >= tau; inside it, primitive pairs whose
+//    (s-type) Schwarz estimate times max Q is below 1e-18 are dropped;
 //  * for a canonical quartet class (P_bra, P_ket) the quartets of bra pair i
 //    with one K-group of ket pairs are a prefix of that group (the ket pairs
 //    with Q >= tau / Q_i), stored as one segment (bra, first ket, count); for
@@ -59,17 +60,17 @@ __global__ void pairs_to_diag_quartets(const int2* __restrict__ pairs, long long
 // One thread per screened shell pair: its primitive-pair records (the
 // GAUSSIANPAIRS step of Algorithm 2, done once per pair instead of once per
 // quartet).
-__global__ void build_prim_pairs(int npairs, const PairMeta* __restrict__ pairs, ShellsDev sh,
-                                 double* __restrict__ prims) {
+__global__ void build_prim_pairs(int npairs, const PairMeta* __restrict__ pairs, const int2* __restrict__ uv,
+                                 ShellsDev sh, double* __restrict__ prims) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= npairs) return;
   const PairMeta m = pairs[i];
   double A[3];
   load_shell_center(sh, m.a, A);
-  const int pa = sh.poff[m.a], pb = sh.poff[m.b], na = sh.nprim[m.a], nb = sh.nprim[m.b];
-  int k = 0;
-  for (int u = 0; u < na; ++u)
-    for (int v = 0; v < nb; ++v, ++k) {
+  const int pa = sh.poff[m.a], pb = sh.poff[m.b];
+  for (int k = 0; k < m.np; ++k) {
+    const int u = uv[m.poff + k].x, v = uv[m.poff + k].y;
+    {
       PrimPair p;
       make_pair(sh.exps[pa + u], sh.coef[pa + u], sh.exps[pb + v], sh.coef[pb + v], A, m.AB, m.rAB2, p);
       double* r = prims + (size_t)(m.poff + k) * kPrimRec;
@@ -84,6 +85,7 @@ __global__ void build_prim_pairs(int npairs, const PairMeta* __restrict__ pairs,
       r[8] = p.K;
       r[9] = 0.0;
     }
+  }
 }
 
 // J_out[i][j] = J_acc[i][j] + J_acc[j][i] for functions of different shells
@@ -223,8 +225,29 @@ int build(eri_plan* p, cudaStream_t st) {
       CUDA_TRY(cudaStreamSynchronize(st));
       for (double x : q) qmax = std::max(qmax, x);
     }
+  // 2b. primitive pairs worth keeping.  With c' the device coefficients, the
+  // pair factor K'_uv = c'_u c'_v exp(-alpha_u beta_v/zeta |AB|^2)/zeta makes
+  // the s-type self repulsion of the primitive distribution K'^2/sqrt(2 zeta);
+  // a primitive pair whose estimate sqrt of that, times the largest shell-pair
+  // Q, is below kPrimTau cannot change any kept integral beyond ~1e-15 and is
+  // dropped.  Its shell pair keeps the remaining primitive pairs.
+  const double kPrimTau = 1e-18;
+  std::vector<double> coef(eri::host::plan_nprim_total(p));
+  CUDA_TRY(cudaMemcpy(coef.data(), eri::host::plan_dcoef(p), coef.size() * sizeof(double), cudaMemcpyDeviceToHost));
+  auto prim_list = [&](int a, int b, double rab2, std::vector<int2>& out) {
+    out.clear();
+    for (int u = 0; u < np[a]; ++u)
+      for (int v = 0; v < np[b]; ++v) {
+        const double al = ex[po[a] + u], be = ex[po[b] + v], z = al + be;
+        const double K = coef[po[a] + u] * coef[po[b] + v] * std::exp(-al * be / z * rab2) / z;
+        const double q = std::fabs(K) * std::pow(2.0 * z, -0.25);
+        if (q * qmax >= kPrimTau) out.push_back(make_int2(u, v));
+      }
+  };
   // 3. survivors, grouped by K (descending) then Q (descending); global pair order
   std::vector<PairMeta> meta;
+  std::vector<int2> uvglob;
+  std::vector<int2> uvtmp;
   std::vector<double> qglob;
   std::vector<int> kglob;
   struct Group {
@@ -234,17 +257,27 @@ int build(eri_plan* p, cudaStream_t st) {
   int prim_total = 0;
   for (int c = 0; c < npc; ++c) {
     std::vector<int> idx;
-    for (int i = 0; i < (int)pc[c].size(); ++i)
-      if (qv[c][i] * qmax >= tau) idx.push_back(i);
+    std::vector<std::vector<int2>> uvs(pc[c].size());
+    for (int i = 0; i < (int)pc[c].size(); ++i) {
+      if (!(qv[c][i] * qmax >= tau)) continue;
+      const int2 pr = pc[c][i];
+      double r2 = 0;
+      for (int x = 0; x < 3; ++x) {
+        const double d = cen[3 * (size_t)pr.x + x] - cen[3 * (size_t)pr.y + x];
+        r2 += d * d;
+      }
+      prim_list(pr.x, pr.y, r2, uvs[i]);
+      if (!uvs[i].empty()) idx.push_back(i);
+    }
     std::sort(idx.begin(), idx.end(), [&](int x, int y) {
-      const int kx = np[pc[c][x].x] * np[pc[c][x].y], ky = np[pc[c][y].x] * np[pc[c][y].y];
+      const int kx = (int)uvs[x].size(), ky = (int)uvs[y].size();
       if (kx != ky) return kx > ky;
       if (qv[c][x] != qv[c][y]) return qv[c][x] > qv[c][y];
       return x < y;
     });
     for (int i : idx) {
       const int2 pr = pc[c][i];
-      const int K = np[pr.x] * np[pr.y];
+      const int K = (int)uvs[i].size();
       if (groups[c].empty() || groups[c].back().K != K) groups[c].push_back({(int)meta.size(), 0, K});
       groups[c].back().count++;
       PairMeta m;
@@ -259,6 +292,7 @@ int build(eri_plan* p, cudaStream_t st) {
       }
       m.rAB2 = r2;
       prim_total += K;
+      uvglob.insert(uvglob.end(), uvs[i].begin(), uvs[i].end());
       meta.push_back(m);
       qglob.push_back(qv[c][i]);
       kglob.push_back(K);
@@ -269,12 +303,17 @@ int build(eri_plan* p, cudaStream_t st) {
   CUDA_TRY(cudaMalloc(&S->dpairs, std::max<size_t>(meta.size(), 1) * sizeof(PairMeta)));
   CUDA_TRY(cudaMalloc(&S->dprims, std::max<size_t>(prim_total, 1) * kPrimRec * sizeof(double)));
   if (!meta.empty()) {
+    DevBuf duv;
+    CUDA_TRY(cudaMalloc(&duv.p, uvglob.size() * sizeof(int2)));
+    CUDA_TRY(cudaMemcpyAsync(duv.p, uvglob.data(), uvglob.size() * sizeof(int2), cudaMemcpyHostToDevice, st));
     CUDA_TRY(cudaMemcpyAsync(S->dpairs, meta.data(), meta.size() * sizeof(PairMeta), cudaMemcpyHostToDevice, st));
     EriLaunch P;
     std::memset(&P, 0, sizeof(P));
     eri::host::fill_plan_inputs(p, P);
-    build_prim_pairs<<<(S->npairs + 127) / 128, 128, 0, st>>>(S->npairs, S->dpairs, P.sh, S->dprims);
+    build_prim_pairs<<<(S->npairs + 127) / 128, 128, 0, st>>>(S->npairs, S->dpairs, (const int2*)duv.p, P.sh,
+                                                              S->dprims);
     CUDA_TRY(cudaGetLastError());
+    CUDA_TRY(cudaStreamSynchronize(st));
   }
   // 5. segments per canonical class
   for (int la = 0; la <= lmax; ++la)

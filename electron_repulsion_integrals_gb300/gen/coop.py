@@ -115,6 +115,9 @@ def plan(cls):
                     ln.append((out, x, i))
                     ops += 2
                     P.nodes += 1
+        # consecutive lanes take consecutive e of one m row: contiguous shared-memory addresses
+        ly.sort(key=lambda t: t[0])
+        ln.sort(key=lambda t: t[0])
         P.bra_nodes_y.append(ly)
         P.bra_nodes_n.append(ln)
     # ---- per-axis e lists for the ket steps
