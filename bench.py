@@ -229,13 +229,15 @@ def run_coulomb(a, rank, world, local_rank):
     # algorithmic flops: per class, quartets x (primitive quartets x VRR + HRR) + 4 per digested integral
     prim_q = 0.0
     flops = 0.0
+    per_class = {}
     for c, n in counts.items():
         if n == 0:
             continue
         st = eri.eri_class_info(c)
-        kavg = plan_avg_primitive_quartets(s, c)
-        prim_q += n * kavg
-        flops += n * (kavg * st["vrr_flops"] + st["hrr_flops"] + 4 * eri.block_size(c))
+        _, pq = eri.eri_plan_class_work(plan.handle, c)
+        prim_q += pq
+        flops += pq * st["vrr_flops"] + n * (st["hrr_flops"] + 4 * eri.block_size(c))
+        per_class["({}{}|{}{})".format(*c)] = {"quartets": n, "primitive_quartets": pq}
     ach = flops / (ms / a.steps / 1e3) / 1e12
     e2e = None
     if a.e2e:
@@ -259,6 +261,7 @@ def run_coulomb(a, rank, world, local_rank):
     line = {"metric": METRIC, "value": value, "unit": "quartets/s", "n_gpus": world, "steps": a.steps,
             "warmup": a.warmup, "ms_per_step": ms / a.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "per_class": per_class,
             "config": {"workload": wl["desc"], "unique_quartets": nq, "primitive_quartets": prim_q, "nbf": nbf,
                        "plan_create_s": plan_s, "l2": "no flush: J digestion re-reads D; kernels are FP64-bound",
                        "parallelism": f"replicas x{world}"},
@@ -272,16 +275,6 @@ def run_coulomb(a, rank, world, local_rank):
     plan.close()
     if dist:
         dist.destroy_process_group()
-
-
-def plan_avg_primitive_quartets(s, cls):
-    """Mean primitive-quartet count of quartets of a class (from the shell
-    contraction degrees; every shell pair of the class weighted equally)."""
-    by_l = {}
-    for L, n in zip(s.L, s.nprim):
-        by_l.setdefault(int(L), []).append(int(n))
-    m = [np.mean(by_l[l]) for l in cls]
-    return float(np.prod(m))
 
 
 def cpu_oracle_rate_cluster(s, counts, budget_s=12.0):

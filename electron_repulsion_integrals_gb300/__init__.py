@@ -68,6 +68,8 @@ def lib():
         L.eri_schwarz.argtypes = [vp, ctypes.c_int, ctypes.c_int, vp, ctypes.c_longlong, dp, vp]
         L.eri_build_J.argtypes = [vp, dp, dp, vp]
         L.eri_plan_quartet_count.argtypes = [vp] + [ctypes.c_int] * 4 + [ctypes.POINTER(ctypes.c_longlong)]
+        L.eri_plan_class_work.argtypes = [vp] + [ctypes.c_int] * 4 + [ctypes.POINTER(ctypes.c_longlong),
+                                                                     ctypes.POINTER(ctypes.c_double)]
         L.eri_class_info.argtypes = [ctypes.c_int] * 4 + [ctypes.POINTER(ClassStats)]
         L.eri_status_string.argtypes = [ctypes.c_int]
         L.eri_status_string.restype = ctypes.c_char_p
@@ -163,6 +165,14 @@ def eri_plan_quartet_count(plan, cls):
     n = ctypes.c_longlong()
     _check("eri_plan_quartet_count", lib().eri_plan_quartet_count(plan, *[int(x) for x in cls], ctypes.byref(n)))
     return n.value
+
+
+def eri_plan_class_work(plan, cls):
+    """(unique quartets, primitive quartets) of a class in the screened plan."""
+    n, pq = ctypes.c_longlong(), ctypes.c_double()
+    _check("eri_plan_class_work", lib().eri_plan_class_work(plan, *[int(x) for x in cls], ctypes.byref(n),
+                                                           ctypes.byref(pq)))
+    return n.value, pq.value
 
 
 def eri_class_info(cls):

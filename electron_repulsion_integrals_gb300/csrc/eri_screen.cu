@@ -110,6 +110,7 @@ struct ClassWork {
   int l[4];
   int nseg = 0;
   long long total = 0;
+  double prim_total = 0;  // primitive quartets evaluated (after pruning)
   int4* dsegs = nullptr;
   long long* dstart = nullptr;
 };
@@ -355,6 +356,7 @@ int build(eri_plan* p, cudaStream_t st) {
                 if (cnt <= 0) continue;
                 segs.push_back(make_int4(i, gk.first, cnt, 0));
                 cost.push_back((long long)gb.K * gk.K);
+                W.prim_total += (double)cnt * gb.K * gk.K;
               }
             }
           if (segs.empty()) {
@@ -438,6 +440,20 @@ int eri_build_J(eri_plan* p, const double* D, double* J, void* stream) {
   symmetrise<<<grid, 128, 0, st>>>(nbf, S->dshell_of, S->Jacc, J);
   CUDA_TRY(cudaGetLastError());
   return ERI_OK;
+}
+
+int eri_plan_class_work(const eri_plan* p, int la, int lb, int lc, int ld, long long* quartets,
+                        double* primitive_quartets) {
+  if (!p || !quartets || !primitive_quartets) return ERI_ERR_INVALID_ARG;
+  eri::screen::Screen* S = eri::host::plan_screen(const_cast<eri_plan*>(p));
+  if (!S) return ERI_ERR_INVALID_ARG;
+  for (const ClassWork& W : S->classes)
+    if (W.l[0] == la && W.l[1] == lb && W.l[2] == lc && W.l[3] == ld) {
+      *quartets = W.total;
+      *primitive_quartets = W.prim_total;
+      return ERI_OK;
+    }
+  return ERI_ERR_UNSUPPORTED_L;
 }
 
 int eri_plan_quartet_count(const eri_plan* p, int la, int lb, int lc, int ld, long long* n) {

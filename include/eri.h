@@ -161,6 +161,12 @@ int eri_build_J(eri_plan* plan, const double* D_dev, double* J_dev, void* stream
  * eri_build_J evaluates (after screening). */
 int eri_plan_quartet_count(const eri_plan* plan, int la, int lb, int lc, int ld, long long* n);
 
+/* Work of canonical class (la lb|lc ld) in eri_build_J: the number of unique
+ * shell quartets and of primitive quartets evaluated (after the Schwarz screen
+ * and the primitive-pair pruning).  Used to express throughput as FLOP/s. */
+int eri_plan_class_work(const eri_plan* plan, int la, int lb, int lc, int ld, long long* quartets,
+                        double* primitive_quartets);
+
 /* Per-class statistics of the generated kernel (canonical class): FP64
  * instructions and flops (FMA = 2) per primitive quartet (pair setup excluded,
  * Boys and VRR included) and per contracted quartet (HRR + spherical
