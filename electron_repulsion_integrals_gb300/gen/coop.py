@@ -268,6 +268,7 @@ def emit_coop_class(cls):
            lambda t: "{0,0,0,0,0,0,0,0}" if t is None else "{%d,%d,%d,%d,%d,%d,%d,%d}" % t))
     nz = [len(P.zlist[a]) for a in range(3)]
     nn = [len(P.nlist[a]) for a in range(3)]
+    w(E.out_scale_table(cls, cname))
     T = f"Traits_{cname}"
     w(f"struct {T} {{")
     w(f"  static constexpr int la = {la}, lb = {lb}, lc = {lc}, ld = {ld}, La = {La}, Lc = {Lc}, L = {L};")
@@ -314,8 +315,10 @@ def emit_coop_class(cls):
     for ln in kem.lines:
         w("  " + ln)
     w(f"  OUTPUT_ROW(r, r / {nsb}, r % {nsb});")
+    w(f"  const double* __restrict__ osc_ = kOutScale_{cname} + r * {nsc * nsd};")
     for cdi, var in enumerate(outs):
-        w(f"  OUTPUT_VAL(r / {nsb}, r % {nsb}, {cdi // nsd}, {cdi % nsd}, {var});")
+        w(f"  const double o{cdi} = {kem.mul(var, f'__ldg(osc_ + {cdi})')};")
+        w(f"  OUTPUT_VAL(r / {nsb}, r % {nsb}, {cdi // nsd}, {cdi % nsd}, o{cdi});")
     w("  OUTPUT_ROW_END();")
     w("}")
     w(f"ERI_COOP_KERNEL(k_{cname}, {T}, bra_hrr_{cname}, ket_hrr_{cname})")

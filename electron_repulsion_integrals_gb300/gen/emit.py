@@ -66,6 +66,8 @@ def lin_comb(em, terms, name, decl="const double"):
         em.w(f"{decl} {name} = 0.0;")
         return name
     c0, x0 = terms[0]
+    if len(terms) == 1 and c0 == 1.0:
+        return x0
     if c0 == 1.0:
         expr = x0
     elif c0 == -1.0:
@@ -186,11 +188,24 @@ def emit_hrr_column(em, la, lb, get_input, prefix, AB):
     return {t: val[t] for t in targets}
 
 
+def sph_scales(l):
+    """Per spherical component m the factor hoisted out of row m of T(l): the
+    largest |coefficient|, so that the remaining row has a coefficient of +-1
+    and single-term rows (e.g. sqrt(3) xy) cost nothing."""
+    T = cart2sph(l)
+    if l <= 1:
+        return [1.0] * len(T)
+    return [max(abs(c) for c in row) for row in T]
+
+
 def emit_sph_pair(em, la, lb, cart_vals, prefix):
     """Apply T(la) x T(lb) to a Cartesian (a,b) block: index a first, then b
-    (section III-B, Eq. (12)).  Returns list of vars in (a', b') row-major."""
+    (section III-B, Eq. (12)), with every row divided by its sph_scales factor;
+    the product of the four indices' factors is applied once per final
+    integral.  Returns list of vars in (a', b') row-major."""
     ca, cb = cart_list(la), cart_list(lb)
     Ta, Tb = cart2sph(la), cart2sph(lb)
+    sa, sb = sph_scales(la), sph_scales(lb)
     na, nb = len(Ta), len(Tb)
     # transform a for each Cartesian b
     if la <= 1:
@@ -200,7 +215,7 @@ def emit_sph_pair(em, la, lb, cart_vals, prefix):
         for i in range(na):
             for b in cb:
                 nm = f"{prefix}a{i}_{cb.index(b)}"
-                half[(i, b)] = lin_comb(em, [(Ta[i][k], cart_vals[(ca[k], b)]) for k in range(len(ca))], nm)
+                half[(i, b)] = lin_comb(em, [(Ta[i][k] / sa[i], cart_vals[(ca[k], b)]) for k in range(len(ca))], nm)
     out = []
     for i in range(na):
         for j in range(nb):
@@ -208,8 +223,28 @@ def emit_sph_pair(em, la, lb, cart_vals, prefix):
                 out.append(half[(i, cb[j])])
             else:
                 nm = f"{prefix}s{i}_{j}"
-                out.append(lin_comb(em, [(Tb[j][k], half[(i, cb[k])]) for k in range(len(cb))], nm))
+                out.append(lin_comb(em, [(Tb[j][k] / sb[j], half[(i, cb[k])]) for k in range(len(cb))], nm))
     return out
+
+
+def lin_comb_alias(terms):
+    terms = [(c, x) for c, x in terms if c != 0.0]
+    return terms[0][1] if len(terms) == 1 and terms[0][0] == 1.0 else None
+
+
+def out_scale_table(cls, cname):
+    """Per-class table of the hoisted spherical scale of every output (row-major
+    over (a'b') rows and (c'd') columns)."""
+    la, lb, lc, ld = cls
+    ns = [len(cart2sph(l)) for l in cls]
+    vals = [out_scale(cls, a, b, c, d) for a in range(ns[0]) for b in range(ns[1]) for c in range(ns[2])
+            for d in range(ns[3])]
+    return f"__device__ const double kOutScale_{cname}[] = {{" + ",".join(_fmt(v) for v in vals) + "};"
+
+
+def out_scale(cls, ia, ib, ic, idd):
+    la, lb, lc, ld = cls
+    return sph_scales(la)[ia] * sph_scales(lb)[ib] * sph_scales(lc)[ic] * sph_scales(ld)[idd]
 
 
 # ----------------------------------------------------------------------------- kernel
@@ -289,6 +324,8 @@ def emit_class(cls, spherical_out=True):
     vops, vflops = vem.ops, vem.flops
 
     # ---- kernel text ----
+    if shape == "staged":
+        w(out_scale_table(cls, cname))
     w(f"template <int MODE, bool CONTRACTED>")
     w(f"__global__ void __launch_bounds__(kThreads) k_{cname}(const EriLaunch P) {{")
     w("  const long long nt = (long long)gridDim.x * blockDim.x;")
@@ -345,6 +382,11 @@ def emit_class(cls, spherical_out=True):
             outs = emit_sph_pair(hem, lc, ld, cart, f"u{r}_")
             hem.w(f"OUTPUT_ROW({r}, {r // nsb}, {r % nsb});")
             for cdi, var in enumerate(outs):
+                sc = out_scale(cls, r // nsb, r % nsb, cdi // nsd, cdi % nsd)
+                if sc != 1.0:
+                    sv = f"o{r}_{cdi}"
+                    hem.w(f"const double {sv} = {hem.mul(var, _fmt(sc))};")
+                    var = sv
                 hem.w(f"OUTPUT_VAL({r // nsb}, {r % nsb}, {cdi // nsd}, {cdi % nsd}, {var});")
             hem.w("OUTPUT_ROW_END();")
         hops = hem.ops
@@ -368,8 +410,11 @@ def emit_class(cls, spherical_out=True):
         cart = emit_hrr_column(kem, lc, ld, lambda f: f"Gr[{fidx[f]} * nt]", "k", ["Q.CD[0]", "Q.CD[1]", "Q.CD[2]"])
         outs = emit_sph_pair(kem, lc, ld, cart, "u")
         kem.w(f"OUTPUT_ROW(r, r / {nsb}, r % {nsb});")
+        kem.w(f"const double* __restrict__ osc_ = kOutScale_{cname} + r * {nsc * nsd};")
         for cdi, var in enumerate(outs):
-            kem.w(f"OUTPUT_VAL(r / {nsb}, r % {nsb}, {cdi // nsd}, {cdi % nsd}, {var});")
+            sv = f"o{cdi}"
+            kem.w(f"const double {sv} = {kem.mul(var, f'__ldg(osc_ + {cdi})')};")
+            kem.w(f"OUTPUT_VAL(r / {nsb}, r % {nsb}, {cdi // nsd}, {cdi % nsd}, {sv});")
         kem.w("OUTPUT_ROW_END();")
         w(f"    for (int r = 0; r < {NR}; ++r) {{")
         for ln in kem.lines:

@@ -286,6 +286,33 @@ def schedule_dsa(nodes):
     return order
 
 
+def schedule_target_dfs(g):
+    """Depth-first order: targets taken by bra component e, ket component f in
+    reverse order; each target's missing ancestors are emitted in post-order.
+    Keeps the frontier of one bra component's ket chain live at a time."""
+    nodes = g.nodes
+    tv = sorted(range(len(g.targets)), key=lambda k: (g.target_ef[k][0], tuple(-x for x in g.target_ef[k][1])))
+    done, order = set(), []
+    for k in tv:
+        st = [(g.targets[k], 0, None)]
+        while st:
+            u, i, ps = st.pop()
+            if u in done:
+                continue
+            if ps is None:
+                ps = sorted(set(nodes[u].parents), key=lambda p: -len(nodes[p].parents))
+            if i < len(ps):
+                st.append((u, i + 1, ps))
+                if ps[i] not in done:
+                    st.append((ps[i], 0, None))
+            else:
+                done.add(u)
+                order.append(u)
+    # base nodes that no target needed (none in a pruned graph) go first
+    rest = [v for v in range(len(nodes)) if v not in done]
+    return rest + order
+
+
 def best_vrr(cls, rules=("ket_first_zyx", "bra_first_zyx"), use_dsa=True):
     """Graph with the fewest FP64 operations, ordered for the smaller PeakLive."""
     best = None
@@ -295,7 +322,7 @@ def best_vrr(cls, rules=("ket_first_zyx", "bra_first_zyx"), use_dsa=True):
         if best is None or ops < best[0]:
             best = (ops, g)
     g = best[1]
-    cands = [("greedy", schedule_greedy(g.nodes))]
+    cands = [("greedy", schedule_greedy(g.nodes)), ("target-dfs", schedule_target_dfs(g))]
     if use_dsa and len(g.nodes) <= 8000:
         cands.append(("dsa", schedule_dsa(g.nodes)))
     scored = [(peak_live(g.nodes, o), name, o) for name, o in cands]

@@ -74,6 +74,10 @@ def translate(src):
         if m:
             out.append(pad + f"for s in range({m.group(1)}): S[s] = 0.0")
             continue
+        m = re.match(r"const double\* __restrict__ osc_ = kOutScale_\w+ \+ r \* (\d+);$", ln)
+        if m:
+            out.append(pad + f"osc_ = r * {m.group(1)}")
+            continue
         m = re.match(r"(?:const )?double\* __restrict__ (\w+) = S \+ \(long long\)(.+) \* nt;$", ln)
         if m:
             out.append(pad + f"{m.group(1)} = {m.group(2)}")
@@ -91,6 +95,7 @@ def translate(src):
         ln = re.sub(r"\b(Hc|Gc|Gr)\[(\d+) \* nt\]", r"S[\1 + \2]", ln)
         ln = re.sub(r"\bS\[(\d+) \* nt\]", r"S[\1]", ln)
         ln = re.sub(r"\bh(\d+)\b", r"h[\1]", ln)
+        ln = re.sub(r"__ldg\(osc_ \+ (\d+)\)", r"OSC[osc_ + \1]", ln)
         out.append(pad + ln)
     return "\n".join(out)
 
@@ -130,10 +135,15 @@ def harness(cls, rng, nprim=1, spread=3.0):
     return S, prims, Qns
 
 
+def osc_table(cls):
+    m = re.search(r"kOutScale_\w+\[\] = \{([^}]*)\}", E.out_scale_table(cls, "x"))
+    return [float(v) for v in m.group(1).split(",")]
+
+
 def run_generated(src, cls, prims, Qns, contracted, shape, meta):
     code = translate(src)
     ns = {"fma": fma, "prims": prims, "Q": Qns, "CONTRACTED": contracted, "OUT": {},
-          "h": [0.0] * meta["ntargets"], "S": {}}
+          "h": [0.0] * meta["ntargets"], "S": {}, "OSC": osc_table(cls)}
     exec(compile(code, f"<gen {cls}>", "exec"), ns)
     nf = meta["nfunc"]
     blk = np.zeros(nf)
@@ -227,7 +237,8 @@ def test_coop_plan_reproduces_vrr_targets(cls):
     S, prims, Qns = harness(cls, rng, nprim=2)
     code = translate(src)
     # run only the primitive loop of the straight-line kernel to get h
-    ns = {"fma": fma, "prims": prims, "Q": Qns, "CONTRACTED": True, "OUT": {}, "h": [0.0] * meta["ntargets"], "S": {}}
+    ns = {"fma": fma, "prims": prims, "Q": Qns, "CONTRACTED": True, "OUT": {}, "h": [0.0] * meta["ntargets"], "S": {},
+          "OSC": osc_table(cls)}
     exec(compile(code, "<vrr>", "exec"), ns)
     from electron_repulsion_integrals_gb300.gen.graph import best_vrr
     g, _, _ = best_vrr(cls)
