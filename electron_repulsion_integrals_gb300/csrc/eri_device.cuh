@@ -407,21 +407,29 @@ __device__ __forceinline__ void quartet_setup(const PrimPair& pb, const PrimPair
 
 // Per-class entry: instantiates the kernel for every mode and contraction flag
 // and exports the generator's per-class statistics.
-#define ERI_LAUNCH_MODE_(KERNEL, M)                                                    \
-  if (contracted)                                                                      \
-    KERNEL<M, true><<<blocks, kThreads, 0, st>>>(*P);                                  \
-  else                                                                                 \
-    KERNEL<M, false><<<blocks, kThreads, 0, st>>>(*P);
+#define ERI_LAUNCH_ONE_(KERNEL, M, C, SMEMB)                                                        \
+  {                                                                                                \
+    if ((SMEMB) > 0)                                                                               \
+      cudaFuncSetAttribute(KERNEL<M, C>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(SMEMB)); \
+    KERNEL<M, C><<<blocks, kThreads, (SMEMB), st>>>(*P);                                           \
+  }
+#define ERI_LAUNCH_MODE_(KERNEL, M, SMEMB) \
+  if (contracted)                          \
+    ERI_LAUNCH_ONE_(KERNEL, M, true, SMEMB) \
+  else                                     \
+    ERI_LAUNCH_ONE_(KERNEL, M, false, SMEMB)
 
-#define ERI_DEFINE_CLASS_LAUNCHER(LA, LB, LC, LD, KERNEL, SLOTS, VOPS, VFLOPS, HOPS, HFLOPS)               \
+// SMEM_SLOTS: shared-memory slots per thread of the staged tier's VRR (dynamic).
+#define ERI_DEFINE_CLASS_LAUNCHER(LA, LB, LC, LD, KERNEL, SLOTS, VOPS, VFLOPS, HOPS, HFLOPS, SMEM_SLOTS)   \
   extern "C" int eri_launch_c##LA##LB##LC##LD(const EriLaunch* P, int mode, int contracted, int blocks,    \
                                                cudaStream_t st) {                                         \
+    const size_t smemb_ = (size_t)(SMEM_SLOTS) * kThreads * sizeof(double);                               \
     if (mode == kStore) {                                                                                 \
-      ERI_LAUNCH_MODE_(KERNEL, kStore)                                                                    \
+      ERI_LAUNCH_MODE_(KERNEL, kStore, smemb_)                                                            \
     } else if (mode == kSchwarz) {                                                                        \
-      ERI_LAUNCH_MODE_(KERNEL, kSchwarz)                                                                  \
+      ERI_LAUNCH_MODE_(KERNEL, kSchwarz, smemb_)                                                          \
     } else if (mode == kCoulomb) {                                                                        \
-      KERNEL<kCoulomb, true><<<blocks, kThreads, 0, st>>>(*P);                                            \
+      ERI_LAUNCH_ONE_(KERNEL, kCoulomb, true, smemb_)                                                     \
     } else {                                                                                              \
       return -1;                                                                                          \
     }                                                                                                     \

@@ -124,6 +124,105 @@ def emit_vrr(em, g, order, sink):
     return name
 
 
+def emit_vrr_staged_regs(em, g, order, sink, R):
+    """Straight-line VRR like emit_vrr, but with at most R VRR values live in
+    registers: when a new value would exceed R, the live value whose next use
+    is farthest away (Belady) moves to a per-thread shared-memory slot
+    (SMEM(slot) = v) and is reloaded just before its next use.  Returns the
+    number of shared-memory slots per thread that the schedule needs."""
+    nodes = g.nodes
+    tpos = {t: k for k, t in enumerate(g.targets)}
+    uses = {v: [] for v in order}
+    for t, v in enumerate(order):
+        nd = nodes[v]
+        for p in (nd.x0, nd.x1, nd.y0, nd.y1, nd.z1):
+            if p >= 0:
+                uses[p].append(t)
+    for v in uses:
+        uses[v].sort()
+    nxt_ptr = {v: 0 for v in order}
+
+    def next_use(v, t):
+        lst = uses[v]
+        i = nxt_ptr[v]
+        while i < len(lst) and lst[i] <= t:
+            i += 1
+        nxt_ptr[v] = i
+        return lst[i] if i < len(lst) else None
+
+    reg = {}          # value -> current variable name (in registers)
+    slot_of = {}      # value -> smem slot (value stored there)
+    free_slots = []
+    nslots = 0
+    version = {}
+
+    def new_name(v):
+        version[v] = version.get(v, -1) + 1
+        return f"v{v}" if version[v] == 0 else f"v{v}_{version[v]}"
+
+    def evict(t, protect):
+        nonlocal nslots
+        cand = [(next_use(u, t - 1) if next_use(u, t - 1) is not None else 1 << 30, u) for u in reg if u not in protect]
+        if not cand:
+            return
+        nu, u = max(cand)
+        if nu != 1 << 30 and u not in slot_of:
+            if free_slots:
+                sl = free_slots.pop()
+            else:
+                sl = nslots
+                nslots += 1
+            slot_of[u] = sl
+            em.w(f"SMEM({sl}) = {reg[u]};")
+        del reg[u]
+
+    def release_dead(t):
+        for u in list(reg):
+            if next_use(u, t) is None:
+                del reg[u]
+        for u in list(slot_of):
+            if next_use(u, t) is None:
+                free_slots.append(slot_of.pop(u))
+
+    for t, v in enumerate(order):
+        nd = nodes[v]
+        parents = [p for p in (nd.x0, nd.x1, nd.y0, nd.y1, nd.z1) if p >= 0]
+        for p in parents:
+            if p not in reg:
+                while len(reg) >= R:
+                    evict(t, set(parents) | {p})
+                nm = new_name(p)
+                em.w(f"const double {nm} = SMEM({slot_of[p]});")
+                reg[p] = nm
+        while len(reg) >= R:
+            evict(t, set(parents))
+        var = new_name(v)
+        e, f, m = nd.key
+        if nd.side == "base":
+            em.w(f"const double {var} = F[{m}];")
+        else:
+            ax = "xyz"[nd.axis]
+            if nd.side == "bra":
+                c0, c1, cy, cr = f"PA{ax}", f"WP{ax}", f"k{nd.ky}_o2z", "roz"
+            else:
+                c0, c1, cy, cr = f"QC{ax}", f"WQ{ax}", f"k{nd.ky}_o2e", "roe"
+            em.w(f"double {var} = {em.mul(c0, reg[nd.x0])};")
+            em.w(f"{var} = {em.fma(c1, reg[nd.x1], var)};")
+            if nd.y0 >= 0:
+                em.w(f"{var} = {em.fma(cy, em.fma('-' + cr, reg[nd.y1], reg[nd.y0]), var)};")
+            if nd.z1 >= 0:
+                em.w(f"{var} = {em.fma(f'k{nd.kz}_o2ze', reg[nd.z1], var)};")
+        reg[v] = var
+        if v in tpos:
+            sink(tpos[v], var)
+        release_dead(t)
+        if STAGED_FENCE and (t + 1) % STAGED_FENCE == 0:
+            # scheduling fence: keeps ptxas from hoisting loads far ahead of
+            # their use across the whole straight-line block (register pressure)
+            em.w("__syncwarp(__activemask());")
+    return nslots
+
+
 def vrr_coef_needs(g):
     need = {"PA": set(), "WP": set(), "QC": set(), "WQ": set(), "o2z": set(), "o2e": set(), "o2ze": set(),
             "roz": False, "roe": False}
@@ -280,6 +379,12 @@ def class_name(cls):
     return "c{}{}{}{}".format(*cls)
 
 
+# VRR values kept in registers by the staged tier; the rest of the frontier
+# goes to per-thread shared-memory slots (SMEM).
+STAGED_VRR_REGS = 64
+STAGED_FENCE = 32
+
+
 def choose_shape(g, peak, cls):
     nacc = len(g.targets)
     return "reg" if (nacc + peak) <= 150 else "staged"
@@ -320,7 +425,11 @@ def emit_class(cls, spherical_out=True):
             e, f = g.target_ef[ti]
             slot = eidx[e] * NF + fidx[f]
             vem.w(f"if (CONTRACTED) {{ S[{slot} * nt] += {var}; }} else {{ S[{slot} * nt] = {var}; }}")
-    emit_vrr(vem, g, order, sink)
+    smem_slots = 0
+    if shape == "staged":
+        smem_slots = emit_vrr_staged_regs(vem, g, order, sink, STAGED_VRR_REGS)
+    else:
+        emit_vrr(vem, g, order, sink)
     vops, vflops = vem.ops, vem.flops
 
     # ---- kernel text ----
@@ -332,6 +441,9 @@ def emit_class(cls, spherical_out=True):
     w("  const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;")
     if shape == "staged":
         w("  double* __restrict__ S = P.scratch + gid;")
+        if smem_slots:
+            w("  extern __shared__ double smem_vrr_[];")
+            w("#define SMEM(k) smem_vrr_[(k) * kThreads + threadIdx.x]")
     w("  for (long long q = gid; q < P.n; q += nt) {")
     w("    Quartet Q;")
     w("    if constexpr (MODE == kCoulomb) {")
@@ -424,10 +536,12 @@ def emit_class(cls, spherical_out=True):
         hem.flops = bem.flops * NF + kem.flops * NR
     w("    OUTPUT_QUARTET_END();")
     w("  }")
+    if shape == "staged" and smem_slots:
+        w("#undef SMEM")
     w("}")
 
     scratch_slots = (NE * NF + NR * NF) if shape == "staged" else 0
-    meta = dict(cls=cls, L=L, shape=shape, nvrr=len(g.nodes), ntargets=len(g.targets), vrr_ops=vops,
+    meta = dict(cls=cls, L=L, shape=shape, nvrr=len(g.nodes), ntargets=len(g.targets), vrr_ops=vops, smem_slots=smem_slots,
                 vrr_flops=vflops, hrr_ops=hops, hrr_flops=hem.flops, scratch_slots=scratch_slots,
                 nfunc=(nsa, nsb, nsc, nsd), ncart=(nca, ncb, ncc, ncd), **info)
     head = HEADER.format(la=la, lb=lb, lc=lc, ld=ld, L=L, nv=len(g.nodes), rule=g.rule, sched=info["schedule"],
@@ -436,10 +550,11 @@ def emit_class(cls, spherical_out=True):
     meta["vrr_ops_total"], meta["vrr_flops_total"] = vops_all, vflops_all
     vops, vflops = vops_all, vflops_all
     hflops = hem.flops
+    smem_slots = meta["smem_slots"]
     tail = f"""
 }}  // namespace gen
 
-ERI_DEFINE_CLASS_LAUNCHER({la}, {lb}, {lc}, {ld}, gen::k_{cname}, {scratch_slots}, {vops}LL, {vflops}LL, {hops}LL, {hflops}LL)
+ERI_DEFINE_CLASS_LAUNCHER({la}, {lb}, {lc}, {ld}, gen::k_{cname}, {scratch_slots}, {vops}LL, {vflops}LL, {hops}LL, {hflops}LL, {smem_slots})
 
 }}  // namespace eri
 """

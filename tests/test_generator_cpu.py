@@ -66,7 +66,7 @@ def translate(src):
             continue
         if ln.startswith("double F[") or ln.startswith("quartet_setup<") or ln.startswith("double h["):
             continue
-        if ln.startswith("double smax_"):
+        if ln.startswith("double smax_") or ln.startswith("extern __shared__") or ln.startswith("#") or ln.startswith("__syncwarp("):
             continue
         if re.match(r"double& h\d+ = h\[\d+\];", ln):
             continue
@@ -96,6 +96,7 @@ def translate(src):
         ln = re.sub(r"\bS\[(\d+) \* nt\]", r"S[\1]", ln)
         ln = re.sub(r"\bh(\d+)\b", r"h[\1]", ln)
         ln = re.sub(r"__ldg\(osc_ \+ (\d+)\)", r"OSC[osc_ + \1]", ln)
+        ln = re.sub(r"\bSMEM\((\d+)\)", r"SM[\1]", ln)
         out.append(pad + ln)
     return "\n".join(out)
 
@@ -143,7 +144,7 @@ def osc_table(cls):
 def run_generated(src, cls, prims, Qns, contracted, shape, meta):
     code = translate(src)
     ns = {"fma": fma, "prims": prims, "Q": Qns, "CONTRACTED": contracted, "OUT": {},
-          "h": [0.0] * meta["ntargets"], "S": {}, "OSC": osc_table(cls)}
+          "h": [0.0] * meta["ntargets"], "S": {}, "OSC": osc_table(cls), "SM": {}}
     exec(compile(code, f"<gen {cls}>", "exec"), ns)
     nf = meta["nfunc"]
     blk = np.zeros(nf)
@@ -238,7 +239,7 @@ def test_coop_plan_reproduces_vrr_targets(cls):
     code = translate(src)
     # run only the primitive loop of the straight-line kernel to get h
     ns = {"fma": fma, "prims": prims, "Q": Qns, "CONTRACTED": True, "OUT": {}, "h": [0.0] * meta["ntargets"], "S": {},
-          "OSC": osc_table(cls)}
+          "OSC": osc_table(cls), "SM": {}}
     exec(compile(code, "<vrr>", "exec"), ns)
     from electron_repulsion_integrals_gb300.gen.graph import best_vrr
     g, _, _ = best_vrr(cls)
