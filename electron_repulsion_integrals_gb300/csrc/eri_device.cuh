@@ -25,17 +25,18 @@ namespace eri {
 constexpr int kThreads = 128;
 
 // ---------------------------------------------------------------- Boys table
-// Grid T_k = k / 8, k = 0..kBoysNgrid-1, covering [0, kBoysTmax].  Row k holds
-// exp(-T_k) followed by F_0(T_k) .. F_{kBoysMaxOrder}(T_k).  Below kBoysTmax the
-// top order is a kBoysTerms-term Taylor series around the nearest grid point
-// (|T - T_k| <= 1/16, truncation < 1e-18 relative) and lower orders follow from
-// the stable downward recursion F_m = (2T F_{m+1} + e^{-T}) / (2m+1).  At and
-// above kBoysTmax, F_0 = sqrt(pi/T)/2 and F_{m+1} = (2m+1) F_m / (2T): the
-// neglected e^{-T} and erfc terms are below 1e-18 relative for m <= 12.
+// Grid T_k = k / 8, k = 0..kBoysNgrid-1, covering [0, kBoysTmax].  For each
+// top order L = 0..kBoysMaxL and grid point k a row holds the Taylor
+// coefficients c_j = F_{L+j}(T_k) / j!, j = 0..kBoysTerms-1, then exp(-T_k).
+// Below kBoysTmax, F_L(T) = sum_j c_j (T_k - T)^j (|T - T_k| <= 1/16, truncation
+// below 1e-18 relative) and the lower orders follow from the stable downward
+// recursion F_m = (2T F_{m+1} + e^{-T}) / (2m+1), with e^{-T} = e^{-T_k} e^{T_k - T}
+// from its own series.  At and above kBoysTmax, F_0 = sqrt(pi/T)/2 and
+// F_{m+1} = (2m+1) F_m / (2T): the neglected e^{-T} and erfc terms are below
+// 1e-18 relative for m <= 12.  All Horner steps are fused multiply-adds.
 constexpr int kBoysTerms = 10;
 constexpr int kBoysMaxL = 16;
-constexpr int kBoysMaxOrder = kBoysMaxL + kBoysTerms;
-constexpr int kBoysCols = kBoysMaxOrder + 2;
+constexpr int kBoysRow = 12;  // kBoysTerms coefficients, exp(-T_k), pad
 constexpr double kBoysTmax = 80.0;
 constexpr int kBoysNgrid = 641;  // 80 * 8 + 1
 
@@ -48,21 +49,24 @@ __device__ __forceinline__ void boys_scaled(double T, double pref, const double*
     const double x = fma(T, 8.0, magic);
     const int k = __double2loint(x);
     const double y = fma(x - magic, 0.125, -T);  // T_k - T
-    const double* __restrict__ row = tab + k * kBoysCols;
-    // y_j = y / j for the Horner form of sum_j c_j y^j / j!
-    double yj[kBoysTerms];
-    yj[1] = y;
+    const double* __restrict__ row = tab + ((size_t)L * kBoysNgrid + k) * kBoysRow;
+    double f = __ldg(row + kBoysTerms - 1);
 #pragma unroll
-    for (int j = 2; j < kBoysTerms; ++j) yj[j] = y * (1.0 / j);
-    double f = __ldg(row + 1 + L + kBoysTerms - 1);
-#pragma unroll
-    for (int j = kBoysTerms - 1; j >= 1; --j) f = fma(f, yj[j], __ldg(row + 1 + L + j - 1));
+    for (int j = kBoysTerms - 2; j >= 0; --j) f = fma(f, y, __ldg(row + j));
     F[L] = pref * f;
     if (L > 0) {
-      double ex = 1.0;
-#pragma unroll
-      for (int j = kBoysTerms - 1; j >= 1; --j) ex = fma(ex, yj[j], 1.0);
-      const double eT = (pref * __ldg(row)) * ex;
+      // e^y = sum_j y^j / j!
+      double ex = 2.7557319223985893e-06;  // 1/9!
+      ex = fma(ex, y, 2.4801587301587302e-05);
+      ex = fma(ex, y, 1.9841269841269841e-04);
+      ex = fma(ex, y, 1.3888888888888889e-03);
+      ex = fma(ex, y, 8.3333333333333333e-03);
+      ex = fma(ex, y, 4.1666666666666667e-02);
+      ex = fma(ex, y, 1.6666666666666667e-01);
+      ex = fma(ex, y, 0.5);
+      ex = fma(ex, y, 1.0);
+      ex = fma(ex, y, 1.0);
+      const double eT = (pref * __ldg(row + kBoysTerms)) * ex;
       const double t2 = T + T;
 #pragma unroll
       for (int m = L - 1; m >= 0; --m) F[m] = fma(t2, F[m + 1], eT) * (1.0 / (2 * m + 1));
@@ -266,7 +270,13 @@ __device__ __forceinline__ void load_quartet_coulomb(const EriLaunch& P, long lo
 // sqrt(zeta+eta)) K_AB K_CD of [00|00]^(m)).
 struct PrimPair {
   double zeta, o2z, P[3], PA[3], K;
+  double q;  // Coulomb plan: Schwarz estimate of the primitive distribution
 };
+
+// Primitive quartets whose Schwarz estimate q_ab q_cd is below this are
+// skipped in the Coulomb build (their contribution to any kept integral is
+// below 1e-15 even summed over every primitive quartet of a shell quartet).
+constexpr double kPrimQuartetTau = 1e-18;
 
 __device__ __forceinline__ void make_pair(double a, double ca, double b, double cb, const double* A, const double* AB,
                                           double rAB2, PrimPair& p) {
@@ -298,6 +308,7 @@ __device__ __forceinline__ void load_prim(const double* __restrict__ prims, int 
   p.PA[1] = a12.x;
   p.PA[2] = a12.y;
   p.K = kk.x;
+  p.q = kk.y;
 }
 
 // Quartet parameters of section II-A: rho = zeta eta/(zeta+eta),
@@ -329,10 +340,13 @@ __device__ __forceinline__ void quartet_setup(const PrimPair& pb, const PrimPair
   {                                                                                                        \
     const int nab_ = MODE == kCoulomb ? Q.nab : CONTRACTED ? Q.na * Q.nb : 1;                              \
     const int ncd_ = MODE == kCoulomb ? Q.ncd : CONTRACTED ? Q.nc * Q.nd : 1;                              \
+    double qk0_ = 0.0;                                                                                     \
+    if constexpr (MODE == kCoulomb) qk0_ = __ldg(P.prims + (size_t)Q.pcd * kPrimRec + 9);                  \
     for (int iab_ = 0; iab_ < nab_; ++iab_) {                                                              \
       PrimPair pb;                                                                                         \
       if constexpr (MODE == kCoulomb) {                                                                    \
         load_prim(P.prims, Q.pab + iab_, pb);                                                              \
+        if (pb.q * qk0_ < kPrimQuartetTau) break;                                                          \
       } else {                                                                                             \
         const int i_ = CONTRACTED ? iab_ / Q.nb : 0, j_ = CONTRACTED ? iab_ - i_ * Q.nb : 0;              \
         make_pair(__ldg(P.sh.exps + Q.pa + i_), __ldg(P.sh.coef + Q.pa + i_), __ldg(P.sh.exps + Q.pb + j_), \
@@ -342,6 +356,7 @@ __device__ __forceinline__ void quartet_setup(const PrimPair& pb, const PrimPair
         PrimPair pk;                                                                                       \
         if constexpr (MODE == kCoulomb) {                                                                  \
           load_prim(P.prims, Q.pcd + icd_, pk);                                                            \
+          if (pb.q * pk.q < kPrimQuartetTau) break;                                                        \
         } else {                                                                                           \
           const int k_ = CONTRACTED ? icd_ / Q.nd : 0, l_ = CONTRACTED ? icd_ - k_ * Q.nd : 0;            \
           make_pair(__ldg(P.sh.exps + Q.pc + k_), __ldg(P.sh.coef + Q.pc + k_), __ldg(P.sh.exps + Q.pd + l_), \

@@ -72,13 +72,14 @@ inline int pair_index(int l1, int l2) { return l1 * (l1 + 1) / 2 + l2; }
   } while (0)
 
 // ------------------------------------------------------------------ Boys table
-// F_m(T_k) at T_k = k/8 for m = 0..kBoysMaxOrder and exp(-T_k), in long
-// double: the highest order from its power series
-//   F_M(T) = e^{-T} sum_i (2T)^i / ((2M+1)(2M+3)...(2M+2i+1)),
-// the others by the downward recursion F_m = (2T F_{m+1} + e^{-T})/(2m+1).
+// F_m(T_k) at T_k = k/8 in long double: the highest order needed from its
+// power series F_M(T) = e^{-T} sum_i (2T)^i / ((2M+1)(2M+3)...(2M+2i+1)), the
+// others by the downward recursion F_m = (2T F_{m+1} + e^{-T})/(2m+1).  Row
+// (L, k) of the device table holds F_{L+j}(T_k)/j! for j < kBoysTerms and
+// exp(-T_k) (layout described in eri_device.cuh).
 std::vector<double> make_boys_table() {
-  std::vector<double> tab((size_t)kBoysNgrid * kBoysCols);
-  const int M = kBoysMaxOrder + 8;
+  std::vector<double> tab((size_t)(kBoysMaxL + 1) * kBoysNgrid * kBoysRow, 0.0);
+  const int M = kBoysMaxL + kBoysTerms + 8;
   std::vector<long double> F(M + 1);
   for (int k = 0; k < kBoysNgrid; ++k) {
     const long double T = (long double)k / 8.0L;
@@ -91,9 +92,15 @@ std::vector<double> make_boys_table() {
     }
     F[M] = eT * sum;
     for (int m = M - 1; m >= 0; --m) F[m] = (2.0L * T * F[m + 1] + eT) / (long double)(2 * m + 1);
-    double* row = &tab[(size_t)k * kBoysCols];
-    row[0] = (double)eT;
-    for (int m = 0; m <= kBoysMaxOrder; ++m) row[1 + m] = (double)F[m];
+    for (int L = 0; L <= kBoysMaxL; ++L) {
+      double* row = &tab[((size_t)L * kBoysNgrid + k) * kBoysRow];
+      long double fact = 1.0L;
+      for (int j = 0; j < kBoysTerms; ++j) {
+        if (j > 0) fact *= j;
+        row[j] = (double)(F[L + j] / fact);
+      }
+      row[kBoysTerms] = (double)eT;
+    }
   }
   return tab;
 }

@@ -17,8 +17,8 @@
 //    with Q >= tau / Q_i), stored as one segment (bra, first ket, count); for
 //    P_bra == P_ket only ket pairs at or before i in the pair order are kept,
 //    so each unordered pair of pairs is evaluated once;
-//  * segments are ordered by K_bra * K_ket (descending), so that the threads of
-//    a warp run the same number of primitive iterations.
+//  * segments are ordered by K_bra * K_ket (descending), then K_bra, K_ket, so
+//    that the threads of a warp run the same primitive loops.
 // The class kernels locate work item t by binary search over the segment
 // starts, read the precomputed primitive-pair records, and digest each block
 // into J with FP64 atomics as soon as it is formed.
@@ -83,7 +83,7 @@ __global__ void build_prim_pairs(int npairs, const PairMeta* __restrict__ pairs,
       r[6] = p.PA[1];
       r[7] = p.PA[2];
       r[8] = p.K;
-      r[9] = 0.0;
+      r[9] = fabs(p.K) * pow(2.0 * p.zeta, -0.25);  // s-type Schwarz estimate of the distribution
     }
   }
 }
@@ -235,15 +235,20 @@ int build(eri_plan* p, cudaStream_t st) {
   const double kPrimTau = 1e-18;
   std::vector<double> coef(eri::host::plan_nprim_total(p));
   CUDA_TRY(cudaMemcpy(coef.data(), eri::host::plan_dcoef(p), coef.size() * sizeof(double), cudaMemcpyDeviceToHost));
+  // kept primitive pairs of a shell pair, largest estimate first (the Coulomb
+  // kernels stop a primitive loop at the first negligible primitive quartet)
   auto prim_list = [&](int a, int b, double rab2, std::vector<int2>& out) {
     out.clear();
+    std::vector<std::pair<double, int2>> tmp;
     for (int u = 0; u < np[a]; ++u)
       for (int v = 0; v < np[b]; ++v) {
         const double al = ex[po[a] + u], be = ex[po[b] + v], z = al + be;
         const double K = coef[po[a] + u] * coef[po[b] + v] * std::exp(-al * be / z * rab2) / z;
         const double q = std::fabs(K) * std::pow(2.0 * z, -0.25);
-        if (q * qmax >= kPrimTau) out.push_back(make_int2(u, v));
+        if (q * qmax >= kPrimTau) tmp.push_back({q, make_int2(u, v)});
       }
+    std::stable_sort(tmp.begin(), tmp.end(), [](const auto& x, const auto& y) { return x.first > y.first; });
+    for (const auto& t : tmp) out.push_back(t.second);
   };
   // 3. survivors, grouped by K (descending) then Q (descending); global pair order
   std::vector<PairMeta> meta;
@@ -330,6 +335,7 @@ int build(eri_plan* p, cudaStream_t st) {
           W.l[3] = ld;
           std::vector<int4> segs;
           std::vector<long long> cost;
+          std::vector<int> kb_of, kk_of;
           for (const Group& gb : groups[cb])
             for (int i = gb.first; i < gb.first + gb.count; ++i) {
               const double qi = qglob[i];
@@ -356,6 +362,8 @@ int build(eri_plan* p, cudaStream_t st) {
                 if (cnt <= 0) continue;
                 segs.push_back(make_int4(i, gk.first, cnt, 0));
                 cost.push_back((long long)gb.K * gk.K);
+                kb_of.push_back(gb.K);
+                kk_of.push_back(gk.K);
                 W.prim_total += (double)cnt * gb.K * gk.K;
               }
             }
@@ -365,7 +373,13 @@ int build(eri_plan* p, cudaStream_t st) {
           }
           std::vector<int> ord(segs.size());
           std::iota(ord.begin(), ord.end(), 0);
-          std::stable_sort(ord.begin(), ord.end(), [&](int x, int y) { return cost[x] > cost[y]; });
+          // equal loop shapes (K_bra, K_ket) adjacent: a warp straddling two
+          // segments then still runs the same primitive loops on every lane
+          std::stable_sort(ord.begin(), ord.end(), [&](int x, int y) {
+            if (cost[x] != cost[y]) return cost[x] > cost[y];
+            if (kb_of[x] != kb_of[y]) return kb_of[x] > kb_of[y];
+            return kk_of[x] > kk_of[y];
+          });
           std::vector<int4> so(segs.size());
           std::vector<long long> start(segs.size() + 1);
           long long t = 0;

@@ -365,13 +365,13 @@ def BOYS_SETUP_OPS(L):
     """FP64 instructions of quartet_setup + boys_scaled (table branch) in
     eri_device.cuh, counting each library call (rsqrt) as one."""
     quartet = 1 + 1 + 1 + 3 + 3 + 3 + 2 + 2
-    boys = 3 + 8 + 9 + 1 + (0 if L == 0 else 9 + 2 + 1 + 2 * L)
+    boys = 3 + 9 + 1 + (0 if L == 0 else 10 + 2 + 1 + 2 * L)
     return quartet + boys
 
 
 def BOYS_SETUP_FLOPS(L):
     quartet = 1 + 1 + 1 + 3 + 3 + 5 + 2 + 2
-    boys = 5 + 8 + 18 + 1 + (0 if L == 0 else 18 + 2 + 1 + 3 * L)
+    boys = 5 + 18 + 1 + (0 if L == 0 else 20 + 2 + 1 + 3 * L)
     return quartet + boys
 
 

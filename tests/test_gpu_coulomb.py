@@ -87,3 +87,25 @@ def test_J_64_atom_cluster_sampled_blocks(dev):
     # Tr(D J) = vec(D)^T ERI vec(D) >= 0 for the PSD density
     assert np.sum(D * J) > 0
     plan.close()
+
+
+def test_J_200_atom_cluster_sampled_blocks(dev):
+    """The 200-atom workload at full size: sampled J blocks against the oracle."""
+    s = W.cluster200()
+    nbf = W.nbf(s)
+    D = W.density(nbf, 4)
+    plan, J = gpu_J(s, D, 1e-10, dev)
+    S = oshells(s)
+    nf = np.array([eri.nfunc(l) for l in s.L])
+    fo = np.concatenate([[0], np.cumsum(nf)])
+    d_shells = [i for i in range(s.n) if s.L[i] == 2]
+    dsh = d_shells[len(d_shells) // 2]
+    pairs = [(dsh, dsh - 5)]  # a d shell and an s shell of the same atom
+    Q = oracle.schwarz(S, True)
+    blocks = oracle.J_blocks(S, D, pairs, spherical=True, tau=1e-10, Q=Q)
+    for (a, b), B in zip(pairs, blocks):
+        G = J[fo[a]:fo[a + 1], fo[b]:fo[b + 1]]
+        assert np.linalg.norm(G - B) <= 1e-10 * max(np.linalg.norm(B), 1e-3), (a, b, np.abs(G - B).max())
+    assert np.allclose(J, J.T, rtol=0, atol=1e-12 * np.abs(J).max())
+    assert np.sum(D * J) > 0
+    plan.close()
