@@ -98,23 +98,31 @@ __device__ __forceinline__ void coop_vrr(double* __restrict__ arena, const doubl
 #pragma unroll 1
   for (int k = 0; k < C::La; ++k) {
     const int y0 = C::bra_y_start()[k], y1 = C::bra_y_start()[k + 1];
-#pragma unroll 2
-    for (int t = y0 + lane; t < y1; t += 32) {
-      const int4 nd = __ldg(C::bra_y() + t);
-      const int ax = nd.w & 3, ky = nd.w >> 2;
-      double v = s[ax] * bra[nd.y];
-      v = fma(s[3 + ax], bra[nd.y + NE], v);
-      v = fma(s[S::KO2Z + ky - 1], fma(-roz, bra[nd.z + NE], bra[nd.z]), v);
-      bra[nd.x] = v;
+    for (int t = y0 + lane; t < y1; t += 64) {
+      const bool two = t + 32 < y1;
+      const int4 na = __ldg(C::bra_y() + t);
+      const int4 nb = __ldg(C::bra_y() + (two ? t + 32 : t));
+      const int axa = na.w & 3, kya = na.w >> 2, axb = nb.w & 3, kyb = nb.w >> 2;
+      double va = s[axa] * bra[na.y];
+      double vb = s[axb] * bra[nb.y];
+      va = fma(s[3 + axa], bra[na.y + NE], va);
+      vb = fma(s[3 + axb], bra[nb.y + NE], vb);
+      va = fma(s[S::KO2Z + kya - 1], fma(-roz, bra[na.z + NE], bra[na.z]), va);
+      vb = fma(s[S::KO2Z + kyb - 1], fma(-roz, bra[nb.z + NE], bra[nb.z]), vb);
+      bra[na.x] = va;
+      if (two) bra[nb.x] = vb;
     }
     const int n0 = C::bra_n_start()[k], n1 = C::bra_n_start()[k + 1];
-#pragma unroll 2
-    for (int t = n0 + lane; t < n1; t += 32) {
-      const int4 nd = __ldg(C::bra_n() + t);
-      const int ax = nd.z;
-      double v = s[ax] * bra[nd.y];
-      v = fma(s[3 + ax], bra[nd.y + NE], v);
-      bra[nd.x] = v;
+    for (int t = n0 + lane; t < n1; t += 64) {
+      const bool two = t + 32 < n1;
+      const int4 na = __ldg(C::bra_n() + t);
+      const int4 nb = __ldg(C::bra_n() + (two ? t + 32 : t));
+      double va = s[na.z] * bra[na.y];
+      double vb = s[nb.z] * bra[nb.y];
+      va = fma(s[3 + na.z], bra[na.y + NE], va);
+      vb = fma(s[3 + nb.z], bra[nb.y + NE], vb);
+      bra[na.x] = va;
+      if (two) bra[nb.x] = vb;
     }
     __syncwarp();
   }
@@ -136,8 +144,23 @@ __device__ __forceinline__ void coop_vrr(double* __restrict__ arena, const doubl
     const bool hy = st.y >= 0;
     const double kyo2e = hy ? s[S::KO2E + st.ky - 1] : 0.0;
     const int rows = C::Lc - st.level + 1;
-    // nodes with e_i > 0 (cross term [e - 1_i | f]^(m+1)); lane walks (m, k)
-    // over the rows x list rectangle in steps of 32 with integer arithmetic only
+    // accumulators of a target column are fetched before the column is built,
+    // so that their global-memory latency overlaps the arithmetic
+    constexpr int kHT = (C::NET + 31) / 32;
+    double hold[kHT];
+    double* Ht = H + (size_t)(st.target >= 0 ? st.target : 0) * C::NET;
+    if (st.target >= 0 && !first) {
+#pragma unroll
+      for (int j = 0; j < kHT; ++j) {
+        const int k = lane + 32 * j;
+        hold[j] = k < C::NET ? Ht[k] : 0.0;
+      }
+    }
+    // nodes with e_i > 0 (cross term [e - 1_i | f]^(m+1)).  Each lane walks
+    // (m, k) over the rows x list rectangle in steps of 32 with integer
+    // arithmetic only, two nodes per iteration so that their dependent FMA
+    // chains overlap (the second node of a lane's last pair repeats the first
+    // and is not stored).
     {
       const int nz = C::nz(st.axis);
       const int4* zl = C::zlist(st.axis);
@@ -147,14 +170,30 @@ __device__ __forceinline__ void coop_vrr(double* __restrict__ arena, const doubl
         ++m;
       }
       while (m < rows) {
-        const int4 z = __ldg(zl + k);
-        const int o = m * NE + z.x;
-        double v = qc * X[o];
-        v = fma(wq, X[o + NE], v);
-        if (hy) v = fma(kyo2e, fma(-roe, Y[o + NE], Y[o]), v);
-        v = fma(s[S::KO2ZE + z.z], X[(m + 1) * NE + z.y], v);
-        O[o] = v;
-        k += 32;
+        int m2 = m, k2 = k + 32;
+        while (k2 >= nz) {
+          k2 -= nz;
+          ++m2;
+        }
+        const bool two = m2 < rows;
+        const int mb = two ? m2 : m, kb = two ? k2 : k;
+        const int4 za = __ldg(zl + k);
+        const int4 zb = __ldg(zl + kb);
+        const int oa = m * NE + za.x, ob = mb * NE + zb.x;
+        double va = qc * X[oa];
+        double vb = qc * X[ob];
+        va = fma(wq, X[oa + NE], va);
+        vb = fma(wq, X[ob + NE], vb);
+        if (hy) {
+          va = fma(kyo2e, fma(-roe, Y[oa + NE], Y[oa]), va);
+          vb = fma(kyo2e, fma(-roe, Y[ob + NE], Y[ob]), vb);
+        }
+        va = fma(s[S::KO2ZE + za.z], X[(m + 1) * NE + za.y], va);
+        vb = fma(s[S::KO2ZE + zb.z], X[(mb + 1) * NE + zb.y], vb);
+        O[oa] = va;
+        if (two) O[ob] = vb;
+        m = m2;
+        k = k2 + 32;
         while (k >= nz) {
           k -= nz;
           ++m;
@@ -171,12 +210,26 @@ __device__ __forceinline__ void coop_vrr(double* __restrict__ arena, const doubl
         ++m;
       }
       while (m < rows) {
-        const int o = m * NE + __ldg(nl + k);
-        double v = qc * X[o];
-        v = fma(wq, X[o + NE], v);
-        if (hy) v = fma(kyo2e, fma(-roe, Y[o + NE], Y[o]), v);
-        O[o] = v;
-        k += 32;
+        int m2 = m, k2 = k + 32;
+        while (k2 >= nn) {
+          k2 -= nn;
+          ++m2;
+        }
+        const bool two = m2 < rows;
+        const int mb = two ? m2 : m, kb = two ? k2 : k;
+        const int oa = m * NE + __ldg(nl + k), ob = mb * NE + __ldg(nl + kb);
+        double va = qc * X[oa];
+        double vb = qc * X[ob];
+        va = fma(wq, X[oa + NE], va);
+        vb = fma(wq, X[ob + NE], vb);
+        if (hy) {
+          va = fma(kyo2e, fma(-roe, Y[oa + NE], Y[oa]), va);
+          vb = fma(kyo2e, fma(-roe, Y[ob + NE], Y[ob]), vb);
+        }
+        O[oa] = va;
+        if (two) O[ob] = vb;
+        m = m2;
+        k = k2 + 32;
         while (k >= nn) {
           k -= nn;
           ++m;
@@ -185,10 +238,13 @@ __device__ __forceinline__ void coop_vrr(double* __restrict__ arena, const doubl
     }
     __syncwarp();
     if (st.target >= 0) {
-      double* Ht = H + (size_t)st.target * C::NET;
-      for (int k = lane; k < C::NET; k += 32) {
-        const double v = O[C::IE_LA + k];
-        Ht[k] = first ? v : Ht[k] + v;
+#pragma unroll
+      for (int j = 0; j < kHT; ++j) {
+        const int k = lane + 32 * j;
+        if (k < C::NET) {
+          const double v = O[C::IE_LA + k];
+          Ht[k] = first ? v : hold[j] + v;
+        }
       }
     }
   }
