@@ -58,6 +58,27 @@ WORKLOADS = {
 }
 
 
+def dram_traffic(cls, n):
+    """DRAM bytes of one launch of the class kernel from the ncu record in
+    profiles/dram_traffic.json (captured on a slice and scaled by the number of
+    quartets, the traffic being per quartet), or None when the kernel sources
+    changed since the capture."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(path):
+        return None
+    rec = json.load(open(path))
+    if not rec["kernel"].startswith("k_c{}{}{}{}".format(*cls)):
+        return None
+    h = hashlib.sha256()
+    for f in rec["sources"]:
+        with open(os.path.join(ROOT, "electron_repulsion_integrals_gb300", f), "rb") as fh:
+            h.update(fh.read())
+    if h.hexdigest() != rec["sha256"]:
+        return None
+    return rec["dram_bytes_per_quartet"] * n
+
+
 def env_int(k, d):
     try:
         return int(os.environ.get(k, d))
@@ -426,7 +447,8 @@ def run_ours(a, rank, world, local_rank):
                        "parallelism": f"replicas x{world}"},
             "per_class": per_class,
             "roofline": {"bound": "alu", "kernel": dname, "achieved": ach, "peak": FP64_PEAK_TFLOPS,
-                         "unit": "TFLOP/s", "frac": ach / FP64_PEAK_TFLOPS, "traffic": None,
+                         "unit": "TFLOP/s", "frac": ach / FP64_PEAK_TFLOPS,
+                         "traffic": dram_traffic(dom["cls"], dom["n"]),
                          "peak_source": "FP64 pipe: 152 SMs x 2 DFMA/clk x 2 flop x 2.07 GHz"},
             "clocks": clk, "e2e": e2e, "cpu_baseline": cpu,
             "gpu_launches": len(batches) * a.steps}
