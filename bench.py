@@ -419,19 +419,30 @@ def run_ours(a, rank, world, local_rank):
                                                          for b in batches)
         d2h = sum(ho.numel() * 8 for ho in host_o)
         e_steps = max(1, min(a.steps, 3))
+        ph = {"plan_create": 0.0, "h2d_quartets_and_compute": 0.0, "d2h_blocks": 0.0}
         torch.cuda.synchronize()
         te = time.perf_counter()
         for _ in range(e_steps):
             for b, hq, ho in zip(batches, host_q, host_o):
+                t0h = time.perf_counter()
                 plan = eri.Plan(b["shells"], spherical=True, stream=stream)
+                torch.cuda.synchronize()
+                t1h = time.perf_counter()
                 qd = hq.to(dev, non_blocking=True)
                 eri.eri_compute_class(plan.handle, b["cls"], qd, b["out"], stream)
+                torch.cuda.synchronize()
+                t2h = time.perf_counter()
                 ho.copy_(b["out"], non_blocking=True)
                 torch.cuda.synchronize()
+                t3h = time.perf_counter()
                 plan.close()
+                ph["plan_create"] += t1h - t0h
+                ph["h2d_quartets_and_compute"] += t2h - t1h
+                ph["d2h_blocks"] += t3h - t2h
         te = time.perf_counter() - te
         e2e = {"value": sum(b["n"] for b in batches) * world * e_steps / te, "unit": "quartets/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "phases_ms_per_step": {k: v / e_steps * 1e3 for k, v in ph.items()}}
 
     cpu = None
     if rank == 0 and a.cpu_baseline:

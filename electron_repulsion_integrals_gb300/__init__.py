@@ -59,6 +59,8 @@ def lib():
         L = ctypes.CDLL(LIB_PATH)
         vp, ip, dp = ctypes.c_void_p, ctypes.POINTER(ctypes.c_int), ctypes.c_void_p
         L.eri_plan_create.argtypes = [vp, ctypes.c_int, ctypes.POINTER(_Options), vp, ctypes.POINTER(vp)]
+        L.eri_plan_create_flat.argtypes = [ctypes.c_int, vp, vp, vp, vp, vp, ctypes.POINTER(_Options), vp,
+                                           ctypes.POINTER(vp)]
         L.eri_plan_destroy.argtypes = [vp]
         L.eri_plan_nbf.argtypes = [vp, ip]
         L.eri_plan_shell_info.argtypes = [vp, ctypes.c_int, ip, ip]
@@ -109,6 +111,7 @@ def shell_records(shells):
 
 
 def eri_plan_create(shells, spherical=True, schwarz_tau=0.0, stream=None):
+    """Plan over an array of eri_shell records (one pointer pair per shell)."""
     rec, keep = shell_records(shells)
     opt = _Options(int(bool(spherical)), float(schwarz_tau), 0)
     out = ctypes.c_void_p()
@@ -116,6 +119,22 @@ def eri_plan_create(shells, spherical=True, schwarz_tau=0.0, stream=None):
                                ctypes.c_void_p(_stream_handle(stream)), ctypes.byref(out))
     del keep
     _check("eri_plan_create", rc)
+    return out
+
+
+def eri_plan_create_flat(shells, spherical=True, schwarz_tau=0.0, stream=None):
+    """Plan over flat shell arrays (centers, L, nprim, exps, coefs)."""
+    c = np.ascontiguousarray(shells.centers, dtype=np.float64)
+    L = np.ascontiguousarray(shells.L, dtype=np.int32)
+    n = np.ascontiguousarray(shells.nprim, dtype=np.int32)
+    e = np.ascontiguousarray(shells.exps, dtype=np.float64)
+    f = np.ascontiguousarray(shells.coefs, dtype=np.float64)
+    opt = _Options(int(bool(spherical)), float(schwarz_tau), 0)
+    out = ctypes.c_void_p()
+    rc = lib().eri_plan_create_flat(int(len(L)), c.ctypes.data, L.ctypes.data, n.ctypes.data, e.ctypes.data,
+                                    f.ctypes.data, ctypes.byref(opt), ctypes.c_void_p(_stream_handle(stream)),
+                                    ctypes.byref(out))
+    _check("eri_plan_create_flat", rc)
     return out
 
 
@@ -195,7 +214,7 @@ class Plan:
     def __init__(self, shells, spherical=True, schwarz_tau=0.0, stream=None):
         self.shells = shells
         self.spherical = spherical
-        self.handle = eri_plan_create(shells, spherical, schwarz_tau, stream)
+        self.handle = eri_plan_create_flat(shells, spherical, schwarz_tau, stream)
         self.nbf = eri_plan_nbf(self.handle)
 
     def compute_class(self, cls, quartets, out=None, stream=None):

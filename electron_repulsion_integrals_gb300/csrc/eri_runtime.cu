@@ -372,61 +372,49 @@ int eri_plan_destroy(eri_plan* p) {
   return ERI_OK;
 }
 
-int eri_plan_create(const eri_shell* shells, int nshell, const eri_options* opt, void* stream, eri_plan** out) {
+int eri_plan_create_flat(int nshell, const double* centers, const int* L, const int* nprim, const double* exps,
+                         const double* coefs, const eri_options* opt, void* stream, eri_plan** out) {
   if (!out) return ERI_ERR_INVALID_ARG;
   *out = nullptr;
-  if (!shells || nshell <= 0 || !opt || opt->flags != 0) return ERI_ERR_INVALID_ARG;
+  if (nshell <= 0 || !centers || !L || !nprim || !exps || !coefs || !opt || opt->flags != 0) return ERI_ERR_INVALID_ARG;
   const int lmax_built = built_lmax();
+  int lmax = 0, lmin = 0, npmin = 1, npmax = 1;
+  size_t np_total = 0;
+  for (int s = 0; s < nshell; ++s) {
+    lmax = std::max(lmax, L[s]);
+    lmin = std::min(lmin, L[s]);
+    npmin = std::min(npmin, nprim[s]);
+    npmax = std::max(npmax, nprim[s]);
+    np_total += (size_t)std::max(nprim[s], 0);
+  }
+  if (lmin < 0 || npmin <= 0 || np_total > ((size_t)1 << 30)) return ERI_ERR_INVALID_ARG;
+  if (lmax > lmax_built) return ERI_ERR_UNSUPPORTED_L;
+  bool finite = true;
+  for (size_t i = 0; i < 3 * (size_t)nshell; ++i) finite &= std::isfinite(centers[i]);
+  for (size_t i = 0; i < np_total; ++i) finite &= std::isfinite(exps[i]) && exps[i] > 0 && std::isfinite(coefs[i]);
+  if (!finite) return ERI_ERR_NOT_FINITE;
   eri_plan* p = new (std::nothrow) eri_plan();
   if (!p) return ERI_ERR_OOM;
   p->nshell = nshell;
   p->spherical = opt->spherical != 0;
   p->tau = opt->schwarz_tau;
-  p->hL.resize(nshell);
-  p->hnprim.resize(nshell);
+  p->lmax = lmax;
+  p->contracted = npmax > 1;
+  p->hL.assign(L, L + nshell);
+  p->hnprim.assign(nprim, nprim + nshell);
+  p->hcen.assign(centers, centers + 3 * (size_t)nshell);
+  p->hexps.assign(exps, exps + np_total);
+  p->hcoef.assign(coefs, coefs + np_total);
   p->hpoff.resize(nshell);
   p->hfo.resize(nshell + 1);
-  p->hcen.resize(3 * (size_t)nshell);
-  int rc = ERI_OK;
-  size_t np_total = 0;
-  for (int s = 0; s < nshell && rc == ERI_OK; ++s) {
-    const eri_shell& sh = shells[s];
-    if (sh.nprim <= 0 || sh.L < 0 || !sh.exps || !sh.coefs) rc = ERI_ERR_INVALID_ARG;
-    else if (sh.L > lmax_built) rc = ERI_ERR_UNSUPPORTED_L;
-    else {
-      for (int x = 0; x < 3; ++x)
-        if (!std::isfinite(sh.center[x])) rc = ERI_ERR_NOT_FINITE;
-      for (int k = 0; k < sh.nprim; ++k)
-        if (!(std::isfinite(sh.exps[k]) && sh.exps[k] > 0) || !std::isfinite(sh.coefs[k])) rc = ERI_ERR_NOT_FINITE;
-    }
-    if (rc) break;
-    p->hL[s] = sh.L;
-    p->hnprim[s] = sh.nprim;
-    p->hpoff[s] = (int)np_total;
-    np_total += sh.nprim;
-    if (np_total > (size_t)1 << 30) rc = ERI_ERR_INVALID_ARG;
-    for (int x = 0; x < 3; ++x) p->hcen[3 * (size_t)s + x] = sh.center[x];
-    p->lmax = std::max(p->lmax, sh.L);
-    if (sh.nprim > 1) p->contracted = true;
-  }
-  if (rc) {
-    delete p;
-    return rc;
-  }
-  p->hexps.resize(np_total);
-  p->hcoef.resize(np_total);
   p->hfo[0] = 0;
+  int off = 0;
   for (int s = 0; s < nshell; ++s) {
-    const eri_shell& sh = shells[s];
-    std::memcpy(&p->hexps[p->hpoff[s]], sh.exps, sh.nprim * sizeof(double));
-    std::memcpy(&p->hcoef[p->hpoff[s]], sh.coefs, sh.nprim * sizeof(double));
-    p->hfo[s + 1] = p->hfo[s] + nfunc(sh.L, p->spherical);
+    p->hpoff[s] = off;
+    off += nprim[s];
+    p->hfo[s + 1] = p->hfo[s] + nfunc(L[s], p->spherical);
   }
   p->nbf = p->hfo[nshell];
-  if (rc) {
-    delete p;
-    return rc;
-  }
   cudaError_t e = cudaGetDevice(&p->device);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&p->nsm, cudaDevAttrMultiProcessorCount, p->device);
   if (e != cudaSuccess) {
@@ -434,6 +422,7 @@ int eri_plan_create(const eri_shell* shells, int nshell, const eri_options* opt,
     delete p;
     return ERI_ERR_CUDA;
   }
+  int rc;
   if ((rc = upload(&p->dcen, p->hcen)) || (rc = upload(&p->dL, p->hL)) || (rc = upload(&p->dnprim, p->hnprim)) ||
       (rc = upload(&p->dpoff, p->hpoff)) || (rc = upload(&p->dfo, p->hfo)) || (rc = upload(&p->dexps, p->hexps)) ||
       (rc = boys_table_for_device(p->device, &p->dboys))) {
@@ -454,6 +443,34 @@ int eri_plan_create(const eri_shell* shells, int nshell, const eri_options* opt,
   }
   *out = p;
   return ERI_OK;
+}
+
+int eri_plan_create(const eri_shell* shells, int nshell, const eri_options* opt, void* stream, eri_plan** out) {
+  if (!out) return ERI_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!shells || nshell <= 0 || !opt) return ERI_ERR_INVALID_ARG;
+  std::vector<double> cen(3 * (size_t)nshell), ex, cf;
+  std::vector<int> L(nshell), np(nshell);
+  size_t total = 0;
+  for (int s = 0; s < nshell; ++s) {
+    if (shells[s].nprim <= 0 || !shells[s].exps || !shells[s].coefs) return ERI_ERR_INVALID_ARG;
+    total += shells[s].nprim;
+  }
+  if (total > ((size_t)1 << 30)) return ERI_ERR_INVALID_ARG;
+  ex.resize(total);
+  cf.resize(total);
+  size_t o = 0;
+  for (int s = 0; s < nshell; ++s) {
+    const eri_shell& sh = shells[s];
+    for (int x = 0; x < 3; ++x) cen[3 * (size_t)s + x] = sh.center[x];
+    L[s] = sh.L;
+    np[s] = sh.nprim;
+    for (int k = 0; k < sh.nprim; ++k, ++o) {
+      ex[o] = sh.exps[k];
+      cf[o] = sh.coefs[k];
+    }
+  }
+  return eri_plan_create_flat(nshell, cen.data(), L.data(), np.data(), ex.data(), cf.data(), opt, stream, out);
 }
 
 int eri_plan_nbf(const eri_plan* p, int* nbf) {

@@ -85,6 +85,14 @@ typedef struct eri_plan eri_plan;
  * (L > 3), NOT_FINITE, OOM, CUDA. */
 int eri_plan_create(const eri_shell* shells, int nshell, const eri_options* opt, void* stream, eri_plan** out);
 
+/* Same as eri_plan_create for shells given as flat arrays (host memory, read
+ * during the call only): centers[3*nshell], L[nshell], nprim[nshell], and the
+ * exponents and coefficients of all shells concatenated in shell order
+ * (sum of nprim values each).  Avoids the per-shell pointers of eri_shell for
+ * large batches (e.g. 4M shells of a homogeneous quartet batch). */
+int eri_plan_create_flat(int nshell, const double* centers, const int* L, const int* nprim, const double* exps,
+                         const double* coefs, const eri_options* opt, void* stream, eri_plan** out);
+
 /* Release every device and host resource of the plan (NULL is allowed). */
 int eri_plan_destroy(eri_plan* plan);
 

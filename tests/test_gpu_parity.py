@@ -182,3 +182,19 @@ def test_schwarz_factors(dev):
             q = plan.schwarz(la, lb, pt).cpu().numpy()
             check(q, [Qref[a, b] for a, b in pairs], f"Schwarz ({la},{lb})")
     plan.close()
+
+
+def test_pointer_and_flat_plan_creation_agree(dev):
+    """eri_plan_create (array of eri_shell records) and eri_plan_create_flat give the same integrals."""
+    cls = (2, 1, 1, 0)
+    s, q = W.homogeneous(cls, 300, 2, seed_index=450)
+    qd = torch.as_tensor(q, device=dev)
+    outs = []
+    for create in (eri.eri_plan_create, eri.eri_plan_create_flat):
+        h = create(s, True, 0.0)
+        out = torch.empty(300 * eri.block_size(cls), dtype=torch.float64, device=dev)
+        eri.eri_compute_class(h, cls, qd, out)
+        torch.cuda.synchronize()
+        outs.append(out.cpu().numpy())
+        eri.eri_plan_destroy(h)
+    assert np.array_equal(outs[0], outs[1])
