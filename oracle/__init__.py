@@ -65,6 +65,8 @@ def _load():
             lib.ora_schwarz.argtypes = shell_args + [ctypes.c_int, dp, ctypes.c_int]
             lib.ora_J_blocks.argtypes = shell_args + [ctypes.c_int, ctypes.c_double, dp, dp, ip, ctypes.c_longlong,
                                                       lp, dp, ctypes.c_int]
+            lib.ora_K_blocks.argtypes = lib.ora_J_blocks.argtypes
+            lib.ora_build_JK.argtypes = shell_args + [ctypes.c_int, ctypes.c_double, dp, dp, dp, dp, ctypes.c_int]
             lib.ora_build_J.argtypes = shell_args + [ctypes.c_int, ctypes.c_double, dp, dp, dp, lp, ctypes.c_int]
             _lib = lib
     return _lib
@@ -210,7 +212,7 @@ def build_J(S: ShellSet, D, spherical=True, tau=1e-10, Q=None, nthreads=None):
     return J, int(kept[0])
 
 
-def J_blocks(S: ShellSet, D, pairs, spherical=True, tau=1e-10, Q=None, nthreads=None):
+def J_blocks(S: ShellSet, D, pairs, spherical=True, tau=1e-10, Q=None, nthreads=None, _fn="ora_J_blocks"):
     """Blocks J[a][b] for the requested shell pairs, from the definition (see oracle.cpp)."""
     pairs = np.ascontiguousarray(pairs, dtype=np.int32).reshape(-1, 2)
     D = np.ascontiguousarray(D, dtype=np.float64)
@@ -223,10 +225,29 @@ def J_blocks(S: ShellSet, D, pairs, spherical=True, tau=1e-10, Q=None, nthreads=
         off[1:] = np.cumsum(sizes)[:-1]
     out = np.zeros(int(sizes.sum()))
     Qkeep = Q
-    rc = _load().ora_J_blocks(*S.args(), int(bool(spherical)), float(tau), Qp, _dp(D), _ip(pairs), len(pairs),
+    rc = getattr(_load(), _fn)(*S.args(), int(bool(spherical)), float(tau), Qp, _dp(D), _ip(pairs), len(pairs),
                               _lp(off), _dp(out), int(nthreads or default_threads()))
     del Qkeep
     if rc:
-        raise ValueError("ora_J_blocks: bad arguments")
+        raise ValueError(f"{_fn}: bad arguments")
     return [out[o:o + sz].reshape(nfunc(S.L[a], spherical), nfunc(S.L[b], spherical))
             for (a, b), o, sz in zip(pairs, off, sizes)]
+
+
+def build_JK(S: ShellSet, D, spherical=True, tau=1e-10, Q=None, nthreads=None):
+    """Coulomb and exchange matrices (see oracle.cpp, ora_build_JK)."""
+    nbf = sum(nfunc(S.L[i], spherical) for i in range(S.n))
+    D = np.ascontiguousarray(D, dtype=np.float64)
+    J = np.zeros((nbf, nbf))
+    K = np.zeros((nbf, nbf))
+    Qa = None if Q is None else np.ascontiguousarray(Q, dtype=np.float64)
+    rc = _load().ora_build_JK(*S.args(), int(bool(spherical)), float(tau), None if Qa is None else _dp(Qa), _dp(D),
+                              _dp(J), _dp(K), int(nthreads or default_threads()))
+    if rc:
+        raise ValueError("ora_build_JK: bad arguments")
+    return J, K
+
+
+def K_blocks(S: ShellSet, D, pairs, spherical=True, tau=1e-10, Q=None, nthreads=None):
+    """Blocks K[a][c] for the requested shell pairs, from the definition (see oracle.cpp)."""
+    return J_blocks(S, D, pairs, spherical, tau, Q, nthreads, _fn="ora_K_blocks")

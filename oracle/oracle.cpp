@@ -631,6 +631,88 @@ int ora_build_J(int nshell, const double* centers, const int* L, const int* npri
   return 0;
 }
 
+// Coulomb and exchange matrices together:
+//   J_{mu nu}     = sum_{lambda sigma} (mu nu|lambda sigma) D_{lambda sigma}
+//   K_{mu lambda} = sum_{nu sigma}     (mu nu|lambda sigma) D_{nu sigma}
+// (the "J, K += SCATTER(G, D)" step of FusionRCG Algorithm 2) over the unique
+// shell quartets kept by the Schwarz screen, each block scattered to the
+// distinct members of its eight permutation images: image (P Q|R S) adds
+// (PQ|RS) D_RS to J_PQ and (PQ|RS) D_QS to K_PR.
+int ora_build_JK(int nshell, const double* centers, const int* L, const int* nprim, const int* off,
+                 const double* exps, const double* coefs, int spherical, double tau, const double* Qin,
+                 const double* D, double* J, double* K, int nthreads) {
+  Shells S{nshell, centers, L, nprim, off, exps, coefs};
+  if (!shells_ok(S) || !D || !J || !K) return -1;
+  std::vector<int> fo(nshell + 1, 0);
+  for (int i = 0; i < nshell; ++i) fo[i + 1] = fo[i] + nfunc(S.L[i], spherical);
+  const int nbf = fo[nshell];
+  std::vector<double> Q;
+  if (Qin) {
+    Q.assign(Qin, Qin + (size_t)nshell * nshell);
+  } else if (tau > 0) {
+    Q.resize((size_t)nshell * nshell);
+    ora_schwarz(nshell, centers, L, nprim, off, exps, coefs, spherical, Q.data(), nthreads);
+  }
+  std::vector<std::array<int, 2>> pairs;
+  for (int a = 0; a < nshell; ++a)
+    for (int b = 0; b <= a; ++b) pairs.push_back({a, b});
+  const long long npair = (long long)pairs.size();
+  int nt = nthreads > 0 ? nthreads : 1;
+  std::vector<std::vector<double>> Jt(nt, std::vector<double>((size_t)nbf * nbf, 0.0));
+  std::vector<std::vector<double>> Kt(nt, std::vector<double>((size_t)nbf * nbf, 0.0));
+#pragma omp parallel num_threads(nt)
+  {
+    int tid = 0;
+#ifdef _OPENMP
+    tid = omp_get_thread_num();
+#endif
+    std::vector<double>& Jl = Jt[tid];
+    std::vector<double>& Kl = Kt[tid];
+    std::vector<double> blk;
+#pragma omp for schedule(dynamic, 1)
+    for (long long pab = 0; pab < npair; ++pab) {
+      int a = pairs[pab][0], b = pairs[pab][1];
+      for (long long pcd = 0; pcd <= pab; ++pcd) {
+        int c = pairs[pcd][0], d = pairs[pcd][1];
+        if (tau > 0 && Q[(size_t)a * nshell + b] * Q[(size_t)c * nshell + d] < tau) continue;
+        eri_block<double>(S, a, b, c, d, spherical, blk);
+        const int n[4] = {nfunc(S.L[a], spherical), nfunc(S.L[b], spherical), nfunc(S.L[c], spherical),
+                          nfunc(S.L[d], spherical)};
+        const int sh[4] = {a, b, c, d};
+        static const int perms[8][4] = {{0, 1, 2, 3}, {1, 0, 2, 3}, {0, 1, 3, 2}, {1, 0, 3, 2},
+                                        {2, 3, 0, 1}, {3, 2, 0, 1}, {2, 3, 1, 0}, {3, 2, 1, 0}};
+        std::set<std::array<int, 4>> done;
+        for (const auto& pm : perms) {
+          std::array<int, 4> img = {sh[pm[0]], sh[pm[1]], sh[pm[2]], sh[pm[3]]};
+          if (!done.insert(img).second) continue;
+          int o[4];
+          for (int i0 = 0; i0 < n[pm[0]]; ++i0)
+            for (int i1 = 0; i1 < n[pm[1]]; ++i1)
+              for (int i2 = 0; i2 < n[pm[2]]; ++i2)
+                for (int i3 = 0; i3 < n[pm[3]]; ++i3) {
+                  o[pm[0]] = i0;
+                  o[pm[1]] = i1;
+                  o[pm[2]] = i2;
+                  o[pm[3]] = i3;
+                  const double v = blk[(((size_t)o[0] * n[1] + o[1]) * n[2] + o[2]) * n[3] + o[3]];
+                  const size_t P = fo[img[0]] + i0, Qi = fo[img[1]] + i1, R = fo[img[2]] + i2, Si = fo[img[3]] + i3;
+                  Jl[P * nbf + Qi] += v * D[R * nbf + Si];
+                  Kl[P * nbf + R] += v * D[Qi * nbf + Si];
+                }
+        }
+      }
+    }
+  }
+  std::fill(J, J + (size_t)nbf * nbf, 0.0);
+  std::fill(K, K + (size_t)nbf * nbf, 0.0);
+  for (int t = 0; t < nt; ++t)
+    for (size_t k = 0; k < (size_t)nbf * nbf; ++k) {
+      J[k] += Jt[t][k];
+      K[k] += Kt[t][k];
+    }
+  return 0;
+}
+
 // Selected blocks of the Coulomb matrix straight from its definition:
 //   J[a-block][b-block] = sum over all ordered shell pairs (c, d) with
 //   Q_ab Q_cd >= tau (every pair when tau <= 0) of (ab|cd) . D_cd,
@@ -674,6 +756,55 @@ int ora_J_blocks(int nshell, const double* centers, const int* L, const int* npr
               for (int l = 0; l < nd; ++l)
                 sum += blk[(((size_t)i * nb + j) * nc + k) * nd + l] * D[(size_t)(fo[c] + k) * nbf + fo[d] + l];
             part[tid][(size_t)i * nb + j] += sum;
+          }
+      }
+    }
+    for (int t = 0; t < nt; ++t)
+      for (size_t k = 0; k < acc.size(); ++k) acc[k] += part[t][k];
+    std::memcpy(out + out_off[r], acc.data(), acc.size() * sizeof(double));
+  }
+  return 0;
+}
+
+// Selected blocks of the exchange matrix from its definition:
+//   K[a][c]_{i k} = sum over all ordered shells (b, d) with Q_ab Q_cd >= tau of
+//                   sum_{j l} (a b|c d)_{i j k l} D[b][d]_{j l}.
+int ora_K_blocks(int nshell, const double* centers, const int* L, const int* nprim, const int* off,
+                 const double* exps, const double* coefs, int spherical, double tau, const double* Q,
+                 const double* D, const int* ac_pairs, long long n, const long long* out_off, double* out,
+                 int nthreads) {
+  Shells S{nshell, centers, L, nprim, off, exps, coefs};
+  if (!shells_ok(S) || !D || !ac_pairs || !out || !out_off || n < 0 || (tau > 0 && !Q)) return -1;
+  std::vector<int> fo(nshell + 1, 0);
+  for (int i = 0; i < nshell; ++i) fo[i + 1] = fo[i] + nfunc(S.L[i], spherical);
+  const int nbf = fo[nshell];
+  for (long long r = 0; r < n; ++r) {
+    const int a = ac_pairs[2 * r], c = ac_pairs[2 * r + 1];
+    if (a < 0 || a >= nshell || c < 0 || c >= nshell) return -1;
+    const int na = nfunc(S.L[a], spherical), nc = nfunc(S.L[c], spherical);
+    std::vector<double> acc((size_t)na * nc, 0.0);
+    int nt = nthreads > 0 ? nthreads : 1;
+    std::vector<std::vector<double>> part(nt, std::vector<double>((size_t)na * nc, 0.0));
+#pragma omp parallel num_threads(nt)
+    {
+      int tid = 0;
+#ifdef _OPENMP
+      tid = omp_get_thread_num();
+#endif
+      std::vector<double> blk;
+#pragma omp for schedule(dynamic, 8)
+      for (long long bd = 0; bd < (long long)nshell * nshell; ++bd) {
+        const int b = (int)(bd / nshell), d = (int)(bd % nshell);
+        if (tau > 0 && Q[(size_t)a * nshell + b] * Q[(size_t)c * nshell + d] < tau) continue;
+        eri_block<double>(S, a, b, c, d, spherical, blk);
+        const int nb = nfunc(S.L[b], spherical), nd = nfunc(S.L[d], spherical);
+        for (int i = 0; i < na; ++i)
+          for (int k = 0; k < nc; ++k) {
+            double sum = 0;
+            for (int j = 0; j < nb; ++j)
+              for (int l = 0; l < nd; ++l)
+                sum += blk[(((size_t)i * nb + j) * nc + k) * nd + l] * D[(size_t)(fo[b] + j) * nbf + fo[d] + l];
+            part[tid][(size_t)i * nc + k] += sum;
           }
       }
     }

@@ -388,3 +388,34 @@ def test_J_screening_changes_little():
     assert k1 <= k0
     assert np.linalg.norm(J1 - J0) <= 1e-8 * np.linalg.norm(J0)
     assert np.allclose(J1, J1.T, atol=1e-12)
+
+
+def test_K_equals_tensor_contraction_and_is_positive():
+    S = _tiny_set(4)
+    T = oracle.eri_tensor(S, spherical=False)
+    nbf = T.shape[0]
+    rng = np.random.default_rng(2)
+    C = rng.normal(size=(nbf, nbf // 4))
+    D = C @ C.T
+    J, K = oracle.build_JK(S, D, spherical=False, tau=0.0)
+    assert np.allclose(J, np.einsum("ijkl,kl->ij", T, D), rtol=1e-12, atol=1e-12)
+    assert np.allclose(K, np.einsum("ijkl,jl->ik", T, D), rtol=1e-12, atol=1e-12)
+    assert np.allclose(K, K.T, atol=1e-12)
+    # sum_{mu nu lambda sigma} D_{mu lambda} (mu nu|lambda sigma) D_{nu sigma} >= 0 for PSD D
+    assert np.sum(D * K) > 0
+    J0, _ = oracle.build_J(S, D, spherical=False, tau=0.0)
+    assert np.allclose(J, J0, rtol=1e-13, atol=1e-13)
+
+
+def test_K_blocks_match_contraction():
+    S = _tiny_set(4)
+    T = oracle.eri_tensor(S, spherical=True)
+    nbf = T.shape[0]
+    rng = np.random.default_rng(5)
+    D = rng.normal(size=(nbf, nbf))
+    D = D + D.T
+    fo = np.concatenate([[0], np.cumsum([oracle.nfunc(l, True) for l in S.L])])
+    Kfull = np.einsum("ijkl,jl->ik", T, D)
+    pairs = [(0, 0), (1, 3), (3, 2)]
+    for (a, c), B in zip(pairs, oracle.K_blocks(S, D, pairs, spherical=True, tau=0.0)):
+        assert np.allclose(B, Kfull[fo[a]:fo[a + 1], fo[c]:fo[c + 1]], rtol=1e-12, atol=1e-12)
