@@ -55,6 +55,11 @@ WORKLOADS = {
     "cluster200": {"desc": "200-atom synthetic cluster (same composition), Coulomb J over all unique quartets "
                            "surviving Schwarz 1e-10, spherical, D = C C^T (C: N x N/4, N(0,1)/sqrt(N))",
                    "cluster": (200, 4)},
+    "cluster64_jk": {"desc": "64-atom synthetic cluster as cluster64: Coulomb J and exchange K together in one "
+                             "pass over all unique quartets surviving Schwarz 1e-10", "cluster": (64, 3), "jk": True},
+    "cluster200_jk": {"desc": "200-atom synthetic cluster as cluster200: Coulomb J and exchange K together in one "
+                              "pass over all unique quartets surviving Schwarz 1e-10", "cluster": (200, 4),
+                      "jk": True},
 }
 
 
@@ -196,7 +201,7 @@ def run_reference(a, rank, world):
 
 
 def run_coulomb(a, rank, world, local_rank):
-    """Cluster workloads: one step = eri_build_J over every surviving unique quartet."""
+    """Cluster workloads: one step = eri_build_J (or eri_build_JK) over every surviving unique quartet."""
     import torch
     import electron_repulsion_integrals_gb300 as eri
     from electron_repulsion_integrals_gb300 import workloads as W
@@ -222,8 +227,17 @@ def run_coulomb(a, rank, world, local_rank):
     nq = sum(counts.values())
     Dd = torch.as_tensor(D, device=dev)
     J = torch.empty_like(Dd)
+    K = torch.empty_like(Dd)
+    jk = bool(wl.get("jk"))
+
+    def digest():
+        if jk:
+            plan.build_JK(Dd, J, K, stream)
+        else:
+            plan.build_J(Dd, J, stream)
+
     for _ in range(a.warmup):
-        plan.build_J(Dd, J, stream)
+        digest()
     torch.cuda.synchronize()
     clocks = ClockSampler(local_rank)
     clocks.start()
@@ -235,7 +249,7 @@ def run_coulomb(a, rank, world, local_rank):
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
     for _ in range(a.steps):
-        plan.build_J(Dd, J, stream)
+        digest()
     t1.record(stream)
     torch.cuda.synchronize()
     if dist:
@@ -247,7 +261,8 @@ def run_coulomb(a, rank, world, local_rank):
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         ms = float(tt.item())
     value = nq * world * a.steps / (ms / 1e3)
-    # algorithmic flops: per class, quartets x (primitive quartets x VRR + HRR) + 4 per digested integral
+    # algorithmic flops: per class, quartets x (primitive quartets x VRR + HRR) + per digested integral
+    # 2 FMA for J (+ 4 FMA for K)
     prim_q = 0.0
     flops = 0.0
     per_class = {}
@@ -257,24 +272,29 @@ def run_coulomb(a, rank, world, local_rank):
         st = eri.eri_class_info(c)
         _, pq = eri.eri_plan_class_work(plan.handle, c)
         prim_q += pq
-        flops += pq * st["vrr_flops"] + n * (st["hrr_flops"] + 4 * eri.block_size(c))
+        flops += pq * st["vrr_flops"] + n * (st["hrr_flops"] + (12 if jk else 4) * eri.block_size(c))
         per_class["({}{}|{}{})".format(*c)] = {"quartets": n, "primitive_quartets": pq}
     ach = flops / (ms / a.steps / 1e3) / 1e12
     e2e = None
     if a.e2e:
         hD = torch.from_numpy(D).pin_memory()
         hJ = torch.empty_like(hD).pin_memory()
+        hK = torch.empty_like(hD).pin_memory()
         torch.cuda.synchronize()
         te = time.perf_counter()
         p2 = eri.Plan(s, spherical=True, schwarz_tau=1e-10, stream=stream)
         dd = hD.to(dev, non_blocking=True)
-        Jd = p2.build_J(dd, None, stream)
+        if jk:
+            Jd, Kd = p2.build_JK(dd, None, None, stream)
+            hK.copy_(Kd, non_blocking=True)
+        else:
+            Jd = p2.build_J(dd, None, stream)
         hJ.copy_(Jd, non_blocking=True)
         torch.cuda.synchronize()
         te = time.perf_counter() - te
         p2.close()
         e2e = {"value": nq * world / te, "unit": "quartets/s", "h2d_bytes_per_step": hD.numel() * 8 + s.n * 48 +
-               s.exps.size * 16, "d2h_bytes_per_step": hJ.numel() * 8}
+               s.exps.size * 16, "d2h_bytes_per_step": hJ.numel() * 8 * (2 if jk else 1)}
     cpu = None
     if rank == 0 and a.cpu_baseline:
         rate, desc, cores = cpu_oracle_rate_cluster(s, counts, budget_s=a.ref_budget)
@@ -286,11 +306,11 @@ def run_coulomb(a, rank, world, local_rank):
             "config": {"workload": wl["desc"], "unique_quartets": nq, "primitive_quartets": prim_q, "nbf": nbf,
                        "plan_create_s": plan_s, "l2": "no flush: J digestion re-reads D; kernels are FP64-bound",
                        "parallelism": f"replicas x{world}"},
-            "roofline": {"bound": "alu", "kernel": "all class kernels of eri_build_J", "achieved": ach,
+            "roofline": {"bound": "alu", "kernel": "all class kernels of " + ("eri_build_JK" if jk else "eri_build_J"), "achieved": ach,
                          "peak": FP64_PEAK_TFLOPS, "unit": "TFLOP/s", "frac": ach / FP64_PEAK_TFLOPS,
                          "traffic": None, "peak_source": "FP64 pipe: 152 SMs x 2 DFMA/clk x 2 flop x 2.07 GHz"},
             "clocks": clk, "e2e": e2e, "cpu_baseline": cpu,
-            "gpu_launches": a.steps * (sum(1 for n in counts.values() if n) + 1)}
+            "gpu_launches": a.steps * (sum(1 for n in counts.values() if n) + (2 if jk else 1))}
     if rank == 0:
         print(json.dumps(line), flush=True)
     plan.close()

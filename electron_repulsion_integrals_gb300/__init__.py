@@ -69,6 +69,7 @@ def lib():
                                                                              ctypes.c_longlong, vp]
         L.eri_schwarz.argtypes = [vp, ctypes.c_int, ctypes.c_int, vp, ctypes.c_longlong, dp, vp]
         L.eri_build_J.argtypes = [vp, dp, dp, vp]
+        L.eri_build_JK.argtypes = [vp, dp, dp, dp, vp]
         L.eri_plan_quartet_count.argtypes = [vp] + [ctypes.c_int] * 4 + [ctypes.POINTER(ctypes.c_longlong)]
         L.eri_plan_class_work.argtypes = [vp] + [ctypes.c_int] * 4 + [ctypes.POINTER(ctypes.c_longlong),
                                                                      ctypes.POINTER(ctypes.c_double)]
@@ -180,6 +181,11 @@ def eri_build_J(plan, D, J, stream=None):
     _check("eri_build_J", lib().eri_build_J(plan, _ptr(D), _ptr(J), ctypes.c_void_p(_stream_handle(stream))))
 
 
+def eri_build_JK(plan, D, J, K, stream=None):
+    _check("eri_build_JK", lib().eri_build_JK(plan, _ptr(D), _ptr(J), _ptr(K),
+                                              ctypes.c_void_p(_stream_handle(stream))))
+
+
 def eri_plan_quartet_count(plan, cls):
     n = ctypes.c_longlong()
     _check("eri_plan_quartet_count", lib().eri_plan_quartet_count(plan, *[int(x) for x in cls], ctypes.byref(n)))
@@ -237,6 +243,13 @@ class Plan:
             J = torch.empty_like(D)
         eri_build_J(self.handle, D, J, stream)
         return J
+
+    def build_JK(self, D, J=None, K=None, stream=None):
+        import torch
+        J = torch.empty_like(D) if J is None else J
+        K = torch.empty_like(D) if K is None else K
+        eri_build_JK(self.handle, D, J, K, stream)
+        return J, K
 
     def quartet_count(self, cls):
         return eri_plan_quartet_count(self.handle, cls)

@@ -83,7 +83,8 @@ __device__ __forceinline__ void boys_scaled(double T, double pref, const double*
 }
 
 // ---------------------------------------------------------------- launch data
-enum OutputMode { kStore = 0, kSchwarz = 1, kCoulomb = 2 };
+// kCoulomb digests every block into J; kExchange into J and K together.
+enum OutputMode { kStore = 0, kSchwarz = 1, kCoulomb = 2, kExchange = 3 };
 
 struct ShellsDev {
   const double* cen;    // [nshell][3]
@@ -110,6 +111,7 @@ struct EriLaunch {
   // segs[k].x with ket pairs segs[k].y .. segs[k].y + segs[k].z - 1.
   const double* D;       // density, nbf x nbf row-major
   double* J;             // accumulator, nbf x nbf row-major (pair-oriented blocks)
+  double* K;             // exchange mode: accumulator T with K = T + T^T
   const int* fo;         // first basis function of each shell
   int nbf;
   const struct PairMeta* pairs;
@@ -142,6 +144,7 @@ struct Quartet {
   int pab, nab, pcd, ncd;
   int fa, fb, fc, fd;  // first basis functions of the four shells
   double fab, fcd;     // 2 for a pair of distinct shells, else 1
+  double wk;           // 1 / (number of the 8 index permutations that leave the quartet unchanged)
   int ost[4];          // store mode: output stride of canonical axes a, b, c, d
 };
 
@@ -260,6 +263,7 @@ __device__ __forceinline__ void load_quartet_coulomb(const EriLaunch& P, long lo
   Q.fd = __ldg(P.fo + Q.s[3]);
   Q.fab = Q.s[0] != Q.s[1] ? 2.0 : 1.0;
   Q.fcd = Q.s[2] != Q.s[3] ? 2.0 : 1.0;
+  Q.wk = (Q.s[0] == Q.s[1] ? 0.5 : 1.0) * (Q.s[2] == Q.s[3] ? 0.5 : 1.0) * (Q.bra == Q.ket ? 0.5 : 1.0);
 }
 
 // Gaussian product of two primitives (alpha at A, beta at B):
@@ -338,13 +342,13 @@ __device__ __forceinline__ void quartet_setup(const PrimPair& pb, const PrimPair
 // has exactly one primitive and the loops disappear.
 #define PRIM_LOOP_BEGIN(P, Q)                                                                              \
   {                                                                                                        \
-    const int nab_ = MODE == kCoulomb ? Q.nab : CONTRACTED ? Q.na * Q.nb : 1;                              \
-    const int ncd_ = MODE == kCoulomb ? Q.ncd : CONTRACTED ? Q.nc * Q.nd : 1;                              \
+    const int nab_ = MODE >= kCoulomb ? Q.nab : CONTRACTED ? Q.na * Q.nb : 1;                              \
+    const int ncd_ = MODE >= kCoulomb ? Q.ncd : CONTRACTED ? Q.nc * Q.nd : 1;                              \
     double qk0_ = 0.0;                                                                                     \
-    if constexpr (MODE == kCoulomb) qk0_ = __ldg(P.prims + (size_t)Q.pcd * kPrimRec + 9);                  \
+    if constexpr (MODE >= kCoulomb) qk0_ = __ldg(P.prims + (size_t)Q.pcd * kPrimRec + 9);                  \
     for (int iab_ = 0; iab_ < nab_; ++iab_) {                                                              \
       PrimPair pb;                                                                                         \
-      if constexpr (MODE == kCoulomb) {                                                                    \
+      if constexpr (MODE >= kCoulomb) {                                                                    \
         load_prim(P.prims, Q.pab + iab_, pb);                                                              \
         if (pb.q * qk0_ < kPrimQuartetTau) break;                                                          \
       } else {                                                                                             \
@@ -354,7 +358,7 @@ __device__ __forceinline__ void quartet_setup(const PrimPair& pb, const PrimPair
       }                                                                                                    \
       for (int icd_ = 0; icd_ < ncd_; ++icd_) {                                                            \
         PrimPair pk;                                                                                       \
-        if constexpr (MODE == kCoulomb) {                                                                  \
+        if constexpr (MODE >= kCoulomb) {                                                                  \
           load_prim(P.prims, Q.pcd + icd_, pk);                                                            \
           if (pb.q * pk.q < kPrimQuartetTau) break;                                                        \
         } else {                                                                                           \
@@ -374,17 +378,38 @@ __device__ __forceinline__ void quartet_setup(const PrimPair& pb, const PrimPair
 // OUTPUT_VAL(ia, ib, ic, id, v)    one final integral (ab|cd) in canonical order
 // OUTPUT_ROW_END()                 end of the row
 // OUTPUT_QUARTET_END()             end of the quartet
+// Rows come in order ia-major.  The kernel declares kNSB_, kNSC_, kNSD_ (function
+// counts of shells b, c, d), kNCD_ = kNSC_ kNSD_, jcd_[kNCD_] and, for the
+// exchange mode, kac_[kNSC_] and kad_[kNSD_] (zeroed once per quartet).
+//
+// Exchange digestion of one unique quartet (ab|cd) with weight w = Q.wk: the
+// four images (ab|cd), (ba|cd), (ab|dc), (ba|dc) add
+//   T_ac += w I D_bd,  T_bc += w I D_ad,  T_ad += w I D_bc,  T_bd += w I D_ac
+// (I contracted over the indices of the D factor) and the four bra-ket swapped
+// images add the transposes, so K = T + T^T for a symmetric D.  T_bc and T_bd
+// rows change with ib and are flushed every row; T_ac and T_ad rows change with
+// ia only and are flushed after the last ib of that ia.
 #define OUTPUT_ROW(r, ia, ib)                                               \
   {                                                                         \
     double* __restrict__ orow_ = nullptr;                                   \
     double jrow_ = 0.0, dab_ = 0.0;                                         \
     double* jdst_ = nullptr;                                                \
+    const double* __restrict__ da_ = nullptr;                               \
+    const double* __restrict__ db_ = nullptr;                               \
+    double kbc_[kNSC_], kbd_[kNSD_];                                        \
+    const int ia_ = (ia), ib_ = (ib);                                       \
     if constexpr (MODE == kStore) {                                         \
       orow_ = P.out + q * P.out_stride + (ia) * Q.ost[0] + (ib) * Q.ost[1]; \
-    } else if constexpr (MODE == kCoulomb) {                                \
+    } else if constexpr (MODE >= kCoulomb) {                                \
       const size_t rowoff_ = (size_t)(Q.fa + (ia)) * P.nbf + Q.fb + (ib);   \
       dab_ = Q.fab * __ldg(P.D + rowoff_);                                  \
       jdst_ = P.J + rowoff_;                                                \
+    }                                                                       \
+    if constexpr (MODE == kExchange) {                                      \
+      da_ = P.D + (size_t)(Q.fa + (ia)) * P.nbf;                            \
+      db_ = P.D + (size_t)(Q.fb + (ib)) * P.nbf;                            \
+      _Pragma("unroll") for (int k_ = 0; k_ < kNSC_; ++k_) kbc_[k_] = 0.0;  \
+      _Pragma("unroll") for (int k_ = 0; k_ < kNSD_; ++k_) kbd_[k_] = 0.0;  \
     }
 
 #define OUTPUT_VAL(ia, ib, ic, id, v)                                          \
@@ -395,22 +420,50 @@ __device__ __forceinline__ void quartet_setup(const PrimPair& pb, const PrimPair
   } else {                                                                     \
     jrow_ = fma((v), __ldg(P.D + (size_t)(Q.fc + (ic)) * P.nbf + Q.fd + (id)), jrow_); \
     jcd_[(ic) * kNSD_ + (id)] = fma((v), dab_, jcd_[(ic) * kNSD_ + (id)]);   \
+    if constexpr (MODE == kExchange) {                                         \
+      kac_[ic] = fma((v), __ldg(db_ + Q.fd + (id)), kac_[ic]);                \
+      kad_[id] = fma((v), __ldg(db_ + Q.fc + (ic)), kad_[id]);                \
+      kbc_[ic] = fma((v), __ldg(da_ + Q.fd + (id)), kbc_[ic]);                \
+      kbd_[id] = fma((v), __ldg(da_ + Q.fc + (ic)), kbd_[id]);                \
+    }                                                                          \
   }
 
-#define OUTPUT_ROW_END()                                    \
-  if constexpr (MODE == kCoulomb) {                         \
-    atomicAdd(jdst_, Q.fcd * jrow_);                        \
-  }                                                         \
-  (void)orow_;                                              \
-  (void)jrow_;                                              \
-  (void)dab_;                                               \
-  (void)jdst_;                                              \
+#define OUTPUT_ROW_END()                                                            \
+  if constexpr (MODE >= kCoulomb) {                                                 \
+    atomicAdd(jdst_, Q.fcd * jrow_);                                                \
+  }                                                                                 \
+  if constexpr (MODE == kExchange) {                                                \
+    double* __restrict__ kb_ = P.K + (size_t)(Q.fb + ib_) * P.nbf;                  \
+    _Pragma("unroll") for (int k_ = 0; k_ < kNSC_; ++k_) atomicAdd(kb_ + Q.fc + k_, Q.wk * kbc_[k_]); \
+    _Pragma("unroll") for (int k_ = 0; k_ < kNSD_; ++k_) atomicAdd(kb_ + Q.fd + k_, Q.wk * kbd_[k_]); \
+    if (ib_ == kNSB_ - 1) {                                                         \
+      double* __restrict__ ka_ = P.K + (size_t)(Q.fa + ia_) * P.nbf;                \
+      _Pragma("unroll") for (int k_ = 0; k_ < kNSC_; ++k_) {                        \
+        atomicAdd(ka_ + Q.fc + k_, Q.wk * kac_[k_]);                                \
+        kac_[k_] = 0.0;                                                             \
+      }                                                                             \
+      _Pragma("unroll") for (int k_ = 0; k_ < kNSD_; ++k_) {                        \
+        atomicAdd(ka_ + Q.fd + k_, Q.wk * kad_[k_]);                                \
+        kad_[k_] = 0.0;                                                             \
+      }                                                                             \
+    }                                                                               \
+  }                                                                                 \
+  (void)orow_;                                                                      \
+  (void)jrow_;                                                                      \
+  (void)dab_;                                                                       \
+  (void)jdst_;                                                                      \
+  (void)da_;                                                                        \
+  (void)db_;                                                                        \
+  (void)kbc_;                                                                       \
+  (void)kbd_;                                                                       \
+  (void)ia_;                                                                        \
+  (void)ib_;                                                                        \
   }
 
 #define OUTPUT_QUARTET_END()                                                             \
   if constexpr (MODE == kSchwarz) {                                                      \
     P.q_out[q] = sqrt(smax_);                                                            \
-  } else if constexpr (MODE == kCoulomb) {                                               \
+  } else if constexpr (MODE >= kCoulomb) {                                               \
     if (Q.bra != Q.ket) {                                                                \
       _Pragma("unroll") for (int k_ = 0; k_ < kNCD_; ++k_) {                             \
         atomicAdd(P.J + (size_t)(Q.fc + k_ / kNSD_) * P.nbf + Q.fd + k_ % kNSD_, jcd_[k_]); \
@@ -445,6 +498,8 @@ __device__ __forceinline__ void quartet_setup(const PrimPair& pb, const PrimPair
       ERI_LAUNCH_MODE_(KERNEL, kSchwarz, smemb_)                                                          \
     } else if (mode == kCoulomb) {                                                                        \
       ERI_LAUNCH_ONE_(KERNEL, kCoulomb, true, smemb_)                                                     \
+    } else if (mode == kExchange) {                                                                       \
+      ERI_LAUNCH_ONE_(KERNEL, kExchange, true, smemb_)                                                    \
     } else {                                                                                              \
       return -1;                                                                                          \
     }                                                                                                     \

@@ -101,6 +101,14 @@ __global__ void symmetrise(int nbf, const int* __restrict__ shell_of, const doub
   J[(size_t)i * nbf + j] = v;
 }
 
+// K = T + T^T for the exchange accumulator T.
+__global__ void add_transpose(int nbf, const double* __restrict__ T, double* __restrict__ K) {
+  const int j = blockIdx.x * blockDim.x + threadIdx.x;
+  const int i = blockIdx.y;
+  if (j >= nbf) return;
+  K[(size_t)i * nbf + j] = T[(size_t)i * nbf + j] + T[(size_t)j * nbf + i];
+}
+
 struct DevBuf {
   void* p = nullptr;
   ~DevBuf() { cudaFree(p); }
@@ -126,12 +134,14 @@ struct Screen {
   double* dprims = nullptr;
   int* dshell_of = nullptr;
   double* Jacc = nullptr;
+  double* Kacc = nullptr;  // allocated by the first eri_build_JK
   std::vector<ClassWork> classes;
   ~Screen() {
     cudaFree(dpairs);
     cudaFree(dprims);
     cudaFree(dshell_of);
     cudaFree(Jacc);
+    cudaFree(Kacc);
     for (auto& c : classes) {
       cudaFree(c.dsegs);
       cudaFree(c.dstart);
@@ -414,6 +424,55 @@ int build(eri_plan* p, cudaStream_t st) {
 }  // namespace screen
 }  // namespace eri
 
+namespace {
+
+// One digestion pass over every screened class: J alone (K == nullptr) or J
+// and K together.
+int build_digest(eri_plan* p, const double* D, double* J, double* K, cudaStream_t st) {
+  eri::screen::Screen* S = eri::host::plan_screen(p);
+  if (!S) return ERI_ERR_INVALID_ARG;  // plan created with schwarz_tau <= 0 has no screen
+  const int ns = eri::host::plan_nshell(p);
+  const int nbf = eri::host::plan_fo(p)[ns];
+  const size_t bytes = (size_t)nbf * nbf * sizeof(double);
+  if (K && !S->Kacc) {
+    if (cudaMalloc(&S->Kacc, std::max<size_t>(bytes, sizeof(double))) != cudaSuccess) {
+      S->Kacc = nullptr;
+      return ERI_ERR_OOM;
+    }
+  }
+  CUDA_TRY(cudaMemsetAsync(S->Jacc, 0, bytes, st));
+  if (K) CUDA_TRY(cudaMemsetAsync(S->Kacc, 0, bytes, st));
+  for (const ClassWork& W : S->classes) {
+    if (W.total == 0) continue;
+    EriLaunch P;
+    std::memset(&P, 0, sizeof(P));
+    P.n = W.total;
+    P.D = D;
+    P.J = S->Jacc;
+    P.K = K ? S->Kacc : nullptr;
+    P.fo = eri::host::plan_dfo(p);
+    P.nbf = nbf;
+    P.pairs = S->dpairs;
+    P.prims = S->dprims;
+    P.segs = W.dsegs;
+    P.seg_start = W.dstart;
+    P.nseg = W.nseg;
+    int rc = eri::host::launch_class(p, W.l, P, K ? kExchange : kCoulomb, st);
+    if (rc) return rc;
+  }
+  if (nbf == 0) return ERI_OK;
+  dim3 grid((nbf + 127) / 128, nbf);
+  symmetrise<<<grid, 128, 0, st>>>(nbf, S->dshell_of, S->Jacc, J);
+  CUDA_TRY(cudaGetLastError());
+  if (K) {
+    add_transpose<<<grid, 128, 0, st>>>(nbf, S->Kacc, K);
+    CUDA_TRY(cudaGetLastError());
+  }
+  return ERI_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 int eri_schwarz(eri_plan* p, int la, int lb, const int* pairs_dev, long long n, double* q_out_dev, void* stream) {
@@ -427,33 +486,12 @@ int eri_schwarz(eri_plan* p, int la, int lb, const int* pairs_dev, long long n, 
 
 int eri_build_J(eri_plan* p, const double* D, double* J, void* stream) {
   if (!p || !D || !J) return ERI_ERR_INVALID_ARG;
-  eri::screen::Screen* S = eri::host::plan_screen(p);
-  if (!S) return ERI_ERR_INVALID_ARG;  // plan created with schwarz_tau <= 0 has no screen
-  cudaStream_t st = (cudaStream_t)stream;
-  const int ns = eri::host::plan_nshell(p);
-  const int nbf = eri::host::plan_fo(p)[ns];
-  CUDA_TRY(cudaMemsetAsync(S->Jacc, 0, (size_t)nbf * nbf * sizeof(double), st));
-  for (const ClassWork& W : S->classes) {
-    if (W.total == 0) continue;
-    EriLaunch P;
-    std::memset(&P, 0, sizeof(P));
-    P.n = W.total;
-    P.D = D;
-    P.J = S->Jacc;
-    P.fo = eri::host::plan_dfo(p);
-    P.nbf = nbf;
-    P.pairs = S->dpairs;
-    P.prims = S->dprims;
-    P.segs = W.dsegs;
-    P.seg_start = W.dstart;
-    P.nseg = W.nseg;
-    int rc = eri::host::launch_class(p, W.l, P, kCoulomb, st);
-    if (rc) return rc;
-  }
-  dim3 grid((nbf + 127) / 128, nbf);
-  symmetrise<<<grid, 128, 0, st>>>(nbf, S->dshell_of, S->Jacc, J);
-  CUDA_TRY(cudaGetLastError());
-  return ERI_OK;
+  return build_digest(p, D, J, nullptr, (cudaStream_t)stream);
+}
+
+int eri_build_JK(eri_plan* p, const double* D, double* J, double* K, void* stream) {
+  if (!p || !D || !J || !K) return ERI_ERR_INVALID_ARG;
+  return build_digest(p, D, J, K, (cudaStream_t)stream);
 }
 
 int eri_plan_class_work(const eri_plan* p, int la, int lb, int lc, int ld, long long* quartets,

@@ -309,9 +309,11 @@ def emit_coop_class(cls):
     w(f"__device__ __forceinline__ void ket_hrr_{cname}(const EriLaunch& P, const Quartet& Q, long long q, int r, "
       f"const double* __restrict__ G, double& smax_) {{")
     w(f"  const double* __restrict__ Gr = G + r * {GS};")
-    w("  constexpr int kNSD_ = 1;")
-    w("  double jcd_[1];")
+    w("  constexpr int kNSB_ = 1, kNSC_ = 1, kNSD_ = 1;")
+    w("  double jcd_[1], kac_[1], kad_[1];")
     w("  (void)jcd_;")
+    w("  (void)kac_;")
+    w("  (void)kad_;")
     for ln in kem.lines:
         w("  " + ln)
     w(f"  OUTPUT_ROW(r, r / {nsb}, r % {nsb});")

@@ -446,20 +446,26 @@ def emit_class(cls, spherical_out=True):
             w("#define SMEM(k) smem_vrr_[(k) * kThreads + threadIdx.x]")
     w("  for (long long q = gid; q < P.n; q += nt) {")
     w("    Quartet Q;")
-    w("    if constexpr (MODE == kCoulomb) {")
+    w("    if constexpr (MODE >= kCoulomb) {")
     w("      load_quartet_coulomb(P, q, Q);")
     w("    } else {")
     w(f"      load_quartet<{'true' if la == lb else 'false'}, {'true' if lc == ld else 'false'}>(P, q, Q);")
     w("    }")
     w("    double smax_ = 0.0;")
     w("    (void)smax_;")
+    w(f"    constexpr int kNSB_ = {nsb};")
+    w(f"    constexpr int kNSC_ = {nsc};")
     w(f"    constexpr int kNSD_ = {nsd};")
     w(f"    constexpr int kNCD_ = {nsc * nsd};")
-    w("    double jcd_[kNCD_];")
-    w("    if constexpr (MODE == kCoulomb) {")
+    w("    double jcd_[kNCD_], kac_[kNSC_], kad_[kNSD_];")
+    w("    if constexpr (MODE >= kCoulomb) {")
     w("      _Pragma(\"unroll\") for (int k_ = 0; k_ < kNCD_; ++k_) jcd_[k_] = 0.0;")
+    w("      _Pragma(\"unroll\") for (int k_ = 0; k_ < kNSC_; ++k_) kac_[k_] = 0.0;")
+    w("      _Pragma(\"unroll\") for (int k_ = 0; k_ < kNSD_; ++k_) kad_[k_] = 0.0;")
     w("    }")
     w("    (void)jcd_;")
+    w("    (void)kac_;")
+    w("    (void)kad_;")
     if shape == "reg":
         w(f"    double h[{len(g.targets)}];")
         for ti in range(len(g.targets)):

@@ -165,6 +165,20 @@ int eri_schwarz(eri_plan* plan, int la, int lb, const int* pairs_dev, long long 
  * CUDA, OOM. */
 int eri_build_J(eri_plan* plan, const double* D_dev, double* J_dev, void* stream);
 
+/* Coulomb and exchange matrices from one pass over the screened quartets (the
+ * "J, K += SCATTER(G, D)" digestion step of FusionRCG Algorithm 2):
+ *   J_{mu nu}     = sum_{lambda sigma} (mu nu|lambda sigma) D_{lambda sigma}
+ *   K_{mu lambda} = sum_{nu sigma}     (mu nu|lambda sigma) D_{nu sigma}
+ * over the unique shell quartets that pass Q_ab Q_cd >= schwarz_tau, each
+ * block scattered to the distinct members of its eight permutation images.
+ * D_dev, J_dev and K_dev are device nbf x nbf row-major double matrices; D must
+ * be symmetric; J and K are overwritten and come out symmetric.  J equals what
+ * eri_build_J returns up to the order of its atomic additions.  The first call
+ * on a plan allocates an nbf x nbf device accumulator for K that the plan keeps
+ * until eri_plan_destroy.  Errors: INVALID_ARG (NULL argument, plan without a
+ * screen), OOM, CUDA. */
+int eri_build_JK(eri_plan* plan, const double* D_dev, double* J_dev, double* K_dev, void* stream);
+
 /* Number of unique shell quartets of canonical class (la lb|lc ld) that
  * eri_build_J evaluates (after screening). */
 int eri_plan_quartet_count(const eri_plan* plan, int la, int lb, int lc, int ld, long long* n);
