@@ -1,7 +1,8 @@
 """Benchmark: ERI quartets/s and FP64 GFLOP/s per angular class on one GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload homogeneous|high_l] [--scale S]
+                    [--workload homogeneous|high_l|g_shells|cluster64|cluster200|cluster64_jk|cluster200_jk]
+                    [--scale S]
 
 A step is one pass of the hot path over the workload's batch: for every class
 of the workload, the class kernel evaluates all its quartets (Gaussian-pair
@@ -49,6 +50,9 @@ WORKLOADS = {
                     "classes": [((1, 1, 1, 1), 1 << 20, 1, 1), ((2, 2, 2, 2), 1 << 20, 1, 101)]},
     "high_l": {"desc": "high-L batch: (ff|ff) x 131,072 + (fd|fd) x 262,144 quartets, degree 2, spherical",
                "classes": [((3, 3, 3, 3), 131072, 2, 2), ((3, 2, 3, 2), 262144, 2, 102)]},
+    "g_shells": {"desc": "g-shell batch: (gg|gg) x 16,384 + (gd|gd) x 65,536 quartets, degree 2, centers U[0,10]^3 "
+                         "bohr, exponents log-U[0.05,100], spherical",
+                 "classes": [((4, 4, 4, 4), 16384, 2, 3), ((4, 2, 4, 2), 65536, 2, 103)]},
     "cluster64": {"desc": "64-atom synthetic cluster (radius 12 bohr, 32 heavy 3s2p1d + 32 light 2s1p, 1-6 "
                           "primitives, exponents log-U[0.1,5000]): Coulomb J over all unique quartets surviving "
                           "Schwarz 1e-10, spherical, D = C C^T", "cluster": (64, 3)},
@@ -491,6 +495,119 @@ def run_ours(a, rank, world, local_rank):
         dist.destroy_process_group()
 
 
+# ---------------------------------------------------------------- ablations
+def ablation_n(cls):
+    """Quartets per class in the ablation runs: outputs above L2 where the
+    block allows, launches of a millisecond or more."""
+    L = sum(cls)
+    return {0: 1 << 22, 2: 1 << 21, 4: 1 << 20, 6: 1 << 18, 7: 1 << 17, 8: 1 << 17, 10: 1 << 15, 12: 1 << 13,
+            14: 1 << 12, 16: 1 << 11}[L]
+
+
+def run_ablation_worker(a):
+    """One library (ERI_GB300_LIBRARY, else the main build): every class it
+    holds, timed and checked against the oracle on a sample."""
+    import torch
+    import oracle
+    import electron_repulsion_integrals_gb300 as eri
+    from electron_repulsion_integrals_gb300 import workloads as W
+    from electron_repulsion_integrals_gb300 import ablation
+    dev = torch.device("cuda", 0)
+    eri.lib()
+    if a.ablation_worker == "full":
+        classes = sorted(set(map(tuple, ablation.GRAPH_CLASSES + ablation.TIER_CLASSES)), key=lambda c: (sum(c), c))
+    else:
+        classes = ablation.VARIANTS[a.ablation_worker][0]
+    stream = torch.cuda.current_stream()
+    res = {}
+    for cls in classes:
+        n = ablation_n(cls)
+        s, q = W.homogeneous(cls, n, 1, seed_index=60 + sum(cls))
+        plan = eri.Plan(s, spherical=True)
+        qd = torch.as_tensor(q, device=dev)
+        out = torch.empty(n * eri.block_size(cls), dtype=torch.float64, device=dev)
+        for _ in range(max(a.warmup, 1)):
+            eri.eri_compute_class(plan.handle, cls, qd, out, stream)
+        torch.cuda.synchronize()
+        evs = []
+        for _ in range(a.steps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            eri.eri_compute_class(plan.handle, cls, qd, out, stream)
+            e1.record(stream)
+            evs.append((e0, e1))
+        torch.cuda.synchronize()
+        ms = statistics.median(e0.elapsed_time(e1) for e0, e1 in evs)
+        idx = np.sort(np.random.default_rng(9).choice(n, 12, replace=False))
+        got = out.view(n, -1)[torch.as_tensor(idx, device=dev)].cpu().numpy().ravel()
+        ref = oracle.eri_blocks(oracle.ShellSet(s.centers, s.L, s.nprim, s.exps, s.coefs), q[idx], spherical=True)
+        tol = np.maximum(1e-12, 1e-10 * np.abs(ref))
+        if max(cls) >= 4:  # g shells: 1e-6 of the block maximum
+            bs = ref.size // len(idx)
+            tol = np.maximum(tol, 1e-6 * np.repeat(np.abs(ref).reshape(-1, bs).max(axis=1), bs))
+        ok = bool(np.all(np.abs(got - ref) <= tol))
+        st = eri.eri_class_info(cls)
+        res["{}{}{}{}".format(*cls)] = {"quartets_per_s": n / (ms / 1e3), "ms_per_launch": ms, "quartets": n,
+                                       "parity_ok": ok, "vrr_ops": st["vrr_ops"], "hrr_ops": st["hrr_ops"],
+                                       "tier": ["reg", "staged", "coop"][st["staged"]]}
+        plan.close()
+        del out, qd
+        torch.cuda.empty_cache()
+    print(json.dumps(res), flush=True)
+
+
+def run_ablation(a):
+    """Each ablation library against the main build, class by class."""
+    import subprocess
+    import electron_repulsion_integrals_gb300 as eri
+    from electron_repulsion_integrals_gb300 import ablation
+    names = a.ablation.split(",") if a.ablation != "all" else list(ablation.VARIANTS)
+    t = time.perf_counter()
+    paths = ablation.build_all(names)
+    build_s = time.perf_counter() - t
+    out = {"metric": "ablation: quartets/s per class and library (FusionRCG section V-B switches)", "unit": "quartets/s",
+           "steps": a.steps, "warmup": a.warmup, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": "per class: homogeneous batch, degree 1, centers U[0,10]^3 bohr, exponents "
+                                  "log-U[0.05,100], spherical; quartets per class by total angular momentum"},
+           "build_s": build_s, "libraries": {}}
+    for name in ["full"] + names:
+        env = dict(os.environ)
+        if name != "full":
+            env["ERI_GB300_LIBRARY"] = paths[name]
+        cmd = [sys.executable, os.path.abspath(__file__), "--ablation-worker", name, "--steps", str(a.steps),
+               "--warmup", str(a.warmup)]
+        r = subprocess.run(cmd, env=env, capture_output=True, text=True)
+        if r.returncode != 0:
+            out["libraries"][name] = {"error": r.stderr[-2000:]}
+            continue
+        res = json.loads(r.stdout.strip().splitlines()[-1])
+        meta = {}
+        if name != "full":
+            cj = json.load(open(os.path.join(os.path.dirname(paths[name]), "classes.json")))
+            meta = cj["classes"]
+            ptx = json.load(open(os.path.join(os.path.dirname(paths[name]), "ptxas.json")))
+        else:
+            meta = json.load(open(os.path.join(ROOT, "electron_repulsion_integrals_gb300", "csrc", "generated",
+                                               "classes.json")))["classes"]
+            meta = {"{}{}{}{}".format(*m["cls"]) if isinstance(m, dict) and "cls" in m else k: m
+                    for k, m in (meta.items() if isinstance(meta, dict) else enumerate(meta))}
+            ptx = json.load(open(os.path.join(os.path.dirname(eri.LIB_PATH), "ptxas.json")))
+        for c, v in res.items():
+            m = meta.get(c, {})
+            v.update({k: m.get(k) for k in ("peak_live", "schedule", "rule", "shape", "sph_fusion", "arena")
+                      if k in m})
+            kern = [k for k in ptx if f"k_c{c}I" in k and "ILi0E" in k]
+            if kern:
+                v["registers"] = max(ptx[k].get("registers", 0) for k in kern)
+                v["spill_bytes"] = max(ptx[k].get("spill_stores", 0) + ptx[k].get("spill_loads", 0) for k in kern)
+        out["libraries"][name] = res
+    full = out["libraries"].get("full", {})
+    out["speedup_vs_full"] = {name: {c: v["quartets_per_s"] / full[c]["quartets_per_s"]
+                                     for c, v in lib.items() if c in full and "quartets_per_s" in v}
+                              for name, lib in out["libraries"].items() if name != "full" and "error" not in lib}
+    print(json.dumps(out), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -502,7 +619,15 @@ def main():
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--ref-budget", type=float, default=12.0, help="seconds of oracle work per sample")
+    ap.add_argument("--ablation", default=None, help="'all' or comma-separated ablation libraries to time")
+    ap.add_argument("--ablation-worker", default=None, help=argparse.SUPPRESS)
     a = ap.parse_args()
+    if a.ablation_worker:
+        run_ablation_worker(a)
+        return
+    if a.ablation:
+        run_ablation(a)
+        return
     rank = env_int("RANK", 0)
     world = env_int("WORLD_SIZE", 1)
     local_rank = env_int("LOCAL_RANK", 0)

@@ -50,13 +50,16 @@ class ClassStats(ctypes.Structure):
 
 
 def lib():
-    """The loaded liberi.so (raises if it has not been built)."""
+    """The loaded liberi.so (raises if it has not been built).  The environment
+    variable ERI_GB300_LIBRARY may name another build of the same C ABI (the
+    ablation libraries of build.build_variant)."""
     global _lib
     if _lib is None:
-        if not os.path.exists(LIB_PATH):
-            raise RuntimeError(f"liberi.so not found at {LIB_PATH}; run `python -m electron_repulsion_integrals_gb300.build` "
+        path = os.environ.get("ERI_GB300_LIBRARY") or LIB_PATH
+        if not os.path.exists(path):
+            raise RuntimeError(f"liberi.so not found at {path}; run `python -m electron_repulsion_integrals_gb300.build` "
                                "(there is no CPU fallback)")
-        L = ctypes.CDLL(LIB_PATH)
+        L = ctypes.CDLL(path)
         vp, ip, dp = ctypes.c_void_p, ctypes.POINTER(ctypes.c_int), ctypes.c_void_p
         L.eri_plan_create.argtypes = [vp, ctypes.c_int, ctypes.POINTER(_Options), vp, ctypes.POINTER(vp)]
         L.eri_plan_create_flat.argtypes = [ctypes.c_int, vp, vp, vp, vp, vp, ctypes.POINTER(_Options), vp,

@@ -45,14 +45,15 @@ def _headers_mtime():
     return max(os.path.getmtime(h) for h in hs if os.path.exists(h))
 
 
-def _compile(src, force):
-    rel = os.path.relpath(src, CSRC).replace(os.sep, "_")
-    obj = os.path.join(BUILD, "obj", rel + ".o")
+def _compile(src, force, objdir=None, extra=()):
+    rel = os.path.relpath(src, CSRC).replace(os.sep, "_") if objdir is None else os.path.basename(src)
+    obj = os.path.join(objdir or os.path.join(BUILD, "obj"), rel + ".o")
     log = obj + ".ptxas.txt"
     if not force and os.path.exists(obj) and os.path.getmtime(obj) >= max(os.path.getmtime(src), _headers_mtime()):
         return obj, None
     os.makedirs(os.path.dirname(obj), exist_ok=True)
-    cmd = [nvcc()] + ARCH + FLAGS + ["-I", INCLUDE, "-c", src, "-o", obj + ".tmp"]
+    cmd = [nvcc()] + ARCH + FLAGS + ["-I", INCLUDE, "-I", os.path.join(CSRC, "generated")] + list(extra) + \
+        ["-c", src, "-o", obj + ".tmp"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc failed for {src}:\n{r.stderr[-6000:]}")
@@ -115,6 +116,74 @@ def build(force: bool = False, jobs: int | None = None, verbose: bool = False) -
     with open(os.path.join(BUILD, "ptxas.json"), "w") as f:
         json.dump(report, f, indent=1, sort_keys=True)
     return LIB
+
+
+def build_variant(name: str, entries, force: bool = False, jobs: int | None = None) -> str:
+    """Build a complete library over another set of class kernels: `entries`
+    lists (class, opts) pairs, each class emitted with the generator switches
+    `opts` (see gen.emit.emit_class; {"tier": "coop"} emits the cooperative
+    tier).  Used to measure one design choice at a time (the ablations of
+    FusionRCG section V-B, where every variant is compiled as a complete
+    library).  Returns the path of _build/variants/<name>/liberi.so."""
+    from .gen.emit import emit_class
+    from .gen.coop import emit_coop_class
+    vdir = os.path.join(BUILD, "variants", name)
+    gdir = os.path.join(vdir, "generated")
+    os.makedirs(gdir, exist_ok=True)
+    stats = {}
+    srcs = []
+    classes = [tuple(c) for c, _ in entries]
+    for cls, opts in entries:
+        cls = tuple(cls)
+        if opts.get("tier") == "coop":
+            src, meta = emit_coop_class(cls)
+        else:
+            src, meta = emit_class(cls, **opts)
+        path = os.path.join(gdir, "c{}{}{}{}.cu".format(*cls))
+        if not os.path.exists(path) or open(path).read() != src:
+            with open(path, "w") as f:
+                f.write(src)
+        srcs.append(path)
+        stats["{}{}{}{}".format(*cls)] = meta
+    reg = os.path.join(gdir, "registry.inc")
+    text = "".join("ERI_CLASS({}, {}, {}, {})\n".format(*c) for c in classes)
+    if not os.path.exists(reg) or open(reg).read() != text:
+        with open(reg, "w") as f:
+            f.write(text)
+    with open(os.path.join(vdir, "classes.json"), "w") as f:
+        json.dump({"entries": [[list(c), o] for c, o in entries], "classes": stats}, f, indent=1, sort_keys=True,
+                  default=str)
+    runtime = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    objdir = os.path.join(vdir, "obj")
+    extra = ["-DERI_REGISTRY_INC=\"" + reg + "\""]
+    jobs = jobs or max(1, min(len(srcs) + len(runtime), os.cpu_count() or 4))
+    objs = []
+    with cf.ThreadPoolExecutor(jobs) as ex:
+        futs = [ex.submit(_compile, s_, force or s_ in runtime and _newer(reg, s_, objdir), objdir,
+                          extra if s_ in runtime else ()) for s_ in runtime + srcs]
+        for fu in futs:
+            objs.append(fu.result()[0])
+    lib = os.path.join(vdir, "liberi.so")
+    if force or not os.path.exists(lib) or os.path.getmtime(lib) < max(os.path.getmtime(o) for o in objs):
+        tmp = lib + ".tmp%d" % os.getpid()
+        r = subprocess.run([nvcc()] + ARCH + ["-shared", "-o", tmp] + objs + ["-lcudart"], capture_output=True,
+                           text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"link failed:\n{r.stderr[-4000:]}")
+        os.replace(tmp, lib)
+    report = {}
+    for log in glob.glob(os.path.join(objdir, "*.ptxas.txt")):
+        with open(log) as f:
+            report.update(parse_ptxas(f.read()))
+    with open(os.path.join(vdir, "ptxas.json"), "w") as f:
+        json.dump(report, f, indent=1, sort_keys=True)
+    return lib
+
+
+def _newer(path, src, objdir):
+    """True when `path` changed after the object of `src` in `objdir` was built."""
+    obj = os.path.join(objdir, os.path.basename(src) + ".o")
+    return not os.path.exists(obj) or os.path.getmtime(path) > os.path.getmtime(obj)
 
 
 def main():

@@ -83,7 +83,8 @@ __device__ __forceinline__ void coop_setup_one(const EriLaunch& P, const Quartet
 }
 
 // VRR of one primitive quartet with parameters s[] into the arena; targets
-// accumulated into H (global, [target column][e - e_la]).
+// accumulated into H (global, [target column][e - e_lo], e_lo the first
+// component with |e| = min(la, lb)).
 template <class C>
 __device__ __forceinline__ void coop_vrr(double* __restrict__ arena, const double* __restrict__ s,
                                          double* __restrict__ H, int lane, bool first) {
@@ -126,10 +127,10 @@ __device__ __forceinline__ void coop_vrr(double* __restrict__ arena, const doubl
     }
     __syncwarp();
   }
-  if constexpr (C::lc == 0) {
+  if constexpr (C::LCMIN == 0) {
     // column 0 is a target column (ket component (0,0,0))
     for (int k = lane; k < C::NET; k += 32) {
-      const double v = bra[C::IE_LA + k];
+      const double v = bra[C::IE_LO + k];
       H[k] = first ? v : H[k] + v;
     }
   }
@@ -242,7 +243,7 @@ __device__ __forceinline__ void coop_vrr(double* __restrict__ arena, const doubl
       for (int j = 0; j < kHT; ++j) {
         const int k = lane + 32 * j;
         if (k < C::NET) {
-          const double v = O[C::IE_LA + k];
+          const double v = O[C::IE_LO + k];
           Ht[k] = first ? v : hold[j] + v;
         }
       }
@@ -253,9 +254,11 @@ __device__ __forceinline__ void coop_vrr(double* __restrict__ arena, const doubl
 
 }  // namespace eri
 
-// Kernel body shared by every cooperative class.  C: traits; BRA_HRR(fi, Hc, G)
-// and KET_HRR(r, Gr) are the generated per-column / per-row HRR functions.
-#define ERI_COOP_KERNEL(NAME, C, BRA_FN, KET_FN)                                                          \
+// Kernel body shared by every cooperative class.  C: traits; BRA_FN / KET_FN
+// are the generated per-column / per-row HRR functions and BRA_REV_FN /
+// KET_REV_FN their reversed forms (pair evaluated with the VRR on its
+// lower-l shell; the same functions when la == lb / lc == ld).
+#define ERI_COOP_KERNEL(NAME, C, BRA_FN, BRA_REV_FN, KET_FN, KET_REV_FN)                                                        \
   template <int MODE, bool CONTRACTED>                                                                    \
   __global__ void __launch_bounds__(kCoopThreads) NAME(const EriLaunch P) {                               \
     extern __shared__ double smem_[];                                                                     \
@@ -271,7 +274,7 @@ __device__ __forceinline__ void coop_vrr(double* __restrict__ arena, const doubl
       if constexpr (MODE == kCoulomb) {                                                                   \
         load_quartet_coulomb(P, q, Q);                                                                    \
       } else {                                                                                            \
-        load_quartet<C::la == C::lb, C::lc == C::ld>(P, q, Q);                                            \
+        load_quartet<C::la == C::lb ? 1 : 2, C::lc == C::ld ? 1 : 2, C::La, C::Lc>(P, q, Q);                \
       }                                                                                                   \
       const int nab = MODE == kCoulomb ? Q.nab : Q.na * Q.nb;                                             \
       const int ncd = MODE == kCoulomb ? Q.ncd : Q.nc * Q.nd;                                             \
@@ -287,10 +290,17 @@ __device__ __forceinline__ void coop_vrr(double* __restrict__ arena, const doubl
       }                                                                                                   \
       /* HRR bra + T x T: one lane per ket column; G[r][f] in the arena */                               \
       double* G = arena;                                                                                  \
-      for (int fi = lane; fi < C::NF; fi += 32) BRA_FN(Q, H, fi, G);                                      \
+      /* columns below |f| = lc feed only the reversed ket HRR */                                         \
+      for (int fi = (Q.rk ? 0 : C::FI_LC) + lane; fi < C::NF; fi += 32) {                                 \
+        if (Q.rb) BRA_REV_FN(Q, H, fi, G);                                                                \
+        else BRA_FN(Q, H, fi, G);                                                                         \
+      }                                                                                                   \
       __syncwarp();                                                                                       \
       double smax_ = 0.0;                                                                                 \
-      for (int r = lane; r < C::NR; r += 32) KET_FN<MODE>(P, Q, q, r, G, smax_);                          \
+      for (int r = lane; r < C::NR; r += 32) {                                                            \
+        if (Q.rk) KET_REV_FN<MODE>(P, Q, q, r, G, smax_);                                                 \
+        else KET_FN<MODE>(P, Q, q, r, G, smax_);                                                          \
+      }                                                                                                   \
       if constexpr (MODE == kSchwarz) {                                                                   \
         _Pragma("unroll") for (int o = 16; o > 0; o >>= 1) smax_ = fmax(smax_, __shfl_xor_sync(0xffffffffu, smax_, o)); \
         if (lane == 0) P.q_out[q] = sqrt(smax_);                                                          \

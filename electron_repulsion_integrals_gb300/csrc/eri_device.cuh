@@ -106,9 +106,11 @@ struct EriLaunch {
   int ostr[4];           // stride of canonical axis k in the requested block layout
   // Schwarz mode: q_out[i] = sqrt(max diag |(ab|ab)|) of quartet i
   double* q_out;
-  // Coulomb mode: quartet t of the class is found through the segment list;
-  // segment k covers work items [seg_start[k], seg_start[k+1]) = bra pair
-  // segs[k].x with ket pairs segs[k].y .. segs[k].y + segs[k].z - 1.
+  // Coulomb mode: work item t of the class is found through the segment list;
+  // segment k covers work items [seg_start[k], seg_start[k+1]): bra pair
+  // segs[k].x with ket pairs segs[k].y .. segs[k].y + segs[k].z - 1, each
+  // quartet cut into sb x sk items (segs[k].w = sb | sk << 16) that take the
+  // sb-th and sk-th parts of its bra and ket primitive pairs.
   const double* D;       // density, nbf x nbf row-major
   double* J;             // accumulator, nbf x nbf row-major (pair-oriented blocks)
   double* K;             // exchange mode: accumulator T with K = T + T^T
@@ -142,36 +144,53 @@ struct Quartet {
   // Coulomb mode
   int bra, ket;       // pair ids
   int pab, nab, pcd, ncd;
+  int iab0, iab1, icd0, icd1;  // primitive pairs of this work item: [iab0, iab1) x [icd0, icd1)
   int fa, fb, fc, fd;  // first basis functions of the four shells
   double fab, fcd;     // 2 for a pair of distinct shells, else 1
   double wk;           // 1 / (number of the 8 index permutations that leave the quartet unchanged)
   int ost[4];          // store mode: output stride of canonical axes a, b, c, d
+  int rb, rk;          // cooperative tier: bra / ket pair reversed (VRR on the lower-l shell)
 };
 
-// Which shell of a pair of equal angular momentum should carry the VRR.  The
-// HRR of Eq. (3) rebuilds (ab| from [e0| functions of x_A; when A's Gaussians
-// are diffuse and B's tight and the centers far apart, the product center P
-// lies near B, the [e0| grow like |P-A|^(la+lb) and the HRR cancels them back
-// down, losing many digits.  Building on the center P lies closest to keeps
-// the intermediates at the size of the result.  Over all primitive pairs,
-// |P - A| / |AB| is at most beta_max/(alpha_min + beta_max) and |P - B| / |AB|
-// at most alpha_max/(alpha_max + beta_min); returns true when B is the better
-// VRR center.  (A heuristic decision: FP32 is enough.)
+// Which shell of a pair (total angular momentum N = la + lb) should carry the
+// VRR.  The HRR of Eq. (3) rebuilds (ab| from [e0| functions of x_A; when the
+// product centers P lie far from A the [e0| grow like |P-A|^N and the HRR cancels
+// them back down, losing digits (FP64 keeps the error small only while those
+// intermediates stay near the size of the result).  Each primitive pair
+// weighs in with its size, |c_u c_v| exp(-alpha beta/zeta |AB|^2) zeta^(-3/2)
+// (c: the normalised coefficients), times (|P-A|/|AB|)^N = (beta/zeta)^N for a
+// VRR on A or (alpha/zeta)^N for one on B; returns true when the sum for B is
+// the smaller.  A heuristic decision: FP32 is enough (an underflow of every
+// weight keeps A).
+template <int N>
 __device__ __forceinline__ bool second_is_better_center(const ShellsDev& sh, int a, int b) {
   const int pa = __ldg(sh.poff + a), na = __ldg(sh.nprim + a);
   const int pb = __ldg(sh.poff + b), nb = __ldg(sh.nprim + b);
-  float amin = 3.0e38f, amax = 0.0f, bmin = 3.0e38f, bmax = 0.0f;
+  float r2 = 0.0f;
+#pragma unroll
+  for (int x = 0; x < 3; ++x) {
+    const float d = (float)(__ldg(sh.cen + 3 * a + x) - __ldg(sh.cen + 3 * b + x));
+    r2 = fmaf(d, d, r2);
+  }
+  float sa = 0.0f, sb = 0.0f;
   for (int i = 0; i < na; ++i) {
-    const float x = (float)__ldg(sh.exps + pa + i);
-    amin = fminf(amin, x);
-    amax = fmaxf(amax, x);
+    const float al = (float)__ldg(sh.exps + pa + i), ca = fabsf((float)__ldg(sh.coef + pa + i));
+    for (int j = 0; j < nb; ++j) {
+      const float be = (float)__ldg(sh.exps + pb + j), cb = fabsf((float)__ldg(sh.coef + pb + j));
+      const float iz = 1.0f / (al + be);
+      const float w = ca * cb * expf(-al * be * iz * r2) * iz * sqrtf(iz);
+      const float ua = be * iz, ub = al * iz;
+      float pa2 = 1.0f, pb2 = 1.0f;
+#pragma unroll
+      for (int k = 0; k < N; ++k) {
+        pa2 *= ua;
+        pb2 *= ub;
+      }
+      sa = fmaf(w, pa2, sa);
+      sb = fmaf(w, pb2, sb);
+    }
   }
-  for (int i = 0; i < nb; ++i) {
-    const float x = (float)__ldg(sh.exps + pb + i);
-    bmin = fminf(bmin, x);
-    bmax = fmaxf(bmax, x);
-  }
-  return amax / (amax + bmin) < bmax / (amin + bmax);
+  return sb < sa;
 }
 
 __device__ __forceinline__ void load_shell_center(const ShellsDev& sh, int s, double* c) {
@@ -180,10 +199,14 @@ __device__ __forceinline__ void load_shell_center(const ShellsDev& sh, int s, do
   c[2] = __ldg(sh.cen + 3 * s + 2);
 }
 
-// SYM_AB / SYM_CD: the class has la == lb / lc == ld, so the two shells of that
-// pair may be exchanged (with their output strides) to put the VRR on the
-// better-conditioned center.
-template <bool SYM_AB, bool SYM_CD>
+// OAB / OCD: what may happen to the bra / ket pair (NAB = la + lb, NCD = lc + ld):
+//   0  nothing;
+//   1  (la == lb) the two shells are exchanged together with their output
+//      strides when the second is the better VRR center;
+//   2  (cooperative tier, la != lb) the shells are exchanged but not the
+//      strides, and Q.rb / Q.rk is set: the kernel then runs the VRR on the
+//      lower-l shell and the reversed HRR, which writes canonical order.
+template <int OAB, int OCD, int NAB, int NCD>
 __device__ __forceinline__ void load_quartet(const EriLaunch& P, long long q, Quartet& Q) {
   const int4 r = __ldg(reinterpret_cast<const int4*>(P.quartets) + q);
   const int req[4] = {r.x, r.y, r.z, r.w};
@@ -193,21 +216,31 @@ __device__ __forceinline__ void load_quartet(const EriLaunch& P, long long q, Qu
     Q.s[k] = c == 0 ? req[0] : c == 1 ? req[1] : c == 2 ? req[2] : req[3];
     Q.ost[k] = P.ostr[k];
   }
-  if (SYM_AB && Q.s[0] != Q.s[1] && second_is_better_center(P.sh, Q.s[0], Q.s[1])) {
+  Q.rb = 0;
+  Q.rk = 0;
+  if (OAB != 0 && Q.s[0] != Q.s[1] && second_is_better_center<NAB>(P.sh, Q.s[0], Q.s[1])) {
     const int t = Q.s[0];
     Q.s[0] = Q.s[1];
     Q.s[1] = t;
-    const int u = Q.ost[0];
-    Q.ost[0] = Q.ost[1];
-    Q.ost[1] = u;
+    if (OAB == 1) {
+      const int u = Q.ost[0];
+      Q.ost[0] = Q.ost[1];
+      Q.ost[1] = u;
+    } else {
+      Q.rb = 1;
+    }
   }
-  if (SYM_CD && Q.s[2] != Q.s[3] && second_is_better_center(P.sh, Q.s[2], Q.s[3])) {
+  if (OCD != 0 && Q.s[2] != Q.s[3] && second_is_better_center<NCD>(P.sh, Q.s[2], Q.s[3])) {
     const int t = Q.s[2];
     Q.s[2] = Q.s[3];
     Q.s[3] = t;
-    const int u = Q.ost[2];
-    Q.ost[2] = Q.ost[3];
-    Q.ost[3] = u;
+    if (OCD == 1) {
+      const int u = Q.ost[2];
+      Q.ost[2] = Q.ost[3];
+      Q.ost[3] = u;
+    } else {
+      Q.rk = 1;
+    }
   }
   load_shell_center(P.sh, Q.s[0], Q.A);
   load_shell_center(P.sh, Q.s[1], Q.B);
@@ -240,8 +273,13 @@ __device__ __forceinline__ void load_quartet_coulomb(const EriLaunch& P, long lo
     else hi = mid - 1;
   }
   const int4 sg = __ldg(P.segs + lo);
+  const int sb = sg.w & 0xffff, sk = sg.w >> 16;
+  const long long u = t - __ldg(P.seg_start + lo);
+  const long long qo = u / (sb * sk);
+  const int ch = (int)(u - qo * (sb * sk));
+  const int cb = ch / sk, ck = ch - cb * sk;
   Q.bra = sg.x;
-  Q.ket = sg.y + (int)(t - __ldg(P.seg_start + lo));
+  Q.ket = sg.y + (int)qo;
   const PairMeta* mb = P.pairs + Q.bra;
   const PairMeta* mk = P.pairs + Q.ket;
   Q.s[0] = __ldg(&mb->a);
@@ -252,6 +290,10 @@ __device__ __forceinline__ void load_quartet_coulomb(const EriLaunch& P, long lo
   Q.nab = __ldg(&mb->np);
   Q.pcd = __ldg(&mk->poff);
   Q.ncd = __ldg(&mk->np);
+  Q.iab0 = cb * Q.nab / sb;
+  Q.iab1 = (cb + 1) * Q.nab / sb;
+  Q.icd0 = ck * Q.ncd / sk;
+  Q.icd1 = (ck + 1) * Q.ncd / sk;
 #pragma unroll
   for (int x = 0; x < 3; ++x) {
     Q.AB[x] = __ldg(&mb->AB[x]);
@@ -264,6 +306,8 @@ __device__ __forceinline__ void load_quartet_coulomb(const EriLaunch& P, long lo
   Q.fab = Q.s[0] != Q.s[1] ? 2.0 : 1.0;
   Q.fcd = Q.s[2] != Q.s[3] ? 2.0 : 1.0;
   Q.wk = (Q.s[0] == Q.s[1] ? 0.5 : 1.0) * (Q.s[2] == Q.s[3] ? 0.5 : 1.0) * (Q.bra == Q.ket ? 0.5 : 1.0);
+  Q.rb = 0;
+  Q.rk = 0;
 }
 
 // Gaussian product of two primitives (alpha at A, beta at B):
@@ -342,11 +386,13 @@ __device__ __forceinline__ void quartet_setup(const PrimPair& pb, const PrimPair
 // has exactly one primitive and the loops disappear.
 #define PRIM_LOOP_BEGIN(P, Q)                                                                              \
   {                                                                                                        \
-    const int nab_ = MODE >= kCoulomb ? Q.nab : CONTRACTED ? Q.na * Q.nb : 1;                              \
-    const int ncd_ = MODE >= kCoulomb ? Q.ncd : CONTRACTED ? Q.nc * Q.nd : 1;                              \
+    const int ab0_ = MODE >= kCoulomb ? Q.iab0 : 0;                                                        \
+    const int nab_ = MODE >= kCoulomb ? Q.iab1 : CONTRACTED ? Q.na * Q.nb : 1;                             \
+    const int cd0_ = MODE >= kCoulomb ? Q.icd0 : 0;                                                        \
+    const int ncd_ = MODE >= kCoulomb ? Q.icd1 : CONTRACTED ? Q.nc * Q.nd : 1;                             \
     double qk0_ = 0.0;                                                                                     \
-    if constexpr (MODE >= kCoulomb) qk0_ = __ldg(P.prims + (size_t)Q.pcd * kPrimRec + 9);                  \
-    for (int iab_ = 0; iab_ < nab_; ++iab_) {                                                              \
+    if constexpr (MODE >= kCoulomb) qk0_ = __ldg(P.prims + (size_t)(Q.pcd + cd0_) * kPrimRec + 9);         \
+    for (int iab_ = ab0_; iab_ < nab_; ++iab_) {                                                           \
       PrimPair pb;                                                                                         \
       if constexpr (MODE >= kCoulomb) {                                                                    \
         load_prim(P.prims, Q.pab + iab_, pb);                                                              \
@@ -356,7 +402,7 @@ __device__ __forceinline__ void quartet_setup(const PrimPair& pb, const PrimPair
         make_pair(__ldg(P.sh.exps + Q.pa + i_), __ldg(P.sh.coef + Q.pa + i_), __ldg(P.sh.exps + Q.pb + j_), \
                   __ldg(P.sh.coef + Q.pb + j_), Q.A, Q.AB, Q.rAB2, pb);                                    \
       }                                                                                                    \
-      for (int icd_ = 0; icd_ < ncd_; ++icd_) {                                                            \
+      for (int icd_ = cd0_; icd_ < ncd_; ++icd_) {                                                         \
         PrimPair pk;                                                                                       \
         if constexpr (MODE >= kCoulomb) {                                                                  \
           load_prim(P.prims, Q.pcd + icd_, pk);                                                            \

@@ -27,6 +27,7 @@ const int* plan_fo(const eri_plan* p);
 const int* plan_poff(const eri_plan* p);
 const double* plan_centers(const eri_plan* p);
 const double* plan_exps(const eri_plan* p);
+const double* plan_coefs(const eri_plan* p);  // the caller's raw contraction coefficients
 int plan_nsm(const eri_plan* p);
 int* plan_dfo(const eri_plan* p);
 screen::Screen*& plan_screen(eri_plan* p);

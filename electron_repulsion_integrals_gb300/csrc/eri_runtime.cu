@@ -21,12 +21,17 @@
 using namespace eri;
 
 // ------------------------------------------------------------------ registry
+// The class list: generated/registry.inc, or the file ERI_REGISTRY_INC names
+// (a quoted path) when a library is built over another set of class kernels.
+#ifndef ERI_REGISTRY_INC
+#define ERI_REGISTRY_INC "generated/registry.inc"
+#endif
 #define ERI_CLASS(a, b, c, d)                                                                   \
   extern "C" int eri_launch_c##a##b##c##d(const EriLaunch*, int, int, int, cudaStream_t);       \
   extern "C" int eri_slots_c##a##b##c##d();                                                     \
   extern "C" int eri_grid_c##a##b##c##d(int, long long, long long*, long long*);                \
   extern "C" void eri_stats_c##a##b##c##d(long long*);
-#include "generated/registry.inc"
+#include ERI_REGISTRY_INC
 #undef ERI_CLASS
 
 namespace {
@@ -42,7 +47,7 @@ struct ClassEntry {
 const ClassEntry kClasses[] = {
 #define ERI_CLASS(a, b, c, d) \
   {{a, b, c, d}, eri_launch_c##a##b##c##d, eri_slots_c##a##b##c##d, eri_stats_c##a##b##c##d, eri_grid_c##a##b##c##d},
-#include "generated/registry.inc"
+#include ERI_REGISTRY_INC
 #undef ERI_CLASS
 };
 
@@ -334,6 +339,7 @@ const int* eri::host::plan_nprim(const eri_plan* p) { return p->hnprim.data(); }
 const int* eri::host::plan_fo(const eri_plan* p) { return p->hfo.data(); }
 const double* eri::host::plan_centers(const eri_plan* p) { return p->hcen.data(); }
 const double* eri::host::plan_exps(const eri_plan* p) { return p->hexps.data(); }
+const double* eri::host::plan_coefs(const eri_plan* p) { return p->hcoef.data(); }
 const int* eri::host::plan_poff(const eri_plan* p) { return p->hpoff.data(); }
 int eri::host::plan_nsm(const eri_plan* p) { return p->nsm; }
 int* eri::host::plan_dfo(const eri_plan* p) { return p->dfo; }

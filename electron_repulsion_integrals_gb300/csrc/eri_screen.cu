@@ -38,6 +38,14 @@ using namespace eri;
 
 namespace {
 
+// Largest number of primitive quartets one thread evaluates for one work item
+// of the J/K build.  A contracted quartet of 6-primitive shells has 1,296; run
+// by one thread it would set the kernel's critical path (one FP64 instruction
+// per dependent-latency interval, ~64 cycles) long after the other threads
+// are done.  Digestion is linear in the integrals, so each part of a quartet
+// is transformed and scattered on its own.
+constexpr long long kMaxPrimPerItem = 64;
+
 #define CUDA_TRY(x)                                                        \
   do {                                                                     \
     cudaError_t e_ = (x);                                                  \
@@ -117,7 +125,8 @@ struct DevBuf {
 struct ClassWork {
   int l[4];
   int nseg = 0;
-  long long total = 0;
+  long long total = 0;    // unique shell quartets
+  long long items = 0;    // work items (quartets cut into primitive chunks)
   double prim_total = 0;  // primitive quartets evaluated (after pruning)
   int4* dsegs = nullptr;
   long long* dstart = nullptr;
@@ -195,19 +204,25 @@ int build(eri_plan* p, cudaStream_t st) {
   std::vector<std::vector<int2>> pc(npc);
   const double* ex = eri::host::plan_exps(p);
   const int* po = eri::host::plan_poff(p);
-  // equal-L pairs carry the VRR on the center the Gaussian products lie
-  // closest to (see second_is_better_center in eri_device.cuh)
+  // equal-L pairs carry the VRR on the better-conditioned center, by the
+  // weighting of second_is_better_center in eri_device.cuh (here with the
+  // caller's coefficients times the primitive norms alpha^((2l+3)/4): the
+  // contraction's own normalisation is common to both sums)
+  const double* cf = eri::host::plan_coefs(p);
   auto second_better = [&](int a, int b) {
-    double amin = 1e300, amax = 0, bmin = 1e300, bmax = 0;
-    for (int i = 0; i < np[a]; ++i) {
-      amin = std::min(amin, ex[po[a] + i]);
-      amax = std::max(amax, ex[po[a] + i]);
-    }
-    for (int i = 0; i < np[b]; ++i) {
-      bmin = std::min(bmin, ex[po[b] + i]);
-      bmax = std::max(bmax, ex[po[b] + i]);
-    }
-    return amax / (amax + bmin) < bmax / (amin + bmax);
+    const int l = L[a];
+    double r2 = 0;
+    for (int x = 0; x < 3; ++x) r2 += (cen[3 * a + x] - cen[3 * b + x]) * (cen[3 * a + x] - cen[3 * b + x]);
+    double sa = 0, sb = 0;
+    for (int i = 0; i < np[a]; ++i)
+      for (int j = 0; j < np[b]; ++j) {
+        const double al = ex[po[a] + i], be = ex[po[b] + j], iz = 1.0 / (al + be);
+        const double w = std::fabs(cf[po[a] + i] * cf[po[b] + j]) * std::pow(al * be, (2 * l + 3) / 4.0) *
+                         std::exp(-al * be * iz * r2) * iz * std::sqrt(iz);
+        sa += w * std::pow(be * iz, 2 * l);
+        sb += w * std::pow(al * iz, 2 * l);
+      }
+    return sb < sa;
   };
   for (int a = 0; a < ns; ++a)
     for (int b = 0; b < ns; ++b) {
@@ -370,7 +385,17 @@ int build(eri_plan* p, cudaStream_t st) {
                 }
                 if (cb == ck && gk.first <= i && i < gk.first + gk.count) cnt = std::min(cnt, i - gk.first + 1);
                 if (cnt <= 0) continue;
-                segs.push_back(make_int4(i, gk.first, cnt, 0));
+                // cut heavy quartets into work items of at most kMaxPrimPerItem
+                // primitive quartets: sb parts of the bra primitive pairs,
+                // then sk parts of the ket ones
+                int sb = 1, sk = 1;
+                if ((long long)gb.K * gk.K > kMaxPrimPerItem) {
+                  sb = (int)std::min<long long>(gb.K, ((long long)gb.K * gk.K + kMaxPrimPerItem - 1) / kMaxPrimPerItem);
+                  const long long per_b = (gb.K + sb - 1) / sb;
+                  if (per_b * gk.K > kMaxPrimPerItem)
+                    sk = (int)std::min<long long>(gk.K, (per_b * gk.K + kMaxPrimPerItem - 1) / kMaxPrimPerItem);
+                }
+                segs.push_back(make_int4(i, gk.first, cnt, sb | (sk << 16)));
                 cost.push_back((long long)gb.K * gk.K);
                 kb_of.push_back(gb.K);
                 kk_of.push_back(gk.K);
@@ -393,14 +418,17 @@ int build(eri_plan* p, cudaStream_t st) {
           std::vector<int4> so(segs.size());
           std::vector<long long> start(segs.size() + 1);
           long long t = 0;
+          long long nq = 0;
           for (size_t k = 0; k < ord.size(); ++k) {
             so[k] = segs[ord[k]];
             start[k] = t;
-            t += so[k].z;
+            t += (long long)so[k].z * (so[k].w & 0xffff) * (so[k].w >> 16);
+            nq += so[k].z;
           }
           start[segs.size()] = t;
           W.nseg = (int)segs.size();
-          W.total = t;
+          W.total = nq;
+          W.items = t;
           CUDA_TRY(cudaMalloc(&W.dsegs, so.size() * sizeof(int4)));
           CUDA_TRY(cudaMalloc(&W.dstart, start.size() * sizeof(long long)));
           CUDA_TRY(cudaMemcpyAsync(W.dsegs, so.data(), so.size() * sizeof(int4), cudaMemcpyHostToDevice, st));
@@ -446,7 +474,7 @@ int build_digest(eri_plan* p, const double* D, double* J, double* K, cudaStream_
     if (W.total == 0) continue;
     EriLaunch P;
     std::memset(&P, 0, sizeof(P));
-    P.n = W.total;
+    P.n = W.items;
     P.D = D;
     P.J = S->Jacc;
     P.K = K ? S->Kacc : nullptr;

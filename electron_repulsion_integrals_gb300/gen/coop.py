@@ -21,11 +21,18 @@ divergence.  Columns live in a per-warp shared-memory arena; the order of the
 column steps (depth first along the axis chains) and a first-fit allocator
 keep the live arena small, e.g. 29 KB for (ff|ff).
 
-Targets [e|g]^(0), |e| >= la, |g| >= lc, are added to per-warp accumulators in
-global memory (L2-resident) as soon as column g is complete.  After the
-primitive loop the bra HRR + spherical transform runs with one lane per ket
-column and the ket HRR + transform with one lane per bra row (straight-line
-code from the register-tier emitter).
+Targets [e|g]^(0), |e| >= min(la, lb), |g| >= min(lc, ld), are added to
+per-warp accumulators in global memory (L2-resident) as soon as column g is
+complete.  After the primitive loop the bra HRR + spherical transform runs with
+one lane per ket column and the ket HRR + transform with one lane per bra row
+(straight-line code from the register-tier emitter).
+
+A pair of unequal angular momenta may also be evaluated reversed: the shells
+exchanged so that the VRR runs on the lower-l one (the better-conditioned
+center for a tight lower-l shell opposite a diffuse higher-l one), hence the
+target range from min(la, lb), and the HRR of Eq. (3) run for (lb, la),
+writing the block back in canonical order.  The choice is made per quartet,
+the same on every lane of the warp.
 """
 
 from __future__ import annotations
@@ -72,8 +79,8 @@ class CoopPlan:
     L: int
     NE: int                    # bra components |e| <= La
     e_list: list
-    ie_la: int                 # first e with |e| >= la (targets)
-    f_targets: list            # ket components with |f| in [lc, Lc]
+    ie_lo: int                 # first e with |e| >= min(la, lb) (targets)
+    f_targets: list            # ket components with |f| in [min(lc, ld), Lc]
     bra_nodes_y: list = field(default_factory=list)    # per level: list of (out, x, y, axis, ky)
     bra_nodes_n: list = field(default_factory=list)    # per level: list of (out, x, axis)
     cols: list = field(default_factory=list)
@@ -92,10 +99,11 @@ def plan(cls):
     e_list = [e for k in range(La + 1) for e in cart_list(k)]
     eidx = {e: i for i, e in enumerate(e_list)}
     NE = len(e_list)
-    ie_la = sum(ncart(k) for k in range(la))
-    f_targets = [f for j in range(lc, Lc + 1) for f in cart_list(j)]
+    ie_lo = sum(ncart(k) for k in range(min(la, lb)))
+    lcmin = min(lc, ld)
+    f_targets = [f for j in range(lcmin, Lc + 1) for f in cart_list(j)]
     fidx = {f: i for i, f in enumerate(f_targets)}
-    P = CoopPlan(tuple(cls), La, Lc, L, NE, e_list, ie_la, f_targets)
+    P = CoopPlan(tuple(cls), La, Lc, L, NE, e_list, ie_lo, f_targets)
     ops = 0
     # ---- bra part (column 0): level k nodes (m, e), |e| = k, m <= L - k
     for k in range(1, La + 1):
@@ -191,7 +199,7 @@ def plan(cls):
             i, f, h = src[g]
             j = sum(g)
             st = ColStep(g, j, i, f[i], where[g], where[f], where[h] if h is not None else -1,
-                         fidx.get(g, -1) if j >= lc else -1)
+                         fidx.get(g, -1) if j >= lcmin else -1)
             P.cols.append(st)
             rows = Lc - j + 1
             nz = len(P.zlist[i])
@@ -229,7 +237,7 @@ def emit_coop_class(cls):
     la, lb, lc, ld = cls
     cname = E.class_name(cls)
     NE, La, Lc, L = P.NE, P.La, P.Lc, P.L
-    NET = NE - P.ie_la
+    NET = NE - P.ie_lo
     NF = len(P.f_targets)
     nsa, nsb, nsc, nsd = (len(cart2sph(l)) for l in cls)
     NR = nsa * nsb
@@ -272,7 +280,9 @@ def emit_coop_class(cls):
     T = f"Traits_{cname}"
     w(f"struct {T} {{")
     w(f"  static constexpr int la = {la}, lb = {lb}, lc = {lc}, ld = {ld}, La = {La}, Lc = {Lc}, L = {L};")
-    w(f"  static constexpr int NE = {NE}, NET = {NET}, IE_LA = {P.ie_la}, NF = {NF}, NR = {NR}, GS = {GS};")
+    fi_lc = sum(1 for f in P.f_targets if sum(f) < lc)
+    w(f"  static constexpr int NE = {NE}, NET = {NET}, IE_LO = {P.ie_lo}, NF = {NF}, NR = {NR}, GS = {GS};")
+    w(f"  static constexpr int LCMIN = {min(lc, ld)}, FI_LC = {fi_lc};")
     w(f"  static constexpr int NCOL = {len(P.cols)}, BRA_COL = {bc}, ARENA = {arena}, NH = {NF * NET};")
     w(f"  static constexpr int WARP_SMEM = ARENA + kCoopBatch * CoopSetup<La, Lc>::STRIDE;")
     w(f"  static __device__ __forceinline__ const int4* bra_y() {{ return kBraY_{cname}; }}")
@@ -287,48 +297,74 @@ def emit_coop_class(cls):
     w(f"  static __device__ __forceinline__ const int* nlist(int a) {{ return kN_{cname} + (a == 0 ? 0 : a == 1 ? "
       f"{nn[0]} : {nn[0] + nn[1]}); }}")
     w("};")
-    # bra HRR + sph for one ket column
-    E_targets = [e for k in range(la, La + 1) for e in cart_list(k)]
+    # bra HRR + sph for one ket column (and, for la != lb, the reversed form:
+    # VRR on the lb shell, HRR for (lb, la), rows written in canonical order)
+    E_targets = [e for k in range(min(la, lb), La + 1) for e in cart_list(k)]
     eidx = {e: i for i, e in enumerate(E_targets)}
     fidx = {f: i for i, f in enumerate(P.f_targets)}
-    bem = E.Emitter()
-    cart = E.emit_hrr_column(bem, la, lb, lambda e: f"Hc[{eidx[e]}]", "b", ["Q.AB[0]", "Q.AB[1]", "Q.AB[2]"])
-    rows = E.emit_sph_pair(bem, la, lb, cart, "t")
-    w(f"__device__ __forceinline__ void bra_hrr_{cname}(const Quartet& Q, const double* __restrict__ H, int fi, "
-      f"double* __restrict__ G) {{")
-    w(f"  const double* __restrict__ Hc = H + (size_t)fi * {NET};")
-    for ln in bem.lines:
-        w("  " + ln)
-    for r, var in enumerate(rows):
-        w(f"  G[{r * GS} + fi] = {var};")
-    w("}")
-    kem = E.Emitter()
-    cart = E.emit_hrr_column(kem, lc, ld, lambda f: f"Gr[{fidx[f]}]", "k", ["Q.CD[0]", "Q.CD[1]", "Q.CD[2]"])
-    outs = E.emit_sph_pair(kem, lc, ld, cart, "u")
-    w("template <int MODE>")
-    w(f"__device__ __forceinline__ void ket_hrr_{cname}(const EriLaunch& P, const Quartet& Q, long long q, int r, "
-      f"const double* __restrict__ G, double& smax_) {{")
-    w(f"  const double* __restrict__ Gr = G + r * {GS};")
-    w("  constexpr int kNSB_ = 1, kNSC_ = 1, kNSD_ = 1;")
-    w("  double jcd_[1], kac_[1], kad_[1];")
-    w("  (void)jcd_;")
-    w("  (void)kac_;")
-    w("  (void)kad_;")
-    for ln in kem.lines:
-        w("  " + ln)
-    w(f"  OUTPUT_ROW(r, r / {nsb}, r % {nsb});")
-    w(f"  const double* __restrict__ osc_ = kOutScale_{cname} + r * {nsc * nsd};")
-    for cdi, var in enumerate(outs):
-        w(f"  const double o{cdi} = {kem.mul(var, f'__ldg(osc_ + {cdi})')};")
-        w(f"  OUTPUT_VAL(r / {nsb}, r % {nsb}, {cdi // nsd}, {cdi % nsd}, o{cdi});")
-    w("  OUTPUT_ROW_END();")
-    w("}")
-    w(f"ERI_COOP_KERNEL(k_{cname}, {T}, bra_hrr_{cname}, ket_hrr_{cname})")
+
+    def bra_fn(name, l1, l2, rev):
+        bem = E.Emitter()
+        cart = E.emit_hrr_column(bem, l1, l2, lambda e: f"Hc[{eidx[e]}]", "b", ["Q.AB[0]", "Q.AB[1]", "Q.AB[2]"])
+        rows = E.emit_sph_pair(bem, l1, l2, cart, "t")
+        w(f"__device__ __forceinline__ void {name}(const Quartet& Q, const double* __restrict__ H, int fi, "
+          f"double* __restrict__ G) {{")
+        w(f"  const double* __restrict__ Hc = H + (size_t)fi * {NET};")
+        for ln in bem.lines:
+            w("  " + ln)
+        n1, n2 = len(cart2sph(l1)), len(cart2sph(l2))
+        for r, var in enumerate(rows):
+            i1, i2 = r // n2, r % n2
+            rc = i2 * nsb + i1 if rev else r   # reversed: (ib, ia) -> canonical row ia * nsb + ib
+            w(f"  G[{rc * GS} + fi] = {var};")
+        w("}")
+        return bem
+
+    bem = bra_fn(f"bra_hrr_{cname}", la, lb, False)
+    bra_rev = f"bra_hrr_{cname}"
+    if la != lb:
+        bra_rev = f"bra_hrr_rev_{cname}"
+        bra_fn(bra_rev, lb, la, True)
+
+    def ket_fn(name, l1, l2, rev):
+        kem = E.Emitter()
+        cart = E.emit_hrr_column(kem, l1, l2, lambda f: f"Gr[{fidx[f]}]", "k", ["Q.CD[0]", "Q.CD[1]", "Q.CD[2]"])
+        outs = E.emit_sph_pair(kem, l1, l2, cart, "u")
+        w("template <int MODE>")
+        w(f"__device__ __forceinline__ void {name}(const EriLaunch& P, const Quartet& Q, long long q, int r, "
+          f"const double* __restrict__ G, double& smax_) {{")
+        w(f"  const double* __restrict__ Gr = G + r * {GS};")
+        w("  constexpr int kNSB_ = 1, kNSC_ = 1, kNSD_ = 1;")
+        w("  double jcd_[1], kac_[1], kad_[1];")
+        w("  (void)jcd_;")
+        w("  (void)kac_;")
+        w("  (void)kad_;")
+        for ln in kem.lines:
+            w("  " + ln)
+        w(f"  OUTPUT_ROW(r, r / {nsb}, r % {nsb});")
+        w(f"  const double* __restrict__ osc_ = kOutScale_{cname} + r * {nsc * nsd};")
+        n2 = len(cart2sph(l2))
+        for k, var in enumerate(outs):
+            i1, i2 = k // n2, k % n2
+            ic, idd = (i2, i1) if rev else (i1, i2)
+            cdi = ic * nsd + idd
+            w(f"  const double o{k} = {kem.mul(var, f'__ldg(osc_ + {cdi})')};")
+            w(f"  OUTPUT_VAL(r / {nsb}, r % {nsb}, {ic}, {idd}, o{k});")
+        w("  OUTPUT_ROW_END();")
+        w("}")
+        return kem
+
+    kem = ket_fn(f"ket_hrr_{cname}", lc, ld, False)
+    ket_rev = f"ket_hrr_{cname}"
+    if lc != ld:
+        ket_rev = f"ket_hrr_rev_{cname}"
+        ket_fn(ket_rev, ld, lc, True)
+    w(f"ERI_COOP_KERNEL(k_{cname}, {T}, bra_hrr_{cname}, {bra_rev}, ket_hrr_{cname}, {ket_rev})")
     w("}  // namespace gen")
     vops = P.fp64_ops + E.BOYS_SETUP_OPS(L)
     vflops = 2 * P.fp64_ops - P.nodes + E.BOYS_SETUP_FLOPS(L)
-    hops = bem.ops * NF + kem.ops * NR
-    hflops = bem.flops * NF + kem.flops * NR
+    hops = bem.ops * (NF - fi_lc) + kem.ops * NR
+    hflops = bem.flops * (NF - fi_lc) + kem.flops * NR
     w(f"ERI_DEFINE_COOP_LAUNCHER({la}, {lb}, {lc}, {ld}, gen::k_{cname}, gen::{T}, {vops}LL, {vflops}LL, {hops}LL, "
       f"{hflops}LL)")
     w("}  // namespace eri")

@@ -390,12 +390,25 @@ def choose_shape(g, peak, cls):
     return "reg" if (nacc + peak) <= 150 else "staged"
 
 
-def emit_class(cls, spherical_out=True):
+def emit_class(cls, spherical_out=True, rule=None, schedule=None, sph_fusion=True, tier=None):
+    """Kernel text and statistics of one class.  The keyword options switch off
+    one design choice each, for ablation builds (section V-B): `rule` forces a
+    VRR axis rule (graph.AXIS_RULES), `schedule="topo"` keeps the graph's plain
+    topological order instead of the PeakLive-minimising one, `sph_fusion=False`
+    runs both HRRs in Cartesian form and applies T(la) x T(lb) x T(lc) x T(ld) to
+    the materialised block (Eq. (17)), `tier` forces "reg" or "staged"."""
     la, lb, lc, ld = cls
     La, Lc = la + lb, lc + ld
     L = La + Lc
-    g, order, info = G.best_vrr(cls)
-    shape = choose_shape(g, info["peak_live"], cls)
+    g, order, info = G.best_vrr(cls, rules=(rule,)) if rule else G.best_vrr(cls)
+    if schedule == "topo":
+        order = list(range(len(g.nodes)))
+        info = dict(info, schedule="topo", peak_live=G.peak_live(g.nodes, order))
+    elif schedule is not None:
+        raise ValueError(f"unknown schedule {schedule!r}")
+    shape = tier or choose_shape(g, info["peak_live"], cls)
+    if shape not in ("reg", "staged"):
+        raise ValueError(f"unknown tier {shape!r}")
     E = [e for k in range(la, La + 1) for e in cart_list(k)]
     Fc = [f for k in range(lc, Lc + 1) for f in cart_list(k)]
     NE, NF = len(E), len(Fc)
@@ -405,6 +418,8 @@ def emit_class(cls, spherical_out=True):
     nsa, nsb, nsc, nsd = (len(cart2sph(l)) for l in cls)
     nca, ncb, ncc, ncd = (len(cart_list(l)) for l in cls)
     NR = nsa * nsb
+    NRB = NR if sph_fusion else nca * ncb   # bra rows entering the ket HRR
+    NSCD = nsc * nsd
 
     body = Emitter()
     w = body.w
@@ -433,7 +448,7 @@ def emit_class(cls, spherical_out=True):
     vops, vflops = vem.ops, vem.flops
 
     # ---- kernel text ----
-    if shape == "staged":
+    if shape == "staged" and sph_fusion:
         w(out_scale_table(cls, cname))
     w(f"template <int MODE, bool CONTRACTED>")
     w(f"__global__ void __launch_bounds__(kThreads) k_{cname}(const EriLaunch P) {{")
@@ -449,7 +464,7 @@ def emit_class(cls, spherical_out=True):
     w("    if constexpr (MODE >= kCoulomb) {")
     w("      load_quartet_coulomb(P, q, Q);")
     w("    } else {")
-    w(f"      load_quartet<{'true' if la == lb else 'false'}, {'true' if lc == ld else 'false'}>(P, q, Q);")
+    w(f"      load_quartet<{1 if la == lb else 0}, {1 if lc == ld else 0}, {la + lb}, {lc + ld}>(P, q, Q);")
     w("    }")
     w("    double smax_ = 0.0;")
     w("    (void)smax_;")
@@ -485,19 +500,46 @@ def emit_class(cls, spherical_out=True):
 
     # ---- HRR + sph ----
     hem = Emitter()
+    ca_l, cb_l = cart_list(la), cart_list(lb)
+    Ta, Tb = cart2sph(la), cart2sph(lb)
+    sa, sb = sph_scales(la), sph_scales(lb)
+
+    def bra_rows(em, cart, prefix):
+        # bra block -> rows entering the ket HRR: T(la) x T(lb) now (stepwise
+        # fusion), or the Cartesian rows (a, b) row-major when fusion is off
+        if sph_fusion:
+            return emit_sph_pair(em, la, lb, cart, prefix)
+        return [cart[(a, b)] for a in ca_l for b in cb_l]
+
+    def final_bra_terms(ia, ib):
+        # sph_fusion off: output row (ia, ib) from the Cartesian rows, divided
+        # by the hoisted scales like emit_sph_pair's rows
+        terms = []
+        for ka, a in enumerate(ca_l):
+            for kb, b in enumerate(cb_l):
+                c = Ta[ia][ka] * Tb[ib][kb] / (sa[ia] * sb[ib])
+                if c != 0.0:
+                    terms.append((c, ka * len(cb_l) + kb))
+        return terms
+
     if shape == "reg":
         # G[r][f] for every ket column f
         gvals = {}
         for f in Fc:
             cart = emit_hrr_column(hem, la, lb, lambda e, f=f: f"h{g.target_ef.index((e, f))}", f"b{fidx[f]}_",
                                    ["Q.AB[0]", "Q.AB[1]", "Q.AB[2]"])
-            rows = emit_sph_pair(hem, la, lb, cart, f"t{fidx[f]}_")
+            rows = bra_rows(hem, cart, f"t{fidx[f]}_")
             for r, var in enumerate(rows):
                 gvals[(r, f)] = var
-        for r in range(NR):
+        xvals = {}
+        for r in range(NRB):
             cart = emit_hrr_column(hem, lc, ld, lambda f, r=r: gvals[(r, f)], f"k{r}_",
                                    ["Q.CD[0]", "Q.CD[1]", "Q.CD[2]"])
             outs = emit_sph_pair(hem, lc, ld, cart, f"u{r}_")
+            if not sph_fusion:
+                for cdi, var in enumerate(outs):
+                    xvals[(r, cdi)] = var
+                continue
             hem.w(f"OUTPUT_ROW({r}, {r // nsb}, {r % nsb});")
             for cdi, var in enumerate(outs):
                 sc = out_scale(cls, r // nsb, r % nsb, cdi // nsd, cdi % nsd)
@@ -507,6 +549,20 @@ def emit_class(cls, spherical_out=True):
                     var = sv
                 hem.w(f"OUTPUT_VAL({r // nsb}, {r % nsb}, {cdi // nsd}, {cdi % nsd}, {var});")
             hem.w("OUTPUT_ROW_END();")
+        if not sph_fusion:
+            for r in range(NR):
+                ia, ib = r // nsb, r % nsb
+                terms = final_bra_terms(ia, ib)
+                hem.w(f"OUTPUT_ROW({r}, {ia}, {ib});")
+                for cdi in range(NSCD):
+                    var = lin_comb(hem, [(c, xvals[(rc, cdi)]) for c, rc in terms], f"z{r}_{cdi}")
+                    sc = out_scale(cls, ia, ib, cdi // nsd, cdi % nsd)
+                    if sc != 1.0:
+                        sv = f"o{r}_{cdi}"
+                        hem.w(f"const double {sv} = {hem.mul(var, _fmt(sc))};")
+                        var = sv
+                    hem.w(f"OUTPUT_VAL({ia}, {ib}, {cdi // nsd}, {cdi % nsd}, {var});")
+                hem.w("OUTPUT_ROW_END();")
         hops = hem.ops
         for ln in hem.lines:
             w("    " + ln)
@@ -515,7 +571,7 @@ def emit_class(cls, spherical_out=True):
         bem = Emitter()
         bem.w(f"const double* __restrict__ Hc = S + (long long)fi * nt;")
         cart = emit_hrr_column(bem, la, lb, lambda e: f"Hc[{eidx[e] * NF} * nt]", "b", ["Q.AB[0]", "Q.AB[1]", "Q.AB[2]"])
-        rows = emit_sph_pair(bem, la, lb, cart, "t")
+        rows = bra_rows(bem, cart, "t")
         bem.w(f"double* __restrict__ Gc = S + (long long)({NE * NF} + fi) * nt;")
         for r, var in enumerate(rows):
             bem.w(f"Gc[{r * NF} * nt] = {var};")
@@ -527,29 +583,64 @@ def emit_class(cls, spherical_out=True):
         kem.w(f"const double* __restrict__ Gr = S + (long long)({NE * NF} + r * {NF}) * nt;")
         cart = emit_hrr_column(kem, lc, ld, lambda f: f"Gr[{fidx[f]} * nt]", "k", ["Q.CD[0]", "Q.CD[1]", "Q.CD[2]"])
         outs = emit_sph_pair(kem, lc, ld, cart, "u")
-        kem.w(f"OUTPUT_ROW(r, r / {nsb}, r % {nsb});")
-        kem.w(f"const double* __restrict__ osc_ = kOutScale_{cname} + r * {nsc * nsd};")
-        for cdi, var in enumerate(outs):
-            sv = f"o{cdi}"
-            kem.w(f"const double {sv} = {kem.mul(var, f'__ldg(osc_ + {cdi})')};")
-            kem.w(f"OUTPUT_VAL(r / {nsb}, r % {nsb}, {cdi // nsd}, {cdi % nsd}, {sv});")
-        kem.w("OUTPUT_ROW_END();")
-        w(f"    for (int r = 0; r < {NR}; ++r) {{")
+        # sph_fusion off: the ket-transformed Cartesian rows X[r][c'd'] reuse the
+        # H area when it is large enough (H is dead after the bra loop)
+        xbase = 0 if NRB * NSCD <= NE * NF else NE * NF + NRB * NF
+        if sph_fusion:
+            kem.w(f"OUTPUT_ROW(r, r / {nsb}, r % {nsb});")
+            kem.w(f"const double* __restrict__ osc_ = kOutScale_{cname} + r * {nsc * nsd};")
+            for cdi, var in enumerate(outs):
+                sv = f"o{cdi}"
+                kem.w(f"const double {sv} = {kem.mul(var, f'__ldg(osc_ + {cdi})')};")
+                kem.w(f"OUTPUT_VAL(r / {nsb}, r % {nsb}, {cdi // nsd}, {cdi % nsd}, {sv});")
+            kem.w("OUTPUT_ROW_END();")
+        else:
+            kem.w(f"double* __restrict__ Xr = S + (long long)({xbase} + r * {NSCD}) * nt;")
+            for cdi, var in enumerate(outs):
+                kem.w(f"Xr[{cdi} * nt] = {var};")
+        w(f"    for (int r = 0; r < {NRB}; ++r) {{")
         for ln in kem.lines:
             w("      " + ln)
         w("    }")
-        hops = bem.ops * NF + kem.ops * NR
-        hem.flops = bem.flops * NF + kem.flops * NR
+        hops = bem.ops * NF + kem.ops * NRB
+        hem.flops = bem.flops * NF + kem.flops * NRB
+        if not sph_fusion:
+            fem = Emitter()
+            fem.w(f"const double* __restrict__ X = S + (long long){xbase} * nt;")
+            for r in range(NR):
+                ia, ib = r // nsb, r % nsb
+                terms = final_bra_terms(ia, ib)
+                fem.w(f"OUTPUT_ROW({r}, {ia}, {ib});")
+                for cdi in range(NSCD):
+                    var = lin_comb(fem, [(c, f"X[{rc * NSCD + cdi} * nt]") for c, rc in terms], f"z{r}_{cdi}")
+                    if not var.isidentifier():
+                        fem.w(f"const double z{r}_{cdi} = {var};")
+                        var = f"z{r}_{cdi}"
+                    sc = out_scale(cls, ia, ib, cdi // nsd, cdi % nsd)
+                    if sc != 1.0:
+                        sv = f"o{r}_{cdi}"
+                        fem.w(f"const double {sv} = {fem.mul(var, _fmt(sc))};")
+                        var = sv
+                    fem.w(f"OUTPUT_VAL({ia}, {ib}, {cdi // nsd}, {cdi % nsd}, {var});")
+                fem.w("OUTPUT_ROW_END();")
+            for ln in fem.lines:
+                w("    " + ln)
+            hops += fem.ops
+            hem.flops += fem.flops
     w("    OUTPUT_QUARTET_END();")
     w("  }")
     if shape == "staged" and smem_slots:
         w("#undef SMEM")
     w("}")
 
-    scratch_slots = (NE * NF + NR * NF) if shape == "staged" else 0
+    scratch_slots = 0
+    if shape == "staged":
+        scratch_slots = NE * NF + NRB * NF
+        if not sph_fusion and NRB * NSCD > NE * NF:
+            scratch_slots += NRB * NSCD
     meta = dict(cls=cls, L=L, shape=shape, nvrr=len(g.nodes), ntargets=len(g.targets), vrr_ops=vops, smem_slots=smem_slots,
                 vrr_flops=vflops, hrr_ops=hops, hrr_flops=hem.flops, scratch_slots=scratch_slots,
-                nfunc=(nsa, nsb, nsc, nsd), ncart=(nca, ncb, ncc, ncd), **info)
+                nfunc=(nsa, nsb, nsc, nsd), ncart=(nca, ncb, ncc, ncd), sph_fusion=sph_fusion, **info)
     head = HEADER.format(la=la, lb=lb, lc=lc, ld=ld, L=L, nv=len(g.nodes), rule=g.rule, sched=info["schedule"],
                          pl=info["peak_live"], nt=len(g.targets), shape=shape, vops=vops, hops=hops)
     vops_all, vflops_all = vops + BOYS_SETUP_OPS(L), vflops + BOYS_SETUP_FLOPS(L)

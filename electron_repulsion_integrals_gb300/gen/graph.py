@@ -79,8 +79,20 @@ def axis_bra_first_zyx(e, f):
     return None
 
 
+def axis_bra_first_xyz(e, f):
+    """The conventional order (bra before ket, x before y before z): the
+    baseline that the axis-priority ablation of section V-B compares against."""
+    for i in (0, 1, 2):
+        if e[i] > 0:
+            return ("bra", i)
+    for i in (0, 1, 2):
+        if f[i] > 0:
+            return ("ket", i)
+    return None
+
+
 AXIS_RULES = {"ket_first_zyx": axis_ket_first_zyx, "alg1_literal": axis_alg1_literal,
-              "bra_first_zyx": axis_bra_first_zyx}
+              "bra_first_zyx": axis_bra_first_zyx, "bra_first_xyz": axis_bra_first_xyz}
 
 
 # --------------------------------------------------------------------- VRR graph

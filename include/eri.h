@@ -9,8 +9,9 @@
  * that page: Boys function base values, the vertical recurrence Eq. (2), the
  * horizontal recurrence Eq. (3) / Eq. (13), and the stepwise Cartesian-to-
  * spherical transform of section III-B (Eqs. (8), (16)), one generated CUDA
- * kernel per angular-momentum class.  It digests the integrals into the
- * Coulomb matrix, the "J += SCATTER(G, D)" step of Algorithm 2.
+ * kernel per angular-momentum class (s through g shells).  It digests the
+ * integrals into the Coulomb and exchange matrices, the "J, K += SCATTER(G, D)"
+ * step of Algorithm 2.
  *
  * Conventions (the page leaves them open; these are the library's readings):
  *   - primitive g = x_A^i y_A^j z_A^k exp(-alpha r_A^2) times
@@ -45,7 +46,7 @@ extern "C" {
 typedef enum {
   ERI_OK = 0,
   ERI_ERR_INVALID_ARG = -1,      /* NULL pointer, negative count, bad shell data, mismatched class */
-  ERI_ERR_UNSUPPORTED_L = -2,    /* angular momentum above the built maximum (3) or Cartesian d/f output */
+  ERI_ERR_UNSUPPORTED_L = -2,    /* angular momentum above the built maximum (4) or Cartesian d/f/g output */
   ERI_ERR_BUFFER_TOO_SMALL = -3, /* output length smaller than the batch needs */
   ERI_ERR_CUDA = -4,             /* a CUDA runtime call failed (also reports earlier asynchronous faults) */
   ERI_ERR_OOM = -5,              /* device or host allocation failed */
@@ -59,14 +60,14 @@ typedef enum {
  * normalised primitives (see above). */
 typedef struct {
   double center[3]; /* bohr */
-  int L;            /* 0..3 */
+  int L;            /* 0..4 (s, p, d, f, g) */
   int nprim;        /* >= 1 */
   const double* exps;
   const double* coefs;
 } eri_shell;
 
 typedef struct {
-  int spherical;      /* 1: spherical functions for l >= 2 (required for d and f shells); 0: Cartesian */
+  int spherical;      /* 1: spherical functions for l >= 2 (required for d, f and g shells); 0: Cartesian */
   double schwarz_tau; /* Schwarz threshold for eri_build_J / eri_plan_quartet_count; <= 0 keeps every quartet */
   int flags;          /* reserved, must be 0 */
 } eri_options;
@@ -161,8 +162,10 @@ int eri_schwarz(eri_plan* plan, int la, int lb, const int* pairs_dev, long long 
  * double matrices; D must be symmetric; J is overwritten (not accumulated) and
  * comes out symmetric.  The class kernels digest each block as soon as it is
  * formed (no integral is written to memory); J is accumulated with FP64
- * atomics, so its last bits depend on scheduling.  Errors: INVALID_ARG,
- * CUDA, OOM. */
+ * atomics, so its last bits depend on scheduling.  The digestion is built for
+ * the register and staged tiers (total angular momentum la+lb+lc+ld <= 8, e.g.
+ * every class of s, p, d shells): a screened class above that returns
+ * ERI_ERR_NOT_IMPLEMENTED.  Errors: INVALID_ARG, NOT_IMPLEMENTED, CUDA, OOM. */
 int eri_build_J(eri_plan* plan, const double* D_dev, double* J_dev, void* stream);
 
 /* Coulomb and exchange matrices from one pass over the screened quartets (the
@@ -175,8 +178,9 @@ int eri_build_J(eri_plan* plan, const double* D_dev, double* J_dev, void* stream
  * be symmetric; J and K are overwritten and come out symmetric.  J equals what
  * eri_build_J returns up to the order of its atomic additions.  The first call
  * on a plan allocates an nbf x nbf device accumulator for K that the plan keeps
- * until eri_plan_destroy.  Errors: INVALID_ARG (NULL argument, plan without a
- * screen), OOM, CUDA. */
+ * until eri_plan_destroy.  Same class limit as eri_build_J.  Errors:
+ * INVALID_ARG (NULL argument, plan without a screen), NOT_IMPLEMENTED, OOM,
+ * CUDA. */
 int eri_build_JK(eri_plan* plan, const double* D_dev, double* J_dev, double* K_dev, void* stream);
 
 /* Number of unique shell quartets of canonical class (la lb|lc ld) that

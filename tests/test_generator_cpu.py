@@ -21,6 +21,7 @@ import numpy as np
 import pytest
 
 import oracle
+from electron_repulsion_integrals_gb300.gen.sph import cart_list
 from electron_repulsion_integrals_gb300.gen import emit as E
 from electron_repulsion_integrals_gb300.gen.eri_gen import canonical_classes
 
@@ -92,7 +93,7 @@ def translate(src):
             continue
         ln = ln.rstrip(";")
         ln = re.sub(r"^(const )?double ", "", ln)
-        ln = re.sub(r"\b(Hc|Gc|Gr)\[(\d+) \* nt\]", r"S[\1 + \2]", ln)
+        ln = re.sub(r"\b(Hc|Gc|Gr|Xr|X)\[(\d+) \* nt\]", r"S[\1 + \2]", ln)
         ln = re.sub(r"\bS\[(\d+) \* nt\]", r"S[\1]", ln)
         ln = re.sub(r"\bh(\d+)\b", r"h[\1]", ln)
         ln = re.sub(r"__ldg\(osc_ \+ (\d+)\)", r"OSC[osc_ + \1]", ln)
@@ -189,7 +190,7 @@ def emulate_coop(cls, prims):
     from electron_repulsion_integrals_gb300.gen import coop
     P = coop.plan(cls)
     NE, L, La, Lc = P.NE, P.L, P.La, P.Lc
-    NET = NE - P.ie_la
+    NET = NE - P.ie_lo
     H = np.zeros((len(P.f_targets), NET))
     for pb, pk, qs, F in prims:
         A = np.zeros(max(P.arena, 1) + 4 * NE)
@@ -205,8 +206,8 @@ def emulate_coop(cls, prims):
                 A[bc + out] = PA[ax] * A[bc + x] + WP[ax] * A[bc + x + NE] + ky * o2z * (A[bc + y] - qs.roz * A[bc + y + NE])
             for out, x, ax in P.bra_nodes_n[k]:
                 A[bc + out] = PA[ax] * A[bc + x] + WP[ax] * A[bc + x + NE]
-        if cls[2] == 0:
-            H[0] += A[bc + P.ie_la:bc + NE]
+        if min(cls[2], cls[3]) == 0:
+            H[0] += A[bc + P.ie_lo:bc + NE]
         for st in P.cols:
             rows = Lc - st.level + 1
             for m in range(rows):
@@ -224,7 +225,7 @@ def emulate_coop(cls, prims):
                         v += st.ky * o2e * (A[st.y + o] - qs.roe * A[st.y + o + NE])
                     A[st.out + o] = v
             if st.target >= 0:
-                H[st.target] += A[st.out + P.ie_la:st.out + NE]
+                H[st.target] += A[st.out + P.ie_lo:st.out + NE]
     return H, P
 
 
@@ -246,11 +247,33 @@ def test_coop_plan_reproduces_vrr_targets(cls):
     H, P = emulate_coop(cls, prims)
     eidx = {e: i for i, e in enumerate(P.e_list)}
     fidx = {f: i for i, f in enumerate(P.f_targets)}
+    la, lb, lc, ld = cls
+    E_sl = [e for k in range(la, la + lb + 1) for e in cart_list(k)]
+    F_sl = [f for k in range(lc, lc + ld + 1) for f in cart_list(k)]
     for ti, (e, f) in enumerate(g.target_ef):
         if meta["shape"] == "reg":
             ref = ns["h"][ti]
         else:
-            slot = (eidx[e] - P.ie_la) * len(P.f_targets) + fidx[f]
+            slot = E_sl.index(e) * len(F_sl) + F_sl.index(f)
             ref = ns["S"][slot]
-        got = H[fidx[f], eidx[e] - P.ie_la]
+        got = H[fidx[f], eidx[e] - P.ie_lo]
         assert abs(got - ref) <= 1e-12 * max(1.0, abs(ref)), (e, f, got, ref)
+
+
+ABLATIONS = [dict(rule="alg1_literal"), dict(rule="bra_first_xyz"), dict(schedule="topo"), dict(sph_fusion=False),
+             dict(sph_fusion=False, tier="staged"), dict(tier="staged"), dict(tier="reg")]
+
+
+@pytest.mark.parametrize("opts", ABLATIONS, ids=["-".join(f"{k}={v}" for k, v in o.items()) for o in ABLATIONS])
+@pytest.mark.parametrize("cls", [(1, 1, 0, 0), (2, 1, 1, 1), (2, 2, 2, 0)], ids=["1100", "2111", "2220"])
+def test_ablation_variants_match_oracle(cls, opts):
+    """Every ablation switch of the emitter still computes the same integrals."""
+    rng = np.random.default_rng(7 + sum(cls))
+    src, meta = E.emit_class(cls, **opts)
+    for k, v in opts.items():
+        assert meta["shape" if k == "tier" else k] == v
+    S, prims, Qns = harness(cls, rng, nprim=2)
+    got, nout = run_generated(src, cls, prims, Qns, True, meta["shape"], meta)
+    assert nout == got.size
+    ref = oracle.eri_block(S, 0, 1, 2, 3, spherical=True)
+    assert np.allclose(got, ref, rtol=1e-10, atol=1e-13)

@@ -89,12 +89,17 @@ def test_J_64_atom_cluster_sampled_blocks(dev):
     plan.close()
 
 
-def test_J_200_atom_cluster_sampled_blocks(dev):
-    """The 200-atom workload at full size: sampled J blocks against the oracle."""
+def test_JK_200_atom_cluster_sampled_blocks(dev):
+    """The 200-atom workload at full size through the fused J+K pass: sampled J
+    and K blocks against the oracle (the fused J equals eri_build_J's, checked
+    on small clusters in test_gpu_exchange.py)."""
     s = W.cluster200()
     nbf = W.nbf(s)
     D = W.density(nbf, 4)
-    plan, J = gpu_J(s, D, 1e-10, dev)
+    plan = eri.Plan(s, spherical=True, schwarz_tau=1e-10)
+    Jd, Kd = plan.build_JK(torch.as_tensor(D, device=dev))
+    torch.cuda.synchronize()
+    J, K = Jd.cpu().numpy(), Kd.cpu().numpy()
     S = oshells(s)
     nf = np.array([eri.nfunc(l) for l in s.L])
     fo = np.concatenate([[0], np.cumsum(nf)])
@@ -102,10 +107,11 @@ def test_J_200_atom_cluster_sampled_blocks(dev):
     dsh = d_shells[len(d_shells) // 2]
     pairs = [(dsh, dsh - 5)]  # a d shell and an s shell of the same atom
     Q = oracle.schwarz(S, True)
-    blocks = oracle.J_blocks(S, D, pairs, spherical=True, tau=1e-10, Q=Q)
-    for (a, b), B in zip(pairs, blocks):
-        G = J[fo[a]:fo[a + 1], fo[b]:fo[b + 1]]
-        assert np.linalg.norm(G - B) <= 1e-10 * max(np.linalg.norm(B), 1e-3), (a, b, np.abs(G - B).max())
-    assert np.allclose(J, J.T, rtol=0, atol=1e-12 * np.abs(J).max())
-    assert np.sum(D * J) > 0
+    for M, blocks in ((J, oracle.J_blocks(S, D, pairs, spherical=True, tau=1e-10, Q=Q)),
+                      (K, oracle.K_blocks(S, D, pairs, spherical=True, tau=1e-10, Q=Q))):
+        for (a, b), B in zip(pairs, blocks):
+            G = M[fo[a]:fo[a + 1], fo[b]:fo[b + 1]]
+            assert np.linalg.norm(G - B) <= 1e-10 * max(np.linalg.norm(B), 1e-3), (a, b, np.abs(G - B).max())
+        assert np.allclose(M, M.T, rtol=0, atol=1e-12 * np.abs(M).max())
+        assert np.sum(D * M) > 0
     plan.close()
