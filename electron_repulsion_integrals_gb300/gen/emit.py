@@ -128,8 +128,10 @@ def emit_vrr_staged_regs(em, g, order, sink, R):
     """Straight-line VRR like emit_vrr, but with at most R VRR values live in
     registers: when a new value would exceed R, the live value whose next use
     is farthest away (Belady) moves to a per-thread shared-memory slot
-    (SMEM(slot) = v) and is reloaded just before its next use.  Returns the
-    number of shared-memory slots per thread that the schedule needs."""
+    (SMEM(slot) = v) and is reloaded just before its next use; slots beyond
+    STAGED_SMEM_SLOTS_MAX live in per-thread global scratch (GSL(slot)).
+    Returns the number of slots per thread the schedule needs (shared and
+    global together)."""
     nodes = g.nodes
     tpos = {t: k for k, t in enumerate(g.targets)}
     uses = {v: [] for v in order}
@@ -156,6 +158,9 @@ def emit_vrr_staged_regs(em, g, order, sink, R):
     nslots = 0
     version = {}
 
+    def loc(sl):
+        return f"SMEM({sl})" if sl < STAGED_SMEM_SLOTS_MAX else f"GSL({sl - STAGED_SMEM_SLOTS_MAX})"
+
     def new_name(v):
         version[v] = version.get(v, -1) + 1
         return f"v{v}" if version[v] == 0 else f"v{v}_{version[v]}"
@@ -173,7 +178,7 @@ def emit_vrr_staged_regs(em, g, order, sink, R):
                 sl = nslots
                 nslots += 1
             slot_of[u] = sl
-            em.w(f"SMEM({sl}) = {reg[u]};")
+            em.w(f"{loc(sl)} = {reg[u]};")
         del reg[u]
 
     def release_dead(t):
@@ -192,7 +197,7 @@ def emit_vrr_staged_regs(em, g, order, sink, R):
                 while len(reg) >= R:
                     evict(t, set(parents) | {p})
                 nm = new_name(p)
-                em.w(f"const double {nm} = SMEM({slot_of[p]});")
+                em.w(f"const double {nm} = {loc(slot_of[p])};")
                 reg[p] = nm
         while len(reg) >= R:
             evict(t, set(parents))
@@ -383,6 +388,9 @@ def class_name(cls):
 # goes to per-thread shared-memory slots (SMEM).
 STAGED_VRR_REGS = 64
 STAGED_FENCE = 32
+# shared-memory slots per thread at most (x 128 threads x 8 B = 200 KB of the
+# 227 KB a block may have); further evicted values go to global scratch (GSL)
+STAGED_SMEM_SLOTS_MAX = 200
 
 
 def choose_shape(g, peak, cls):
@@ -440,12 +448,21 @@ def emit_class(cls, spherical_out=True, rule=None, schedule=None, sph_fusion=Tru
             e, f = g.target_ef[ti]
             slot = eidx[e] * NF + fidx[f]
             vem.w(f"if (CONTRACTED) {{ S[{slot} * nt] += {var}; }} else {{ S[{slot} * nt] = {var}; }}")
-    smem_slots = 0
+    smem_slots = gsl_slots = 0
     if shape == "staged":
-        smem_slots = emit_vrr_staged_regs(vem, g, order, sink, STAGED_VRR_REGS)
+        nsl = emit_vrr_staged_regs(vem, g, order, sink, STAGED_VRR_REGS)
+        smem_slots = min(nsl, STAGED_SMEM_SLOTS_MAX)
+        gsl_slots = nsl - smem_slots
     else:
         emit_vrr(vem, g, order, sink)
     vops, vflops = vem.ops, vem.flops
+
+    scratch_slots = 0
+    if shape == "staged":
+        scratch_slots = NE * NF + NRB * NF
+        if not sph_fusion and NRB * NSCD > NE * NF:
+            scratch_slots += NRB * NSCD
+    gsl_base = scratch_slots     # global VRR slots follow H, G (and X)
 
     # ---- kernel text ----
     if shape == "staged" and sph_fusion:
@@ -459,6 +476,8 @@ def emit_class(cls, spherical_out=True, rule=None, schedule=None, sph_fusion=Tru
         if smem_slots:
             w("  extern __shared__ double smem_vrr_[];")
             w("#define SMEM(k) smem_vrr_[(k) * kThreads + threadIdx.x]")
+        if gsl_slots:
+            w(f"#define GSL(k) S[({gsl_base} + (k)) * nt]")
     w("  for (long long q = gid; q < P.n; q += nt) {")
     w("    Quartet Q;")
     w("    if constexpr (MODE >= kCoulomb) {")
@@ -631,14 +650,13 @@ def emit_class(cls, spherical_out=True, rule=None, schedule=None, sph_fusion=Tru
     w("  }")
     if shape == "staged" and smem_slots:
         w("#undef SMEM")
+    if shape == "staged" and gsl_slots:
+        w("#undef GSL")
     w("}")
 
-    scratch_slots = 0
-    if shape == "staged":
-        scratch_slots = NE * NF + NRB * NF
-        if not sph_fusion and NRB * NSCD > NE * NF:
-            scratch_slots += NRB * NSCD
+    scratch_slots += gsl_slots
     meta = dict(cls=cls, L=L, shape=shape, nvrr=len(g.nodes), ntargets=len(g.targets), vrr_ops=vops, smem_slots=smem_slots,
+                gsl_slots=gsl_slots,
                 vrr_flops=vflops, hrr_ops=hops, hrr_flops=hem.flops, scratch_slots=scratch_slots,
                 nfunc=(nsa, nsb, nsc, nsd), ncart=(nca, ncb, ncc, ncd), sph_fusion=sph_fusion, **info)
     head = HEADER.format(la=la, lb=lb, lc=lc, ld=ld, L=L, nv=len(g.nodes), rule=g.rule, sched=info["schedule"],

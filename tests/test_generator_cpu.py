@@ -98,6 +98,7 @@ def translate(src):
         ln = re.sub(r"\bh(\d+)\b", r"h[\1]", ln)
         ln = re.sub(r"__ldg\(osc_ \+ (\d+)\)", r"OSC[osc_ + \1]", ln)
         ln = re.sub(r"\bSMEM\((\d+)\)", r"SM[\1]", ln)
+        ln = re.sub(r"\bGSL\((\d+)\)", r"SM[-1 - \1]", ln)
         out.append(pad + ln)
     return "\n".join(out)
 
@@ -275,5 +276,18 @@ def test_ablation_variants_match_oracle(cls, opts):
     S, prims, Qns = harness(cls, rng, nprim=2)
     got, nout = run_generated(src, cls, prims, Qns, True, meta["shape"], meta)
     assert nout == got.size
+    ref = oracle.eri_block(S, 0, 1, 2, 3, spherical=True)
+    assert np.allclose(got, ref, rtol=1e-10, atol=1e-13)
+
+
+def test_staged_slots_beyond_shared_memory_go_to_global_scratch(monkeypatch):
+    """With the shared-memory slot cap forced low, evicted VRR values overflow
+    into global scratch slots and the kernel still computes the same block."""
+    monkeypatch.setattr(E, "STAGED_SMEM_SLOTS_MAX", 2)
+    cls = (2, 1, 1, 1)
+    src, meta = E.emit_class(cls, tier="staged", schedule="topo")
+    assert meta["gsl_slots"] > 0 and meta["smem_slots"] == 2
+    S, prims, Qns = harness(cls, np.random.default_rng(21), nprim=2)
+    got, _ = run_generated(src, cls, prims, Qns, True, "staged", meta)
     ref = oracle.eri_block(S, 0, 1, 2, 3, spherical=True)
     assert np.allclose(got, ref, rtol=1e-10, atol=1e-13)
