@@ -66,6 +66,7 @@ def _load():
             lib.ora_J_blocks.argtypes = shell_args + [ctypes.c_int, ctypes.c_double, dp, dp, ip, ctypes.c_longlong,
                                                       lp, dp, ctypes.c_int]
             lib.ora_K_blocks.argtypes = lib.ora_J_blocks.argtypes
+            lib.ora_eri_deriv_blocks.argtypes = shell_args + [ip, ctypes.c_longlong, ctypes.c_int, lp, dp, ctypes.c_int]
             lib.ora_build_JK.argtypes = shell_args + [ctypes.c_int, ctypes.c_double, dp, dp, dp, dp, ctypes.c_int]
             lib.ora_build_J.argtypes = shell_args + [ctypes.c_int, ctypes.c_double, dp, dp, dp, lp, ctypes.c_int]
             _lib = lib
@@ -251,3 +252,22 @@ def build_JK(S: ShellSet, D, spherical=True, tau=1e-10, Q=None, nthreads=None):
 def K_blocks(S: ShellSet, D, pairs, spherical=True, tau=1e-10, Q=None, nthreads=None):
     """Blocks K[a][c] for the requested shell pairs, from the definition (see oracle.cpp)."""
     return J_blocks(S, D, pairs, spherical, tau, Q, nthreads, _fn="ora_K_blocks")
+
+
+def eri_deriv_blocks(S: ShellSet, quartets, spherical=True, nthreads=None) -> np.ndarray:
+    """First derivatives of each block (a b|c d) with respect to the centres
+    of a, b, c, d: array [n][centre 4][axis 3][na][nb][nc][nd] (see oracle.cpp)."""
+    q = np.ascontiguousarray(quartets, dtype=np.int32).reshape(-1, 4)
+    nf = [[nfunc(S.L[x], spherical) for x in row] for row in q]
+    sizes = np.array([12 * int(np.prod(f)) for f in nf], dtype=np.int64)
+    off = np.zeros(len(q), dtype=np.int64)
+    if len(q) > 1:
+        off[1:] = np.cumsum(sizes)[:-1]
+    out = np.zeros(int(sizes.sum()))
+    rc = _load().ora_eri_deriv_blocks(*S.args(), _ip(q), len(q), int(bool(spherical)), _lp(off), _dp(out),
+                                      int(nthreads or default_threads()))
+    if rc:
+        raise ValueError("ora_eri_deriv_blocks: bad arguments")
+    if len(set(map(tuple, nf))) == 1 and len(q):
+        return out.reshape((len(q), 4, 3) + tuple(nf[0]))
+    return [out[o:o + sz].reshape((4, 3) + tuple(f)) for o, sz, f in zip(off, sizes, nf)]

@@ -282,23 +282,29 @@ struct HermiteCoulomb {
 };
 
 // One contracted Cartesian block (ab|cd), row-major [a][b][c][d].
+// One Cartesian block over four shells given as centres, angular momenta l[],
+// primitive exponents and the final coefficient of each primitive Gaussian
+// x^i y^j z^k exp(-alpha r^2) (no normalisation applied here).
 template <class R>
-void eri_cart_block(const Shells& S, int A, int B, int C, int D, std::vector<R>& out) {
-  const int sh[4] = {A, B, C, D};
+struct RawShell {
+  const double* center;
+  int l, np;
+  const double* exps;
+  std::vector<R> coef;
+};
+
+template <class R>
+void eri_cart_block_raw(const RawShell<R>* sh, std::vector<R>& out) {
   int l[4];
-  for (int i = 0; i < 4; ++i) l[i] = S.L[sh[i]];
+  for (int i = 0; i < 4; ++i) l[i] = sh[i].l;
   std::vector<std::array<int, 3>> ex[4];
   for (int i = 0; i < 4; ++i) cart_exponents(l[i], ex[i]);
   const int na = ncart(l[0]), nb = ncart(l[1]), nc = ncart(l[2]), nd = ncart(l[3]);
   out.assign((size_t)na * nb * nc * nd, R(0));
-  std::vector<R> co[4];
-  for (int i = 0; i < 4; ++i) {
-    co[i].resize(S.nprim[sh[i]]);
-    normalised_coefs<R>(l[i], S.nprim[sh[i]], S.exps + S.off[sh[i]], S.coefs + S.off[sh[i]], co[i].data());
-  }
+  const std::vector<R>* co[4] = {&sh[0].coef, &sh[1].coef, &sh[2].coef, &sh[3].coef};
   R Ac[4][3];
   for (int i = 0; i < 4; ++i)
-    for (int x = 0; x < 3; ++x) Ac[i][x] = S.centers[3 * sh[i] + x];
+    for (int x = 0; x < 3; ++x) Ac[i][x] = sh[i].center[x];
   const int Lab = l[0] + l[1], Lcd = l[2] + l[3], Ltot = Lab + Lcd;
   const R pi = r_pi<R>();
   // Hermite index lists
@@ -306,9 +312,9 @@ void eri_cart_block(const Shells& S, int A, int B, int C, int D, std::vector<R>&
   Hermite1D<R> Eab[3], Ecd[3];
   HermiteCoulomb<R> Rc;
   std::vector<R> W((size_t)nc * nd * (Lab + 1) * (Lab + 1) * (Lab + 1));
-  for (int i = 0; i < S.nprim[A]; ++i)
-    for (int j = 0; j < S.nprim[B]; ++j) {
-      R a = S.exps[S.off[A] + i], b = S.exps[S.off[B] + j];
+  for (int i = 0; i < sh[0].np; ++i)
+    for (int j = 0; j < sh[1].np; ++j) {
+      R a = sh[0].exps[i], b = sh[1].exps[j];
       R p = a + b;
       R P[3], KAB = 1;
       for (int x = 0; x < 3; ++x) {
@@ -317,9 +323,9 @@ void eri_cart_block(const Shells& S, int A, int B, int C, int D, std::vector<R>&
         KAB *= r_exp<R>(-a * b / p * d * d);
       }
       for (int x = 0; x < 3; ++x) Eab[x].build(l[0], l[1], p, P[x] - Ac[0][x], P[x] - Ac[1][x]);
-      for (int k = 0; k < S.nprim[C]; ++k)
-        for (int m = 0; m < S.nprim[D]; ++m) {
-          R c = S.exps[S.off[C] + k], d = S.exps[S.off[D] + m];
+      for (int k = 0; k < sh[2].np; ++k)
+        for (int m = 0; m < sh[3].np; ++m) {
+          R c = sh[2].exps[k], d = sh[3].exps[m];
           R q = c + d;
           R Q[3], KCD = 1;
           for (int x = 0; x < 3; ++x) {
@@ -330,8 +336,8 @@ void eri_cart_block(const Shells& S, int A, int B, int C, int D, std::vector<R>&
           for (int x = 0; x < 3; ++x) Ecd[x].build(l[2], l[3], q, Q[x] - Ac[2][x], Q[x] - Ac[3][x]);
           R alpha = p * q / (p + q);
           Rc.build(Ltot, alpha, P[0] - Q[0], P[1] - Q[1], P[2] - Q[2]);
-          R pref = R(2) * std::pow(pi, R(2.5)) / (p * q * r_sqrt<R>(p + q)) * KAB * KCD * co[0][i] * co[1][j] *
-                   co[2][k] * co[3][m];
+          R pref = R(2) * std::pow(pi, R(2.5)) / (p * q * r_sqrt<R>(p + q)) * KAB * KCD * (*co[0])[i] *
+                   (*co[1])[j] * (*co[2])[k] * (*co[3])[m];
           // ket half: W_cd[tuv] = sum_{tau,nu,phi} (-1)^{tau+nu+phi} E^cd_{tau nu phi} R_{t+tau,u+nu,v+phi}
           const int HL = Lab + 1;
           for (int ic = 0; ic < nc; ++ic)
@@ -379,6 +385,20 @@ void eri_cart_block(const Shells& S, int A, int B, int C, int D, std::vector<R>&
             }
         }
     }
+}
+
+template <class R>
+RawShell<R> raw_shell(const Shells& S, int s) {
+  RawShell<R> r{S.centers + 3 * s, S.L[s], S.nprim[s], S.exps + S.off[s], std::vector<R>(S.nprim[s])};
+  normalised_coefs<R>(S.L[s], S.nprim[s], S.exps + S.off[s], S.coefs + S.off[s], r.coef.data());
+  return r;
+}
+
+// Cartesian block (ab|cd) of four contracted, normalised shells (Eq. (1)).
+template <class R>
+void eri_cart_block(const Shells& S, int A, int B, int C, int D, std::vector<R>& out) {
+  const RawShell<R> sh[4] = {raw_shell<R>(S, A), raw_shell<R>(S, B), raw_shell<R>(S, C), raw_shell<R>(S, D)};
+  eri_cart_block_raw<R>(sh, out);
 }
 
 // Apply T^(la) (x) T^(lb) (x) T^(lc) (x) T^(ld) to a Cartesian block (Eq. (17)).
@@ -811,6 +831,86 @@ int ora_K_blocks(int nshell, const double* centers, const int* L, const int* npr
     for (int t = 0; t < nt; ++t)
       for (size_t k = 0; k < acc.size(); ++k) acc[k] += part[t][k];
     std::memcpy(out + out_off[r], acc.data(), acc.size() * sizeof(double));
+  }
+  return 0;
+}
+
+// First derivatives of the block (ab|cd) with respect to the centres.  A
+// primitive Cartesian Gaussian obeys d/dA_i [x_A^{a_i} ... e^{-alpha r_A^2}] =
+// 2 alpha (a + 1_i) - a_i (a - 1_i) (the raising/lowering pair of the
+// Obara-Saika scheme), so the derivative block of shell k along axis i is the
+// block with shell k raised to l+1 and every primitive weighted by 2 alpha,
+// minus a_i times the block with shell k lowered to l-1 (same normalised
+// coefficients), then the spherical transform.  out (per quartet) holds
+// [centre k = 0..3 in the given order][axis x, y, z][block].
+int ora_eri_deriv_blocks(int nshell, const double* centers, const int* L, const int* nprim, const int* off,
+                         const double* exps, const double* coefs, const int* quartets, long long n, int spherical,
+                         const long long* out_off, double* out, int nthreads) {
+  Shells S{nshell, centers, L, nprim, off, exps, coefs};
+  if (!shells_ok(S) || !quartets || !out || !out_off || n < 0) return -1;
+  for (long long r = 0; r < 4 * n; ++r)
+    if (quartets[r] < 0 || quartets[r] >= nshell) return -1;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads > 0 ? nthreads : 1)
+  for (long long qi = 0; qi < n; ++qi) {
+    const int* q = quartets + 4 * qi;
+    const RawShell<double> base[4] = {raw_shell<double>(S, q[0]), raw_shell<double>(S, q[1]),
+                                      raw_shell<double>(S, q[2]), raw_shell<double>(S, q[3])};
+    int l[4], nc[4];
+    for (int k = 0; k < 4; ++k) {
+      l[k] = base[k].l;
+      nc[k] = ncart(l[k]);
+    }
+    size_t bs = 1;
+    for (int k = 0; k < 4; ++k) bs *= (size_t)nfunc(l[k], spherical);
+    std::vector<std::array<int, 3>> ce[4];
+    for (int k = 0; k < 4; ++k) cart_exponents(l[k], ce[k]);
+    for (int k = 0; k < 4; ++k) {
+      RawShell<double> sh[4] = {base[0], base[1], base[2], base[3]};
+      sh[k].l = l[k] + 1;
+      for (int p = 0; p < sh[k].np; ++p) sh[k].coef[p] = base[k].coef[p] * 2.0 * sh[k].exps[p];
+      std::vector<double> up, dn;
+      eri_cart_block_raw<double>(sh, up);
+      std::vector<std::array<int, 3>> eup, edn;
+      cart_exponents(l[k] + 1, eup);
+      if (l[k] > 0) {
+        sh[k].l = l[k] - 1;
+        sh[k].coef = base[k].coef;
+        eri_cart_block_raw<double>(sh, dn);
+        cart_exponents(l[k] - 1, edn);
+      }
+      int du[4] = {nc[0], nc[1], nc[2], nc[3]}, dd[4] = {nc[0], nc[1], nc[2], nc[3]};
+      du[k] = ncart(l[k] + 1);
+      dd[k] = l[k] > 0 ? ncart(l[k] - 1) : 0;
+      for (int ax = 0; ax < 3; ++ax) {
+        std::vector<double> cart((size_t)nc[0] * nc[1] * nc[2] * nc[3]);
+        int o[4];
+        for (o[0] = 0; o[0] < nc[0]; ++o[0])
+          for (o[1] = 0; o[1] < nc[1]; ++o[1])
+            for (o[2] = 0; o[2] < nc[2]; ++o[2])
+              for (o[3] = 0; o[3] < nc[3]; ++o[3]) {
+                std::array<int, 3> e = ce[k][o[k]];
+                e[ax] += 1;
+                int iu = (int)(std::find(eup.begin(), eup.end(), e) - eup.begin());
+                int u[4] = {o[0], o[1], o[2], o[3]};
+                u[k] = iu;
+                double v = up[(((size_t)u[0] * du[1] + u[1]) * du[2] + u[2]) * du[3] + u[3]];
+                e[ax] -= 2;
+                if (e[ax] >= 0) {
+                  int idn = (int)(std::find(edn.begin(), edn.end(), e) - edn.begin());
+                  int d[4] = {o[0], o[1], o[2], o[3]};
+                  d[k] = idn;
+                  v -= (e[ax] + 1) * dn[(((size_t)d[0] * dd[1] + d[1]) * dd[2] + d[2]) * dd[3] + d[3]];
+                }
+                cart[(((size_t)o[0] * nc[1] + o[1]) * nc[2] + o[2]) * nc[3] + o[3]] = v;
+              }
+        std::vector<double> res;
+        if (spherical)
+          cart_to_sph_block<double>(l, cart, res);
+        else
+          res.swap(cart);
+        std::memcpy(out + out_off[qi] + (size_t)(3 * k + ax) * bs, res.data(), bs * sizeof(double));
+      }
+    }
   }
   return 0;
 }

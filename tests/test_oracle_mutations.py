@@ -30,6 +30,9 @@ MUTATIONS = [
     ("J diagonal double count", "Jl[(size_t)(fo[img[0]] + i0) * nbf + fo[img[1]] + i1] += s;",
      "Jl[(size_t)(fo[img[0]] + i0) * nbf + fo[img[1]] + i1] += (img[0] == img[1] ? 0.5 : 1.0) * s;"),
     ("normalisation overlap power", "std::pow(R(2) * p, R(l))", "std::pow(R(2) * p, R(l + 1))"),
+    ("derivative: raising weight", "sh[k].coef[p] = base[k].coef[p] * 2.0 * sh[k].exps[p];",
+     "sh[k].coef[p] = base[k].coef[p] * sh[k].exps[p];"),
+    ("derivative: lowering factor", "v -= (e[ax] + 1) * dn[", "v -= e[ax] * dn["),
 ]
 
 

@@ -419,3 +419,42 @@ def test_K_blocks_match_contraction():
     pairs = [(0, 0), (1, 3), (3, 2)]
     for (a, c), B in zip(pairs, oracle.K_blocks(S, D, pairs, spherical=True, tau=0.0)):
         assert np.allclose(B, Kfull[fo[a]:fo[a + 1], fo[c]:fo[c + 1]], rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------- first derivatives
+
+
+@pytest.mark.parametrize("Ls", [(0, 0, 0, 0), (1, 0, 1, 1), (2, 1, 0, 2), (2, 2, 2, 1), (3, 1, 2, 0)])
+def test_derivative_blocks_match_finite_differences(Ls):
+    """d(ab|cd)/dR_k,i against central differences (Richardson) of the oracle's
+    own integrals with shell k's centre moved along axis i."""
+    rng = np.random.default_rng(40 + sum(Ls))
+    cen = rand_centers(rng, 4, 1.3)
+    nps = [2, 1, 2, 1]
+    ex = np.exp(rng.uniform(np.log(0.3), np.log(6.0), sum(nps)))
+    cf = rng.uniform(0.2, 1.0, sum(nps))
+    S = oracle.ShellSet(cen, list(Ls), nps, ex, cf)
+    got = oracle.eri_deriv_blocks(S, [(0, 1, 2, 3)], spherical=True)[0]
+    for k in range(4):
+        for ax in range(3):
+            def f(x, k=k, ax=ax):
+                c = [np.array(v, dtype=float) for v in cen]
+                c[k][ax] += x
+                return oracle.eri_block(oracle.ShellSet(c, list(Ls), nps, ex, cf), 0, 1, 2, 3, spherical=True)
+            fd = _deriv(f, 0.0, h=4e-3)
+            scale = max(np.abs(fd).max(), 1e-6)
+            assert np.abs(got[k, ax] - fd).max() <= 2e-8 * scale, (Ls, k, ax)
+
+
+def test_derivative_blocks_translation_invariance_and_symmetry():
+    rng = np.random.default_rng(77)
+    Ls = (2, 1, 2, 2)
+    S = oracle.ShellSet(rand_centers(rng, 4, 2.0), list(Ls), [3, 2, 1, 2],
+                        np.exp(rng.uniform(np.log(0.2), np.log(20.0), 8)), rng.uniform(0.1, 1.0, 8))
+    d = oracle.eri_deriv_blocks(S, [(0, 1, 2, 3), (2, 3, 0, 1)], spherical=True)
+    scale = np.abs(d[0]).max()
+    # sum over the four centres vanishes for every axis
+    assert np.abs(d[0].sum(axis=0)).max() <= 1e-12 * scale
+    # (cd|ab) derivatives are the transposed (ab|cd) ones with the centres relabelled
+    t = np.transpose(d[1], (0, 1, 4, 5, 2, 3))[[2, 3, 0, 1]]
+    assert np.allclose(t, d[0], rtol=1e-12, atol=1e-14 * scale)
