@@ -53,6 +53,9 @@ WORKLOADS = {
     "g_shells": {"desc": "g-shell batch: (gg|gg) x 16,384 + (gd|gd) x 65,536 quartets, degree 2, centers U[0,10]^3 "
                          "bohr, exponents log-U[0.05,100], spherical",
                  "classes": [((4, 4, 4, 4), 16384, 2, 3), ((4, 2, 4, 2), 65536, 2, 103)]},
+    "deriv": {"desc": "first derivatives (12 blocks per quartet): (pp|pp) x 524,288 + (dd|dd) x 131,072 quartets, "
+                      "degree 1, centers U[0,10]^3 bohr, exponents log-U[0.05,100], spherical",
+              "classes": [((1, 1, 1, 1), 1 << 19, 1, 4), ((2, 2, 2, 2), 1 << 17, 1, 104)], "deriv": True},
     "cluster64": {"desc": "64-atom synthetic cluster (radius 12 bohr, 32 heavy 3s2p1d + 32 light 2s1p, 1-6 "
                           "primitives, exponents log-U[0.1,5000]): Coulomb J over all unique quartets surviving "
                           "Schwarz 1e-10, spherical, D = C C^T", "cluster": (64, 3)},
@@ -165,7 +168,10 @@ def cpu_oracle_rate(wl, budget_s=20.0, nthreads=None):
             s, q = W.homogeneous(cls, m, deg, seed_index=seed + 7000 + done)
             S = oracle.ShellSet(s.centers, s.L, s.nprim, s.exps, s.coefs)
             t0 = time.perf_counter()
-            oracle.eri_blocks(S, q, spherical=True, nthreads=nthreads)
+            if wl.get("deriv"):
+                oracle.eri_deriv_blocks(S, q, spherical=True, nthreads=nthreads)
+            else:
+                oracle.eri_blocks(S, q, spherical=True, nthreads=nthreads)
             dt = time.perf_counter() - t0
             spent += dt
             done += m
@@ -353,6 +359,13 @@ def cpu_oracle_rate_cluster(s, counts, budget_s=12.0):
         f"screened class mix", oracle.default_threads()
 
 
+def deriv_stats(cls):
+    """Generator statistics of a derivative kernel (csrc/generated/classes.json)."""
+    meta = json.load(open(os.path.join(ROOT, "electron_repulsion_integrals_gb300", "csrc", "generated",
+                                       "classes.json")))["classes"]["d{}{}{}{}".format(*cls)]
+    return {"vrr_flops": meta["vrr_flops"], "hrr_flops": meta["hrr_flops"]}
+
+
 def run_ours(a, rank, world, local_rank):
     import torch
     import electron_repulsion_integrals_gb300 as eri
@@ -375,18 +388,23 @@ def run_ours(a, rank, world, local_rank):
         s, q = W.homogeneous(cls, n, deg, seed_index=seed)
         plan = eri.Plan(s, spherical=True)
         qd = torch.as_tensor(q, device=dev)
-        out = torch.empty(n * eri.block_size(cls), dtype=torch.float64, device=dev)
+        deriv = bool(wl.get("deriv"))
+        out = torch.empty(n * eri.block_size(cls) * (12 if deriv else 1), dtype=torch.float64, device=dev)
         st = eri.eri_class_info(cls)
+        if deriv:
+            st = dict(st, **deriv_stats(cls))
+            st["staged"] = 2
         flops_q = st["vrr_flops"] * deg ** 4 + st["hrr_flops"]
         batches.append(dict(cls=cls, n=n, deg=deg, shells=s, q=q, plan=plan, qd=qd, out=out, flops=flops_q,
                             stats=st))
     torch.cuda.synchronize()
+    compute = eri.eri_compute_class_deriv if wl.get("deriv") else eri.eri_compute_class
 
     def step(record=None):
         for b in batches:
             if record is not None:
                 record[b["cls"]][0].record(stream)
-            eri.eri_compute_class(b["plan"].handle, b["cls"], b["qd"], b["out"], stream)
+            compute(b["plan"].handle, b["cls"], b["qd"], b["out"], stream)
             if record is not None:
                 record[b["cls"]][1].record(stream)
 
@@ -453,7 +471,7 @@ def run_ours(a, rank, world, local_rank):
                 torch.cuda.synchronize()
                 t1h = time.perf_counter()
                 qd = hq.to(dev, non_blocking=True)
-                eri.eri_compute_class(plan.handle, b["cls"], qd, b["out"], stream)
+                compute(plan.handle, b["cls"], qd, b["out"], stream)
                 torch.cuda.synchronize()
                 t2h = time.perf_counter()
                 ho.copy_(b["out"], non_blocking=True)
@@ -483,7 +501,7 @@ def run_ours(a, rank, world, local_rank):
             "per_class": per_class,
             "roofline": {"bound": "alu", "kernel": dname, "achieved": ach, "peak": FP64_PEAK_TFLOPS,
                          "unit": "TFLOP/s", "frac": ach / FP64_PEAK_TFLOPS,
-                         "traffic": dram_traffic(dom["cls"], dom["n"]),
+                         "traffic": None if wl.get("deriv") else dram_traffic(dom["cls"], dom["n"]),
                          "peak_source": "FP64 pipe: 152 SMs x 2 DFMA/clk x 2 flop x 2.07 GHz"},
             "clocks": clk, "e2e": e2e, "cpu_baseline": cpu,
             "gpu_launches": len(batches) * a.steps}

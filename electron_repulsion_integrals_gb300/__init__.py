@@ -70,6 +70,8 @@ def lib():
         L.eri_compute_class.argtypes = [vp] + [ctypes.c_int] * 4 + [vp, ctypes.c_longlong, dp, ctypes.c_longlong, vp]
         L.eri_compute_class_noalloc.argtypes = [vp] + [ctypes.c_int] * 4 + [vp, ctypes.c_longlong, dp,
                                                                              ctypes.c_longlong, vp]
+        L.eri_compute_class_deriv.argtypes = [vp] + [ctypes.c_int] * 4 + [vp, ctypes.c_longlong, dp, ctypes.c_longlong,
+                                                                          vp]
         L.eri_schwarz.argtypes = [vp, ctypes.c_int, ctypes.c_int, vp, ctypes.c_longlong, dp, vp]
         L.eri_build_J.argtypes = [vp, dp, dp, vp]
         L.eri_build_JK.argtypes = [vp, dp, dp, dp, vp]
@@ -174,6 +176,16 @@ def eri_compute_class_noalloc(plan, cls, quartets, out, stream=None):
     _check("eri_compute_class_noalloc", rc)
 
 
+def eri_compute_class_deriv(plan, cls, quartets, out, stream=None):
+    """First derivatives of the blocks of eri_compute_class: out holds, per
+    quartet, 12 blocks [shell position 0..3][axis x, y, z][block]."""
+    n = int(quartets.shape[0])
+    rc = lib().eri_compute_class_deriv(plan, *[int(x) for x in cls], _ptr(quartets) if n else None, n,
+                                       _ptr(out) if n else None, int(out.numel()),
+                                       ctypes.c_void_p(_stream_handle(stream)))
+    _check("eri_compute_class_deriv", rc)
+
+
 def eri_schwarz(plan, la, lb, pairs, q_out, stream=None):
     rc = lib().eri_schwarz(plan, int(la), int(lb), _ptr(pairs), int(pairs.shape[0]), _ptr(q_out),
                            ctypes.c_void_p(_stream_handle(stream)))
@@ -232,6 +244,15 @@ class Plan:
         if out is None:
             out = torch.empty(n * block_size(cls, self.spherical), dtype=torch.float64, device=quartets.device)
         eri_compute_class(self.handle, cls, quartets, out, stream)
+        return out
+
+    def compute_class_deriv(self, cls, quartets, out=None, stream=None):
+        import torch
+        n = int(quartets.shape[0])
+        if out is None:
+            out = torch.empty(max(n, 1) * 12 * block_size(cls, self.spherical), dtype=torch.float64,
+                              device=quartets.device)
+        eri_compute_class_deriv(self.handle, cls, quartets, out, stream)
         return out
 
     def schwarz(self, la, lb, pairs, stream=None):

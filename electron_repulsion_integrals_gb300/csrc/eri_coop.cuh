@@ -28,14 +28,17 @@ constexpr int kCoopBatch = 16;                // primitive quartets set up at on
 //   0..2 P-A, 3..5 W-P, 6..8 Q-C, 9..11 W-Q, 12 rho/zeta, 13 rho/eta,
 //   14.. k/(2 zeta) for k = 1..La, then k/(2 eta) for k = 1..Lc, then
 //   k/(2(zeta+eta)) for k = 0..max(La, Lc), then F'_0..F'_L.
-template <int La, int Lc>
+//   With NW > 0 (derivative classes) NW accumulation weights follow:
+//   2 alpha, 2 beta, 2 gamma of the primitive quartet's A, B, C primitives.
+template <int La, int Lc, int NW = 0>
 struct CoopSetup {
   static constexpr int L = La + Lc;
   static constexpr int KO2Z = 14;
   static constexpr int KO2E = KO2Z + La;
   static constexpr int KO2ZE = KO2E + Lc;
   static constexpr int F = KO2ZE + (La > Lc ? La : Lc) + 1;
-  static constexpr int SIZE = F + L + 1;
+  static constexpr int WGT = F + L + 1;
+  static constexpr int SIZE = WGT + NW;
   static constexpr int STRIDE = SIZE | 1;  // odd stride: lanes hit different banks
 };
 
@@ -44,9 +47,9 @@ struct CoopCol {
 };
 
 // Parameters of primitive quartet (iab, icd) of quartet Q into s[] (one lane).
-template <int MODE, int La, int Lc>
+template <int MODE, int La, int Lc, int NW = 0>
 __device__ __forceinline__ void coop_setup_one(const EriLaunch& P, const Quartet& Q, int iab, int icd, double* s) {
-  using S = CoopSetup<La, Lc>;
+  using S = CoopSetup<La, Lc, NW>;
   PrimPair pb, pk;
   if constexpr (MODE == kCoulomb) {
     load_prim(P.prims, Q.pab + iab, pb);
@@ -58,6 +61,11 @@ __device__ __forceinline__ void coop_setup_one(const EriLaunch& P, const Quartet
               __ldg(P.sh.coef + Q.pb + j), Q.A, Q.AB, Q.rAB2, pb);
     make_pair(__ldg(P.sh.exps + Q.pc + k), __ldg(P.sh.coef + Q.pc + k), __ldg(P.sh.exps + Q.pd + l),
               __ldg(P.sh.coef + Q.pd + l), Q.C, Q.CD, Q.rCD2, pk);
+    if constexpr (NW > 0) {
+      s[S::WGT] = 2.0 * __ldg(P.sh.exps + Q.pa + i);
+      s[S::WGT + 1] = 2.0 * __ldg(P.sh.exps + Q.pb + j);
+      s[S::WGT + 2] = 2.0 * __ldg(P.sh.exps + Q.pc + k);
+    }
   }
   QuartetSetup qs;
   double F[S::L + 1];
@@ -88,7 +96,7 @@ __device__ __forceinline__ void coop_setup_one(const EriLaunch& P, const Quartet
 template <class C>
 __device__ __forceinline__ void coop_vrr(double* __restrict__ arena, const double* __restrict__ s,
                                          double* __restrict__ H, int lane, bool first) {
-  using S = CoopSetup<C::La, C::Lc>;
+  using S = CoopSetup<C::La, C::Lc, C::NW>;
   constexpr int NE = C::NE;
   double* bra = arena + C::BRA_COL;
   // column 0: Boys values [00|00]^(m)
@@ -132,6 +140,12 @@ __device__ __forceinline__ void coop_vrr(double* __restrict__ arena, const doubl
     for (int k = lane; k < C::NET; k += 32) {
       const double v = bra[C::IE_LO + k];
       H[k] = first ? v : H[k] + v;
+#pragma unroll
+      for (int w = 1; w <= C::NW; ++w) {
+        const double wt = s[S::WGT + w - 1];
+        double* Hw = H + (size_t)w * C::NH;
+        Hw[k] = first ? wt * v : fma(wt, v, Hw[k]);
+      }
     }
   }
   // ket columns
@@ -245,6 +259,12 @@ __device__ __forceinline__ void coop_vrr(double* __restrict__ arena, const doubl
         if (k < C::NET) {
           const double v = O[C::IE_LO + k];
           Ht[k] = first ? v : hold[j] + v;
+#pragma unroll
+          for (int w = 1; w <= C::NW; ++w) {
+            const double wt = s[S::WGT + w - 1];
+            double* Hw = Ht + (size_t)w * C::NH;
+            Hw[k] = first ? wt * v : fma(wt, v, Hw[k]);
+          }
         }
       }
     }

@@ -1,0 +1,102 @@
+// First derivatives of contracted ERI blocks with respect to the four centres.
+//
+// For a primitive Cartesian Gaussian, d/dA_i [x_A^{a_i} ... e^{-alpha r_A^2}]
+// = 2 alpha (a + 1_i) - a_i (a - 1_i).  The derivative kernels therefore run
+// the cooperative tier's VRR for the class extended by one on the bra and on
+// the ket, and accumulate four sets of targets per contracted quartet: plain,
+// and weighted by 2 alpha, 2 beta, 2 gamma (exponents of the A, B, C
+// primitives).  The generated HRR functions then form, per ket column,
+//   d/dA_i: (a+1_i b| from the 2 alpha set minus a_i (a-1_i b| from the plain set,
+//   d/dB_i: (a b+1_i| from the 2 beta set  minus b_i (a b-1_i| from the plain set,
+// transform them to spherical form, and run the ket HRR + transform; d/dC_i
+// combines (c+1_i d) from the 2 gamma set with c_i (c-1_i d) in the ket step.
+// d/dD = -(d/dA + d/dB + d/dC) (translation invariance).  Output per quartet:
+// 12 blocks, [requested position of the shell 0..3][axis x, y, z][block].
+#pragma once
+
+#include "eri_coop.cuh"
+
+namespace eri {
+
+// Derivative-output helpers used by the generated ket functions.  Block
+// (slot k, axis x) of quartet q, element offset o within the block.
+__device__ __forceinline__ double* deriv_out(const EriLaunch& P, const Quartet& Q, long long q, int k, int x) {
+  return P.out + q * P.out_stride + (long long)(Q.pos[k] * 3 + x) * P.dblock;
+}
+
+}  // namespace eri
+
+// Kernel of one derivative class.  C: traits (NW = 3); BRA_A / BRA_B fill the
+// three axis sets of d/dA / d/dB rows, BRA_0G the plain and 2-gamma rows;
+// KET_AB(P, Q, q, r, G, k) writes d/d(slot k) for the three axes from three
+// row sets, KET_C(P, Q, q, r, G) writes d/dC.
+#define ERI_DERIV_KERNEL(NAME, C, BRA_A, BRA_B, BRA_0G, KET_AB, KET_C)                                   \
+  template <bool CONTRACTED>                                                                              \
+  __global__ void __launch_bounds__(kCoopThreads) NAME(const EriLaunch P) {                               \
+    extern __shared__ double smem_[];                                                                     \
+    using S_ = CoopSetup<C::La, C::Lc, C::NW>;                                                            \
+    const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;                                            \
+    double* arena = smem_ + (size_t)wib * C::WARP_SMEM;                                                   \
+    double* setup = arena + C::ARENA;                                                                     \
+    const long long nw = (long long)gridDim.x * kCoopWarps;                                               \
+    const long long wid = (long long)blockIdx.x * kCoopWarps + wib;                                       \
+    double* H = P.scratch + (size_t)wid * C::NH * (C::NW + 1);                                            \
+    for (long long q = wid; q < P.n; q += nw) {                                                           \
+      Quartet Q;                                                                                          \
+      load_quartet<C::la == C::lb ? 1 : 0, C::lc == C::ld ? 1 : 0, C::la + C::lb, C::lc + C::ld>(P, q, Q); \
+      const int nab = Q.na * Q.nb, ncd = Q.nc * Q.nd, nprim = nab * ncd;                                  \
+      for (int base = 0; base < nprim; base += kCoopBatch) {                                              \
+        const int p = base + lane;                                                                        \
+        if (p < nprim) coop_setup_one<kStore, C::La, C::Lc, C::NW>(P, Q, p / ncd, p - (p / ncd) * ncd,    \
+                                                                   setup + lane * S_::STRIDE);            \
+        __syncwarp();                                                                                     \
+        const int cnt = nprim - base < kCoopBatch ? nprim - base : kCoopBatch;                            \
+        for (int pp = 0; pp < cnt; ++pp) coop_vrr<C>(arena, setup + pp * S_::STRIDE, H, lane, base + pp == 0); \
+        __syncwarp();                                                                                     \
+      }                                                                                                   \
+      double* G = arena;                                                                                  \
+      for (int fi = lane; fi < C::NF; fi += 32) BRA_A(Q, H, fi, G);                                       \
+      __syncwarp();                                                                                       \
+      for (int r = lane; r < C::NR; r += 32) KET_AB(P, Q, q, r, G, 0);                                    \
+      __syncwarp();                                                                                       \
+      for (int fi = lane; fi < C::NF; fi += 32) BRA_B(Q, H, fi, G);                                       \
+      __syncwarp();                                                                                       \
+      for (int r = lane; r < C::NR; r += 32) KET_AB(P, Q, q, r, G, 1);                                    \
+      __syncwarp();                                                                                       \
+      for (int fi = lane; fi < C::NF; fi += 32) BRA_0G(Q, H, fi, G);                                      \
+      __syncwarp();                                                                                       \
+      for (int r = lane; r < C::NR; r += 32) KET_C(P, Q, q, r, G);                                        \
+      __syncwarp();                                                                                       \
+    }                                                                                                     \
+  }
+
+#define ERI_DERIV_SMEM_(T) ((size_t)kCoopWarps * (T::WARP_SMEM) * sizeof(double))
+// Per-class entry points: launch (store mode, contracted or not), grid and
+// scratch sizing (four accumulator sets per warp).
+#define ERI_DEFINE_DERIV_LAUNCHER(LA, LB, LC, LD, KERNEL, T)                                             \
+  extern "C" int eri_dlaunch_c##LA##LB##LC##LD(const EriLaunch* P, int contracted, int blocks, cudaStream_t st) { \
+    if (contracted) {                                                                                    \
+      cudaFuncSetAttribute(KERNEL<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ERI_DERIV_SMEM_(T)); \
+      KERNEL<true><<<blocks, kCoopThreads, ERI_DERIV_SMEM_(T), st>>>(*P);                                \
+    } else {                                                                                             \
+      cudaFuncSetAttribute(KERNEL<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ERI_DERIV_SMEM_(T)); \
+      KERNEL<false><<<blocks, kCoopThreads, ERI_DERIV_SMEM_(T), st>>>(*P);                               \
+    }                                                                                                    \
+    return (int)cudaGetLastError();                                                                      \
+  }                                                                                                      \
+  extern "C" int eri_dgrid_c##LA##LB##LC##LD(int nsm, long long n, long long* blocks, long long* scratch) { \
+    int occ = 0;                                                                                         \
+    cudaFuncSetAttribute(KERNEL<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ERI_DERIV_SMEM_(T)); \
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, KERNEL<true>, kCoopThreads, ERI_DERIV_SMEM_(T)) != \
+            cudaSuccess || occ < 1) {                                                                    \
+      (void)cudaGetLastError();                                                                          \
+      occ = 1;                                                                                           \
+    }                                                                                                    \
+    long long b = (long long)nsm * occ;                                                                  \
+    const long long need = (n + kCoopWarps - 1) / kCoopWarps;                                            \
+    if (b > need) b = need;                                                                              \
+    if (b < 1) b = 1;                                                                                    \
+    *blocks = b;                                                                                         \
+    *scratch = b * kCoopWarps * (long long)T::NH * (T::NW + 1);                                          \
+    return 0;                                                                                            \
+  }

@@ -104,6 +104,7 @@ struct EriLaunch {
   double* out;
   long long out_stride;  // doubles per block
   int ostr[4];           // stride of canonical axis k in the requested block layout
+  long long dblock;      // derivative blocks: doubles per block (12 blocks per quartet)
   // Schwarz mode: q_out[i] = sqrt(max diag |(ab|ab)|) of quartet i
   double* q_out;
   // Coulomb mode: work item t of the class is found through the segment list;
@@ -150,6 +151,7 @@ struct Quartet {
   double wk;           // 1 / (number of the 8 index permutations that leave the quartet unchanged)
   int ost[4];          // store mode: output stride of canonical axes a, b, c, d
   int rb, rk;          // cooperative tier: bra / ket pair reversed (VRR on the lower-l shell)
+  int pos[4];          // requested position of the shell in canonical slot k
 };
 
 // Which shell of a pair (total angular momentum N = la + lb) should carry the
@@ -215,6 +217,7 @@ __device__ __forceinline__ void load_quartet(const EriLaunch& P, long long q, Qu
     const int c = P.canon[k];
     Q.s[k] = c == 0 ? req[0] : c == 1 ? req[1] : c == 2 ? req[2] : req[3];
     Q.ost[k] = P.ostr[k];
+    Q.pos[k] = c;
   }
   Q.rb = 0;
   Q.rk = 0;
@@ -226,6 +229,9 @@ __device__ __forceinline__ void load_quartet(const EriLaunch& P, long long q, Qu
       const int u = Q.ost[0];
       Q.ost[0] = Q.ost[1];
       Q.ost[1] = u;
+      const int w = Q.pos[0];
+      Q.pos[0] = Q.pos[1];
+      Q.pos[1] = w;
     } else {
       Q.rb = 1;
     }
@@ -238,6 +244,9 @@ __device__ __forceinline__ void load_quartet(const EriLaunch& P, long long q, Qu
       const int u = Q.ost[2];
       Q.ost[2] = Q.ost[3];
       Q.ost[3] = u;
+      const int w = Q.pos[2];
+      Q.pos[2] = Q.pos[3];
+      Q.pos[3] = w;
     } else {
       Q.rk = 1;
     }

@@ -34,6 +34,7 @@ screen::Screen*& plan_screen(eri_plan* p);
 int class_launcher(const int l[4], int (**launch)(const EriLaunch*, int, int, int, cudaStream_t), int* slots);
 void fill_plan_inputs(const eri_plan* p, EriLaunch& P);
 bool plan_contracted(const eri_plan* p);
+double* plan_scratch(eri_plan* p, size_t doubles, int* rc);  // grows the plan's scratch; rc = eri_status
 int plan_device(const eri_plan* p);
 int built_lmax();
 double plan_tau(const eri_plan* p);

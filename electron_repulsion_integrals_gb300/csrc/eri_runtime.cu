@@ -326,6 +326,10 @@ void eri::host::fill_plan_inputs(const eri_plan* p, EriLaunch& P) {
   P.boys = p->dboys;
 }
 bool eri::host::plan_contracted(const eri_plan* p) { return p->contracted; }
+double* eri::host::plan_scratch(eri_plan* p, size_t doubles, int* rc) {
+  *rc = ensure_scratch(p, doubles);
+  return *rc ? nullptr : p->scratch;
+}
 double eri::host::plan_tau(const eri_plan* p) { return p->tau; }
 size_t eri::host::plan_nprim_total(const eri_plan* p) { return p->hexps.size(); }
 const double* eri::host::plan_dcoef(const eri_plan* p) { return p->dcoef; }

@@ -38,13 +38,14 @@ using namespace eri;
 
 namespace {
 
-// Largest number of primitive quartets one thread evaluates for one work item
-// of the J/K build.  A contracted quartet of 6-primitive shells has 1,296; run
-// by one thread it would set the kernel's critical path (one FP64 instruction
-// per dependent-latency interval, ~64 cycles) long after the other threads
-// are done.  Digestion is linear in the integrals, so each part of a quartet
-// is transformed and scattered on its own.
-constexpr long long kMaxPrimPerItem = 64;
+// Work items of the J/K build.  A contracted quartet of 6-primitive shells has
+// 1,296 primitive quartets; run by one thread it can set the kernel's critical
+// path (one FP64 instruction per dependent-latency interval, ~64 cycles) long
+// after the other threads are done.  Digestion is linear in the integrals, so
+// a quartet may be cut into parts that are transformed and scattered on their
+// own.  kThreadsPerClass: threads of one class launch (152 SMs x 256).
+constexpr long long kMinPrimPerItem = 64;
+constexpr double kThreadsPerClass = 152.0 * 256.0;
 
 #define CUDA_TRY(x)                                                        \
   do {                                                                     \
@@ -385,17 +386,7 @@ int build(eri_plan* p, cudaStream_t st) {
                 }
                 if (cb == ck && gk.first <= i && i < gk.first + gk.count) cnt = std::min(cnt, i - gk.first + 1);
                 if (cnt <= 0) continue;
-                // cut heavy quartets into work items of at most kMaxPrimPerItem
-                // primitive quartets: sb parts of the bra primitive pairs,
-                // then sk parts of the ket ones
-                int sb = 1, sk = 1;
-                if ((long long)gb.K * gk.K > kMaxPrimPerItem) {
-                  sb = (int)std::min<long long>(gb.K, ((long long)gb.K * gk.K + kMaxPrimPerItem - 1) / kMaxPrimPerItem);
-                  const long long per_b = (gb.K + sb - 1) / sb;
-                  if (per_b * gk.K > kMaxPrimPerItem)
-                    sk = (int)std::min<long long>(gk.K, (per_b * gk.K + kMaxPrimPerItem - 1) / kMaxPrimPerItem);
-                }
-                segs.push_back(make_int4(i, gk.first, cnt, sb | (sk << 16)));
+                segs.push_back(make_int4(i, gk.first, cnt, 1 | (1 << 16)));
                 cost.push_back((long long)gb.K * gk.K);
                 kb_of.push_back(gb.K);
                 kk_of.push_back(gk.K);
@@ -405,6 +396,24 @@ int build(eri_plan* p, cudaStream_t st) {
           if (segs.empty()) {
             S->classes.push_back(W);
             continue;
+          }
+          // Cut heavy quartets into work items: sb parts of the bra primitive
+          // pairs, then sk parts of the ket ones, so that no item holds more
+          // than pmax primitive quartets.  pmax is kMinPrimPerItem or half the
+          // class's average primitive quartets per thread, whichever is larger:
+          // a class with work enough for every thread keeps its quartets whole
+          // (each cut repeats the HRR, transform and scatter of the quartet).
+          const double per_thread = W.prim_total / (double)kThreadsPerClass;
+          const long long pmax = std::max<long long>(kMinPrimPerItem, (long long)(0.5 * per_thread));
+          for (size_t k = 0; k < segs.size(); ++k) {
+            const long long Kb = kb_of[k], Kk = kk_of[k];
+            int sb = 1, sk = 1;
+            if (Kb * Kk > pmax) {
+              sb = (int)std::min<long long>(Kb, (Kb * Kk + pmax - 1) / pmax);
+              const long long per_b = (Kb + sb - 1) / sb;
+              if (per_b * Kk > pmax) sk = (int)std::min<long long>(Kk, (per_b * Kk + pmax - 1) / pmax);
+            }
+            segs[k].w = sb | (sk << 16);
           }
           std::vector<int> ord(segs.size());
           std::iota(ord.begin(), ord.end(), 0);

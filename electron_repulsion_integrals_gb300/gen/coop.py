@@ -92,15 +92,17 @@ class CoopPlan:
     nodes: int = 0             # VRR nodes per primitive quartet (one DMUL each, the rest FMAs)
 
 
-def plan(cls):
+def plan(cls, e_lo=None, f_lo=None):
+    """Column schedule of class cls; targets [e|f] with |e| >= e_lo (default
+    min(la, lb)) and |f| >= f_lo (default min(lc, ld))."""
     la, lb, lc, ld = cls
     La, Lc = la + lb, lc + ld
     L = La + Lc
     e_list = [e for k in range(La + 1) for e in cart_list(k)]
     eidx = {e: i for i, e in enumerate(e_list)}
     NE = len(e_list)
-    ie_lo = sum(ncart(k) for k in range(min(la, lb)))
-    lcmin = min(lc, ld)
+    ie_lo = sum(ncart(k) for k in range(min(la, lb) if e_lo is None else e_lo))
+    lcmin = min(lc, ld) if f_lo is None else f_lo
     f_targets = [f for j in range(lcmin, Lc + 1) for f in cart_list(j)]
     fidx = {f: i for i, f in enumerate(f_targets)}
     P = CoopPlan(tuple(cls), La, Lc, L, NE, e_list, ie_lo, f_targets)
@@ -228,6 +230,48 @@ def _arr(name, ctype, items, fmt):
     return f"__device__ const {ctype} {name}[] = {{{body}}};"
 
 
+def plan_tables(P, cname):
+    """Device tables of a column schedule (bra nodes, per-axis e lists, ket
+    column steps) and the trait accessors that expose them; returns
+    (table lines, accessor lines, number of bra nodes)."""
+    by = [x for lev in P.bra_nodes_y for x in lev]
+    bys = [0]
+    for lev in P.bra_nodes_y:
+        bys.append(bys[-1] + len(lev))
+    bn = [x for lev in P.bra_nodes_n for x in lev]
+    bns = [0]
+    for lev in P.bra_nodes_n:
+        bns.append(bns[-1] + len(lev))
+    bc = P.bra_col
+    i4 = lambda t: "{0,0,0,0}" if t is None else "{%d,%d,%d,%d}" % t
+    t = []
+    t.append(_arr(f"kBraY_{cname}", "int4", [(bc + o, bc + x, bc + y, ax | (ky << 2)) for o, x, y, ax, ky in by], i4))
+    t.append(_arr(f"kBraYS_{cname}", "int", bys, lambda v: "0" if v is None else str(v)))
+    t.append(_arr(f"kBraN_{cname}", "int4", [(bc + o, bc + x, ax, 0) for o, x, ax in bn], i4))
+    t.append(_arr(f"kBraNS_{cname}", "int", bns, lambda v: "0" if v is None else str(v)))
+    zall = [z for ax in range(3) for z in P.zlist[ax]]
+    t.append(_arr(f"kZ_{cname}", "int4", [(a, b, c, 0) for a, b, c in zall], i4))
+    nall = [z for ax in range(3) for z in P.nlist[ax]]
+    t.append(_arr(f"kN_{cname}", "int", nall, lambda v: "0" if v is None else str(v)))
+    t.append(_arr(f"kCols_{cname}", "CoopCol", [(c.out, c.x, c.y, c.axis, c.ky, c.level, c.target, 0) for c in P.cols],
+                  lambda v: "{0,0,0,0,0,0,0,0}" if v is None else "{%d,%d,%d,%d,%d,%d,%d,%d}" % v))
+    nz = [len(P.zlist[a]) for a in range(3)]
+    nn = [len(P.nlist[a]) for a in range(3)]
+    a = []
+    a.append(f"  static __device__ __forceinline__ const int4* bra_y() {{ return kBraY_{cname}; }}")
+    a.append(f"  static __device__ __forceinline__ const int* bra_y_start() {{ return kBraYS_{cname}; }}")
+    a.append(f"  static __device__ __forceinline__ const int4* bra_n() {{ return kBraN_{cname}; }}")
+    a.append(f"  static __device__ __forceinline__ const int* bra_n_start() {{ return kBraNS_{cname}; }}")
+    a.append(f"  static __device__ __forceinline__ const CoopCol* cols() {{ return kCols_{cname}; }}")
+    a.append(f"  static __device__ __forceinline__ int nz(int a) {{ return a == 0 ? {nz[0]} : a == 1 ? {nz[1]} : {nz[2]}; }}")
+    a.append(f"  static __device__ __forceinline__ int nn(int a) {{ return a == 0 ? {nn[0]} : a == 1 ? {nn[1]} : {nn[2]}; }}")
+    a.append(f"  static __device__ __forceinline__ const int4* zlist(int a) {{ return kZ_{cname} + (a == 0 ? 0 : a == 1 ? "
+             f"{nz[0]} : {nz[0] + nz[1]}); }}")
+    a.append(f"  static __device__ __forceinline__ const int* nlist(int a) {{ return kN_{cname} + (a == 0 ? 0 : a == 1 ? "
+             f"{nn[0]} : {nn[0] + nn[1]}); }}")
+    return t, a, len(by) + len(bn)
+
+
 def emit_coop_class(cls):
     """CUDA source of the cooperative-tier kernel for canonical class cls."""
     from . import emit as E
@@ -243,39 +287,20 @@ def emit_coop_class(cls):
     NR = nsa * nsb
     GS = NF | 1
     arena = max(P.arena, NR * GS)
-    # tables
-    by = [x for lev in P.bra_nodes_y for x in lev]
-    bys = [0]
-    for lev in P.bra_nodes_y:
-        bys.append(bys[-1] + len(lev))
-    bn = [x for lev in P.bra_nodes_n for x in lev]
-    bns = [0]
-    for lev in P.bra_nodes_n:
-        bns.append(bns[-1] + len(lev))
+    tables, accessors, nbra = plan_tables(P, cname)
     bc = P.bra_col
-    i4 = lambda t: "{0,0,0,0}" if t is None else "{%d,%d,%d,%d}" % t
     lines = []
     w = lines.append
     w(f"// Generated by electron_repulsion_integrals_gb300/gen/eri_gen.py -- do not edit.")
     w(f"// Class ({la}{lb}|{lc}{ld}): L = {L}, warp-cooperative tier; {len(P.cols)} ket column steps, "
-      f"{len(by) + len(bn)} bra nodes, arena {arena} doubles per warp, VRR {P.fp64_ops} FP64 instructions "
+      f"{nbra} bra nodes, arena {arena} doubles per warp, VRR {P.fp64_ops} FP64 instructions "
       f"per primitive quartet.")
     w('#include "../eri_coop.cuh"')
     w("")
     w("namespace eri {")
     w("namespace gen {")
-    w(_arr(f"kBraY_{cname}", "int4", [(bc + o, bc + x, bc + y, ax | (ky << 2)) for o, x, y, ax, ky in by], i4))
-    w(_arr(f"kBraYS_{cname}", "int", bys, lambda v: "0" if v is None else str(v)))
-    w(_arr(f"kBraN_{cname}", "int4", [(bc + o, bc + x, ax, 0) for o, x, ax in bn], i4))
-    w(_arr(f"kBraNS_{cname}", "int", bns, lambda v: "0" if v is None else str(v)))
-    zall = [t for ax in range(3) for t in P.zlist[ax]]
-    w(_arr(f"kZ_{cname}", "int4", [(a, b, c, 0) for a, b, c in zall], i4))
-    nall = [t for ax in range(3) for t in P.nlist[ax]]
-    w(_arr(f"kN_{cname}", "int", nall, lambda v: "0" if v is None else str(v)))
-    w(_arr(f"kCols_{cname}", "CoopCol", [(c.out, c.x, c.y, c.axis, c.ky, c.level, c.target, 0) for c in P.cols],
-           lambda t: "{0,0,0,0,0,0,0,0}" if t is None else "{%d,%d,%d,%d,%d,%d,%d,%d}" % t))
-    nz = [len(P.zlist[a]) for a in range(3)]
-    nn = [len(P.nlist[a]) for a in range(3)]
+    for ln in tables:
+        w(ln)
     w(E.out_scale_table(cls, cname))
     T = f"Traits_{cname}"
     w(f"struct {T} {{")
@@ -283,19 +308,11 @@ def emit_coop_class(cls):
     fi_lc = sum(1 for f in P.f_targets if sum(f) < lc)
     w(f"  static constexpr int NE = {NE}, NET = {NET}, IE_LO = {P.ie_lo}, NF = {NF}, NR = {NR}, GS = {GS};")
     w(f"  static constexpr int LCMIN = {min(lc, ld)}, FI_LC = {fi_lc};")
+    w("  static constexpr int NW = 0;")
     w(f"  static constexpr int NCOL = {len(P.cols)}, BRA_COL = {bc}, ARENA = {arena}, NH = {NF * NET};")
     w(f"  static constexpr int WARP_SMEM = ARENA + kCoopBatch * CoopSetup<La, Lc>::STRIDE;")
-    w(f"  static __device__ __forceinline__ const int4* bra_y() {{ return kBraY_{cname}; }}")
-    w(f"  static __device__ __forceinline__ const int* bra_y_start() {{ return kBraYS_{cname}; }}")
-    w(f"  static __device__ __forceinline__ const int4* bra_n() {{ return kBraN_{cname}; }}")
-    w(f"  static __device__ __forceinline__ const int* bra_n_start() {{ return kBraNS_{cname}; }}")
-    w(f"  static __device__ __forceinline__ const CoopCol* cols() {{ return kCols_{cname}; }}")
-    w(f"  static __device__ __forceinline__ int nz(int a) {{ return a == 0 ? {nz[0]} : a == 1 ? {nz[1]} : {nz[2]}; }}")
-    w(f"  static __device__ __forceinline__ int nn(int a) {{ return a == 0 ? {nn[0]} : a == 1 ? {nn[1]} : {nn[2]}; }}")
-    w(f"  static __device__ __forceinline__ const int4* zlist(int a) {{ return kZ_{cname} + (a == 0 ? 0 : a == 1 ? "
-      f"{nz[0]} : {nz[0] + nz[1]}); }}")
-    w(f"  static __device__ __forceinline__ const int* nlist(int a) {{ return kN_{cname} + (a == 0 ? 0 : a == 1 ? "
-      f"{nn[0]} : {nn[0] + nn[1]}); }}")
+    for ln in accessors:
+        w(ln)
     w("};")
     # bra HRR + sph for one ket column (and, for la != lb, the reversed form:
     # VRR on the lb shell, HRR for (lb, la), rows written in canonical order)

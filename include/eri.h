@@ -149,6 +149,22 @@ int eri_compute_class(eri_plan* plan, int la, int lb, int lc, int ld, const int*
 int eri_compute_class_noalloc(eri_plan* plan, int la, int lb, int lc, int ld, const int* quartets_dev, long long n,
                               double* out_dev, long long out_len, void* stream);
 
+/* First derivatives of the blocks eri_compute_class would return, with
+ * respect to the centres of the four shells: d(ab|cd)/dR_{k,i} for shell
+ * position k = 0..3 (a, b, c, d as requested) and axis i = x, y, z.  Built from
+ * the raising/lowering relation of Cartesian Gaussians,
+ * d/dA_i [x_A^{a_i} ... e^{-alpha r_A^2}] = 2 alpha (a + 1_i) - a_i (a - 1_i),
+ * applied inside the HRR of Eq. (3) to a VRR of the class extended by one on
+ * the bra and the ket (the first-derivative kernel variants of FusionRCG
+ * section IV, "Build system"); d/dD = -(d/dA + d/dB + d/dC) by translation
+ * invariance.
+ * Classes of s, p and d shells (la, lb, lc, ld <= 2).
+ * Layout: per quartet 12 consecutive blocks, [position k][axis i][block], each
+ * block row-major [a][b][c][d] as in eri_compute_class; out_len (doubles) must
+ * be >= 12 n x block size.  Errors: as eri_compute_class; UNSUPPORTED_L above d. */
+int eri_compute_class_deriv(eri_plan* plan, int la, int lb, int lc, int ld, const int* quartets_dev, long long n,
+                            double* out_dev, long long out_len, void* stream);
+
 /* Schwarz factors of `n` shell pairs of class (la, lb): q_out_dev[i] =
  * sqrt(max_{mu in a, nu in b} |(mu nu|mu nu)|) for pairs_dev[i] = (a, b)
  * (device int32 [n][2], shell a of angular momentum la, b of lb), computed on
