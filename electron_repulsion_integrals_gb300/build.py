@@ -145,6 +145,10 @@ def build_variant(name: str, entries, force: bool = False, jobs: int | None = No
                 f.write(src)
         srcs.append(path)
         stats["{}{}{}{}".format(*cls)] = meta
+    dreg = os.path.join(gdir, "registry_deriv.inc")   # no derivative kernels in a variant
+    if not os.path.exists(dreg):
+        with open(dreg, "w") as f:
+            f.write("")
     reg = os.path.join(gdir, "registry.inc")
     text = "".join("ERI_CLASS({}, {}, {}, {})\n".format(*c) for c in classes)
     if not os.path.exists(reg) or open(reg).read() != text:
@@ -155,7 +159,7 @@ def build_variant(name: str, entries, force: bool = False, jobs: int | None = No
                   default=str)
     runtime = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     objdir = os.path.join(vdir, "obj")
-    extra = ["-DERI_REGISTRY_INC=\"" + reg + "\""]
+    extra = ["-DERI_REGISTRY_INC=\"" + reg + "\"", "-DERI_DERIV_REGISTRY_INC=\"" + dreg + "\""]
     jobs = jobs or max(1, min(len(srcs) + len(runtime), os.cpu_count() or 4))
     objs = []
     with cf.ThreadPoolExecutor(jobs) as ex:

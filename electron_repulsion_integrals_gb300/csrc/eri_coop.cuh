@@ -107,31 +107,50 @@ __device__ __forceinline__ void coop_vrr(double* __restrict__ arena, const doubl
 #pragma unroll 1
   for (int k = 0; k < C::La; ++k) {
     const int y0 = C::bra_y_start()[k], y1 = C::bra_y_start()[k + 1];
-    for (int t = y0 + lane; t < y1; t += 64) {
-      const bool two = t + 32 < y1;
-      const int4 na = __ldg(C::bra_y() + t);
-      const int4 nb = __ldg(C::bra_y() + (two ? t + 32 : t));
-      const int axa = na.w & 3, kya = na.w >> 2, axb = nb.w & 3, kyb = nb.w >> 2;
-      double va = s[axa] * bra[na.y];
-      double vb = s[axb] * bra[nb.y];
-      va = fma(s[3 + axa], bra[na.y + NE], va);
-      vb = fma(s[3 + axb], bra[nb.y + NE], vb);
-      va = fma(s[S::KO2Z + kya - 1], fma(-roz, bra[na.z + NE], bra[na.z]), va);
-      vb = fma(s[S::KO2Z + kyb - 1], fma(-roz, bra[nb.z + NE], bra[nb.z]), vb);
-      bra[na.x] = va;
-      if (two) bra[nb.x] = vb;
+    // two nodes per lane while more than 32 remain (warp-uniform test), then one
+    for (int t0 = y0; t0 < y1; t0 += 64) {
+      const int t = t0 + lane;
+      if (t0 + 32 < y1) {
+        const bool two = t + 32 < y1;
+        const int4 na = __ldg(C::bra_y() + t);
+        const int4 nb = __ldg(C::bra_y() + (two ? t + 32 : t));
+        const int axa = na.w & 3, kya = na.w >> 2, axb = nb.w & 3, kyb = nb.w >> 2;
+        double va = s[axa] * bra[na.y];
+        double vb = s[axb] * bra[nb.y];
+        va = fma(s[3 + axa], bra[na.y + NE], va);
+        vb = fma(s[3 + axb], bra[nb.y + NE], vb);
+        va = fma(s[S::KO2Z + kya - 1], fma(-roz, bra[na.z + NE], bra[na.z]), va);
+        vb = fma(s[S::KO2Z + kyb - 1], fma(-roz, bra[nb.z + NE], bra[nb.z]), vb);
+        bra[na.x] = va;
+        if (two) bra[nb.x] = vb;
+      } else if (t < y1) {
+        const int4 na = __ldg(C::bra_y() + t);
+        const int axa = na.w & 3, kya = na.w >> 2;
+        double va = s[axa] * bra[na.y];
+        va = fma(s[3 + axa], bra[na.y + NE], va);
+        va = fma(s[S::KO2Z + kya - 1], fma(-roz, bra[na.z + NE], bra[na.z]), va);
+        bra[na.x] = va;
+      }
     }
     const int n0 = C::bra_n_start()[k], n1 = C::bra_n_start()[k + 1];
-    for (int t = n0 + lane; t < n1; t += 64) {
-      const bool two = t + 32 < n1;
-      const int4 na = __ldg(C::bra_n() + t);
-      const int4 nb = __ldg(C::bra_n() + (two ? t + 32 : t));
-      double va = s[na.z] * bra[na.y];
-      double vb = s[nb.z] * bra[nb.y];
-      va = fma(s[3 + na.z], bra[na.y + NE], va);
-      vb = fma(s[3 + nb.z], bra[nb.y + NE], vb);
-      bra[na.x] = va;
-      if (two) bra[nb.x] = vb;
+    for (int t0 = n0; t0 < n1; t0 += 64) {
+      const int t = t0 + lane;
+      if (t0 + 32 < n1) {
+        const bool two = t + 32 < n1;
+        const int4 na = __ldg(C::bra_n() + t);
+        const int4 nb = __ldg(C::bra_n() + (two ? t + 32 : t));
+        double va = s[na.z] * bra[na.y];
+        double vb = s[nb.z] * bra[nb.y];
+        va = fma(s[3 + na.z], bra[na.y + NE], va);
+        vb = fma(s[3 + nb.z], bra[nb.y + NE], vb);
+        bra[na.x] = va;
+        if (two) bra[nb.x] = vb;
+      } else if (t < n1) {
+        const int4 na = __ldg(C::bra_n() + t);
+        double va = s[na.z] * bra[na.y];
+        va = fma(s[3 + na.z], bra[na.y + NE], va);
+        bra[na.x] = va;
+      }
     }
     __syncwarp();
   }
@@ -171,20 +190,23 @@ __device__ __forceinline__ void coop_vrr(double* __restrict__ arena, const doubl
         hold[j] = k < C::NET ? Ht[k] : 0.0;
       }
     }
-    // nodes with e_i > 0 (cross term [e - 1_i | f]^(m+1)).  Each lane walks
-    // (m, k) over the rows x list rectangle in steps of 32 with integer
-    // arithmetic only, two nodes per iteration so that their dependent FMA
-    // chains overlap (the second node of a lane's last pair repeats the first
-    // and is not stored).
+    // nodes with e_i > 0 (cross term [e - 1_i | f]^(m+1)).  Node u = m nz + k
+    // of the rows x list rectangle; lane l takes u = u0 + l and u0 + l + 32 in
+    // iteration u0 (steps of 64, integer stepping of (m, k) only), so that two
+    // dependent FMA chains overlap; when at most 32 nodes remain (a
+    // warp-uniform test) one node per lane.  A lane without a second node in a
+    // two-node iteration repeats its first and does not store it.
     {
       const int nz = C::nz(st.axis);
       const int4* zl = C::zlist(st.axis);
-      int m = 0, k = lane;
-      while (k >= nz) {
+      const int total = nz > 0 ? rows * nz : 0;  // (no e_i > 0 only when la + lb = 0)
+      int m = 0, k = nz > 0 ? lane : 0;
+      while (nz > 0 && k >= nz) {
         k -= nz;
         ++m;
       }
-      while (m < rows) {
+      for (int u0 = 0; u0 < total; u0 += 64) {
+       if (u0 + 32 < total) {
         int m2 = m, k2 = k + 32;
         while (k2 >= nz) {
           k2 -= nz;
@@ -213,18 +235,29 @@ __device__ __forceinline__ void coop_vrr(double* __restrict__ arena, const doubl
           k -= nz;
           ++m;
         }
+       } else if (m < rows) {
+        const int4 za = __ldg(zl + k);
+        const int oa = m * NE + za.x;
+        double va = qc * X[oa];
+        va = fma(wq, X[oa + NE], va);
+        if (hy) va = fma(kyo2e, fma(-roe, Y[oa + NE], Y[oa]), va);
+        va = fma(s[S::KO2ZE + za.z], X[(m + 1) * NE + za.y], va);
+        O[oa] = va;
+       }
       }
     }
     // nodes with e_i = 0
     {
       const int nn = C::nn(st.axis);
       const int* nl = C::nlist(st.axis);
+      const int total = rows * nn;
       int m = 0, k = lane;
       while (k >= nn) {
         k -= nn;
         ++m;
       }
-      while (m < rows) {
+      for (int u0 = 0; u0 < total; u0 += 64) {
+       if (u0 + 32 < total) {
         int m2 = m, k2 = k + 32;
         while (k2 >= nn) {
           k2 -= nn;
@@ -249,6 +282,13 @@ __device__ __forceinline__ void coop_vrr(double* __restrict__ arena, const doubl
           k -= nn;
           ++m;
         }
+       } else if (m < rows) {
+        const int oa = m * NE + __ldg(nl + k);
+        double va = qc * X[oa];
+        va = fma(wq, X[oa + NE], va);
+        if (hy) va = fma(kyo2e, fma(-roe, Y[oa + NE], Y[oa]), va);
+        O[oa] = va;
+       }
       }
     }
     __syncwarp();

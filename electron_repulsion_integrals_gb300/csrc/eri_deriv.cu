@@ -12,10 +12,16 @@
 
 using namespace eri;
 
+// The derivative class list: generated/registry_deriv.inc, or the file
+// ERI_DERIV_REGISTRY_INC names (a quoted path) in a library built over
+// another set of class kernels.
+#ifndef ERI_DERIV_REGISTRY_INC
+#define ERI_DERIV_REGISTRY_INC "generated/registry_deriv.inc"
+#endif
 #define ERI_DCLASS(a, b, c, d)                                                                     \
   extern "C" int eri_dlaunch_c##a##b##c##d(const EriLaunch*, int, int, cudaStream_t);            \
   extern "C" int eri_dgrid_c##a##b##c##d(int, long long, long long*, long long*);
-#include "generated/registry_deriv.inc"
+#include ERI_DERIV_REGISTRY_INC
 #undef ERI_DCLASS
 
 namespace {
@@ -28,13 +34,13 @@ struct DerivEntry {
 
 const DerivEntry kDeriv[] = {
 #define ERI_DCLASS(a, b, c, d) {{a, b, c, d}, eri_dlaunch_c##a##b##c##d, eri_dgrid_c##a##b##c##d},
-#include "generated/registry_deriv.inc"
+#include ERI_DERIV_REGISTRY_INC
 #undef ERI_DCLASS
-};
+    {{-1, -1, -1, -1}, nullptr, nullptr}};  // end marker (the list may be empty)
 
 const DerivEntry* find_deriv(const int l[4]) {
   for (const auto& e : kDeriv)
-    if (e.l[0] == l[0] && e.l[1] == l[1] && e.l[2] == l[2] && e.l[3] == l[3]) return &e;
+    if (e.launch && e.l[0] == l[0] && e.l[1] == l[1] && e.l[2] == l[2] && e.l[3] == l[3]) return &e;
   return nullptr;
 }
 

@@ -83,8 +83,11 @@ __device__ __forceinline__ void boys_scaled(double T, double pref, const double*
 }
 
 // ---------------------------------------------------------------- launch data
-// kCoulomb digests every block into J; kExchange into J and K together.
-enum OutputMode { kStore = 0, kSchwarz = 1, kCoulomb = 2, kExchange = 3 };
+// kSchwarz reduces each diagonal block (ab|ab) to sqrt(max |diagonal|);
+// kSchwarzPart adds one part of the primitive sum of the diagonal elements to
+// a buffer (work item = quartet x part, see schwarz_part); kCoulomb digests
+// every block into J; kExchange into J and K together.
+enum OutputMode { kStore = 0, kSchwarz = 1, kSchwarzPart = 2, kCoulomb = 3, kExchange = 4 };
 
 struct ShellsDev {
   const double* cen;    // [nshell][3]
@@ -105,8 +108,13 @@ struct EriLaunch {
   long long out_stride;  // doubles per block
   int ostr[4];           // stride of canonical axis k in the requested block layout
   long long dblock;      // derivative blocks: doubles per block (12 blocks per quartet)
-  // Schwarz mode: q_out[i] = sqrt(max diag |(ab|ab)|) of quartet i
+  // Schwarz mode: q_out[i] = sqrt(max diag |(ab|ab)|) of quartet i.
+  // Schwarz-part mode: item t is part (t mod split_b split_k) of quartet
+  // t / (split_b split_k); diagonal element (ia, ib) is added to
+  // q_out[quartet * q_stride + ia * nfunc(b) + ib]
   double* q_out;
+  int split_b, split_k;
+  long long q_stride;
   // Coulomb mode: work item t of the class is found through the segment list;
   // segment k covers work items [seg_start[k], seg_start[k+1]): bra pair
   // segs[k].x with ket pairs segs[k].y .. segs[k].y + segs[k].z - 1, each
@@ -146,6 +154,7 @@ struct Quartet {
   int bra, ket;       // pair ids
   int pab, nab, pcd, ncd;
   int iab0, iab1, icd0, icd1;  // primitive pairs of this work item: [iab0, iab1) x [icd0, icd1)
+  long long qi;                // Schwarz-part mode: quartet of the work item
   int fa, fb, fc, fd;  // first basis functions of the four shells
   double fab, fcd;     // 2 for a pair of distinct shells, else 1
   double wk;           // 1 / (number of the 8 index permutations that leave the quartet unchanged)
@@ -272,6 +281,24 @@ __device__ __forceinline__ void load_quartet(const EriLaunch& P, long long q, Qu
   Q.nd = __ldg(P.sh.nprim + Q.s[3]);
 }
 
+// Schwarz-part mode: item t -> quartet t / (sb sk) and its part: the cb-th of
+// sb slices of the bra primitive pairs times the ck-th of sk slices of the ket
+// ones (after load_quartet of that quartet).
+__device__ __forceinline__ long long schwarz_part_quartet(const EriLaunch& P, long long t) {
+  return t / ((long long)P.split_b * P.split_k);
+}
+__device__ __forceinline__ void schwarz_part(const EriLaunch& P, long long t, Quartet& Q) {
+  const int per = P.split_b * P.split_k;
+  Q.qi = t / per;
+  const int ch = (int)(t - Q.qi * per);
+  const int cb = ch / P.split_k, ck = ch - cb * P.split_k;
+  const int nab = Q.na * Q.nb, ncd = Q.nc * Q.nd;
+  Q.iab0 = cb * nab / P.split_b;
+  Q.iab1 = (cb + 1) * nab / P.split_b;
+  Q.icd0 = ck * ncd / P.split_k;
+  Q.icd1 = (ck + 1) * ncd / P.split_k;
+}
+
 // Coulomb mode: work item t -> (bra pair, ket pair) by binary search over the
 // segment starts, then the pair records.
 __device__ __forceinline__ void load_quartet_coulomb(const EriLaunch& P, long long t, Quartet& Q) {
@@ -395,10 +422,11 @@ __device__ __forceinline__ void quartet_setup(const PrimPair& pb, const PrimPair
 // has exactly one primitive and the loops disappear.
 #define PRIM_LOOP_BEGIN(P, Q)                                                                              \
   {                                                                                                        \
-    const int ab0_ = MODE >= kCoulomb ? Q.iab0 : 0;                                                        \
-    const int nab_ = MODE >= kCoulomb ? Q.iab1 : CONTRACTED ? Q.na * Q.nb : 1;                             \
-    const int cd0_ = MODE >= kCoulomb ? Q.icd0 : 0;                                                        \
-    const int ncd_ = MODE >= kCoulomb ? Q.icd1 : CONTRACTED ? Q.nc * Q.nd : 1;                             \
+    constexpr bool part_ = MODE >= kCoulomb || MODE == kSchwarzPart;                                       \
+    const int ab0_ = part_ ? Q.iab0 : 0;                                                                   \
+    const int nab_ = part_ ? Q.iab1 : CONTRACTED ? Q.na * Q.nb : 1;                                        \
+    const int cd0_ = part_ ? Q.icd0 : 0;                                                                   \
+    const int ncd_ = part_ ? Q.icd1 : CONTRACTED ? Q.nc * Q.nd : 1;                                        \
     double qk0_ = 0.0;                                                                                     \
     if constexpr (MODE >= kCoulomb) qk0_ = __ldg(P.prims + (size_t)(Q.pcd + cd0_) * kPrimRec + 9);         \
     for (int iab_ = ab0_; iab_ < nab_; ++iab_) {                                                           \
@@ -472,6 +500,9 @@ __device__ __forceinline__ void quartet_setup(const PrimPair& pb, const PrimPair
     orow_[(ic) * Q.ost[2] + (id) * Q.ost[3]] = (v);                            \
   } else if constexpr (MODE == kSchwarz) {                                     \
     if ((ia) == (ic) && (ib) == (id)) smax_ = fmax(smax_, fabs(v));            \
+  } else if constexpr (MODE == kSchwarzPart) {                                 \
+    if ((ia) == (ic) && (ib) == (id))                                          \
+      atomicAdd(P.q_out + Q.qi * P.q_stride + (ia) * kNSB_ + (ib), (v));       \
   } else {                                                                     \
     jrow_ = fma((v), __ldg(P.D + (size_t)(Q.fc + (ic)) * P.nbf + Q.fd + (id)), jrow_); \
     jcd_[(ic) * kNSD_ + (id)] = fma((v), dab_, jcd_[(ic) * kNSD_ + (id)]);   \
@@ -551,6 +582,8 @@ __device__ __forceinline__ void quartet_setup(const PrimPair& pb, const PrimPair
       ERI_LAUNCH_MODE_(KERNEL, kStore, smemb_)                                                            \
     } else if (mode == kSchwarz) {                                                                        \
       ERI_LAUNCH_MODE_(KERNEL, kSchwarz, smemb_)                                                          \
+    } else if (mode == kSchwarzPart) {                                                                    \
+      ERI_LAUNCH_ONE_(KERNEL, kSchwarzPart, true, smemb_)                                                 \
     } else if (mode == kCoulomb) {                                                                        \
       ERI_LAUNCH_ONE_(KERNEL, kCoulomb, true, smemb_)                                                     \
     } else if (mode == kExchange) {                                                                       \

@@ -97,6 +97,15 @@ __global__ void build_prim_pairs(int npairs, const PairMeta* __restrict__ pairs,
   }
 }
 
+// q[i] = sqrt(max_k |diag[i][k]|): Schwarz factors from summed diagonal parts.
+__global__ void schwarz_reduce(long long n, int nd, const double* __restrict__ diag, double* __restrict__ q) {
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  double m = 0.0;
+  for (int k = 0; k < nd; ++k) m = fmax(m, fabs(diag[i * nd + k]));
+  q[i] = sqrt(m);
+}
+
 // J_out[i][j] = J_acc[i][j] + J_acc[j][i] for functions of different shells
 // (each unique pair was accumulated in one orientation only), J_acc[i][j]
 // inside a diagonal shell block.
@@ -180,6 +189,39 @@ int schwarz_dev(eri_plan* p, int la, int lb, const int2* pairs, long long n, dou
   P.n = n;
   for (int k = 0; k < 4; ++k) P.canon[k] = canon[k];
   P.q_out = q;
+  // A diagonal quartet of contracted shells has up to (K_a K_b)^2 primitive
+  // quartets (1,296 for 6-primitive pairs); one thread each would set the
+  // critical path of the launch.  Cut each into parts of at most 8 x 8
+  // primitive pairs, sum their diagonal elements with atomics and reduce.
+  const int* L = eri::host::plan_L(p);
+  const int* np = eri::host::plan_nprim(p);
+  int ka = 1, kb = 1;
+  for (int s = 0; s < eri::host::plan_nshell(p); ++s) {
+    if (L[s] == la) ka = std::max(ka, np[s]);
+    if (L[s] == lb) kb = std::max(kb, np[s]);
+  }
+  const int split = (ka * kb + 7) / 8;
+  if (split > 1) {
+    auto nfn = [&](int l) { return (eri::host::plan_spherical(p) && l >= 2) ? 2 * l + 1 : (l + 1) * (l + 2) / 2; };
+    const int nd = nfn(cl[0]) * nfn(cl[1]);
+    DevBuf db;
+    CUDA_TRY(cudaMalloc(&db.p, (size_t)n * nd * sizeof(double)));
+    CUDA_TRY(cudaMemsetAsync(db.p, 0, (size_t)n * nd * sizeof(double), st));
+    EriLaunch Pp = P;
+    Pp.n = n * split * split;
+    Pp.split_b = split;
+    Pp.split_k = split;
+    Pp.q_out = static_cast<double*>(db.p);
+    Pp.q_stride = nd;
+    int rc = eri::host::launch_class(p, cl, Pp, kSchwarzPart, st);
+    if (rc == ERI_OK) {
+      schwarz_reduce<<<(int)((n + 127) / 128), 128, 0, st>>>(n, nd, static_cast<const double*>(db.p), q);
+      CUDA_TRY(cudaGetLastError());
+      CUDA_TRY(cudaStreamSynchronize(st));
+      return ERI_OK;
+    }
+    if (rc != ERI_ERR_NOT_IMPLEMENTED) return rc;  // cooperative classes: one warp per quartet below
+  }
   int rc = eri::host::launch_class(p, cl, P, kSchwarz, st);
   if (rc) return rc;
   CUDA_TRY(cudaStreamSynchronize(st));

@@ -480,10 +480,15 @@ def emit_class(cls, spherical_out=True, rule=None, schedule=None, sph_fusion=Tru
             w(f"#define GSL(k) S[({gsl_base} + (k)) * nt]")
     w("  for (long long q = gid; q < P.n; q += nt) {")
     w("    Quartet Q;")
+    lq = f"load_quartet<{1 if la == lb else 0}, {1 if lc == ld else 0}, {la + lb}, {lc + ld}>"
     w("    if constexpr (MODE >= kCoulomb) {")
     w("      load_quartet_coulomb(P, q, Q);")
+    w("    } else if constexpr (MODE == kSchwarzPart) {")
+    w(f"      {lq}(P, schwarz_part_quartet(P, q), Q);")
+    w("      schwarz_part(P, q, Q);")
+    w("      if (Q.iab0 >= Q.iab1 || Q.icd0 >= Q.icd1) continue;")
     w("    } else {")
-    w(f"      load_quartet<{1 if la == lb else 0}, {1 if lc == ld else 0}, {la + lb}, {lc + ld}>(P, q, Q);")
+    w(f"      {lq}(P, q, Q);")
     w("    }")
     w("    double smax_ = 0.0;")
     w("    (void)smax_;")

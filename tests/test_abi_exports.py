@@ -65,3 +65,14 @@ def test_argument_errors_before_cuda(lib):
     assert lib.eri_compute_class(None, 1, 1, 1, 1, None, 0, None, 0, None) == -1
     assert lib.eri_compute_class_noalloc(None, 1, 1, 1, 1, None, 0, None, 0, None) == -1
     assert lib.eri_build_J(None, None, None, None) == -1
+
+
+def test_variant_library_links_completely():
+    """A library built over another class list (build.build_variant) resolves
+    every symbol of the runtime, derivative entry point included."""
+    import subprocess
+    from electron_repulsion_integrals_gb300.build import build_variant
+    path = build_variant("abi_check", [((1, 0, 0, 0), {"tier": "staged"})])
+    r = subprocess.run(["nm", "-D", "--undefined-only", path], capture_output=True, text=True)
+    assert r.returncode == 0
+    assert not [ln for ln in r.stdout.splitlines() if " eri_" in ln], r.stdout
