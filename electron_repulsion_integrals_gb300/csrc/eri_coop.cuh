@@ -205,49 +205,7 @@ __device__ __forceinline__ void coop_vrr(double* __restrict__ arena, const doubl
         k -= nz;
         ++m;
       }
-      int u0 = 0;
-      // full iterations: four nodes per lane, all present
-      for (; u0 + 128 <= total; u0 += 128) {
-        int mm[4], kk[4];
-        mm[0] = m;
-        kk[0] = k;
-#pragma unroll
-        for (int j = 1; j < 4; ++j) {
-          mm[j] = mm[j - 1];
-          kk[j] = kk[j - 1] + 32;
-          while (kk[j] >= nz) {
-            kk[j] -= nz;
-            ++mm[j];
-          }
-        }
-        double v[4];
-        int o[4];
-        int4 z[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          z[j] = __ldg(zl + kk[j]);
-          o[j] = mm[j] * NE + z[j].x;
-          v[j] = qc * X[o[j]];
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) v[j] = fma(wq, X[o[j] + NE], v[j]);
-        if (hy) {
-#pragma unroll
-          for (int j = 0; j < 4; ++j) v[j] = fma(kyo2e, fma(-roe, Y[o[j] + NE], Y[o[j]]), v[j]);
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          v[j] = fma(s[S::KO2ZE + z[j].z], X[(mm[j] + 1) * NE + z[j].y], v[j]);
-          O[o[j]] = v[j];
-        }
-        m = mm[3];
-        k = kk[3] + 32;
-        while (k >= nz) {
-          k -= nz;
-          ++m;
-        }
-      }
-      for (; u0 < total; u0 += 64) {
+      for (int u0 = 0; u0 < total; u0 += 64) {
        if (u0 + 32 < total) {
         int m2 = m, k2 = k + 32;
         while (k2 >= nz) {
@@ -298,43 +256,7 @@ __device__ __forceinline__ void coop_vrr(double* __restrict__ arena, const doubl
         k -= nn;
         ++m;
       }
-      int u0 = 0;
-      for (; u0 + 128 <= total; u0 += 128) {
-        int mm[4], kk[4];
-        mm[0] = m;
-        kk[0] = k;
-#pragma unroll
-        for (int j = 1; j < 4; ++j) {
-          mm[j] = mm[j - 1];
-          kk[j] = kk[j - 1] + 32;
-          while (kk[j] >= nn) {
-            kk[j] -= nn;
-            ++mm[j];
-          }
-        }
-        double v[4];
-        int o[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          o[j] = mm[j] * NE + __ldg(nl + kk[j]);
-          v[j] = qc * X[o[j]];
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) v[j] = fma(wq, X[o[j] + NE], v[j]);
-        if (hy) {
-#pragma unroll
-          for (int j = 0; j < 4; ++j) v[j] = fma(kyo2e, fma(-roe, Y[o[j] + NE], Y[o[j]]), v[j]);
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) O[o[j]] = v[j];
-        m = mm[3];
-        k = kk[3] + 32;
-        while (k >= nn) {
-          k -= nn;
-          ++m;
-        }
-      }
-      for (; u0 < total; u0 += 64) {
+      for (int u0 = 0; u0 < total; u0 += 64) {
        if (u0 + 32 < total) {
         int m2 = m, k2 = k + 32;
         while (k2 >= nn) {

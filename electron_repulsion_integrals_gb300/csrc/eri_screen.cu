@@ -44,7 +44,7 @@ namespace {
 // after the other threads are done.  Digestion is linear in the integrals, so
 // a quartet may be cut into parts that are transformed and scattered on their
 // own.  kThreadsPerClass: threads of one class launch (152 SMs x 256).
-constexpr long long kMinPrimPerItem = 64;
+constexpr long long kMinPrimPerItem = 8;
 constexpr double kThreadsPerClass = 152.0 * 256.0;
 
 #define CUDA_TRY(x)                                                        \
