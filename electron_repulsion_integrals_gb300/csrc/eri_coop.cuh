@@ -341,7 +341,8 @@ __device__ __forceinline__ void coop_vrr(double* __restrict__ arena, const doubl
       const int nprim = nab * ncd;                                                                        \
       for (int base = 0; base < nprim; base += kCoopBatch) {                                              \
         const int p = base + lane;                                                                        \
-        if (p < nprim) coop_setup_one<MODE, C::La, C::Lc>(P, Q, p / ncd, p - (p / ncd) * ncd,             \
+        if (lane < kCoopBatch && p < nprim)                                                               \
+          coop_setup_one<MODE, C::La, C::Lc>(P, Q, p / ncd, p - (p / ncd) * ncd,                         \
                                                           setup + lane * S_::STRIDE);                     \
         __syncwarp();                                                                                     \
         const int cnt = nprim - base < kCoopBatch ? nprim - base : kCoopBatch;                            \

@@ -47,7 +47,8 @@ __device__ __forceinline__ double* deriv_out(const EriLaunch& P, const Quartet& 
       const int nab = Q.na * Q.nb, ncd = Q.nc * Q.nd, nprim = nab * ncd;                                  \
       for (int base = 0; base < nprim; base += kCoopBatch) {                                              \
         const int p = base + lane;                                                                        \
-        if (p < nprim) coop_setup_one<kStore, C::La, C::Lc, C::NW>(P, Q, p / ncd, p - (p / ncd) * ncd,    \
+        if (lane < kCoopBatch && p < nprim)                                                               \
+          coop_setup_one<kStore, C::La, C::Lc, C::NW>(P, Q, p / ncd, p - (p / ncd) * ncd,                \
                                                                    setup + lane * S_::STRIDE);            \
         __syncwarp();                                                                                     \
         const int cnt = nprim - base < kCoopBatch ? nprim - base : kCoopBatch;                            \

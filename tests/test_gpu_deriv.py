@@ -116,3 +116,10 @@ def test_errors(dev):
         eri.eri_compute_class_deriv(plan.handle, (3, 1, 1, 1), qt, small)
     assert ei.value.code == -2
     plan.close()
+
+
+@pytest.mark.parametrize("cls", [(1, 1, 1, 1), (2, 2, 1, 1), (2, 1, 2, 1)])
+def test_degree_3_several_setup_batches(dev, cls):
+    """81 primitive quartets per quartet: several batches of primitive setups."""
+    s, q = W.homogeneous(cls, 23, 3, seed_index=760 + sum(cls))
+    check_deriv(run(s, cls, q, dev), oracle.eri_deriv_blocks(oshells(s), q, spherical=True), f"d{cls} degree 3")

@@ -234,3 +234,12 @@ def test_pointer_and_flat_plan_creation_agree(dev):
         outs.append(out.cpu().numpy())
         eri.eri_plan_destroy(h)
     assert np.array_equal(outs[0], outs[1])
+
+
+@pytest.mark.parametrize("cls", [(3, 2, 2, 2), (3, 3, 3, 3), (4, 2, 3, 1)])
+def test_cooperative_tier_more_than_one_setup_batch(dev, cls):
+    """Contraction degree 3 (81 primitive quartets per quartet): the cooperative
+    kernels set primitive quartets up 16 at a time, over several batches."""
+    if max(cls) > built_lmax():
+        pytest.skip("class not built")
+    _homogeneous_check(dev, cls, 19, 3, seed_index=470 + sum(cls))
