@@ -42,6 +42,18 @@ struct CoopSetup {
   static constexpr int STRIDE = SIZE | 1;  // odd stride: lanes hit different banks
 };
 
+// Synchronisation of the lanes that share one quartet: one warp (LN = 32), or
+// the whole block when a group of 2 or 4 warps shares the quartet (one group
+// per block).
+template <int LN>
+__device__ __forceinline__ void coop_sync() {
+  if constexpr (LN == 32) {
+    __syncwarp();
+  } else {
+    __syncthreads();
+  }
+}
+
 struct CoopCol {
   int out, x, y, axis, ky, level, target, pad;
 };
@@ -98,22 +110,23 @@ __device__ __forceinline__ void coop_vrr(double* __restrict__ arena, const doubl
                                          double* __restrict__ H, int lane, bool first) {
   using S = CoopSetup<C::La, C::Lc, C::NW>;
   constexpr int NE = C::NE;
+  constexpr int LN = C::LANES;
   double* bra = arena + C::BRA_COL;
   // column 0: Boys values [00|00]^(m)
   if (lane <= C::L) bra[lane * NE] = s[S::F + lane];
-  __syncwarp();
+  coop_sync<LN>();
   const double roz = s[12], roe = s[13];
   // bra levels
 #pragma unroll 1
   for (int k = 0; k < C::La; ++k) {
     const int y0 = C::bra_y_start()[k], y1 = C::bra_y_start()[k + 1];
     // two nodes per lane while more than 32 remain (warp-uniform test), then one
-    for (int t0 = y0; t0 < y1; t0 += 64) {
+    for (int t0 = y0; t0 < y1; t0 += 2 * LN) {
       const int t = t0 + lane;
-      if (t0 + 32 < y1) {
-        const bool two = t + 32 < y1;
+      if (t0 + LN < y1) {
+        const bool two = t + LN < y1;
         const int4 na = __ldg(C::bra_y() + t);
-        const int4 nb = __ldg(C::bra_y() + (two ? t + 32 : t));
+        const int4 nb = __ldg(C::bra_y() + (two ? t + LN : t));
         const int axa = na.w & 3, kya = na.w >> 2, axb = nb.w & 3, kyb = nb.w >> 2;
         double va = s[axa] * bra[na.y];
         double vb = s[axb] * bra[nb.y];
@@ -133,12 +146,12 @@ __device__ __forceinline__ void coop_vrr(double* __restrict__ arena, const doubl
       }
     }
     const int n0 = C::bra_n_start()[k], n1 = C::bra_n_start()[k + 1];
-    for (int t0 = n0; t0 < n1; t0 += 64) {
+    for (int t0 = n0; t0 < n1; t0 += 2 * LN) {
       const int t = t0 + lane;
-      if (t0 + 32 < n1) {
-        const bool two = t + 32 < n1;
+      if (t0 + LN < n1) {
+        const bool two = t + LN < n1;
         const int4 na = __ldg(C::bra_n() + t);
-        const int4 nb = __ldg(C::bra_n() + (two ? t + 32 : t));
+        const int4 nb = __ldg(C::bra_n() + (two ? t + LN : t));
         double va = s[na.z] * bra[na.y];
         double vb = s[nb.z] * bra[nb.y];
         va = fma(s[3 + na.z], bra[na.y + NE], va);
@@ -152,11 +165,11 @@ __device__ __forceinline__ void coop_vrr(double* __restrict__ arena, const doubl
         bra[na.x] = va;
       }
     }
-    __syncwarp();
+    coop_sync<LN>();
   }
   if constexpr (C::LCMIN == 0) {
     // column 0 is a target column (ket component (0,0,0))
-    for (int k = lane; k < C::NET; k += 32) {
+    for (int k = lane; k < C::NET; k += LN) {
       const double v = bra[C::IE_LO + k];
       H[k] = first ? v : H[k] + v;
 #pragma unroll
@@ -180,13 +193,13 @@ __device__ __forceinline__ void coop_vrr(double* __restrict__ arena, const doubl
     const int rows = C::Lc - st.level + 1;
     // accumulators of a target column are fetched before the column is built,
     // so that their global-memory latency overlaps the arithmetic
-    constexpr int kHT = (C::NET + 31) / 32;
+    constexpr int kHT = (C::NET + LN - 1) / LN;
     double hold[kHT];
     double* Ht = H + (size_t)(st.target >= 0 ? st.target : 0) * C::NET;
     if (st.target >= 0 && !first) {
 #pragma unroll
       for (int j = 0; j < kHT; ++j) {
-        const int k = lane + 32 * j;
+        const int k = lane + LN * j;
         hold[j] = k < C::NET ? Ht[k] : 0.0;
       }
     }
@@ -205,9 +218,9 @@ __device__ __forceinline__ void coop_vrr(double* __restrict__ arena, const doubl
         k -= nz;
         ++m;
       }
-      for (int u0 = 0; u0 < total; u0 += 64) {
-       if (u0 + 32 < total) {
-        int m2 = m, k2 = k + 32;
+      for (int u0 = 0; u0 < total; u0 += 2 * LN) {
+       if (u0 + LN < total) {
+        int m2 = m, k2 = k + LN;
         while (k2 >= nz) {
           k2 -= nz;
           ++m2;
@@ -230,7 +243,7 @@ __device__ __forceinline__ void coop_vrr(double* __restrict__ arena, const doubl
         O[oa] = va;
         if (two) O[ob] = vb;
         m = m2;
-        k = k2 + 32;
+        k = k2 + LN;
         while (k >= nz) {
           k -= nz;
           ++m;
@@ -256,9 +269,9 @@ __device__ __forceinline__ void coop_vrr(double* __restrict__ arena, const doubl
         k -= nn;
         ++m;
       }
-      for (int u0 = 0; u0 < total; u0 += 64) {
-       if (u0 + 32 < total) {
-        int m2 = m, k2 = k + 32;
+      for (int u0 = 0; u0 < total; u0 += 2 * LN) {
+       if (u0 + LN < total) {
+        int m2 = m, k2 = k + LN;
         while (k2 >= nn) {
           k2 -= nn;
           ++m2;
@@ -277,7 +290,7 @@ __device__ __forceinline__ void coop_vrr(double* __restrict__ arena, const doubl
         O[oa] = va;
         if (two) O[ob] = vb;
         m = m2;
-        k = k2 + 32;
+        k = k2 + LN;
         while (k >= nn) {
           k -= nn;
           ++m;
@@ -291,11 +304,11 @@ __device__ __forceinline__ void coop_vrr(double* __restrict__ arena, const doubl
        }
       }
     }
-    __syncwarp();
+    coop_sync<LN>();
     if (st.target >= 0) {
 #pragma unroll
       for (int j = 0; j < kHT; ++j) {
-        const int k = lane + 32 * j;
+        const int k = lane + LN * j;
         if (k < C::NET) {
           const double v = O[C::IE_LO + k];
           Ht[k] = first ? v : hold[j] + v;
@@ -309,7 +322,7 @@ __device__ __forceinline__ void coop_vrr(double* __restrict__ arena, const doubl
       }
     }
   }
-  __syncwarp();
+  coop_sync<LN>();
 }
 
 }  // namespace eri
@@ -320,14 +333,16 @@ __device__ __forceinline__ void coop_vrr(double* __restrict__ arena, const doubl
 // lower-l shell; the same functions when la == lb / lc == ld).
 #define ERI_COOP_KERNEL(NAME, C, BRA_FN, BRA_REV_FN, KET_FN, KET_REV_FN)                                                        \
   template <int MODE, bool CONTRACTED>                                                                    \
-  __global__ void __launch_bounds__(kCoopThreads) NAME(const EriLaunch P) {                               \
+  __global__ void __launch_bounds__(C::THREADS) NAME(const EriLaunch P) {                                 \
     extern __shared__ double smem_[];                                                                     \
+    __shared__ double red_[4];                                                                            \
     using S_ = CoopSetup<C::La, C::Lc>;                                                                   \
-    const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;                                            \
+    constexpr int LN_ = C::LANES;                                                                         \
+    const int lane = threadIdx.x % LN_, wib = threadIdx.x / LN_;                                          \
     double* arena = smem_ + (size_t)wib * C::WARP_SMEM;                                                   \
     double* setup = arena + C::ARENA;                                                                     \
-    const long long nw = (long long)gridDim.x * kCoopWarps;                                               \
-    const long long wid = (long long)blockIdx.x * kCoopWarps + wib;                                       \
+    const long long nw = (long long)gridDim.x * C::GROUPS;                                                \
+    const long long wid = (long long)blockIdx.x * C::GROUPS + wib;                                        \
     double* H = P.scratch + (size_t)wid * C::NH;                                                          \
     for (long long q = wid; q < P.n; q += nw) {                                                           \
       Quartet Q;                                                                                          \
@@ -344,39 +359,49 @@ __device__ __forceinline__ void coop_vrr(double* __restrict__ arena, const doubl
         if (lane < kCoopBatch && p < nprim)                                                               \
           coop_setup_one<MODE, C::La, C::Lc>(P, Q, p / ncd, p - (p / ncd) * ncd,                         \
                                                           setup + lane * S_::STRIDE);                     \
-        __syncwarp();                                                                                     \
+        coop_sync<LN_>();                                                                                 \
         const int cnt = nprim - base < kCoopBatch ? nprim - base : kCoopBatch;                            \
         for (int pp = 0; pp < cnt; ++pp) coop_vrr<C>(arena, setup + pp * S_::STRIDE, H, lane, base + pp == 0); \
-        __syncwarp();                                                                                     \
+        coop_sync<LN_>();                                                                                 \
       }                                                                                                   \
       /* HRR bra + T x T: one lane per ket column; G[r][f] in the arena */                               \
       double* G = arena;                                                                                  \
       /* columns below |f| = lc feed only the reversed ket HRR */                                         \
-      for (int fi = (Q.rk ? 0 : C::FI_LC) + lane; fi < C::NF; fi += 32) {                                 \
+      for (int fi = (Q.rk ? 0 : C::FI_LC) + lane; fi < C::NF; fi += LN_) {                                \
         if (Q.rb) BRA_REV_FN(Q, H, fi, G);                                                                \
         else BRA_FN(Q, H, fi, G);                                                                         \
       }                                                                                                   \
-      __syncwarp();                                                                                       \
+      coop_sync<LN_>();                                                                                   \
       double smax_ = 0.0;                                                                                 \
-      for (int r = lane; r < C::NR; r += 32) {                                                            \
+      for (int r = lane; r < C::NR; r += LN_) {                                                           \
         if (Q.rk) KET_REV_FN<MODE>(P, Q, q, r, G, smax_);                                                 \
         else KET_FN<MODE>(P, Q, q, r, G, smax_);                                                          \
       }                                                                                                   \
       if constexpr (MODE == kSchwarz) {                                                                   \
         _Pragma("unroll") for (int o = 16; o > 0; o >>= 1) smax_ = fmax(smax_, __shfl_xor_sync(0xffffffffu, smax_, o)); \
-        if (lane == 0) P.q_out[q] = sqrt(smax_);                                                          \
+        if constexpr (LN_ == 32) {                                                                        \
+          if (lane == 0) P.q_out[q] = sqrt(smax_);                                                        \
+        } else {                                                                                          \
+          if ((lane & 31) == 0) red_[lane >> 5] = smax_;                                                  \
+          coop_sync<LN_>();                                                                               \
+          if (lane == 0) {                                                                                \
+            double m_ = red_[0];                                                                          \
+            for (int w_ = 1; w_ < LN_ / 32; ++w_) m_ = fmax(m_, red_[w_]);                                \
+            P.q_out[q] = sqrt(m_);                                                                        \
+          }                                                                                               \
+        }                                                                                                 \
       }                                                                                                   \
-      __syncwarp();                                                                                       \
+      coop_sync<LN_>();                                                                                   \
     }                                                                                                     \
   }
 
 // Per-class entry points of a cooperative class (same interface as
 // ERI_DEFINE_CLASS_LAUNCHER): launch, grid/scratch sizing, statistics.
-#define ERI_COOP_SMEM_(T) ((size_t)kCoopWarps * (T::WARP_SMEM) * sizeof(double))
+#define ERI_COOP_SMEM_(T) ((size_t)(T::GROUPS) * (T::WARP_SMEM) * sizeof(double))
 #define ERI_COOP_LAUNCH_(KERNEL, T, M, C)                                                                \
   {                                                                                                      \
     cudaFuncSetAttribute(KERNEL<M, C>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ERI_COOP_SMEM_(T)); \
-    KERNEL<M, C><<<blocks, kCoopThreads, ERI_COOP_SMEM_(T), st>>>(*P);                                   \
+    KERNEL<M, C><<<blocks, T::THREADS, ERI_COOP_SMEM_(T), st>>>(*P);                                     \
   }
 
 #define ERI_DEFINE_COOP_LAUNCHER(LA, LB, LC, LD, KERNEL, T, VOPS, VFLOPS, HOPS, HFLOPS)                  \
@@ -392,17 +417,17 @@ __device__ __forceinline__ void coop_vrr(double* __restrict__ arena, const doubl
     int occ = 0;                                                                                         \
     cudaFuncSetAttribute(KERNEL<kStore, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,              \
                          (int)ERI_COOP_SMEM_(T));                                                        \
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, KERNEL<kStore, true>, kCoopThreads,          \
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, KERNEL<kStore, true>, T::THREADS,            \
                                                       ERI_COOP_SMEM_(T)) != cudaSuccess || occ < 1) {    \
       (void)cudaGetLastError();                                                                          \
       occ = 1;                                                                                           \
     }                                                                                                    \
     long long b = (long long)nsm * occ;                                                                  \
-    const long long need = (n + kCoopWarps - 1) / kCoopWarps;                                            \
+    const long long need = (n + T::GROUPS - 1) / T::GROUPS;                                              \
     if (b > need) b = need;                                                                              \
     if (b < 1) b = 1;                                                                                    \
     *blocks = b;                                                                                         \
-    *scratch = b * kCoopWarps * (long long)T::NH;                                                        \
+    *scratch = b * T::GROUPS * (long long)T::NH;                                                         \
     return 0;                                                                                            \
   }                                                                                                      \
   extern "C" int eri_slots_c##LA##LB##LC##LD() { return 0; }                                             \

@@ -230,6 +230,28 @@ def _arr(name, ctype, items, fmt):
     return f"__device__ const {ctype} {name}[] = {{{body}}};"
 
 
+SMEM_PER_SM = 233472    # bytes of shared memory per SM
+MAX_GROUPS_FOR_WIDE = 3  # quartets per SM at or below which four warps share one
+
+
+def setup_stride(La, Lc, nw=0):
+    """Doubles per primitive-quartet setup record (CoopSetup in eri_coop.cuh)."""
+    L = La + Lc
+    f = 14 + La + Lc + max(La, Lc) + 1
+    return (f + L + 1 + nw) | 1
+
+
+def lanes_for(arena, La, Lc, batch=16):
+    """Lanes that share one quartet: one warp, unless the per-quartet shared
+    memory leaves at most MAX_GROUPS_FOR_WIDE quartets on an SM; then four
+    warps (one group per block).  Measured: four-warp groups doubled (gg|gg)
+    (2 -> 8 warps per SM), while two-warp groups for (ff|ff) (6 -> 8 warps)
+    ran 4 % slower than one warp per quartet."""
+    per_group = (arena + batch * setup_stride(La, Lc)) * 8
+    groups = max(1, SMEM_PER_SM // per_group)
+    return 32 if groups > MAX_GROUPS_FOR_WIDE else 128
+
+
 def plan_tables(P, cname):
     """Device tables of a column schedule (bra nodes, per-axis e lists, ket
     column steps) and the trait accessors that expose them; returns
@@ -309,6 +331,8 @@ def emit_coop_class(cls):
     w(f"  static constexpr int NE = {NE}, NET = {NET}, IE_LO = {P.ie_lo}, NF = {NF}, NR = {NR}, GS = {GS};")
     w(f"  static constexpr int LCMIN = {min(lc, ld)}, FI_LC = {fi_lc};")
     w("  static constexpr int NW = 0;")
+    lanes = lanes_for(arena, La, Lc)
+    w(f"  static constexpr int LANES = {lanes}, GROUPS = LANES == 32 ? kCoopWarps : 1, THREADS = LANES * GROUPS;")
     w(f"  static constexpr int NCOL = {len(P.cols)}, BRA_COL = {bc}, ARENA = {arena}, NH = {NF * NET};")
     w(f"  static constexpr int WARP_SMEM = ARENA + kCoopBatch * CoopSetup<La, Lc>::STRIDE;")
     for ln in accessors:
