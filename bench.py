@@ -1,16 +1,19 @@
 """Benchmark: ERI quartets/s and FP64 GFLOP/s per angular class on one GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload homogeneous|high_l|g_shells|cluster64|cluster200|cluster64_jk|cluster200_jk]
-                    [--scale S]
+                    [--workload homogeneous|high_l|g_shells|deriv|cluster64|cluster200|cluster64_jk|cluster200_jk]
+                    [--scale S] [--ablation all|NAME,...]
 
 A step is one pass of the hot path over the workload's batch: for every class
 of the workload, the class kernel evaluates all its quartets (Gaussian-pair
 parameters, Boys function, VRR, contraction, HRR with the stepwise spherical
 transform, block store).  ``value`` is the whole job's shell quartets per second
 with inputs resident in HBM; ``e2e`` is the same metric through the C ABI with
-host buffers (plan creation from host shells, pinned host->device copy of the
-quartet lists, device->host copy of every block).
+host buffers (every step: plan creation from host shells, pinned host->device
+copy of the quartet lists, device->host copy of every block into pinned host
+memory; the class batches on separate streams so that their host and device
+work overlap).  ``--ablation`` builds and times the generator-ablation
+libraries (electron_repulsion_integrals_gb300/ablation.py) against the main one.
 
 Default workload (N=1): the homogeneous class batch, 1,048,576 (pp|pp) and
 1,048,576 (dd|dd) quartets, centers uniform in a 10 bohr cube, exponents
@@ -288,8 +291,8 @@ def run_coulomb(a, rank, world, local_rank):
     e2e = None
     if a.e2e:
         hD = torch.from_numpy(D).pin_memory()
-        hJ = torch.empty_like(hD).pin_memory()
-        hK = torch.empty_like(hD).pin_memory()
+        hJ = torch.empty(hD.shape, dtype=torch.float64, pin_memory=True)
+        hK = torch.empty(hD.shape, dtype=torch.float64, pin_memory=True)
         torch.cuda.synchronize()
         te = time.perf_counter()
         p2 = eri.Plan(s, spherical=True, schwarz_tau=1e-10, stream=stream)
@@ -452,39 +455,45 @@ def run_ours(a, rank, world, local_rank):
     dname = "({}{}|{}{})".format(*dom["cls"])
     ach = per_class[dname]["fp64_gflops"] / 1e3
 
-    # end to end through the C ABI with host buffers
+    # end to end through the C ABI with host buffers: every step creates each
+    # class's plan from host shells, copies its quartet list from pinned host
+    # memory, computes, and reads all blocks back into pinned host memory.  The
+    # class batches run on their own streams, heaviest first, so that one
+    # batch's plan creation (host work) overlaps the other's compute and copies.
     e2e = None
     if a.e2e:
         host_q = [torch.from_numpy(b["q"]).pin_memory() for b in batches]
-        host_o = [torch.empty(b["out"].numel(), dtype=torch.float64).pin_memory() for b in batches]
+        host_o = [torch.empty(b["out"].numel(), dtype=torch.float64, pin_memory=True) for b in batches]
+        streams = [torch.cuda.Stream() for _ in batches]
+        order = sorted(range(len(batches)), key=lambda i: -batches[i]["flops"] * batches[i]["n"])
         h2d = sum(hq.numel() * 4 for hq in host_q) + sum(b["shells"].n * 48 + b["shells"].exps.size * 16
                                                          for b in batches)
         d2h = sum(ho.numel() * 8 for ho in host_o)
         e_steps = max(1, min(a.steps, 3))
-        ph = {"plan_create": 0.0, "h2d_quartets_and_compute": 0.0, "d2h_blocks": 0.0}
+
+        def e2e_step():
+            plans = []
+            for i in order:
+                b, hq, ho, st_i = batches[i], host_q[i], host_o[i], streams[i]
+                with torch.cuda.stream(st_i):
+                    plan = eri.Plan(b["shells"], spherical=True, stream=st_i)
+                    qd = hq.to(dev, non_blocking=True)
+                    compute(plan.handle, b["cls"], qd, b["out"], st_i)
+                    ho.copy_(b["out"], non_blocking=True)
+                plans.append(plan)
+            torch.cuda.synchronize()
+            for plan in plans:
+                plan.close()
+
+        e2e_step()  # untimed: first use of the streams and of the pinned buffers
         torch.cuda.synchronize()
         te = time.perf_counter()
         for _ in range(e_steps):
-            for b, hq, ho in zip(batches, host_q, host_o):
-                t0h = time.perf_counter()
-                plan = eri.Plan(b["shells"], spherical=True, stream=stream)
-                torch.cuda.synchronize()
-                t1h = time.perf_counter()
-                qd = hq.to(dev, non_blocking=True)
-                compute(plan.handle, b["cls"], qd, b["out"], stream)
-                torch.cuda.synchronize()
-                t2h = time.perf_counter()
-                ho.copy_(b["out"], non_blocking=True)
-                torch.cuda.synchronize()
-                t3h = time.perf_counter()
-                plan.close()
-                ph["plan_create"] += t1h - t0h
-                ph["h2d_quartets_and_compute"] += t2h - t1h
-                ph["d2h_blocks"] += t3h - t2h
+            e2e_step()
         te = time.perf_counter() - te
         e2e = {"value": sum(b["n"] for b in batches) * world * e_steps / te, "unit": "quartets/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "phases_ms_per_step": {k: v / e_steps * 1e3 for k, v in ph.items()}}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": te / e_steps * 1e3,
+               "schedule": "class batches on separate CUDA streams, heaviest first"}
 
     cpu = None
     if rank == 0 and a.cpu_baseline:

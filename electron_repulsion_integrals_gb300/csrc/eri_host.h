@@ -25,6 +25,8 @@ const int* plan_L(const eri_plan* p);
 const int* plan_nprim(const eri_plan* p);
 const int* plan_fo(const eri_plan* p);
 const int* plan_poff(const eri_plan* p);
+// host copies of the caller's shell data; present only when the plan has a
+// screen (schwarz_tau > 0)
 const double* plan_centers(const eri_plan* p);
 const double* plan_exps(const eri_plan* p);
 const double* plan_coefs(const eri_plan* p);  // the caller's raw contraction coefficients

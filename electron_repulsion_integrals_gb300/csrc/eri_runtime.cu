@@ -193,7 +193,10 @@ struct eri_plan {
   double tau = 0;
   int lmax = 0;
   std::vector<int> hL, hnprim, hpoff, hfo;
-  std::vector<double> hcen, hexps, hcoef;  // hcoef: the caller's raw coefficients
+  // host copies of the caller's centres, exponents and raw coefficients: kept
+  // only for the screen (schwarz_tau > 0), which reads them on the host
+  std::vector<double> hcen, hexps, hcoef;
+  size_t np_total = 0;
   int nbf = 0;
   // device copies
   double* dcen = nullptr;
@@ -203,6 +206,8 @@ struct eri_plan {
   int* dfo = nullptr;
   double* dexps = nullptr;
   double* dcoef = nullptr;
+  double* draw = nullptr;   // the caller's coefficients on the device (normalisation input)
+  int* dbad = nullptr;      // normalisation status flag
   const double* dboys = nullptr;
   // scratch
   double* scratch = nullptr;
@@ -214,12 +219,26 @@ struct eri_plan {
 
 namespace {
 
+// Device copy of n host values, ordered on stream st (st == 0: the legacy
+// default stream).  The host data may be released once the call returns.
 template <class T>
-int upload(T** dst, const std::vector<T>& src) {
-  size_t bytes = std::max<size_t>(src.size(), 1) * sizeof(T);
+int upload(T** dst, const T* src, size_t n, cudaStream_t st = 0) {
+  size_t bytes = std::max<size_t>(n, 1) * sizeof(T);
   CUDA_TRY(cudaMalloc(dst, bytes));
-  if (!src.empty()) CUDA_TRY(cudaMemcpy(*dst, src.data(), src.size() * sizeof(T), cudaMemcpyHostToDevice));
+  if (n) {
+    if (st) {
+      CUDA_TRY(cudaMemcpyAsync(*dst, src, n * sizeof(T), cudaMemcpyHostToDevice, st));
+      CUDA_TRY(cudaStreamSynchronize(st));
+    } else {
+      CUDA_TRY(cudaMemcpy(*dst, src, n * sizeof(T), cudaMemcpyHostToDevice));
+    }
+  }
   return ERI_OK;
+}
+
+template <class T>
+int upload(T** dst, const std::vector<T>& src, cudaStream_t st = 0) {
+  return upload(dst, src.data(), src.size(), st);
 }
 
 int ensure_scratch(eri_plan* p, size_t doubles) {
@@ -229,8 +248,8 @@ int ensure_scratch(eri_plan* p, size_t doubles) {
     p->scratch = nullptr;
     p->scratch_len = 0;
   }
+  // no clearing: the kernels write every scratch slot before they read it
   CUDA_TRY(cudaMalloc(&p->scratch, doubles * sizeof(double)));
-  CUDA_TRY(cudaMemset(p->scratch, 0, doubles * sizeof(double)));
   p->scratch_len = doubles;
   return ERI_OK;
 }
@@ -244,24 +263,22 @@ void fill_shells(const eri_plan* p, ShellsDev& sh) {
   sh.coef = p->dcoef;
 }
 
-int normalise_on_device(eri_plan* p, cudaStream_t st) {
-  double* raw = nullptr;
-  int* bad = nullptr;
-  int rc = upload(&raw, p->hcoef);
+// The temporaries stay with the plan (freed by eri_plan_destroy): a cudaFree
+// here would wait for all work on the device, e.g. another plan's kernels.
+int normalise_on_device(eri_plan* p, const double* coefs, cudaStream_t st) {
+  int rc = upload(&p->draw, coefs, p->np_total, st);
   if (rc) return rc;
-  cudaError_t e = cudaMalloc(&p->dcoef, std::max<size_t>(p->hcoef.size(), 1) * sizeof(double));
-  if (e == cudaSuccess) e = cudaMalloc(&bad, sizeof(int));
-  if (e == cudaSuccess) e = cudaMemsetAsync(bad, 0, sizeof(int), st);
+  cudaError_t e = cudaMalloc(&p->dcoef, std::max<size_t>(p->np_total, 1) * sizeof(double));
+  if (e == cudaSuccess) e = cudaMalloc(&p->dbad, sizeof(int));
+  if (e == cudaSuccess) e = cudaMemsetAsync(p->dbad, 0, sizeof(int), st);
   if (e == cudaSuccess) {
     normalise_shells_kernel<<<(p->nshell + 255) / 256, 256, 0, st>>>(p->nshell, p->dL, p->dnprim, p->dpoff, p->dexps,
-                                                                     raw, p->dcoef, bad);
+                                                                     p->draw, p->dcoef, p->dbad);
     e = cudaGetLastError();
   }
   int hbad = 0;
-  if (e == cudaSuccess) e = cudaMemcpyAsync(&hbad, bad, sizeof(int), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(&hbad, p->dbad, sizeof(int), cudaMemcpyDeviceToHost, st);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
-  cudaFree(raw);
-  cudaFree(bad);
   if (e != cudaSuccess) {
     (void)cudaGetLastError();
     return e == cudaErrorMemoryAllocation ? ERI_ERR_OOM : ERI_ERR_CUDA;
@@ -331,7 +348,7 @@ double* eri::host::plan_scratch(eri_plan* p, size_t doubles, int* rc) {
   return *rc ? nullptr : p->scratch;
 }
 double eri::host::plan_tau(const eri_plan* p) { return p->tau; }
-size_t eri::host::plan_nprim_total(const eri_plan* p) { return p->hexps.size(); }
+size_t eri::host::plan_nprim_total(const eri_plan* p) { return p->np_total; }
 const double* eri::host::plan_dcoef(const eri_plan* p) { return p->dcoef; }
 int eri::host::plan_device(const eri_plan* p) { return p->device; }
 int eri::host::built_lmax() { return ::built_lmax(); }
@@ -376,6 +393,8 @@ int eri_plan_destroy(eri_plan* p) {
   cudaFree(p->dfo);
   cudaFree(p->dexps);
   cudaFree(p->dcoef);
+  cudaFree(p->draw);
+  cudaFree(p->dbad);
   cudaFree(p->scratch);
   cudaFree(p->qbuf);
   delete p;
@@ -412,9 +431,12 @@ int eri_plan_create_flat(int nshell, const double* centers, const int* L, const 
   p->contracted = npmax > 1;
   p->hL.assign(L, L + nshell);
   p->hnprim.assign(nprim, nprim + nshell);
-  p->hcen.assign(centers, centers + 3 * (size_t)nshell);
-  p->hexps.assign(exps, exps + np_total);
-  p->hcoef.assign(coefs, coefs + np_total);
+  p->np_total = np_total;
+  if (p->tau > 0) {
+    p->hcen.assign(centers, centers + 3 * (size_t)nshell);
+    p->hexps.assign(exps, exps + np_total);
+    p->hcoef.assign(coefs, coefs + np_total);
+  }
   p->hpoff.resize(nshell);
   p->hfo.resize(nshell + 1);
   p->hfo[0] = 0;
@@ -433,13 +455,15 @@ int eri_plan_create_flat(int nshell, const double* centers, const int* L, const 
     return ERI_ERR_CUDA;
   }
   int rc;
-  if ((rc = upload(&p->dcen, p->hcen)) || (rc = upload(&p->dL, p->hL)) || (rc = upload(&p->dnprim, p->hnprim)) ||
-      (rc = upload(&p->dpoff, p->hpoff)) || (rc = upload(&p->dfo, p->hfo)) || (rc = upload(&p->dexps, p->hexps)) ||
+  cudaStream_t cst = (cudaStream_t)stream;
+  if ((rc = upload(&p->dcen, centers, 3 * (size_t)nshell, cst)) || (rc = upload(&p->dL, p->hL, cst)) ||
+      (rc = upload(&p->dnprim, p->hnprim, cst)) || (rc = upload(&p->dpoff, p->hpoff, cst)) ||
+      (rc = upload(&p->dfo, p->hfo, cst)) || (rc = upload(&p->dexps, exps, np_total, cst)) ||
       (rc = boys_table_for_device(p->device, &p->dboys))) {
     eri_plan_destroy(p);
     return rc;
   }
-  rc = normalise_on_device(p, (cudaStream_t)stream);
+  rc = normalise_on_device(p, coefs, (cudaStream_t)stream);
   if (rc) {
     eri_plan_destroy(p);
     return rc;
