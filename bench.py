@@ -94,6 +94,23 @@ def dram_traffic(cls, n):
     return rec["dram_bytes_per_quartet"] * n
 
 
+def max_over_ranks(ms, dist, device):
+    """The slowest rank's time (all ranks receive it); ms itself without a
+    process group."""
+    if not dist:
+        return ms
+    import torch
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_rate(per_rank_units, world, steps, ms):
+    """Whole-job throughput of replicas: every rank processes per_rank_units
+    per step; the job takes the slowest rank's time."""
+    return per_rank_units * world * steps / (ms / 1e3)
+
+
 def env_int(k, d):
     try:
         return int(os.environ.get(k, d))
@@ -269,11 +286,8 @@ def run_coulomb(a, rank, world, local_rank):
         dist.barrier()
     clk = clocks.stop()
     ms = t0.elapsed_time(t1)
-    if dist:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
-    value = nq * world * a.steps / (ms / 1e3)
+    ms = max_over_ranks(ms, dist, dev)
+    value = replica_rate(nq, world, a.steps, ms)
     # algorithmic flops: per class, quartets x (primitive quartets x VRR + HRR) + per digested integral
     # 2 FMA for J (+ 4 FMA for K)
     prim_q = 0.0
@@ -436,12 +450,9 @@ def run_ours(a, rank, world, local_rank):
         dist.barrier()
     clk = clocks.stop()
     ms = t0.elapsed_time(t1)
-    if dist:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(ms, dist, dev)
     total_q = sum(b["n"] for b in batches) * world
-    value = total_q * a.steps / (ms / 1e3)
+    value = replica_rate(sum(b["n"] for b in batches), world, a.steps, ms)
 
     per_class = {}
     for b in batches:
