@@ -451,7 +451,6 @@ def run_ours(a, rank, world, local_rank):
     clk = clocks.stop()
     ms = t0.elapsed_time(t1)
     ms = max_over_ranks(ms, dist, dev)
-    total_q = sum(b["n"] for b in batches) * world
     value = replica_rate(sum(b["n"] for b in batches), world, a.steps, ms)
 
     per_class = {}
