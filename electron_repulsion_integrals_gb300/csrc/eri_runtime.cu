@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cstdint>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -138,13 +139,21 @@ int boys_table_for_device(int dev, const double** out) {
 // prefactor 2 pi^{5/2} / (zeta eta sqrt(zeta + eta)).
 //   N(alpha, l) = (2 alpha/pi)^{3/4} (4 alpha)^{l/2} / sqrt((2l-1)!!)
 //   S = sum_{k,k'} c_k c_k' N_k N_k' (2l-1)!! / (2 p)^l (pi/p)^{3/2},  p = alpha_k + alpha_k'
+// It also checks the caller's data: a non-finite centre, a non-finite or
+// non-positive exponent or a non-finite coefficient sets *bad.
 __global__ void normalise_shells_kernel(int nshell, const int* __restrict__ L, const int* __restrict__ nprim,
-                                        const int* __restrict__ poff, const double* __restrict__ ex,
-                                        const double* __restrict__ raw, double* __restrict__ out,
-                                        int* __restrict__ bad) {
+                                        const int* __restrict__ poff, const double* __restrict__ cen,
+                                        const double* __restrict__ ex, const double* __restrict__ raw,
+                                        double* __restrict__ out, int* __restrict__ bad) {
   const int s = blockIdx.x * blockDim.x + threadIdx.x;
   if (s >= nshell) return;
   const int l = L[s], np = nprim[s], o = poff[s];
+  bool ok = isfinite(cen[3 * (size_t)s]) && isfinite(cen[3 * (size_t)s + 1]) && isfinite(cen[3 * (size_t)s + 2]);
+  for (int i = 0; i < np; ++i) ok = ok && isfinite(ex[o + i]) && ex[o + i] > 0.0 && isfinite(raw[o + i]);
+  if (!ok) {
+    atomicExch(bad, 1);
+    return;
+  }
   const double pi = 3.14159265358979323846;
   double dl = 1.0;
   for (int k = 2 * l - 1; k > 1; k -= 2) dl *= k;
@@ -272,8 +281,8 @@ int normalise_on_device(eri_plan* p, const double* coefs, cudaStream_t st) {
   if (e == cudaSuccess) e = cudaMalloc(&p->dbad, sizeof(int));
   if (e == cudaSuccess) e = cudaMemsetAsync(p->dbad, 0, sizeof(int), st);
   if (e == cudaSuccess) {
-    normalise_shells_kernel<<<(p->nshell + 255) / 256, 256, 0, st>>>(p->nshell, p->dL, p->dnprim, p->dpoff, p->dexps,
-                                                                     p->draw, p->dcoef, p->dbad);
+    normalise_shells_kernel<<<(p->nshell + 255) / 256, 256, 0, st>>>(p->nshell, p->dL, p->dnprim, p->dpoff, p->dcen,
+                                                                     p->dexps, p->draw, p->dcoef, p->dbad);
     e = cudaGetLastError();
   }
   int hbad = 0;
@@ -407,44 +416,48 @@ int eri_plan_create_flat(int nshell, const double* centers, const int* L, const 
   *out = nullptr;
   if (nshell <= 0 || !centers || !L || !nprim || !exps || !coefs || !opt || opt->flags != 0) return ERI_ERR_INVALID_ARG;
   const int lmax_built = built_lmax();
-  int lmax = 0, lmin = 0, npmin = 1, npmax = 1;
-  size_t np_total = 0;
-  for (int s = 0; s < nshell; ++s) {
-    lmax = std::max(lmax, L[s]);
-    lmin = std::min(lmin, L[s]);
-    npmin = std::min(npmin, nprim[s]);
-    npmax = std::max(npmax, nprim[s]);
-    np_total += (size_t)std::max(nprim[s], 0);
-  }
-  if (lmin < 0 || npmin <= 0 || np_total > ((size_t)1 << 30)) return ERI_ERR_INVALID_ARG;
-  if (lmax > lmax_built) return ERI_ERR_UNSUPPORTED_L;
-  bool finite = true;
-  for (size_t i = 0; i < 3 * (size_t)nshell; ++i) finite &= std::isfinite(centers[i]);
-  for (size_t i = 0; i < np_total; ++i) finite &= std::isfinite(exps[i]) && exps[i] > 0 && std::isfinite(coefs[i]);
-  if (!finite) return ERI_ERR_NOT_FINITE;
   eri_plan* p = new (std::nothrow) eri_plan();
   if (!p) return ERI_ERR_OOM;
   p->nshell = nshell;
   p->spherical = opt->spherical != 0;
   p->tau = opt->schwarz_tau;
-  p->lmax = lmax;
-  p->contracted = npmax > 1;
+  // one pass: angular momenta and primitive counts checked, primitive offsets
+  // and first basis functions (the centres, exponents and coefficients are
+  // checked on the device, by the normalisation kernel)
+  int lmax = 0, lmin = 0, npmin = 1, npmax = 1;
+  size_t np_total = 0;
+  long long nbf = 0;
   p->hL.assign(L, L + nshell);
   p->hnprim.assign(nprim, nprim + nshell);
+  p->hpoff.resize(nshell);
+  p->hfo.resize(nshell + 1);
+  for (int s = 0; s < nshell; ++s) {
+    const int l = L[s], np = nprim[s];
+    lmax = std::max(lmax, l);
+    lmin = std::min(lmin, l);
+    npmin = std::min(npmin, np);
+    npmax = std::max(npmax, np);
+    p->hpoff[s] = (int)std::min<size_t>(np_total, (size_t)INT32_MAX);
+    p->hfo[s] = (int)std::min<long long>(nbf, INT32_MAX);
+    np_total += (size_t)std::max(np, 0);
+    nbf += l >= 0 ? nfunc(l, p->spherical) : 0;
+  }
+  p->hfo[nshell] = (int)std::min<long long>(nbf, INT32_MAX);
+  if (lmin < 0 || npmin <= 0 || np_total > ((size_t)1 << 30) || nbf > INT32_MAX) {
+    delete p;
+    return ERI_ERR_INVALID_ARG;
+  }
+  if (lmax > lmax_built) {
+    delete p;
+    return ERI_ERR_UNSUPPORTED_L;
+  }
+  p->lmax = lmax;
+  p->contracted = npmax > 1;
   p->np_total = np_total;
   if (p->tau > 0) {
     p->hcen.assign(centers, centers + 3 * (size_t)nshell);
     p->hexps.assign(exps, exps + np_total);
     p->hcoef.assign(coefs, coefs + np_total);
-  }
-  p->hpoff.resize(nshell);
-  p->hfo.resize(nshell + 1);
-  p->hfo[0] = 0;
-  int off = 0;
-  for (int s = 0; s < nshell; ++s) {
-    p->hpoff[s] = off;
-    off += nprim[s];
-    p->hfo[s + 1] = p->hfo[s] + nfunc(L[s], p->spherical);
   }
   p->nbf = p->hfo[nshell];
   cudaError_t e = cudaGetDevice(&p->device);

@@ -243,3 +243,17 @@ def test_cooperative_tier_more_than_one_setup_batch(dev, cls):
     if max(cls) > built_lmax():
         pytest.skip("class not built")
     _homogeneous_check(dev, cls, 19, 3, seed_index=470 + sum(cls))
+
+
+def test_non_finite_shell_data_is_rejected(dev):
+    """A NaN centre, a non-positive exponent or an infinite coefficient makes
+    plan creation return ERI_ERR_NOT_FINITE (checked on the device)."""
+    for field, idx, value in [("centers", (1, 2), float("nan")), ("exps", 3, -1.0), ("exps", 0, 0.0),
+                              ("coefs", 2, float("inf"))]:
+        s, _ = W.homogeneous((1, 1, 0, 0), 4, 2, seed_index=520)
+        getattr(s, field)[idx] = value
+        with pytest.raises(eri.EriError) as ei:
+            eri.Plan(s, spherical=True)
+        assert ei.value.code == -6, (field, ei.value.code)
+    s, _ = W.homogeneous((1, 1, 0, 0), 4, 2, seed_index=520)
+    eri.Plan(s, spherical=True).close()  # the same data, untouched, is accepted
