@@ -20,9 +20,9 @@
 
 namespace eri {
 
-constexpr int kCoopWarps = 2;                 // warps per block
+constexpr int kCoopWarps = 1;                 // warps per block (one-warp groups)
 constexpr int kCoopThreads = 32 * kCoopWarps;
-constexpr int kCoopBatch = 8;                 // primitive quartets set up at once
+constexpr int kCoopBatch = 4;                 // primitive quartets set up at once
 
 // Layout of one primitive quartet's parameters in shared memory (doubles):
 //   0..2 P-A, 3..5 W-P, 6..8 Q-C, 9..11 W-Q, 12 rho/zeta, 13 rho/eta,

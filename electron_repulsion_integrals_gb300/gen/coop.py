@@ -241,7 +241,7 @@ def setup_stride(La, Lc, nw=0):
     return (f + L + 1 + nw) | 1
 
 
-def lanes_for(arena, La, Lc, batch=8):
+def lanes_for(arena, La, Lc, batch=4):
     """Lanes that share one quartet: one warp, unless the per-quartet shared
     memory leaves at most MAX_GROUPS_FOR_WIDE quartets on an SM; then four
     warps (one group per block).  Measured: four-warp groups doubled (gg|gg)
