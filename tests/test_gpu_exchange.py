@@ -121,3 +121,17 @@ def test_K_64_atom_cluster_sampled_blocks(dev):
     # Tr(D K D) >= 0: sum_{mu nu la si} D_{mu la} (mu nu|la si) D_{nu si} for the PSD density
     assert np.sum(D * K) > 0
     plan.close()
+
+
+def test_J_and_K_report_classes_above_d_as_not_implemented(dev):
+    """The J/K digestion covers the register and staged tiers (every class of
+    s, p, d shells); a screened class of the cooperative tier is reported, not
+    skipped."""
+    s, _ = W.homogeneous((3, 3, 3, 3), 2, 1, seed_index=830, box=2.0)
+    plan = eri.Plan(s, spherical=True, schwarz_tau=1e-10)
+    D = torch.zeros((W.nbf(s), W.nbf(s)), dtype=torch.float64, device=dev)
+    for call in (lambda: plan.build_J(D), lambda: plan.build_JK(D)):
+        with pytest.raises(eri.EriError) as ei:
+            call()
+        assert ei.value.code == -7
+    plan.close()
