@@ -1,8 +1,10 @@
 // Warp-cooperative evaluation of high angular momentum classes.
 //
-// One warp evaluates one contracted shell quartet (FusionRCG Algorithm 2):
-//   * the lanes compute the pair/quartet parameters and Boys values of up to
-//     32 primitive quartets at once (one each) into shared memory;
+// A group of lanes (one warp; four warps for the largest classes; 8 or 16
+// lanes of a warp for small derivative classes) evaluates one contracted shell
+// quartet (FusionRCG Algorithm 2):
+//   * four lanes compute the pair/quartet parameters and Boys values of up to
+//     four primitive quartets at once (one each) into shared memory;
 //   * for each primitive quartet the VRR (Eq. (2) and its ket form) runs as a
 //     sequence of steps over a per-warp shared-memory arena: the bra part
 //     (column 0, [e|0]^(m)) level by level, then the ket columns
@@ -42,12 +44,17 @@ struct CoopSetup {
   static constexpr int STRIDE = SIZE | 1;  // odd stride: lanes hit different banks
 };
 
-// Synchronisation of the lanes that share one quartet: one warp (LN = 32), or
+// Synchronisation of the lanes that share one quartet: an aligned group of LN
+// lanes inside a warp (LN = 4, 8, 16; the other groups of the warp work on
+// other quartets and may be elsewhere in the code), one warp (LN = 32), or
 // the whole block when a group of 2 or 4 warps shares the quartet (one group
 // per block).
 template <int LN>
 __device__ __forceinline__ void coop_sync() {
-  if constexpr (LN == 32) {
+  if constexpr (LN < 32) {
+    static_assert(LN >= 4 && (LN & (LN - 1)) == 0, "sub-warp groups of 4, 8 or 16 lanes");
+    __syncwarp(((1u << LN) - 1u) << (threadIdx.x & 31u & ~(unsigned)(LN - 1)));
+  } else if constexpr (LN == 32) {
     __syncwarp();
   } else {
     __syncthreads();
@@ -113,14 +120,14 @@ __device__ __forceinline__ void coop_vrr(double* __restrict__ arena, const doubl
   constexpr int LN = C::LANES;
   double* bra = arena + C::BRA_COL;
   // column 0: Boys values [00|00]^(m)
-  if (lane <= C::L) bra[lane * NE] = s[S::F + lane];
+  for (int m = lane; m <= C::L; m += LN) bra[m * NE] = s[S::F + m];
   coop_sync<LN>();
   const double roz = s[12], roe = s[13];
   // bra levels
 #pragma unroll 1
   for (int k = 0; k < C::La; ++k) {
     const int y0 = C::bra_y_start()[k], y1 = C::bra_y_start()[k + 1];
-    // two nodes per lane while more than 32 remain (warp-uniform test), then one
+    // two nodes per lane while more than LN remain (group-uniform test), then one
     for (int t0 = y0; t0 < y1; t0 += 2 * LN) {
       const int t = t0 + lane;
       if (t0 + LN < y1) {
@@ -204,10 +211,10 @@ __device__ __forceinline__ void coop_vrr(double* __restrict__ arena, const doubl
       }
     }
     // nodes with e_i > 0 (cross term [e - 1_i | f]^(m+1)).  Node u = m nz + k
-    // of the rows x list rectangle; lane l takes u = u0 + l and u0 + l + 32 in
-    // iteration u0 (steps of 64, integer stepping of (m, k) only), so that two
-    // dependent FMA chains overlap; when at most 32 nodes remain (a
-    // warp-uniform test) one node per lane.  A lane without a second node in a
+    // of the rows x list rectangle; lane l takes u = u0 + l and u0 + l + LN in
+    // iteration u0 (steps of 2 LN, integer stepping of (m, k) only), so that two
+    // dependent FMA chains overlap; when at most LN nodes remain (a
+    // group-uniform test) one node per lane.  A lane without a second node in a
     // two-node iteration repeats its first and does not store it.
     {
       const int nz = C::nz(st.axis);

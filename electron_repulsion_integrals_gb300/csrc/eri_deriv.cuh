@@ -26,20 +26,22 @@ __device__ __forceinline__ double* deriv_out(const EriLaunch& P, const Quartet& 
 
 }  // namespace eri
 
-// Kernel of one derivative class.  C: traits (NW = 3); BRA_A / BRA_B fill the
-// three axis sets of d/dA / d/dB rows, BRA_0G the plain and 2-gamma rows;
-// KET_AB(P, Q, q, r, G, k) writes d/d(slot k) for the three axes from three
-// row sets, KET_C(P, Q, q, r, G) writes d/dC.
+// Kernel of one derivative class.  C: traits (NW = 3; LANES lanes per
+// quartet, GROUPS quartets per block); BRA_A / BRA_B fill the three axis sets
+// of d/dA / d/dB rows, BRA_0G the plain and 2-gamma rows;
+// KET_AB(P, Q, q, r, x, G, k) writes row r of d/d(slot k) along axis x from
+// row set x, KET_C(P, Q, q, r, G) writes row r of d/dC for the three axes.
 #define ERI_DERIV_KERNEL(NAME, C, BRA_A, BRA_B, BRA_0G, KET_AB, KET_C)                                   \
   template <bool CONTRACTED>                                                                              \
-  __global__ void __launch_bounds__(kCoopThreads) NAME(const EriLaunch P) {                               \
+  __global__ void __launch_bounds__(C::THREADS) NAME(const EriLaunch P) {                                 \
     extern __shared__ double smem_[];                                                                     \
     using S_ = CoopSetup<C::La, C::Lc, C::NW>;                                                            \
-    const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;                                            \
+    constexpr int LN_ = C::LANES;                                                                         \
+    const int lane = threadIdx.x % LN_, wib = threadIdx.x / LN_;                                          \
     double* arena = smem_ + (size_t)wib * C::WARP_SMEM;                                                   \
     double* setup = arena + C::ARENA;                                                                     \
-    const long long nw = (long long)gridDim.x * kCoopWarps;                                               \
-    const long long wid = (long long)blockIdx.x * kCoopWarps + wib;                                       \
+    const long long nw = (long long)gridDim.x * C::GROUPS;                                                \
+    const long long wid = (long long)blockIdx.x * C::GROUPS + wib;                                        \
     double* H = P.scratch + (size_t)wid * C::NH * (C::NW + 1);                                            \
     for (long long q = wid; q < P.n; q += nw) {                                                           \
       Quartet Q;                                                                                          \
@@ -50,54 +52,60 @@ __device__ __forceinline__ double* deriv_out(const EriLaunch& P, const Quartet& 
         if (lane < kCoopBatch && p < nprim)                                                               \
           coop_setup_one<kStore, C::La, C::Lc, C::NW>(P, Q, p / ncd, p - (p / ncd) * ncd,                \
                                                                    setup + lane * S_::STRIDE);            \
-        __syncwarp();                                                                                     \
+        coop_sync<LN_>();                                                                                 \
         const int cnt = nprim - base < kCoopBatch ? nprim - base : kCoopBatch;                            \
         for (int pp = 0; pp < cnt; ++pp) coop_vrr<C>(arena, setup + pp * S_::STRIDE, H, lane, base + pp == 0); \
-        __syncwarp();                                                                                     \
+        coop_sync<LN_>();                                                                                 \
       }                                                                                                   \
       double* G = arena;                                                                                  \
-      for (int fi = lane; fi < C::NF; fi += 32) BRA_A(Q, H, fi, G);                                       \
-      __syncwarp();                                                                                       \
-      for (int r = lane; r < C::NR; r += 32) KET_AB(P, Q, q, r, G, 0);                                    \
-      __syncwarp();                                                                                       \
-      for (int fi = lane; fi < C::NF; fi += 32) BRA_B(Q, H, fi, G);                                       \
-      __syncwarp();                                                                                       \
-      for (int r = lane; r < C::NR; r += 32) KET_AB(P, Q, q, r, G, 1);                                    \
-      __syncwarp();                                                                                       \
-      for (int fi = lane; fi < C::NF; fi += 32) BRA_0G(Q, H, fi, G);                                      \
-      __syncwarp();                                                                                       \
-      for (int r = lane; r < C::NR; r += 32) KET_C(P, Q, q, r, G);                                        \
-      __syncwarp();                                                                                       \
+      for (int fi = lane; fi < C::NF; fi += LN_) BRA_A(Q, H, fi, G);                                      \
+      coop_sync<LN_>();                                                                                   \
+      for (int it = lane; it < 3 * C::NR; it += LN_) {                                                    \
+        const int x_ = it / C::NR;                                                                        \
+        KET_AB(P, Q, q, it - x_ * C::NR, x_, G, 0);                                                       \
+      }                                                                                                   \
+      coop_sync<LN_>();                                                                                   \
+      for (int fi = lane; fi < C::NF; fi += LN_) BRA_B(Q, H, fi, G);                                      \
+      coop_sync<LN_>();                                                                                   \
+      for (int it = lane; it < 3 * C::NR; it += LN_) {                                                    \
+        const int x_ = it / C::NR;                                                                        \
+        KET_AB(P, Q, q, it - x_ * C::NR, x_, G, 1);                                                       \
+      }                                                                                                   \
+      coop_sync<LN_>();                                                                                   \
+      for (int fi = lane; fi < C::NF; fi += LN_) BRA_0G(Q, H, fi, G);                                     \
+      coop_sync<LN_>();                                                                                   \
+      for (int r = lane; r < C::NR; r += LN_) KET_C(P, Q, q, r, G);                                       \
+      coop_sync<LN_>();                                                                                   \
     }                                                                                                     \
   }
 
-#define ERI_DERIV_SMEM_(T) ((size_t)kCoopWarps * (T::WARP_SMEM) * sizeof(double))
+#define ERI_DERIV_SMEM_(T) ((size_t)(T::GROUPS) * (T::WARP_SMEM) * sizeof(double))
 // Per-class entry points: launch (store mode, contracted or not), grid and
-// scratch sizing (four accumulator sets per warp).
+// scratch sizing (four accumulator sets per group of lanes).
 #define ERI_DEFINE_DERIV_LAUNCHER(LA, LB, LC, LD, KERNEL, T)                                             \
   extern "C" int eri_dlaunch_c##LA##LB##LC##LD(const EriLaunch* P, int contracted, int blocks, cudaStream_t st) { \
     if (contracted) {                                                                                    \
       cudaFuncSetAttribute(KERNEL<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ERI_DERIV_SMEM_(T)); \
-      KERNEL<true><<<blocks, kCoopThreads, ERI_DERIV_SMEM_(T), st>>>(*P);                                \
+      KERNEL<true><<<blocks, T::THREADS, ERI_DERIV_SMEM_(T), st>>>(*P);                                \
     } else {                                                                                             \
       cudaFuncSetAttribute(KERNEL<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ERI_DERIV_SMEM_(T)); \
-      KERNEL<false><<<blocks, kCoopThreads, ERI_DERIV_SMEM_(T), st>>>(*P);                               \
+      KERNEL<false><<<blocks, T::THREADS, ERI_DERIV_SMEM_(T), st>>>(*P);                               \
     }                                                                                                    \
     return (int)cudaGetLastError();                                                                      \
   }                                                                                                      \
   extern "C" int eri_dgrid_c##LA##LB##LC##LD(int nsm, long long n, long long* blocks, long long* scratch) { \
     int occ = 0;                                                                                         \
     cudaFuncSetAttribute(KERNEL<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ERI_DERIV_SMEM_(T)); \
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, KERNEL<true>, kCoopThreads, ERI_DERIV_SMEM_(T)) != \
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, KERNEL<true>, T::THREADS, ERI_DERIV_SMEM_(T)) != \
             cudaSuccess || occ < 1) {                                                                    \
       (void)cudaGetLastError();                                                                          \
       occ = 1;                                                                                           \
     }                                                                                                    \
     long long b = (long long)nsm * occ;                                                                  \
-    const long long need = (n + kCoopWarps - 1) / kCoopWarps;                                            \
+    const long long need = (n + T::GROUPS - 1) / T::GROUPS;                                            \
     if (b > need) b = need;                                                                              \
     if (b < 1) b = 1;                                                                                    \
     *blocks = b;                                                                                         \
-    *scratch = b * kCoopWarps * (long long)T::NH * (T::NW + 1);                                          \
+    *scratch = b * T::GROUPS * (long long)T::NH * (T::NW + 1);                                          \
     return 0;                                                                                            \
   }
