@@ -46,6 +46,7 @@ sys.path.insert(0, ROOT)
 METRIC = "ERI quartets/s and FP64 GFLOP/s per angular class (fraction of GB300 FP64 peak)"
 # FP64 pipe peak from unit counts and clock: 152 SMs x 2 DFMA/clk x 2 flop x 2.070 GHz
 FP64_PEAK_TFLOPS = 152 * 2 * 2 * 2.070e9 / 1e12
+E2E_CHUNK_BYTES = 0.75e9  # output bytes per e2e chunk: readback of one overlaps compute of the next
 
 WORKLOADS = {
     "homogeneous": {"desc": "homogeneous class batch: (pp|pp) x 1,048,576 + (dd|dd) x 1,048,576 quartets, "
@@ -472,24 +473,51 @@ def run_ours(a, rank, world, local_rank):
     # batch's plan creation (host work) overlaps the other's compute and copies.
     e2e = None
     if a.e2e:
-        host_q = [torch.from_numpy(b["q"]).pin_memory() for b in batches]
+        def pinned(a):
+            t = torch.empty(a.shape, dtype=torch.from_numpy(a[:0]).dtype, pin_memory=True)
+            t.numpy()[...] = a
+            return t.numpy()
+
+        # the step's inputs in page-locked host memory: quartet lists and shells
+        host_q = [torch.from_numpy(pinned(b["q"])) for b in batches]
+        host_s = [W.Shells(*(pinned(x) for x in (b["shells"].centers, b["shells"].L, b["shells"].nprim,
+                                                  b["shells"].exps, b["shells"].coefs))) for b in batches]
         host_o = [torch.empty(b["out"].numel(), dtype=torch.float64, pin_memory=True) for b in batches]
         streams = [torch.cuda.Stream() for _ in batches]
+        copy_streams = [torch.cuda.Stream() for _ in batches]
         order = sorted(range(len(batches)), key=lambda i: -batches[i]["flops"] * batches[i]["n"])
-        h2d = sum(hq.numel() * 4 for hq in host_q) + sum(b["shells"].n * 48 + b["shells"].exps.size * 16
+        # plan creation uploads per shell its centre, l, primitive count, primitive
+        # offset and first function (40 B), per primitive the exponent and coefficient
+        h2d = sum(hq.numel() * 4 for hq in host_q) + sum(b["shells"].n * 40 + b["shells"].exps.size * 16
                                                          for b in batches)
         d2h = sum(ho.numel() * 8 for ho in host_o)
         e_steps = max(1, min(a.steps, 5))
 
+        def chunks(b):
+            # quartet ranges of about E2E_CHUNK_BYTES of output each
+            n = b["n"]
+            k = max(1, min(8, round(b["out"].numel() * 8 / E2E_CHUNK_BYTES)))
+            return [(n * j // k, n * (j + 1) // k) for j in range(k)]
+
         def e2e_step():
             plans = []
             for i in order:
-                b, hq, ho, st_i = batches[i], host_q[i], host_o[i], streams[i]
+                b, hq, ho, st_i, cp_i = batches[i], host_q[i], host_o[i], streams[i], copy_streams[i]
+                per_q = b["out"].numel() // b["n"]
                 with torch.cuda.stream(st_i):
-                    plan = eri.Plan(b["shells"], spherical=True, stream=st_i)
+                    plan = eri.Plan(host_s[i], spherical=True, stream=st_i)
                     qd = hq.to(dev, non_blocking=True)
-                    compute(plan.handle, b["cls"], qd, b["out"], st_i)
-                    ho.copy_(b["out"], non_blocking=True)
+                    # the chunks of one plan run in order on its stream (they
+                    # share the plan's scratch); each chunk's readback runs on a
+                    # copy stream, overlapping the next chunk's compute
+                    for lo, hi in chunks(b):
+                        o = b["out"][lo * per_q:hi * per_q]
+                        compute(plan.handle, b["cls"], qd[lo:hi], o, st_i)
+                        done = torch.cuda.Event()
+                        done.record(st_i)
+                        cp_i.wait_event(done)
+                        with torch.cuda.stream(cp_i):
+                            ho[lo * per_q:hi * per_q].copy_(o, non_blocking=True)
                 plans.append(plan)
             torch.cuda.synchronize()
             for plan in plans:
@@ -509,7 +537,9 @@ def run_ours(a, rank, world, local_rank):
         e2e = {"value": sum(b["n"] for b in batches) * world * e_steps / te, "unit": "quartets/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": te / e_steps * 1e3,
                "ms_per_step_median": statistics.median(steps_ms), "ms_per_step_min": min(steps_ms),
-               "schedule": "class batches on separate CUDA streams, heaviest first"}
+               "ms_steps": [round(t, 1) for t in steps_ms],
+               "schedule": "class batches on separate CUDA streams, heaviest first; each batch in chunks of about "
+                           f"{E2E_CHUNK_BYTES / 1e9:.2g} GB of output whose readback overlaps the next chunk's compute"}
 
     cpu = None
     if rank == 0 and a.cpu_baseline:

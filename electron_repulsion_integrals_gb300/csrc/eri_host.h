@@ -21,12 +21,13 @@ int launch_class(eri_plan* p, const int l[4], EriLaunch& P, int mode, cudaStream
 void canonical_order(const int l[4], int canon[4]);
 bool plan_spherical(const eri_plan* p);
 int plan_nshell(const eri_plan* p);
-const int* plan_L(const eri_plan* p);
-const int* plan_nprim(const eri_plan* p);
 const int* plan_fo(const eri_plan* p);
 const int* plan_poff(const eri_plan* p);
+int plan_npmax(const eri_plan* p, int l);  // largest primitive count of the shells of l
 // host copies of the caller's shell data; present only when the plan has a
 // screen (schwarz_tau > 0)
+const int* plan_L(const eri_plan* p);
+const int* plan_nprim(const eri_plan* p);
 const double* plan_centers(const eri_plan* p);
 const double* plan_exps(const eri_plan* p);
 const double* plan_coefs(const eri_plan* p);  // the caller's raw contraction coefficients

@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <climits>
 #include <cstdint>
 #include <cmath>
 #include <cstdio>
@@ -20,6 +21,10 @@
 #include "eri_host.h"
 
 using namespace eri;
+
+// Largest shell angular momentum any build can hold (four shells of it fill
+// the Boys table's orders).
+constexpr int kMaxL = kBoysMaxL / 4;
 
 // ------------------------------------------------------------------ registry
 // The class list: generated/registry.inc, or the file ERI_REGISTRY_INC names
@@ -190,6 +195,197 @@ __global__ void normalise_shells_kernel(int nshell, const int* __restrict__ L, c
   }
 }
 
+// ------------------------------------------------------------------ shell offsets
+// Primitive offsets poff[s] = sum_{t<s} nprim[t] and first basis functions
+// fo[s] = sum_{t<s} nfunc(L[t]) (exclusive prefix sums), and the checks of the
+// caller's angular momenta and primitive counts, on the device.  Tiles of
+// kScanTile shells: (1) every tile sums itself and folds its minima and maxima
+// into the summary, (2) one block scans the tile sums, (3) every tile scans
+// itself from its offset.  Invalid counts (negative, or sums beyond int) only
+// have to survive until the host reads the summary and rejects the plan.
+constexpr int kScanThreads = 256, kScanPer = 16, kScanTile = kScanThreads * kScanPer;
+constexpr int kScanTopThreads = 1024;
+
+struct ShellSummary {
+  long long np_total, nbf;
+  int lmin, lmax, npmin, npmax;
+  int npmax_l[kMaxL + 1];
+};
+
+__device__ __forceinline__ long long shell_nfunc(int l, bool sph) {
+  if (l < 0) return 0;
+  const long long ll = l;
+  return (sph && l >= 2) ? 2 * ll + 1 : (ll + 1) * (ll + 2) / 2;
+}
+
+// Exclusive scan over a block of NT threads, one value each; *total is the
+// block's sum.  ws: NT / 32 values of shared memory.
+template <int NT>
+__device__ long long block_exclusive_scan(long long v, long long* ws, long long* total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  long long x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) ws[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    long long t = lane < NT / 32 ? ws[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long y = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += y;
+    }
+    if (lane < NT / 32) ws[lane] = t;
+  }
+  __syncthreads();
+  const long long before = w > 0 ? ws[w - 1] : 0;
+  *total = ws[NT / 32 - 1];
+  __syncthreads();
+  return before + x - v;
+}
+
+__global__ void __launch_bounds__(kScanThreads) shell_tile_sums(int n, const int* __restrict__ L,
+                                                                const int* __restrict__ nprim, bool sph,
+                                                                long long* __restrict__ tile_np,
+                                                                long long* __restrict__ tile_nf,
+                                                                ShellSummary* __restrict__ sum) {
+  __shared__ long long ws[kScanThreads / 32];
+  const long long base = (long long)blockIdx.x * kScanTile;
+  long long snp = 0, snf = 0;
+  int lmin = INT_MAX, lmax = INT_MIN, pmin = INT_MAX, pmax = INT_MIN;
+  int pl[kMaxL + 1];
+#pragma unroll
+  for (int q = 0; q <= kMaxL; ++q) pl[q] = 0;
+#pragma unroll 4
+  for (int j = 0; j < kScanPer; ++j) {
+    const long long s = base + j * kScanThreads + threadIdx.x;
+    if (s < n) {
+      const int l = L[s], k = nprim[s];
+      snp += k > 0 ? k : 0;
+      snf += shell_nfunc(l, sph);
+      lmin = min(lmin, l);
+      lmax = max(lmax, l);
+      pmin = min(pmin, k);
+      pmax = max(pmax, k);
+#pragma unroll
+      for (int q = 0; q <= kMaxL; ++q) pl[q] = l == q ? max(pl[q], k) : pl[q];
+    }
+  }
+  lmin = __reduce_min_sync(0xffffffffu, lmin);
+  lmax = __reduce_max_sync(0xffffffffu, lmax);
+  pmin = __reduce_min_sync(0xffffffffu, pmin);
+  pmax = __reduce_max_sync(0xffffffffu, pmax);
+#pragma unroll
+  for (int q = 0; q <= kMaxL; ++q) pl[q] = __reduce_max_sync(0xffffffffu, pl[q]);
+  if ((threadIdx.x & 31) == 0) {
+    atomicMin(&sum->lmin, lmin);
+    atomicMax(&sum->lmax, lmax);
+    atomicMin(&sum->npmin, pmin);
+    atomicMax(&sum->npmax, pmax);
+#pragma unroll
+    for (int q = 0; q <= kMaxL; ++q)
+      if (pl[q] > 0) atomicMax(&sum->npmax_l[q], pl[q]);
+  }
+  long long tnp, tnf;
+  block_exclusive_scan<kScanThreads>(snp, ws, &tnp);
+  block_exclusive_scan<kScanThreads>(snf, ws, &tnf);
+  if (threadIdx.x == 0) {
+    tile_np[blockIdx.x] = tnp;
+    tile_nf[blockIdx.x] = tnf;
+  }
+}
+
+// One block: tile sums -> exclusive tile offsets (in place), the totals into
+// the summary and fo[n].
+__global__ void __launch_bounds__(kScanTopThreads) shell_tile_scan(int ntiles, long long* __restrict__ tile_np,
+                                                                   long long* __restrict__ tile_nf,
+                                                                   ShellSummary* __restrict__ sum, int n,
+                                                                   int* __restrict__ fo) {
+  __shared__ long long ws[kScanTopThreads / 32];
+  const int per = (ntiles + kScanTopThreads - 1) / kScanTopThreads;
+  const int lo = min(ntiles, (int)threadIdx.x * per), hi = min(ntiles, lo + per);
+  long long anp = 0, anf = 0;
+  for (int i = lo; i < hi; ++i) {
+    anp += tile_np[i];
+    anf += tile_nf[i];
+  }
+  long long tnp, tnf;
+  long long onp = block_exclusive_scan<kScanTopThreads>(anp, ws, &tnp);
+  long long onf = block_exclusive_scan<kScanTopThreads>(anf, ws, &tnf);
+  for (int i = lo; i < hi; ++i) {
+    const long long a = tile_np[i], b = tile_nf[i];
+    tile_np[i] = onp;
+    tile_nf[i] = onf;
+    onp += a;
+    onf += b;
+  }
+  if (threadIdx.x == 0) {
+    sum->np_total = tnp;
+    sum->nbf = tnf;
+    fo[n] = (int)min(tnf, (long long)INT_MAX);
+  }
+}
+
+// Shared-memory index with one pad word every 32 (the per-thread runs of
+// kScanPer consecutive shells would otherwise share banks).
+__device__ __forceinline__ int scan_pad(int i) { return i + (i >> 5); }
+
+__global__ void __launch_bounds__(kScanThreads) shell_offsets(int n, const int* __restrict__ L,
+                                                              const int* __restrict__ nprim, bool sph,
+                                                              const long long* __restrict__ tile_np,
+                                                              const long long* __restrict__ tile_nf,
+                                                              int* __restrict__ poff, int* __restrict__ fo) {
+  __shared__ long long ws[kScanThreads / 32];
+  __shared__ int vnp[kScanTile + kScanTile / 32], vnf[kScanTile + kScanTile / 32];
+  const long long base = (long long)blockIdx.x * kScanTile;
+  // coalesced loads into shared memory (values clamped to int: valid counts are small)
+  for (int j = 0; j < kScanPer; ++j) {
+    const int i = j * kScanThreads + threadIdx.x;
+    const long long s = base + i;
+    int a = 0, b = 0;
+    if (s < n) {
+      const int k = nprim[s];
+      a = k > 0 ? k : 0;
+      b = (int)min(shell_nfunc(L[s], sph), (long long)INT_MAX);
+    }
+    vnp[scan_pad(i)] = a;
+    vnf[scan_pad(i)] = b;
+  }
+  __syncthreads();
+  // each thread scans its run of kScanPer consecutive shells
+  const int r0 = threadIdx.x * kScanPer;
+  long long snp = 0, snf = 0;
+#pragma unroll
+  for (int j = 0; j < kScanPer; ++j) {
+    snp += vnp[scan_pad(r0 + j)];
+    snf += vnf[scan_pad(r0 + j)];
+  }
+  long long tot;
+  long long onp = block_exclusive_scan<kScanThreads>(snp, ws, &tot) + tile_np[blockIdx.x];
+  long long onf = block_exclusive_scan<kScanThreads>(snf, ws, &tot) + tile_nf[blockIdx.x];
+#pragma unroll
+  for (int j = 0; j < kScanPer; ++j) {
+    const int i = scan_pad(r0 + j);
+    const int a = vnp[i], b = vnf[i];
+    vnp[i] = (int)min(onp, (long long)INT_MAX);
+    vnf[i] = (int)min(onf, (long long)INT_MAX);
+    onp += a;
+    onf += b;
+  }
+  __syncthreads();
+  for (int j = 0; j < kScanPer; ++j) {
+    const int i = j * kScanThreads + threadIdx.x;
+    const long long s = base + i;
+    if (s < n) {
+      poff[s] = vnp[scan_pad(i)];
+      fo[s] = vnf[scan_pad(i)];
+    }
+  }
+}
+
 }  // namespace
 
 // ------------------------------------------------------------------ plan
@@ -201,9 +397,14 @@ struct eri_plan {
   bool contracted = false;
   double tau = 0;
   int lmax = 0;
-  std::vector<int> hL, hnprim, hpoff, hfo;
-  // host copies of the caller's centres, exponents and raw coefficients: kept
-  // only for the screen (schwarz_tau > 0), which reads them on the host
+  // host copies of the primitive offsets and first basis functions: made for
+  // the screen at creation, else on the first query that needs them
+  mutable std::vector<int> hpoff, hfo;
+  int npmax_l[kMaxL + 1] = {0};  // largest primitive count of the shells of each l
+  // host copies of the caller's angular momenta, primitive counts, centres,
+  // exponents and raw coefficients: kept only for the screen
+  // (schwarz_tau > 0), which reads them on the host
+  std::vector<int> hL, hnprim;
   std::vector<double> hcen, hexps, hcoef;
   size_t np_total = 0;
   int nbf = 0;
@@ -217,6 +418,7 @@ struct eri_plan {
   double* dcoef = nullptr;
   double* draw = nullptr;   // the caller's coefficients on the device (normalisation input)
   int* dbad = nullptr;      // normalisation status flag
+  void* dtmp = nullptr;     // offset-scan tile sums and summary
   const double* dboys = nullptr;
   // scratch
   double* scratch = nullptr;
@@ -229,7 +431,11 @@ struct eri_plan {
 namespace {
 
 // Device copy of n host values, ordered on stream st (st == 0: the legacy
-// default stream).  The host data may be released once the call returns.
+// default stream).  On a stream the copy is only enqueued: from page-locked
+// memory it runs asynchronously, so the host data must stay unchanged until
+// st has been synchronised (plan creation synchronises it before it returns,
+// after the normalisation kernel); from pageable memory the driver stages
+// the data before the call returns.
 template <class T>
 int upload(T** dst, const T* src, size_t n, cudaStream_t st = 0) {
   size_t bytes = std::max<size_t>(n, 1) * sizeof(T);
@@ -237,7 +443,6 @@ int upload(T** dst, const T* src, size_t n, cudaStream_t st = 0) {
   if (n) {
     if (st) {
       CUDA_TRY(cudaMemcpyAsync(*dst, src, n * sizeof(T), cudaMemcpyHostToDevice, st));
-      CUDA_TRY(cudaStreamSynchronize(st));
     } else {
       CUDA_TRY(cudaMemcpy(*dst, src, n * sizeof(T), cudaMemcpyHostToDevice));
     }
@@ -293,6 +498,43 @@ int normalise_on_device(eri_plan* p, const double* coefs, cudaStream_t st) {
     return e == cudaErrorMemoryAllocation ? ERI_ERR_OOM : ERI_ERR_CUDA;
   }
   return hbad ? ERI_ERR_NOT_FINITE : ERI_OK;
+}
+
+// Primitive offsets and first basis functions of every shell into p->dpoff /
+// p->dfo, from p->dL / p->dnprim, and the summary of the caller's angular
+// momenta and primitive counts into *hs (the stream is synchronised).
+int shell_offsets_on_device(eri_plan* p, cudaStream_t st, ShellSummary* hs) {
+  const int n = p->nshell;
+  const int ntiles = (n + kScanTile - 1) / kScanTile;
+  const size_t tiles_bytes = 2 * (size_t)ntiles * sizeof(long long);
+  CUDA_TRY(cudaMalloc(&p->dtmp, tiles_bytes + sizeof(ShellSummary)));
+  long long* tile_np = static_cast<long long*>(p->dtmp);
+  long long* tile_nf = tile_np + ntiles;
+  ShellSummary* dsum = reinterpret_cast<ShellSummary*>(static_cast<char*>(p->dtmp) + tiles_bytes);
+  ShellSummary init{};
+  init.lmin = INT_MAX;
+  init.lmax = INT_MIN;
+  init.npmin = INT_MAX;
+  init.npmax = INT_MIN;
+  CUDA_TRY(cudaMemcpyAsync(dsum, &init, sizeof(init), cudaMemcpyHostToDevice, st));
+  shell_tile_sums<<<ntiles, kScanThreads, 0, st>>>(n, p->dL, p->dnprim, p->spherical, tile_np, tile_nf, dsum);
+  shell_tile_scan<<<1, kScanTopThreads, 0, st>>>(ntiles, tile_np, tile_nf, dsum, n, p->dfo);
+  shell_offsets<<<ntiles, kScanThreads, 0, st>>>(n, p->dL, p->dnprim, p->spherical, tile_np, tile_nf, p->dpoff,
+                                                 p->dfo);
+  CUDA_TRY(cudaGetLastError());
+  CUDA_TRY(cudaMemcpyAsync(hs, dsum, sizeof(*hs), cudaMemcpyDeviceToHost, st));
+  CUDA_TRY(cudaStreamSynchronize(st));
+  return ERI_OK;
+}
+
+// Host copies of the primitive offsets and first basis functions (made once).
+int host_offsets(const eri_plan* p) {
+  if (!p->hfo.empty()) return ERI_OK;
+  p->hpoff.resize(p->nshell);
+  p->hfo.resize((size_t)p->nshell + 1);
+  CUDA_TRY(cudaMemcpy(p->hpoff.data(), p->dpoff, p->hpoff.size() * sizeof(int), cudaMemcpyDeviceToHost));
+  CUDA_TRY(cudaMemcpy(p->hfo.data(), p->dfo, p->hfo.size() * sizeof(int), cudaMemcpyDeviceToHost));
+  return ERI_OK;
 }
 
 }  // namespace
@@ -366,6 +608,7 @@ bool eri::host::plan_spherical(const eri_plan* p) { return p->spherical; }
 int eri::host::plan_nshell(const eri_plan* p) { return p->nshell; }
 const int* eri::host::plan_L(const eri_plan* p) { return p->hL.data(); }
 const int* eri::host::plan_nprim(const eri_plan* p) { return p->hnprim.data(); }
+int eri::host::plan_npmax(const eri_plan* p, int l) { return l >= 0 && l <= kMaxL ? p->npmax_l[l] : 0; }
 const int* eri::host::plan_fo(const eri_plan* p) { return p->hfo.data(); }
 const double* eri::host::plan_centers(const eri_plan* p) { return p->hcen.data(); }
 const double* eri::host::plan_exps(const eri_plan* p) { return p->hexps.data(); }
@@ -404,6 +647,7 @@ int eri_plan_destroy(eri_plan* p) {
   cudaFree(p->dcoef);
   cudaFree(p->draw);
   cudaFree(p->dbad);
+  cudaFree(p->dtmp);
   cudaFree(p->scratch);
   cudaFree(p->qbuf);
   delete p;
@@ -421,45 +665,6 @@ int eri_plan_create_flat(int nshell, const double* centers, const int* L, const 
   p->nshell = nshell;
   p->spherical = opt->spherical != 0;
   p->tau = opt->schwarz_tau;
-  // one pass: angular momenta and primitive counts checked, primitive offsets
-  // and first basis functions (the centres, exponents and coefficients are
-  // checked on the device, by the normalisation kernel)
-  int lmax = 0, lmin = 0, npmin = 1, npmax = 1;
-  size_t np_total = 0;
-  long long nbf = 0;
-  p->hL.assign(L, L + nshell);
-  p->hnprim.assign(nprim, nprim + nshell);
-  p->hpoff.resize(nshell);
-  p->hfo.resize(nshell + 1);
-  for (int s = 0; s < nshell; ++s) {
-    const int l = L[s], np = nprim[s];
-    lmax = std::max(lmax, l);
-    lmin = std::min(lmin, l);
-    npmin = std::min(npmin, np);
-    npmax = std::max(npmax, np);
-    p->hpoff[s] = (int)std::min<size_t>(np_total, (size_t)INT32_MAX);
-    p->hfo[s] = (int)std::min<long long>(nbf, INT32_MAX);
-    np_total += (size_t)std::max(np, 0);
-    nbf += l >= 0 ? nfunc(l, p->spherical) : 0;
-  }
-  p->hfo[nshell] = (int)std::min<long long>(nbf, INT32_MAX);
-  if (lmin < 0 || npmin <= 0 || np_total > ((size_t)1 << 30) || nbf > INT32_MAX) {
-    delete p;
-    return ERI_ERR_INVALID_ARG;
-  }
-  if (lmax > lmax_built) {
-    delete p;
-    return ERI_ERR_UNSUPPORTED_L;
-  }
-  p->lmax = lmax;
-  p->contracted = npmax > 1;
-  p->np_total = np_total;
-  if (p->tau > 0) {
-    p->hcen.assign(centers, centers + 3 * (size_t)nshell);
-    p->hexps.assign(exps, exps + np_total);
-    p->hcoef.assign(coefs, coefs + np_total);
-  }
-  p->nbf = p->hfo[nshell];
   cudaError_t e = cudaGetDevice(&p->device);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&p->nsm, cudaDevAttrMultiProcessorCount, p->device);
   if (e != cudaSuccess) {
@@ -467,12 +672,55 @@ int eri_plan_create_flat(int nshell, const double* centers, const int* L, const 
     delete p;
     return ERI_ERR_CUDA;
   }
+  // angular momenta and primitive counts checked, primitive offsets and first
+  // basis functions formed on the device (the centres, exponents and
+  // coefficients are checked there too, by the normalisation kernel)
   int rc;
   cudaStream_t cst = (cudaStream_t)stream;
-  if ((rc = upload(&p->dcen, centers, 3 * (size_t)nshell, cst)) || (rc = upload(&p->dL, p->hL, cst)) ||
-      (rc = upload(&p->dnprim, p->hnprim, cst)) || (rc = upload(&p->dpoff, p->hpoff, cst)) ||
-      (rc = upload(&p->dfo, p->hfo, cst)) || (rc = upload(&p->dexps, exps, np_total, cst)) ||
-      (rc = boys_table_for_device(p->device, &p->dboys))) {
+  ShellSummary sm{};
+  if ((rc = upload(&p->dcen, centers, 3 * (size_t)nshell, cst)) || (rc = upload(&p->dL, L, (size_t)nshell, cst)) ||
+      (rc = upload(&p->dnprim, nprim, (size_t)nshell, cst))) {
+    eri_plan_destroy(p);
+    return rc;
+  }
+  e = cudaMalloc(&p->dpoff, (size_t)nshell * sizeof(int));
+  if (e == cudaSuccess) e = cudaMalloc(&p->dfo, ((size_t)nshell + 1) * sizeof(int));
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    eri_plan_destroy(p);
+    return e == cudaErrorMemoryAllocation ? ERI_ERR_OOM : ERI_ERR_CUDA;
+  }
+  if ((rc = shell_offsets_on_device(p, cst, &sm))) {
+    eri_plan_destroy(p);
+    return rc;
+  }
+  if (sm.lmin < 0 || sm.npmin <= 0 || sm.np_total > ((long long)1 << 30) || sm.nbf > INT32_MAX) {
+    eri_plan_destroy(p);
+    return ERI_ERR_INVALID_ARG;
+  }
+  if (sm.lmax > lmax_built) {
+    eri_plan_destroy(p);
+    return ERI_ERR_UNSUPPORTED_L;
+  }
+  const size_t np_total = (size_t)sm.np_total;
+  p->lmax = sm.lmax;
+  p->contracted = sm.npmax > 1;
+  p->np_total = np_total;
+  p->nbf = (int)sm.nbf;
+  for (int l = 0; l <= kMaxL; ++l) p->npmax_l[l] = sm.npmax_l[l];
+  if (p->tau > 0) {
+    // host copies for the screen (built on the host from these)
+    p->hL.assign(L, L + nshell);
+    p->hnprim.assign(nprim, nprim + nshell);
+    p->hcen.assign(centers, centers + 3 * (size_t)nshell);
+    p->hexps.assign(exps, exps + np_total);
+    p->hcoef.assign(coefs, coefs + np_total);
+    if ((rc = host_offsets(p))) {
+      eri_plan_destroy(p);
+      return rc;
+    }
+  }
+  if ((rc = upload(&p->dexps, exps, np_total, cst)) || (rc = boys_table_for_device(p->device, &p->dboys))) {
     eri_plan_destroy(p);
     return rc;
   }
@@ -528,6 +776,7 @@ int eri_plan_nbf(const eri_plan* p, int* nbf) {
 
 int eri_plan_shell_info(const eri_plan* p, int s, int* nf, int* first) {
   if (!p || s < 0 || s >= p->nshell) return ERI_ERR_INVALID_ARG;
+  if (const int rc = host_offsets(p)) return rc;
   if (nf) *nf = p->hfo[s + 1] - p->hfo[s];
   if (first) *first = p->hfo[s];
   return ERI_OK;

@@ -193,13 +193,7 @@ int schwarz_dev(eri_plan* p, int la, int lb, const int2* pairs, long long n, dou
   // quartets (1,296 for 6-primitive pairs); one thread each would set the
   // critical path of the launch.  Cut each into parts of at most 8 x 8
   // primitive pairs, sum their diagonal elements with atomics and reduce.
-  const int* L = eri::host::plan_L(p);
-  const int* np = eri::host::plan_nprim(p);
-  int ka = 1, kb = 1;
-  for (int s = 0; s < eri::host::plan_nshell(p); ++s) {
-    if (L[s] == la) ka = std::max(ka, np[s]);
-    if (L[s] == lb) kb = std::max(kb, np[s]);
-  }
+  const int ka = std::max(1, eri::host::plan_npmax(p, la)), kb = std::max(1, eri::host::plan_npmax(p, lb));
   const int split = (ka * kb + 7) / 8;
   if (split > 1) {
     auto nfn = [&](int l) { return (eri::host::plan_spherical(p) && l >= 2) ? 2 * l + 1 : (l + 1) * (l + 2) / 2; };

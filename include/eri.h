@@ -27,7 +27,10 @@
  * Threading and streams: a plan may be used from one host thread at a time.
  * Every entry point that takes `stream` (a cudaStream_t, NULL = legacy default
  * stream) only enqueues work on it and returns; results are ready when the
- * stream has been synchronised.  Asynchronous CUDA errors surface as
+ * stream has been synchronised.  The work of one plan must not overlap on the
+ * GPU: its calls share the plan's device scratch, so calls of one plan on
+ * different streams need an order between them (an event); calls on one
+ * stream are ordered by the stream.  Asynchronous CUDA errors surface as
  * ERI_ERR_CUDA from a later call.
  *
  * Errors: every int-returning function returns ERI_OK (0) or a negative

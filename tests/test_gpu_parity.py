@@ -239,7 +239,7 @@ def test_pointer_and_flat_plan_creation_agree(dev):
 @pytest.mark.parametrize("cls", [(3, 2, 2, 2), (3, 3, 3, 3), (4, 2, 3, 1)])
 def test_cooperative_tier_more_than_one_setup_batch(dev, cls):
     """Contraction degree 3 (81 primitive quartets per quartet): the cooperative
-    kernels set primitive quartets up 16 at a time, over several batches."""
+    kernels set primitive quartets up four at a time, over several batches."""
     if max(cls) > built_lmax():
         pytest.skip("class not built")
     _homogeneous_check(dev, cls, 19, 3, seed_index=470 + sum(cls))
@@ -257,3 +257,38 @@ def test_non_finite_shell_data_is_rejected(dev):
         assert ei.value.code == -6, (field, ei.value.code)
     s, _ = W.homogeneous((1, 1, 0, 0), 4, 2, seed_index=520)
     eri.Plan(s, spherical=True).close()  # the same data, untouched, is accepted
+
+
+def test_shell_offsets_and_count_checks(dev):
+    """Plan creation forms the first basis function of every shell on the
+    device (a scan over tiles of 4,096 shells): three tiles and a ragged tail,
+    against the running sum of 2l+1 / (l+1)(l+2)/2; a negative l or a shell
+    without primitives is ERI_ERR_INVALID_ARG, an l above the build
+    ERI_ERR_UNSUPPORTED_L."""
+    rng = np.random.default_rng(77)
+    n = 3 * 4096 + 77
+    L = rng.integers(0, 3, size=n).astype(np.int32)
+    nprim = rng.integers(1, 7, size=n).astype(np.int32)
+    m = int(nprim.sum())
+    mk = lambda L_, np_: W.Shells(rng.uniform(0, 10, size=(n, 3)), L_, np_, rng.uniform(0.1, 5.0, size=m),
+                                  rng.uniform(0.1, 1.0, size=m))
+    for spherical in (True, False):
+        nf = np.where(L >= 2, 2 * L + 1, (L + 1) * (L + 2) // 2) if spherical else (L + 1) * (L + 2) // 2
+        first = np.concatenate([[0], np.cumsum(nf)])
+        plan = eri.Plan(mk(L, nprim), spherical=spherical)
+        assert plan.nbf == first[-1]
+        for i in list(range(0, n, 997)) + [4095, 4096, 8191, 8192, n - 1]:
+            assert eri.eri_plan_shell_info(plan.handle, i) == (nf[i], first[i]), (spherical, i)
+        plan.close()
+    for bad, code in [(("L", 5000, -1), -1), (("nprim", 9000, 0), -1), (("L", 12000, built_lmax() + 1), -2)]:
+        (field, i, v), L2, n2 = bad, L.copy(), nprim.copy()
+        (L2 if field == "L" else n2)[i] = v
+        if field == "nprim":  # keep the primitive arrays consistent with the counts
+            m2 = int(n2.sum())
+            s = W.Shells(rng.uniform(0, 10, size=(n, 3)), L2, n2, rng.uniform(0.1, 5.0, size=m2),
+                         rng.uniform(0.1, 1.0, size=m2))
+        else:
+            s = mk(L2, n2)
+        with pytest.raises(eri.EriError) as ei:
+            eri.Plan(s, spherical=True)
+        assert ei.value.code == code, (field, ei.value.code)
