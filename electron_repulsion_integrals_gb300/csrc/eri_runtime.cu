@@ -218,6 +218,18 @@ __device__ __forceinline__ long long shell_nfunc(int l, bool sph) {
   return (sph && l >= 2) ? 2 * ll + 1 : (ll + 1) * (ll + 2) / 2;
 }
 
+__global__ void shell_summary_init(ShellSummary* s) {
+  if (threadIdx.x == 0) {
+    s->np_total = 0;
+    s->nbf = 0;
+    s->lmin = INT_MAX;
+    s->lmax = INT_MIN;
+    s->npmin = INT_MAX;
+    s->npmax = INT_MIN;
+    for (int q = 0; q <= kMaxL; ++q) s->npmax_l[q] = 0;
+  }
+}
+
 // Exclusive scan over a block of NT threads, one value each; *total is the
 // block's sum.  ws: NT / 32 values of shared memory.
 template <int NT>
@@ -303,7 +315,8 @@ __global__ void __launch_bounds__(kScanThreads) shell_tile_sums(int n, const int
 __global__ void __launch_bounds__(kScanTopThreads) shell_tile_scan(int ntiles, long long* __restrict__ tile_np,
                                                                    long long* __restrict__ tile_nf,
                                                                    ShellSummary* __restrict__ sum, int n,
-                                                                   int* __restrict__ fo) {
+                                                                   int* __restrict__ fo,
+                                                                   ShellSummary* __restrict__ host_out) {
   __shared__ long long ws[kScanTopThreads / 32];
   const int per = (ntiles + kScanTopThreads - 1) / kScanTopThreads;
   const int lo = min(ntiles, (int)threadIdx.x * per), hi = min(ntiles, lo + per);
@@ -326,7 +339,13 @@ __global__ void __launch_bounds__(kScanTopThreads) shell_tile_scan(int ntiles, l
     sum->np_total = tnp;
     sum->nbf = tnf;
     fo[n] = (int)min(tnf, (long long)INT_MAX);
+    *host_out = *sum;  // mapped host memory: read by the host after the stream
   }
+}
+
+// The normalisation status flag into mapped host memory.
+__global__ void copy_flag_to_host(const int* __restrict__ flag, int* __restrict__ host_out) {
+  if (threadIdx.x == 0) *host_out = *flag;
 }
 
 // Shared-memory index with one pad word every 32 (the per-thread runs of
@@ -430,6 +449,21 @@ struct eri_plan {
 
 namespace {
 
+// A mapped page-locked host slot of kReadbackSlot bytes per host thread
+// (allocated on first use, kept until the process exits) for the small results
+// plan creation reads back: kernels write them there directly.  A
+// device-to-host copy would queue on the copy engine behind the copies
+// already in flight on other streams (a multi-GB readback of another plan's
+// blocks) and wait for all of them.
+constexpr size_t kReadbackSlot = 256;
+int readback_slot(void** host, void** dev) {
+  thread_local void* slot = nullptr;
+  if (!slot) CUDA_TRY(cudaHostAlloc(&slot, kReadbackSlot, cudaHostAllocMapped | cudaHostAllocPortable));
+  CUDA_TRY(cudaHostGetDevicePointer(dev, slot, 0));  // for the current device
+  *host = slot;
+  return ERI_OK;
+}
+
 // Device copy of n host values, ordered on stream st (st == 0: the legacy
 // default stream).  On a stream the copy is only enqueued: from page-locked
 // memory it runs asynchronously, so the host data must stay unchanged until
@@ -490,14 +524,18 @@ int normalise_on_device(eri_plan* p, const double* coefs, cudaStream_t st) {
                                                                      p->dexps, p->draw, p->dcoef, p->dbad);
     e = cudaGetLastError();
   }
-  int hbad = 0;
-  if (e == cudaSuccess) e = cudaMemcpyAsync(&hbad, p->dbad, sizeof(int), cudaMemcpyDeviceToHost, st);
+  void *slot = nullptr, *dslot = nullptr;
+  if (e == cudaSuccess && (rc = readback_slot(&slot, &dslot))) return rc;
+  if (e == cudaSuccess) {
+    copy_flag_to_host<<<1, 32, 0, st>>>(p->dbad, static_cast<int*>(dslot));
+    e = cudaGetLastError();
+  }
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) {
     (void)cudaGetLastError();
     return e == cudaErrorMemoryAllocation ? ERI_ERR_OOM : ERI_ERR_CUDA;
   }
-  return hbad ? ERI_ERR_NOT_FINITE : ERI_OK;
+  return *static_cast<const int*>(slot) ? ERI_ERR_NOT_FINITE : ERI_OK;
 }
 
 // Primitive offsets and first basis functions of every shell into p->dpoff /
@@ -511,19 +549,18 @@ int shell_offsets_on_device(eri_plan* p, cudaStream_t st, ShellSummary* hs) {
   long long* tile_np = static_cast<long long*>(p->dtmp);
   long long* tile_nf = tile_np + ntiles;
   ShellSummary* dsum = reinterpret_cast<ShellSummary*>(static_cast<char*>(p->dtmp) + tiles_bytes);
-  ShellSummary init{};
-  init.lmin = INT_MAX;
-  init.lmax = INT_MIN;
-  init.npmin = INT_MAX;
-  init.npmax = INT_MIN;
-  CUDA_TRY(cudaMemcpyAsync(dsum, &init, sizeof(init), cudaMemcpyHostToDevice, st));
+  static_assert(sizeof(ShellSummary) <= kReadbackSlot, "summary larger than the readback slot");
+  void *slot = nullptr, *dslot = nullptr;
+  if (const int rc = readback_slot(&slot, &dslot)) return rc;
+  shell_summary_init<<<1, 32, 0, st>>>(dsum);
   shell_tile_sums<<<ntiles, kScanThreads, 0, st>>>(n, p->dL, p->dnprim, p->spherical, tile_np, tile_nf, dsum);
-  shell_tile_scan<<<1, kScanTopThreads, 0, st>>>(ntiles, tile_np, tile_nf, dsum, n, p->dfo);
+  shell_tile_scan<<<1, kScanTopThreads, 0, st>>>(ntiles, tile_np, tile_nf, dsum, n, p->dfo,
+                                                 static_cast<ShellSummary*>(dslot));
   shell_offsets<<<ntiles, kScanThreads, 0, st>>>(n, p->dL, p->dnprim, p->spherical, tile_np, tile_nf, p->dpoff,
                                                  p->dfo);
   CUDA_TRY(cudaGetLastError());
-  CUDA_TRY(cudaMemcpyAsync(hs, dsum, sizeof(*hs), cudaMemcpyDeviceToHost, st));
   CUDA_TRY(cudaStreamSynchronize(st));
+  std::memcpy(hs, slot, sizeof(*hs));
   return ERI_OK;
 }
 
