@@ -74,18 +74,21 @@ WORKLOADS = {
 }
 
 
-def dram_traffic(cls, n):
-    """DRAM bytes of one launch of the class kernel from the ncu record in
-    profiles/dram_traffic.json (captured on a slice and scaled by the number of
-    quartets, the traffic being per quartet), or None when the kernel sources
-    changed since the capture."""
+def dram_traffic(cls, n, deriv=False):
+    """DRAM bytes of one launch of the class kernel (the derivative kernel with
+    deriv) from its ncu record in profiles/dram_traffic.json (captured on a
+    slice and scaled by the number of quartets, the traffic being per quartet),
+    or None without a record or when the kernel sources changed since the
+    capture."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     if not os.path.exists(path):
         return None
-    rec = json.load(open(path))
-    if not rec["kernel"].startswith("k_c{}{}{}{}".format(*cls)):
+    name = "k_{}{}{}{}{}".format("d" if deriv else "c", *cls)
+    recs = [r for r in json.load(open(path)) if r["kernel"].split()[0] == name]
+    if not recs:
         return None
+    rec = recs[0]
     h = hashlib.sha256()
     for f in rec["sources"]:
         with open(os.path.join(ROOT, "electron_repulsion_integrals_gb300", f), "rb") as fh:
@@ -556,7 +559,7 @@ def run_ours(a, rank, world, local_rank):
             "per_class": per_class,
             "roofline": {"bound": "alu", "kernel": dname, "achieved": ach, "peak": FP64_PEAK_TFLOPS,
                          "unit": "TFLOP/s", "frac": ach / FP64_PEAK_TFLOPS,
-                         "traffic": None if wl.get("deriv") else dram_traffic(dom["cls"], dom["n"]),
+                         "traffic": dram_traffic(dom["cls"], dom["n"], bool(wl.get("deriv"))),
                          "peak_source": "FP64 pipe: 152 SMs x 2 DFMA/clk x 2 flop x 2.07 GHz"},
             "clocks": clk, "e2e": e2e, "cpu_baseline": cpu,
             "gpu_launches": len(batches) * a.steps}
