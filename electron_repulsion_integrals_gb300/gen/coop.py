@@ -86,7 +86,7 @@ class CoopPlan:
     cols: list = field(default_factory=list)
     zlist: list = field(default_factory=list)          # per axis: [(ie, ie_m1, e_i)] with e_i > 0
     nlist: list = field(default_factory=list)          # per axis: [ie] with e_i = 0
-    arena: int = 0             # doubles per warp
+    arena: int = 0             # doubles per quartet group
     bra_col: int = 0           # arena offset of column 0
     fp64_ops: int = 0          # FP64 instructions per primitive quartet in the VRR (lane-summed)
     nodes: int = 0             # VRR nodes per primitive quartet (one DMUL each, the rest FMAs)
@@ -315,7 +315,7 @@ def emit_coop_class(cls):
     w = lines.append
     w(f"// Generated by electron_repulsion_integrals_gb300/gen/eri_gen.py -- do not edit.")
     w(f"// Class ({la}{lb}|{lc}{ld}): L = {L}, warp-cooperative tier; {len(P.cols)} ket column steps, "
-      f"{nbra} bra nodes, arena {arena} doubles per warp, VRR {P.fp64_ops} FP64 instructions "
+      f"{nbra} bra nodes, arena {arena} doubles per quartet, VRR {P.fp64_ops} FP64 instructions "
       f"per primitive quartet.")
     w('#include "../eri_coop.cuh"')
     w("")
