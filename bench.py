@@ -98,6 +98,13 @@ def dram_traffic(cls, n, deriv=False):
     return rec["dram_bytes_per_quartet"] * n
 
 
+def e2e_chunks(n, out_bytes):
+    """Quartet ranges [lo, hi) covering 0..n in order, about E2E_CHUNK_BYTES of
+    output each (1 to 8 ranges)."""
+    k = max(1, min(8, n, round(out_bytes / E2E_CHUNK_BYTES)))
+    return [(n * j // k, n * (j + 1) // k) for j in range(k)]
+
+
 def max_over_ranks(ms, dist, device):
     """The slowest rank's time (all ranks receive it); ms itself without a
     process group."""
@@ -496,12 +503,6 @@ def run_ours(a, rank, world, local_rank):
         d2h = sum(ho.numel() * 8 for ho in host_o)
         e_steps = max(1, min(a.steps, 5))
 
-        def chunks(b):
-            # quartet ranges of about E2E_CHUNK_BYTES of output each
-            n = b["n"]
-            k = max(1, min(8, round(b["out"].numel() * 8 / E2E_CHUNK_BYTES)))
-            return [(n * j // k, n * (j + 1) // k) for j in range(k)]
-
         def e2e_step():
             plans = []
             for i in order:
@@ -513,7 +514,7 @@ def run_ours(a, rank, world, local_rank):
                     # the chunks of one plan run in order on its stream (they
                     # share the plan's scratch); each chunk's readback runs on a
                     # copy stream, overlapping the next chunk's compute
-                    for lo, hi in chunks(b):
+                    for lo, hi in e2e_chunks(b["n"], b["out"].numel() * 8):
                         o = b["out"][lo * per_q:hi * per_q]
                         compute(plan.handle, b["cls"], qd[lo:hi], o, st_i)
                         done = torch.cuda.Event()

@@ -1,0 +1,61 @@
+"""Host-side logic with no GPU: the end-to-end bench's chunking of a class
+batch, and the derivative kernels' choice of lanes per quartet."""
+
+import os
+import re
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+from electron_repulsion_integrals_gb300.gen import coop as CP  # noqa: E402
+from electron_repulsion_integrals_gb300.gen import deriv as D  # noqa: E402
+from electron_repulsion_integrals_gb300.gen.eri_gen import canonical_classes  # noqa: E402
+
+
+@pytest.mark.parametrize("n,out_bytes", [(1, 10), (5, 1e12), (1 << 20, (1 << 20) * 625 * 8), (1 << 20, 0.68e9),
+                                         (1 << 17, 12 * 625 * 8 * (1 << 17)), (7, 3e9), (1000003, 2.2e9)])
+def test_e2e_chunks_cover_the_batch_in_order(n, out_bytes):
+    bench = pytest.importorskip("bench")
+    ch = bench.e2e_chunks(n, out_bytes)
+    assert 1 <= len(ch) <= 8
+    assert ch[0][0] == 0 and ch[-1][1] == n
+    assert all(a[1] == b[0] for a, b in zip(ch, ch[1:]))       # contiguous, in order
+    sizes = [hi - lo for lo, hi in ch]
+    assert min(sizes) >= 1 and max(sizes) - min(sizes) <= 1
+    if out_bytes / bench.E2E_CHUNK_BYTES >= 8.5 and n >= 8:
+        assert len(ch) == 8
+
+
+def test_e2e_chunks_of_the_homogeneous_batch():
+    bench = pytest.importorskip("bench")
+    assert len(bench.e2e_chunks(1 << 20, (1 << 20) * 625 * 8)) == 7      # (dd|dd): 5.24 GB
+    assert len(bench.e2e_chunks(1 << 20, (1 << 20) * 81 * 8)) == 1       # (pp|pp): 0.68 GB
+
+
+def _lanes(src):
+    return int(re.search(r"LANES = (\d+)", src).group(1))
+
+
+def test_derivative_lanes_are_the_narrowest_that_keep_enough_warps():
+    seen = {}
+    for cls in canonical_classes(D.DERIV_LMAX):
+        src, meta = D.emit_deriv_class(cls)
+        la, lb, lc, ld = cls
+        per_quartet = meta["arena"] + 4 * CP.setup_stride(la + lb + 1, lc + ld + 1, 3)
+        lanes = _lanes(src)
+        assert lanes in (8, 16, 32) and "GROUPS = 32 / LANES, THREADS = 32" in src
+        seen[cls] = lanes
+
+        def warps(w):  # resident warps per SM with w lanes per quartet (one warp per block)
+            blocks = CP.SMEM_PER_SM // ((32 // w) * per_quartet * 8 + 1024)
+            return min(blocks, 32)
+
+        if lanes < 32:
+            assert warps(lanes) >= D.MIN_WARPS_PER_SM
+        for narrower in (8, 16):
+            if narrower < lanes:
+                assert warps(narrower) < D.MIN_WARPS_PER_SM
+    assert seen[(1, 1, 1, 1)] == 8 and seen[(2, 1, 2, 1)] == 16 and seen[(2, 2, 2, 2)] == 32
