@@ -2,9 +2,10 @@
 //
 // The method is that of FusionRCG ("FusionRCG: Orchestrating Recursive
 // Computation Graphs across GPU Memory Hierarchies"): Algorithm 2 (section
-// III-C) evaluates a shell quartet as
-//   for each primitive quartet: GAUSSIANPAIRS -> BOYS -> VRR -> H += c V
-//   HRR bra -> T x T -> HRR ket -> T x T -> scatter.
+// III-C) evaluates a shell quartet by a loop over its primitive quartets
+// (Gaussian products, Boys values, vertical recurrence, accumulation of the
+// targets), then the horizontal recurrence and spherical transform of the
+// bra, the same for the ket, and the output of the block.
 // This header holds the parts that do not depend on the angular class: the
 // Gaussian-pair and quartet parameters (the zeta, eta, rho, P, Q, W, T of
 // section II-A), the Boys function F_m(T) = [00|00]^(m), the primitive loops

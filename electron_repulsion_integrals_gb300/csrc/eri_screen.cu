@@ -2,7 +2,8 @@
 // Coulomb build J = sum (ab|cd) D_cd.
 //
 // FusionRCG batches shell quartets by angular class (section V-C) and ends
-// Algorithm 2 with "J, K += SCATTER(G, D)"; it does not describe screening.
+// Algorithm 2 by scattering each finished block into J and K with the
+// density; it does not describe screening.
 // This library screens with the Schwarz bound |(ab|cd)| <= Q_ab Q_cd,
 // Q_ab = sqrt(max |(ab|ab)|), and keeps a unique quartet when Q_ab Q_cd >= tau.
 //
@@ -67,7 +68,7 @@ __global__ void pairs_to_diag_quartets(const int2* __restrict__ pairs, long long
 }
 
 // One thread per screened shell pair: its primitive-pair records (the
-// GAUSSIANPAIRS step of Algorithm 2, done once per pair instead of once per
+// Gaussian-product step of Algorithm 2, done once per pair instead of once per
 // quartet).
 __global__ void build_prim_pairs(int npairs, const PairMeta* __restrict__ pairs, const int2* __restrict__ uv,
                                  ShellsDev sh, double* __restrict__ prims) {

@@ -10,8 +10,8 @@
  * horizontal recurrence Eq. (3) / Eq. (13), and the stepwise Cartesian-to-
  * spherical transform of section III-B (Eqs. (8), (16)), one generated CUDA
  * kernel per angular-momentum class (s through g shells).  It digests the
- * integrals into the Coulomb and exchange matrices, the "J, K += SCATTER(G, D)"
- * step of Algorithm 2.
+ * integrals into the Coulomb and exchange matrices, the scatter with the
+ * density that ends Algorithm 2.
  *
  * Conventions (the page leaves them open; these are the library's readings):
  *   - primitive g = x_A^i y_A^j z_A^k exp(-alpha r_A^2) times
@@ -77,8 +77,9 @@ typedef struct {
 
 typedef struct eri_plan eri_plan;
 
-/* Create a plan over `nshell` shells (FusionRCG Algorithm 2 input "shell
- * quartet (a,b,c,d) with primitives {(alpha_i, c_i)}").  The plan deep-copies
+/* Create a plan over `nshell` shells (the inputs of FusionRCG Algorithm 2:
+ * shells with their primitive exponents and contraction coefficients, from
+ * which quartets are formed).  The plan deep-copies
  * and normalises the shells on the current CUDA device, uploads the Boys
  * tables (once per device) and, when opt->schwarz_tau > 0, builds the
  * primitive-pair data, the Schwarz factors Q_ab = sqrt(max |(ab|ab)|) on the
@@ -188,7 +189,7 @@ int eri_schwarz(eri_plan* plan, int la, int lb, const int* pairs_dev, long long 
 int eri_build_J(eri_plan* plan, const double* D_dev, double* J_dev, void* stream);
 
 /* Coulomb and exchange matrices from one pass over the screened quartets (the
- * "J, K += SCATTER(G, D)" digestion step of FusionRCG Algorithm 2):
+ * digestion with the density that ends FusionRCG Algorithm 2):
  *   J_{mu nu}     = sum_{lambda sigma} (mu nu|lambda sigma) D_{lambda sigma}
  *   K_{mu lambda} = sum_{nu sigma}     (mu nu|lambda sigma) D_{nu sigma}
  * over the unique shell quartets that pass Q_ab Q_cd >= schwarz_tau, each

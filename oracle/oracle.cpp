@@ -654,7 +654,7 @@ int ora_build_J(int nshell, const double* centers, const int* L, const int* npri
 // Coulomb and exchange matrices together:
 //   J_{mu nu}     = sum_{lambda sigma} (mu nu|lambda sigma) D_{lambda sigma}
 //   K_{mu lambda} = sum_{nu sigma}     (mu nu|lambda sigma) D_{nu sigma}
-// (the "J, K += SCATTER(G, D)" step of FusionRCG Algorithm 2) over the unique
+// (the final scatter of FusionRCG Algorithm 2, written out) over the unique
 // shell quartets kept by the Schwarz screen, each block scattered to the
 // distinct members of its eight permutation images: image (P Q|R S) adds
 // (PQ|RS) D_RS to J_PQ and (PQ|RS) D_QS to K_PR.
