@@ -23,7 +23,6 @@
 namespace eri {
 
 constexpr int kCoopWarps = 1;                 // warps per block (one-warp groups)
-constexpr int kCoopThreads = 32 * kCoopWarps;
 constexpr int kCoopBatch = 4;                 // primitive quartets set up at once
 
 // Layout of one primitive quartet's parameters in shared memory (doubles):
