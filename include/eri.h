@@ -84,10 +84,17 @@ typedef struct eri_plan eri_plan;
  * tables (once per device) and, when opt->schwarz_tau > 0, builds the
  * primitive-pair data, the Schwarz factors Q_ab = sqrt(max |(ab|ab)|) on the
  * GPU and the per-class screened quartet sets used by eri_build_J.  Work is
- * enqueued on `stream` and the call synchronises it before returning.
+ * enqueued on `stream` and the call synchronises it before returning, so the
+ * caller's arrays may be released or reused once it returns; arrays in
+ * page-locked host memory are copied asynchronously within the call.  The
+ * primitive offsets and first basis functions are formed on the device, and
+ * the checks of L and nprim are reduced there; their summary reaches the
+ * host through a 256-byte mapped page-locked buffer that each host thread
+ * creating plans allocates once and keeps until the process exits.
  * Ownership: *out is owned by the caller and released with eri_plan_destroy.
- * Errors: INVALID_ARG (NULL, nshell <= 0, nprim <= 0, L < 0), UNSUPPORTED_L
- * (L > 3), NOT_FINITE, OOM, CUDA. */
+ * Errors: INVALID_ARG (NULL, nshell <= 0, nprim <= 0, L < 0, more than 2^30
+ * primitives, more than INT32_MAX basis functions), UNSUPPORTED_L (L above the
+ * built maximum, 4), NOT_FINITE, OOM, CUDA. */
 int eri_plan_create(const eri_shell* shells, int nshell, const eri_options* opt, void* stream, eri_plan** out);
 
 /* Same as eri_plan_create for shells given as flat arrays (host memory, read
@@ -104,7 +111,10 @@ int eri_plan_destroy(eri_plan* plan);
 /* Number of basis functions of the plan (spherical or Cartesian as chosen). */
 int eri_plan_nbf(const eri_plan* plan, int* nbf);
 
-/* Number of basis functions of shell `s` and the index of its first function. */
+/* Number of basis functions of shell `s` and the index of its first function.
+ * On a plan without a screen the first call copies the table of first
+ * functions from the device (synchronously) and keeps it.  Errors:
+ * INVALID_ARG (NULL plan, s outside 0..nshell-1), CUDA. */
 int eri_plan_shell_info(const eri_plan* plan, int s, int* nfunc, int* first);
 
 /* Evaluate `n` shell quartets of class (la lb|lc ld) and store their blocks.
