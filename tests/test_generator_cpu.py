@@ -10,7 +10,10 @@ contraction coefficients taken from the oracle.  The resulting spherical block
 must match the oracle's McMurchie-Davidson block.
 
 This checks the generator (graph construction, axis rule, schedule, HRR,
-stepwise spherical transform and emission) without a GPU.
+stepwise spherical transform and emission) without a GPU.  The cooperative
+tier's column schedule is emulated from its tables, and the first-derivative
+kernels' generated HRR functions are run over that emulation (four weighted
+accumulator sets) against the oracle's derivative blocks.
 """
 
 import math
@@ -103,15 +106,17 @@ def translate(src):
     return "\n".join(out)
 
 
-def harness(cls, rng, nprim=1, spread=3.0):
-    """Random shells in canonical order; returns (oracle ShellSet, primitive inputs)."""
+def harness(cls, rng, nprim=1, spread=3.0, extra_boys=0):
+    """Random shells in canonical order; returns (oracle ShellSet, primitive inputs).
+    extra_boys: Boys orders beyond sum(cls) (derivative classes run the VRR of
+    the class raised by one on the bra and on the ket)."""
     cen = [rng.uniform(0, spread, 3) for _ in range(4)]
     nps = [nprim] * 4
     ex = [np.exp(rng.uniform(np.log(0.2), np.log(20.0), n)) for n in nps]
     cf = [rng.uniform(0.1, 1.0, n) for n in nps]
     S = oracle.ShellSet(cen, list(cls), nps, np.concatenate(ex), np.concatenate(cf))
     d = [oracle.norm_coefs(l, e, c) for l, e, c in zip(cls, ex, cf)]
-    L = sum(cls)
+    L = sum(cls) + extra_boys
     A, B, C, D = [np.asarray(c) for c in cen]
     prims = []
     for i in range(nprim):
@@ -119,14 +124,14 @@ def harness(cls, rng, nprim=1, spread=3.0):
             a, b = ex[0][i], ex[1][j]
             z = a + b
             P = (a * A + b * B) / z
-            pb = types.SimpleNamespace(zeta=z, o2z=0.5 / z, P=list(P), PA=list(P - A))
+            pb = types.SimpleNamespace(zeta=z, o2z=0.5 / z, P=list(P), PA=list(P - A), alpha=a, beta=b)
             Kab = math.exp(-a * b / z * np.sum((A - B) ** 2)) * d[0][i] * d[1][j]
             for k in range(nprim):
                 for m in range(nprim):
                     c, dd = ex[2][k], ex[3][m]
                     e = c + dd
                     Q = (c * C + dd * D) / e
-                    pk = types.SimpleNamespace(zeta=e, o2z=0.5 / e, P=list(Q), PA=list(Q - C))
+                    pk = types.SimpleNamespace(zeta=e, o2z=0.5 / e, P=list(Q), PA=list(Q - C), gamma=c)
                     Kcd = math.exp(-c * dd / e * np.sum((C - D) ** 2)) * d[2][k] * d[3][m]
                     rho = z * e / (z + e)
                     PQ = Q - P
@@ -190,10 +195,22 @@ def emulate_coop(cls, prims):
     the CPU; returns the accumulators H[target column][e - e_la]."""
     from electron_repulsion_integrals_gb300.gen import coop
     P = coop.plan(cls)
+    return emulate_coop_plan(P, prims)[0], P
+
+
+def emulate_coop_plan(P, prims, weights=None):
+    """The column-step VRR of plan P over the primitive quartets; returns the
+    accumulator sets [set][target column][e - e_lo]: set 0 plain, set w the
+    targets weighted by weights(prim)[w - 1]."""
     NE, L, La, Lc = P.NE, P.L, P.La, P.Lc
     NET = NE - P.ie_lo
-    H = np.zeros((len(P.f_targets), NET))
-    for pb, pk, qs, F in prims:
+    nw = 0 if weights is None else len(weights(prims[0]))
+    Hs = np.zeros((1 + nw, len(P.f_targets), NET))
+    col0_target = tuple(P.f_targets[0]) == (0, 0, 0)
+    for prim in prims:
+        pb, pk, qs, F = prim
+        wts = [1.0] + (list(weights(prim)) if nw else [])
+        H = np.zeros((len(P.f_targets), NET))
         A = np.zeros(max(P.arena, 1) + 4 * NE)
         PA, QC = pb.PA, pk.PA
         WP = [qs.roz * x for x in qs.PQ]
@@ -207,7 +224,7 @@ def emulate_coop(cls, prims):
                 A[bc + out] = PA[ax] * A[bc + x] + WP[ax] * A[bc + x + NE] + ky * o2z * (A[bc + y] - qs.roz * A[bc + y + NE])
             for out, x, ax in P.bra_nodes_n[k]:
                 A[bc + out] = PA[ax] * A[bc + x] + WP[ax] * A[bc + x + NE]
-        if min(cls[2], cls[3]) == 0:
+        if col0_target:
             H[0] += A[bc + P.ie_lo:bc + NE]
         for st in P.cols:
             rows = Lc - st.level + 1
@@ -227,7 +244,9 @@ def emulate_coop(cls, prims):
                     A[st.out + o] = v
             if st.target >= 0:
                 H[st.target] += A[st.out + P.ie_lo:st.out + NE]
-    return H, P
+        for w, wt in enumerate(wts):
+            Hs[w] += wt * H
+    return Hs
 
 
 @pytest.mark.parametrize("cls", [(1, 1, 1, 1), (2, 1, 2, 0), (2, 2, 1, 1), (3, 2, 2, 2), (2, 0, 0, 0), (2, 2, 0, 0)],
@@ -291,3 +310,110 @@ def test_staged_slots_beyond_shared_memory_go_to_global_scratch(monkeypatch):
     got, _ = run_generated(src, cls, prims, Qns, True, "staged", meta)
     ref = oracle.eri_block(S, 0, 1, 2, 3, spherical=True)
     assert np.allclose(got, ref, rtol=1e-10, atol=1e-13)
+
+
+# ---------------------------------------------------------------- derivatives
+class _Ptr:
+    """Pointer arithmetic over a flat array, as the generated functions use it."""
+
+    def __init__(self, a, o=0):
+        self.a, self.o = a, o
+
+    def __add__(self, k):
+        return _Ptr(self.a, self.o + int(k))
+
+    __radd__ = __add__
+
+    def __getitem__(self, i):
+        return self.a[self.o + i]
+
+    def __setitem__(self, i, v):
+        self.a[self.o + i] = v
+
+
+def _translate_function(src, name):
+    """Python function from one generated derivative HRR function (straight-line
+    declarations, fma, pointer offsets and the d/dD update)."""
+    lines = src.splitlines()
+    start = next(i for i, ln in enumerate(lines) if re.search(rf"void {name}\(", ln))
+    sig = lines[start]
+    args = [a.split()[-1].lstrip("&*") for a in sig[sig.index("(") + 1:sig.index(")")].split(",")]
+    out = [f"def {name}({', '.join(args)}):"]
+    for raw in lines[start + 1:]:
+        if raw.startswith("}"):
+            break
+        ln = raw.strip()
+        if ln.startswith("{ "):
+            ln = ln[2:]
+        if not ln or ln == "}" or ln.startswith("//"):
+            continue
+        m = re.match(r"const int (\w+) = (\w+) / (\d+), (\w+) = \2 % \3;$", ln)
+        if m:
+            out.append(f"    {m.group(1)}, {m.group(4)} = {m.group(2)} // {m.group(3)}, {m.group(2)} % {m.group(3)}")
+            continue
+        m = re.match(r"if \(k == 0\) (.+?) = (.+?); else \1 -= (.+?);$", ln)
+        if m:
+            out.append(f"    {m.group(1)} = {m.group(2)} if k == 0 else {m.group(1)} - {m.group(3)}")
+            continue
+        ln = re.sub(r"^(const )?(long long|double|int)(\* __restrict__|\*)? ", "", ln)
+        ln = ln.replace("(size_t)", "").replace("(long long)", "")
+        ln = re.sub(r"__ldg\((\w+) \+ (\d+)\)", r"\1[\2]", ln)
+        assert ln.endswith(";"), ln
+        out.append("    " + ln[:-1])
+    return "\n".join(out)
+
+
+def emulate_deriv(cls, prims, Qns):
+    """The derivative kernel of class cls on the CPU: the cooperative VRR of the
+    raised class with the plain, 2 alpha, 2 beta and 2 gamma accumulator sets,
+    then the generated bra and ket functions in the kernel's order.  Returns the
+    12 blocks [position][axis][block] of one quartet in canonical order."""
+    from electron_repulsion_integrals_gb300.gen import coop as CP
+    from electron_repulsion_integrals_gb300.gen import deriv as D
+    la, lb, lc, ld = cls
+    src, meta = D.emit_deriv_class(cls)
+    P = CP.plan((la + 1, lb, lc + 1, ld), e_lo=max(0, la - 1), f_lo=max(0, lc - 1))
+    Hs = emulate_coop_plan(P, prims, lambda pr: (2 * pr[0].alpha, 2 * pr[0].beta, 2 * pr[1].gamma))
+    cname = "d" + E.class_name(cls)[1:]
+    ns = {"fma": fma}
+    for fn in ("bra_dA", "bra_dB", "bra_0g", "ket_ab", "ket_c"):
+        exec(compile(_translate_function(src, f"{fn}_{cname}"), f"<{fn} {cls}>", "exec"), ns)
+    nf = [2 * l + 1 if l >= 2 else (l + 1) * (l + 2) // 2 for l in cls]
+    bs = nf[0] * nf[1] * nf[2] * nf[3]
+    NF, NR = Hs.shape[1], nf[0] * nf[1]
+    out = np.zeros(12 * bs)
+    Q = types.SimpleNamespace(AB=Qns.AB, CD=Qns.CD, pos=[0, 1, 2, 3],
+                              ost=[nf[1] * nf[2] * nf[3], nf[2] * nf[3], nf[3], 1])
+    ns["deriv_out"] = lambda P_, Q_, q_, k_, x_: _Ptr(out, (Q_.pos[k_] * 3 + x_) * bs)
+    ns[f"kOutScale_{cname}"] = _Ptr(np.asarray(osc_table(cls)))
+    H = _Ptr(Hs.reshape(-1))
+    G = _Ptr(np.zeros(meta["arena"]))
+    for bra, k in (("bra_dA", 0), ("bra_dB", 1)):
+        for fi in range(NF):
+            ns[f"{bra}_{cname}"](Q, H, fi, G)
+        for it in range(3 * NR):
+            ns[f"ket_ab_{cname}"](None, Q, 0, it % NR, it // NR, G, k)
+    for fi in range(NF):
+        ns[f"bra_0g_{cname}"](Q, H, fi, G)
+    for r in range(NR):
+        ns[f"ket_c_{cname}"](None, Q, 0, r, G)
+    return out.reshape(4, 3, bs)
+
+
+DERIV_CLASSES = [(0, 0, 0, 0), (1, 0, 1, 0), (1, 1, 1, 1), (2, 0, 1, 1), (2, 1, 2, 1), (2, 2, 1, 0), (2, 2, 2, 2)]
+
+
+@pytest.mark.parametrize("cls", DERIV_CLASSES, ids=lambda c: "".join(map(str, c)))
+def test_generated_derivative_class_matches_oracle(cls):
+    """The derivative kernels' generated HRR functions, run on the CPU over the
+    emulated cooperative VRR, give the oracle's d(ab|cd)/dR blocks."""
+    rng = np.random.default_rng(500 + sum((i + 1) * 10 ** k for k, i in enumerate(cls)))
+    for nprim in (1, 2):
+        S, prims, Qns = harness(cls, rng, nprim=nprim, extra_boys=2)
+        got = emulate_deriv(cls, prims, Qns)
+        ref = np.asarray(oracle.eri_deriv_blocks(S, np.array([[0, 1, 2, 3]], dtype=np.int32), spherical=True))[0]
+        ref = ref.reshape(got.shape)
+        m = np.abs(ref).max()
+        tol = np.maximum(np.maximum(1e-12, 1e-10 * np.abs(ref)), 1e-12 * m)
+        worst = np.max(np.abs(got - ref) - tol)
+        assert worst <= 0, (cls, nprim, float(np.max(np.abs(got - ref))), float(m))
