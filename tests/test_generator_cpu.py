@@ -11,9 +11,10 @@ must match the oracle's McMurchie-Davidson block.
 
 This checks the generator (graph construction, axis rule, schedule, HRR,
 stepwise spherical transform and emission) without a GPU.  The cooperative
-tier's column schedule is emulated from its tables, and the first-derivative
-kernels' generated HRR functions are run over that emulation (four weighted
-accumulator sets) against the oracle's derivative blocks.
+tier's column schedule is emulated from its tables; its generated HRR
+functions (normal, and reversed for a pair evaluated on its lower-l shell) and
+the first-derivative kernels' HRR functions (four weighted accumulator sets)
+are run over that emulation against the oracle's blocks.
 """
 
 import math
@@ -106,10 +107,12 @@ def translate(src):
     return "\n".join(out)
 
 
-def harness(cls, rng, nprim=1, spread=3.0, extra_boys=0):
+def harness(cls, rng, nprim=1, spread=3.0, extra_boys=0, swap_bra=False, swap_ket=False):
     """Random shells in canonical order; returns (oracle ShellSet, primitive inputs).
     extra_boys: Boys orders beyond sum(cls) (derivative classes run the VRR of
-    the class raised by one on the bra and on the ket)."""
+    the class raised by one on the bra and on the ket).  swap_bra / swap_ket:
+    the VRR and HRR centres of the pair exchanged (B - A, P - B), as the
+    cooperative kernels do for a pair evaluated on its lower-l shell."""
     cen = [rng.uniform(0, spread, 3) for _ in range(4)]
     nps = [nprim] * 4
     ex = [np.exp(rng.uniform(np.log(0.2), np.log(20.0), n)) for n in nps]
@@ -118,20 +121,22 @@ def harness(cls, rng, nprim=1, spread=3.0, extra_boys=0):
     d = [oracle.norm_coefs(l, e, c) for l, e, c in zip(cls, ex, cf)]
     L = sum(cls) + extra_boys
     A, B, C, D = [np.asarray(c) for c in cen]
+    VA, VB = (B, A) if swap_bra else (A, B)
+    VC, VD = (D, C) if swap_ket else (C, D)
     prims = []
     for i in range(nprim):
         for j in range(nprim):
             a, b = ex[0][i], ex[1][j]
             z = a + b
             P = (a * A + b * B) / z
-            pb = types.SimpleNamespace(zeta=z, o2z=0.5 / z, P=list(P), PA=list(P - A), alpha=a, beta=b)
+            pb = types.SimpleNamespace(zeta=z, o2z=0.5 / z, P=list(P), PA=list(P - VA), alpha=a, beta=b)
             Kab = math.exp(-a * b / z * np.sum((A - B) ** 2)) * d[0][i] * d[1][j]
             for k in range(nprim):
                 for m in range(nprim):
                     c, dd = ex[2][k], ex[3][m]
                     e = c + dd
                     Q = (c * C + dd * D) / e
-                    pk = types.SimpleNamespace(zeta=e, o2z=0.5 / e, P=list(Q), PA=list(Q - C), gamma=c)
+                    pk = types.SimpleNamespace(zeta=e, o2z=0.5 / e, P=list(Q), PA=list(Q - VC), gamma=c)
                     Kcd = math.exp(-c * dd / e * np.sum((C - D) ** 2)) * d[2][k] * d[3][m]
                     rho = z * e / (z + e)
                     PQ = Q - P
@@ -139,7 +144,7 @@ def harness(cls, rng, nprim=1, spread=3.0, extra_boys=0):
                     pref = 2 * math.pi ** 2.5 / (z * e * math.sqrt(z + e)) * Kab * Kcd
                     F = list(pref * oracle.boys(L, rho * float(PQ @ PQ)))
                     prims.append((pb, pk, qs, F))
-    Qns = types.SimpleNamespace(AB=list(A - B), CD=list(C - D))
+    Qns = types.SimpleNamespace(AB=list(VA - VB), CD=list(VC - VD))
     return S, prims, Qns
 
 
@@ -338,6 +343,8 @@ def _translate_function(src, name):
     start = next(i for i, ln in enumerate(lines) if re.search(rf"void {name}\(", ln))
     sig = lines[start]
     args = [a.split()[-1].lstrip("&*") for a in sig[sig.index("(") + 1:sig.index(")")].split(",")]
+    if "smax_" in args:
+        args[args.index("smax_")] = "smax_=None"
     out = [f"def {name}({', '.join(args)}):"]
     for raw in lines[start + 1:]:
         if raw.startswith("}"):
@@ -350,6 +357,16 @@ def _translate_function(src, name):
         m = re.match(r"const int (\w+) = (\w+) / (\d+), (\w+) = \2 % \3;$", ln)
         if m:
             out.append(f"    {m.group(1)}, {m.group(4)} = {m.group(2)} // {m.group(3)}, {m.group(2)} % {m.group(3)}")
+            continue
+        if ln.startswith(("constexpr ", "(void)", "double jcd_[", "OUTPUT_ROW_END")):
+            continue
+        m = re.match(r"OUTPUT_ROW\(r, .*\);$", ln)
+        if m:
+            continue
+        m = re.match(r"OUTPUT_VAL\((\w+) / (\d+), \1 % \2, (\d+), (\d+), (\w+)\);$", ln)
+        if m:
+            out.append(f"    OUT[({m.group(1)} // {m.group(2)}, {m.group(1)} % {m.group(2)}, {m.group(3)}, {m.group(4)})]"
+                       f" = {m.group(5)}")
             continue
         m = re.match(r"if \(k == 0\) (.+?) = (.+?); else \1 -= (.+?);$", ln)
         if m:
@@ -417,3 +434,58 @@ def test_generated_derivative_class_matches_oracle(cls):
         tol = np.maximum(np.maximum(1e-12, 1e-10 * np.abs(ref)), 1e-12 * m)
         worst = np.max(np.abs(got - ref) - tol)
         assert worst <= 0, (cls, nprim, float(np.max(np.abs(got - ref))), float(m))
+
+
+def emulate_coop_hrr(cls, prims, Qns, rb, rk):
+    """The cooperative kernel's HRR stage on the CPU: the generated bra (one
+    call per ket column) and ket (one call per bra row) functions, normal or
+    reversed, over the emulated VRR accumulators; returns the spherical block
+    in canonical order."""
+    from electron_repulsion_integrals_gb300.gen import coop as CP
+    src, meta = CP.emit_coop_class(cls)
+    H, P = emulate_coop(cls, prims)
+    cname = E.class_name(cls)
+    bra = f"bra_hrr_rev_{cname}" if rb else f"bra_hrr_{cname}"
+    ket = f"ket_hrr_rev_{cname}" if rk else f"ket_hrr_{cname}"
+    out = {}
+    ns = {"fma": fma, "OUT": out, f"kOutScale_{cname}": _Ptr(np.asarray(osc_table(cls)))}
+    for fn in (bra, ket):
+        exec(compile(_translate_function(src, fn), f"<{fn}>", "exec"), ns)
+    fi_lc = int(re.search(r"FI_LC = (\d+)", src).group(1))
+    nr = int(re.search(r"NR = (\d+)", src).group(1))
+    NF = H.shape[0]
+    G = _Ptr(np.zeros(int(re.search(r"ARENA = (\d+)", src).group(1))))
+    Q = types.SimpleNamespace(AB=Qns.AB, CD=Qns.CD)
+    for fi in range(0 if rk else fi_lc, NF):
+        ns[bra](Q, _Ptr(H.reshape(-1)), fi, G)
+    for r in range(nr):
+        ns[ket](None, Q, 0, r, G)
+    nf = [2 * l + 1 if l >= 2 else (l + 1) * (l + 2) // 2 for l in cls]
+    blk = np.zeros(nf)
+    for k, v in out.items():
+        blk[k] = v
+    return blk, len(out)
+
+
+COOP_HRR = [((3, 2, 3, 2), 0, 0), ((3, 2, 3, 2), 1, 0), ((3, 2, 3, 2), 0, 1), ((3, 2, 3, 2), 1, 1),
+            ((3, 3, 3, 0), 0, 1), ((4, 1, 2, 2), 1, 0), ((3, 3, 3, 3), 0, 0)]
+
+
+@pytest.mark.parametrize("cls,rb,rk", COOP_HRR, ids=lambda v: "".join(map(str, v)) if isinstance(v, tuple) else str(v))
+def test_coop_hrr_functions_match_oracle(cls, rb, rk):
+    """The cooperative tier's generated HRR functions, normal and reversed (pair
+    evaluated with the VRR on its lower-l shell), on the CPU over the emulated
+    column-step VRR, give the oracle's block in canonical order."""
+    rng = np.random.default_rng(900 + 7 * rb + 3 * rk + sum(cls))
+    S, prims, Qns = harness(cls, rng, nprim=2, swap_bra=bool(rb), swap_ket=bool(rk))
+    got, nout = emulate_coop_hrr(cls, prims, Qns, rb, rk)
+    assert nout == got.size
+    ref = oracle.eri_block(S, 0, 1, 2, 3, spherical=True)
+    # per element max(1e-10 |o|, 1e-12 m), m the block maximum: with both pairs
+    # reversed the HRR shifts across AB and CD reach small elements (1e-5 of m)
+    # through cancellations of terms of the block's size, so their rounding is
+    # absolute, about 1e-15 of m
+    m = np.max(np.abs(ref))
+    tol = np.maximum(1e-10 * np.abs(ref), 1e-12 * m)
+    worst = np.max(np.abs(got - ref) - tol)
+    assert worst <= 0, (cls, rb, rk, float(np.max(np.abs(got - ref)) / m))
