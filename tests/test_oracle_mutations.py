@@ -33,6 +33,18 @@ MUTATIONS = [
     ("derivative: raising weight", "sh[k].coef[p] = base[k].coef[p] * 2.0 * sh[k].exps[p];",
      "sh[k].coef[p] = base[k].coef[p] * sh[k].exps[p];"),
     ("derivative: lowering factor", "v -= (e[ax] + 1) * dn[", "v -= e[ax] * dn["),
+    ("J blocks: only c >= d", "const int c = (int)(cd / nshell), d = (int)(cd % nshell);",
+     "const int c = (int)(cd / nshell), d = (int)(cd % nshell);\n        if (d > c) continue;"),
+    ("J blocks: density column offset", "* D[(size_t)(fo[c] + k) * nbf + fo[d] + l];",
+     "* D[(size_t)(fo[c] + k) * nbf + fo[c] + l];"),
+    ("J blocks: screen with the wrong pair",
+     "Q[(size_t)c * nshell + d] < tau) continue;\n        eri_block<double>(S, a, b, c, d, spherical, blk);\n"
+     "        const int nc",
+     "Q[(size_t)a * nshell + d] < tau) continue;\n        eri_block<double>(S, a, b, c, d, spherical, blk);\n"
+     "        const int nc"),
+    ("Schwarz: square root dropped", "Q[(size_t)b * nshell + a] = std::sqrt(mx);", "Q[(size_t)b * nshell + a] = mx;"),
+    ("Schwarz: off-diagonal element", "size_t k = ((size_t)(i * nb + j) * na + i) * nb + j;",
+     "size_t k = ((size_t)(i * nb + j) * na + i) * nb + (nb - 1 - j);"),
 ]
 
 

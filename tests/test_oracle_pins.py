@@ -458,3 +458,78 @@ def test_derivative_blocks_translation_invariance_and_symmetry():
     # (cd|ab) derivatives are the transposed (ab|cd) ones with the centres relabelled
     t = np.transpose(d[1], (0, 1, 4, 5, 2, 3))[[2, 3, 0, 1]]
     assert np.allclose(t, d[0], rtol=1e-12, atol=1e-14 * scale)
+
+
+# ---------------------------------------------------------------- J and K blocks, Schwarz factors
+
+
+def _spd_cluster(radius):
+    """Three atoms (one heavy: 3s 2p 1d; two light: 2s 1p) with 1-6 primitives."""
+    from electron_repulsion_integrals_gb300 import workloads as W
+    s = W.cluster(3, seed_index=91, radius=radius, dmin=1.5)
+    return oracle.ShellSet(s.centers, s.L, s.nprim, s.exps, s.coefs)
+
+
+def _fo(S, spherical=True):
+    return np.concatenate([[0], np.cumsum([oracle.nfunc(l, spherical) for l in S.L])]).astype(int)
+
+
+def test_schwarz_is_root_of_largest_diagonal_integral():
+    """Q_ab = sqrt(max_{mu in a, nu in b} (mu nu|mu nu)), read off the full tensor."""
+    S = _spd_cluster(4.0)
+    T = oracle.eri_tensor(S, spherical=True)
+    fo = _fo(S)
+    Q = oracle.schwarz(S, spherical=True)
+    nbf = T.shape[0]
+    diag = np.einsum("ijij->ij", T.reshape(nbf, nbf, nbf, nbf))
+    assert np.all(diag >= 0)  # exact zeros: tight functions on distant atoms underflow
+    top = math.sqrt(diag.max())
+    for a in range(S.n):
+        for b in range(S.n):
+            ref = math.sqrt(diag[fo[a]:fo[a + 1], fo[b]:fo[b + 1]].max())
+            assert abs(Q[a, b] - ref) <= 1e-13 * ref + 1e-15 * top, (a, b, Q[a, b], ref)
+
+
+def test_J_blocks_match_contraction_and_screened_build():
+    """Every block of ora_J_blocks equals the same block of sum_kl (ij|kl) D_kl
+    unscreened, and of ora_build_J under a screen that drops quartets."""
+    S = _spd_cluster(4.0)
+    T = oracle.eri_tensor(S, spherical=True)
+    fo = _fo(S)
+    nbf = T.shape[0]
+    rng = np.random.default_rng(17)
+    C = rng.normal(size=(nbf, nbf // 4))
+    D = C @ C.T
+    Jref = np.einsum("ijkl,kl->ij", T, D)
+    pairs = [(a, b) for a in range(S.n) for b in range(S.n)]
+    for (a, b), B in zip(pairs, oracle.J_blocks(S, D, pairs, spherical=True, tau=0.0)):
+        assert np.allclose(B, Jref[fo[a]:fo[a + 1], fo[b]:fo[b + 1]], rtol=1e-12, atol=1e-12 * abs(Jref).max())
+    # a threshold that removes a good share of the quartets: the screened sets must agree
+    Q = oracle.schwarz(S, spherical=True)
+    tau = float(np.quantile(np.outer(Q, Q), 0.7))
+    Js, kept = oracle.build_J(S, D, spherical=True, tau=tau, Q=Q)
+    npair = S.n * (S.n + 1) // 2
+    assert 0 < kept < npair * (npair + 1) // 2
+    assert np.linalg.norm(Js - Jref) > 1e-8 * np.linalg.norm(Jref)  # the screen bites
+    for (a, b), B in zip(pairs, oracle.J_blocks(S, D, pairs, spherical=True, tau=tau, Q=Q)):
+        ref = Js[fo[a]:fo[a + 1], fo[b]:fo[b + 1]]
+        assert np.allclose(B, ref, rtol=1e-12, atol=1e-12 * abs(Js).max()), (a, b)
+
+
+def test_K_blocks_match_screened_build():
+    """Screened ora_K_blocks equals the same blocks of ora_build_JK's K."""
+    S = _spd_cluster(4.0)
+    fo = _fo(S)
+    nbf = fo[-1]
+    rng = np.random.default_rng(19)
+    C = rng.normal(size=(nbf, nbf // 4))
+    D = C @ C.T
+    Q = oracle.schwarz(S, spherical=True)
+    tau = float(np.quantile(np.outer(Q, Q), 0.7))
+    _, K = oracle.build_JK(S, D, spherical=True, tau=tau, Q=Q)
+    _, K0 = oracle.build_JK(S, D, spherical=True, tau=0.0)
+    assert np.linalg.norm(K - K0) > 1e-8 * np.linalg.norm(K0)
+    pairs = [(a, c) for a in range(S.n) for c in range(S.n)]
+    for (a, c), B in zip(pairs, oracle.K_blocks(S, D, pairs, spherical=True, tau=tau, Q=Q)):
+        ref = K[fo[a]:fo[a + 1], fo[c]:fo[c + 1]]
+        assert np.allclose(B, ref, rtol=1e-12, atol=1e-12 * abs(K).max()), (a, c)
