@@ -319,10 +319,6 @@ __device__ __forceinline__ void load_quartet_coulomb(const EriLaunch& P, long lo
   Q.ket = sg.y + (int)qo;
   const PairMeta* mb = P.pairs + Q.bra;
   const PairMeta* mk = P.pairs + Q.ket;
-  Q.s[0] = __ldg(&mb->a);
-  Q.s[1] = __ldg(&mb->b);
-  Q.s[2] = __ldg(&mk->a);
-  Q.s[3] = __ldg(&mk->b);
   Q.pab = __ldg(&mb->poff);
   Q.nab = __ldg(&mb->np);
   Q.pcd = __ldg(&mk->poff);
@@ -336,6 +332,21 @@ __device__ __forceinline__ void load_quartet_coulomb(const EriLaunch& P, long lo
     Q.AB[x] = __ldg(&mb->AB[x]);
     Q.CD[x] = __ldg(&mk->AB[x]);
   }
+  Q.rb = 0;
+  Q.rk = 0;
+}
+
+// Coulomb mode, after the primitive loop: what the digestion of the finished
+// block needs (first basis functions, pair factors, the quartet's weight).
+// Loaded here rather than with the quartet so that none of it occupies
+// registers across the primitive loop.
+__device__ __forceinline__ void load_quartet_digest(const EriLaunch& P, Quartet& Q) {
+  const PairMeta* mb = P.pairs + Q.bra;
+  const PairMeta* mk = P.pairs + Q.ket;
+  Q.s[0] = __ldg(&mb->a);
+  Q.s[1] = __ldg(&mb->b);
+  Q.s[2] = __ldg(&mk->a);
+  Q.s[3] = __ldg(&mk->b);
   Q.fa = __ldg(P.fo + Q.s[0]);
   Q.fb = __ldg(P.fo + Q.s[1]);
   Q.fc = __ldg(P.fo + Q.s[2]);
@@ -343,8 +354,6 @@ __device__ __forceinline__ void load_quartet_coulomb(const EriLaunch& P, long lo
   Q.fab = Q.s[0] != Q.s[1] ? 2.0 : 1.0;
   Q.fcd = Q.s[2] != Q.s[3] ? 2.0 : 1.0;
   Q.wk = (Q.s[0] == Q.s[1] ? 0.5 : 1.0) * (Q.s[2] == Q.s[3] ? 0.5 : 1.0) * (Q.bra == Q.ket ? 0.5 : 1.0);
-  Q.rb = 0;
-  Q.rk = 0;
 }
 
 // Gaussian product of two primitives (alpha at A, beta at B):
@@ -473,6 +482,12 @@ __device__ __forceinline__ void quartet_setup(const PrimPair& pb, const PrimPair
 // images add the transposes, so K = T + T^T for a symmetric D.  T_bc and T_bd
 // rows change with ib and are flushed every row; T_ac and T_ad rows change with
 // ia only and are flushed after the last ib of that ia.
+// The density rows a block row reads are the same for every row of the block
+// (D_cd) or for every row of one a or b function; the pointers pass through an
+// empty asm statement so that the compiler reloads those values per row (L1
+// hits) instead of keeping them in registers across the rows, which pushed the
+// large classes' register use past the 255-register limit.
+#define ERI_OPAQUE_PTR(dst, src) asm volatile("mov.b64 %0, %1;" : "=l"(dst) : "l"(src))
 #define OUTPUT_ROW(r, ia, ib)                                               \
   {                                                                         \
     double* __restrict__ orow_ = nullptr;                                   \
@@ -480,6 +495,7 @@ __device__ __forceinline__ void quartet_setup(const PrimPair& pb, const PrimPair
     double* jdst_ = nullptr;                                                \
     const double* __restrict__ da_ = nullptr;                               \
     const double* __restrict__ db_ = nullptr;                               \
+    const double* dcd_ = nullptr;                                           \
     double kbc_[kNSC_], kbd_[kNSD_];                                        \
     const int ia_ = (ia), ib_ = (ib);                                       \
     if constexpr (MODE == kStore) {                                         \
@@ -488,10 +504,11 @@ __device__ __forceinline__ void quartet_setup(const PrimPair& pb, const PrimPair
       const size_t rowoff_ = (size_t)(Q.fa + (ia)) * P.nbf + Q.fb + (ib);   \
       dab_ = Q.fab * __ldg(P.D + rowoff_);                                  \
       jdst_ = P.J + rowoff_;                                                \
+      ERI_OPAQUE_PTR(dcd_, P.D + (size_t)Q.fc * P.nbf + Q.fd);              \
     }                                                                       \
     if constexpr (MODE == kExchange) {                                      \
-      da_ = P.D + (size_t)(Q.fa + (ia)) * P.nbf;                            \
-      db_ = P.D + (size_t)(Q.fb + (ib)) * P.nbf;                            \
+      ERI_OPAQUE_PTR(da_, P.D + (size_t)(Q.fa + (ia)) * P.nbf);             \
+      ERI_OPAQUE_PTR(db_, P.D + (size_t)(Q.fb + (ib)) * P.nbf);             \
       _Pragma("unroll") for (int k_ = 0; k_ < kNSC_; ++k_) kbc_[k_] = 0.0;  \
       _Pragma("unroll") for (int k_ = 0; k_ < kNSD_; ++k_) kbd_[k_] = 0.0;  \
     }
@@ -505,7 +522,7 @@ __device__ __forceinline__ void quartet_setup(const PrimPair& pb, const PrimPair
     if ((ia) == (ic) && (ib) == (id))                                          \
       atomicAdd(P.q_out + Q.qi * P.q_stride + (ia) * kNSB_ + (ib), (v));       \
   } else {                                                                     \
-    jrow_ = fma((v), __ldg(P.D + (size_t)(Q.fc + (ic)) * P.nbf + Q.fd + (id)), jrow_); \
+    jrow_ = fma((v), __ldg(dcd_ + (size_t)(ic) * P.nbf + (id)), jrow_);     \
     jcd_[(ic) * kNSD_ + (id)] = fma((v), dab_, jcd_[(ic) * kNSD_ + (id)]);   \
     if constexpr (MODE == kExchange) {                                         \
       kac_[ic] = fma((v), __ldg(db_ + Q.fd + (id)), kac_[ic]);                \
@@ -541,6 +558,7 @@ __device__ __forceinline__ void quartet_setup(const PrimPair& pb, const PrimPair
   (void)jdst_;                                                                      \
   (void)da_;                                                                        \
   (void)db_;                                                                        \
+  (void)dcd_;                                                                       \
   (void)kbc_;                                                                       \
   (void)kbd_;                                                                       \
   (void)ia_;                                                                        \
@@ -568,27 +586,31 @@ __device__ __forceinline__ void quartet_setup(const PrimPair& pb, const PrimPair
       cudaFuncSetAttribute(KERNEL<M, C>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(SMEMB)); \
     KERNEL<M, C><<<blocks, kThreads, (SMEMB), st>>>(*P);                                           \
   }
-#define ERI_LAUNCH_MODE_(KERNEL, M, SMEMB) \
-  if (contracted)                          \
-    ERI_LAUNCH_ONE_(KERNEL, M, true, SMEMB) \
-  else                                     \
+#define ERI_LAUNCH_MODE_(KERNEL, M, SMEMB, CSMEMB) \
+  if (contracted)                                 \
+    ERI_LAUNCH_ONE_(KERNEL, M, true, CSMEMB)      \
+  else                                            \
     ERI_LAUNCH_ONE_(KERNEL, M, false, SMEMB)
 
-// SMEM_SLOTS: shared-memory slots per thread of the staged tier's VRR (dynamic).
-#define ERI_DEFINE_CLASS_LAUNCHER(LA, LB, LC, LD, KERNEL, SLOTS, VOPS, VFLOPS, HOPS, HFLOPS, SMEM_SLOTS)   \
+// SMEM_SLOTS: shared-memory slots per thread of the staged tier's VRR (dynamic);
+// ACC_SLOTS: further slots per thread that the contracted instantiation of a
+// register-tier class uses for its sums.
+#define ERI_DEFINE_CLASS_LAUNCHER(LA, LB, LC, LD, KERNEL, SLOTS, VOPS, VFLOPS, HOPS, HFLOPS, SMEM_SLOTS,   \
+                                  ACC_SLOTS)                                                              \
   extern "C" int eri_launch_c##LA##LB##LC##LD(const EriLaunch* P, int mode, int contracted, int blocks,    \
                                                cudaStream_t st) {                                         \
     const size_t smemb_ = (size_t)(SMEM_SLOTS) * kThreads * sizeof(double);                               \
+    const size_t csmemb_ = (size_t)((SMEM_SLOTS) + (ACC_SLOTS)) * kThreads * sizeof(double);              \
     if (mode == kStore) {                                                                                 \
-      ERI_LAUNCH_MODE_(KERNEL, kStore, smemb_)                                                            \
+      ERI_LAUNCH_MODE_(KERNEL, kStore, smemb_, csmemb_)                                                   \
     } else if (mode == kSchwarz) {                                                                        \
-      ERI_LAUNCH_MODE_(KERNEL, kSchwarz, smemb_)                                                          \
+      ERI_LAUNCH_MODE_(KERNEL, kSchwarz, smemb_, csmemb_)                                                 \
     } else if (mode == kSchwarzPart) {                                                                    \
-      ERI_LAUNCH_ONE_(KERNEL, kSchwarzPart, true, smemb_)                                                 \
+      ERI_LAUNCH_ONE_(KERNEL, kSchwarzPart, true, csmemb_)                                                \
     } else if (mode == kCoulomb) {                                                                        \
-      ERI_LAUNCH_ONE_(KERNEL, kCoulomb, true, smemb_)                                                     \
+      ERI_LAUNCH_ONE_(KERNEL, kCoulomb, true, csmemb_)                                                    \
     } else if (mode == kExchange) {                                                                       \
-      ERI_LAUNCH_ONE_(KERNEL, kExchange, true, smemb_)                                                    \
+      ERI_LAUNCH_ONE_(KERNEL, kExchange, true, csmemb_)                                                   \
     } else {                                                                                              \
       return -1;                                                                                          \
     }                                                                                                     \

@@ -386,11 +386,16 @@ def class_name(cls):
 
 # VRR values kept in registers by the staged tier; the rest of the frontier
 # goes to per-thread shared-memory slots (SMEM).
-STAGED_VRR_REGS = 64
+STAGED_VRR_REGS = 60
 STAGED_FENCE = 32
 # shared-memory slots per thread at most (x 128 threads x 8 B = 200 KB of the
 # 227 KB a block may have); further evicted values go to global scratch (GSL)
 STAGED_SMEM_SLOTS_MAX = 200
+
+
+# register tier: above this many targets the contracted instantiation keeps its
+# sums in shared memory instead of registers
+REG_ACC_MAX = 64
 
 
 def choose_shape(g, peak, cls):
@@ -439,15 +444,19 @@ def emit_class(cls, spherical_out=True, rule=None, schedule=None, sph_fusion=Tru
     emit_vrr_coefs(vem, vrr_coef_needs(g))
     tvars = [None] * len(g.targets)
 
+    acc_smem = shape == "reg" and len(g.targets) > REG_ACC_MAX
     if shape == "reg":
         def sink(ti, var):
             tvars[ti] = var
-            vem.w(f"if (CONTRACTED) {{ h{ti} += {var}; }} else {{ h{ti} = {var}; }}")
+            if acc_smem:
+                vem.w(f"if constexpr (CONTRACTED) {{ ACC({ti}) += {var}; }} else {{ h{ti} = {var}; }}")
+            else:
+                vem.w(f"if (CONTRACTED) {{ h{ti} += {var}; }} else {{ h{ti} = {var}; }}")
     else:
         def sink(ti, var):
             e, f = g.target_ef[ti]
             slot = eidx[e] * NF + fidx[f]
-            vem.w(f"if (CONTRACTED) {{ S[{slot} * nt] += {var}; }} else {{ S[{slot} * nt] = {var}; }}")
+            vem.w(f"if (CONTRACTED) {{ S[{slot} * kThreads] += {var}; }} else {{ S[{slot} * kThreads] = {var}; }}")
     smem_slots = gsl_slots = 0
     if shape == "staged":
         nsl = emit_vrr_staged_regs(vem, g, order, sink, STAGED_VRR_REGS)
@@ -472,12 +481,22 @@ def emit_class(cls, spherical_out=True, rule=None, schedule=None, sph_fusion=Tru
     w("  const long long nt = (long long)gridDim.x * blockDim.x;")
     w("  const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;")
     if shape == "staged":
-        w("  double* __restrict__ S = P.scratch + gid;")
+        # block-local scratch: the block's slab holds slot k of its thread t at
+        # [k * kThreads + t], so every slot offset is a compile-time immediate
+        # (a runtime stride would cost an address register per slot)
+        w(f"  double* __restrict__ S = P.scratch + (long long)blockIdx.x * ({scratch_slots + gsl_slots} * kThreads) + "
+          "threadIdx.x;")
         if smem_slots:
             w("  extern __shared__ double smem_vrr_[];")
             w("#define SMEM(k) smem_vrr_[(k) * kThreads + threadIdx.x]")
         if gsl_slots:
-            w(f"#define GSL(k) S[({gsl_base} + (k)) * nt]")
+            w(f"#define GSL(k) S[({gsl_base} + (k)) * kThreads]")
+    if acc_smem:
+        # contracted sums of a register-tier class with many targets: one
+        # shared-memory slot per target and thread (kept out of the register
+        # file across the primitive loop), read back once before the HRR
+        w("  extern __shared__ double smem_acc_[];")
+        w("#define ACC(k) smem_acc_[(k) * kThreads + threadIdx.x]")
     w("  for (long long q = gid; q < P.n; q += nt) {")
     w("    Quartet Q;")
     lq = f"load_quartet<{1 if la == lb else 0}, {1 if lc == ld else 0}, {la + lb}, {lc + ld}>"
@@ -509,18 +528,29 @@ def emit_class(cls, spherical_out=True, rule=None, schedule=None, sph_fusion=Tru
         w(f"    double h[{len(g.targets)}];")
         for ti in range(len(g.targets)):
             w(f"    double& h{ti} = h[{ti}];")
-        w("    if (CONTRACTED) {")
-        for ti in range(len(g.targets)):
-            w(f"      h{ti} = 0.0;")
-        w("    }")
+        if acc_smem:
+            w("    if constexpr (CONTRACTED) {")
+            w(f"      for (int s = 0; s < {len(g.targets)}; ++s) ACC(s) = 0.0;")
+            w("    }")
+        else:
+            w("    if (CONTRACTED) {")
+            for ti in range(len(g.targets)):
+                w(f"      h{ti} = 0.0;")
+            w("    }")
     else:
         w("    if (CONTRACTED) {")
-        w(f"      for (int s = 0; s < {len(g.targets)}; ++s) S[s * nt] = 0.0;")
+        w(f"      for (int s = 0; s < {len(g.targets)}; ++s) S[s * kThreads] = 0.0;")
         w("    }")
     w("    PRIM_LOOP_BEGIN(P, Q)")
     for ln in vem.lines:
         w("      " + ln)
     w("    PRIM_LOOP_END")
+    w("    if constexpr (MODE >= kCoulomb) load_quartet_digest(P, Q);")
+    if acc_smem:
+        w("    if constexpr (CONTRACTED) {")
+        for ti in range(len(g.targets)):
+            w(f"      h{ti} = ACC({ti});")
+        w("    }")
 
     # ---- HRR + sph ----
     hem = Emitter()
@@ -555,9 +585,26 @@ def emit_class(cls, spherical_out=True, rule=None, schedule=None, sph_fusion=Tru
             rows = bra_rows(hem, cart, f"t{fidx[f]}_")
             for r, var in enumerate(rows):
                 gvals[(r, f)] = var
+        # J+K digestion of a class whose contracted sums sit in shared memory:
+        # the half-transformed block G moves into that (now free) region and
+        # each ket row reads its part back, so that G and the exchange
+        # accumulators are not all held in registers at once
+        g_park = acc_smem and NRB * NF <= len(g.targets)
+        if g_park:
+            hem.w("if constexpr (MODE == kExchange) {")
+            for (r, f), var in gvals.items():
+                hem.w(f"  ACC({r * NF + fidx[f]}) = {var};")
+            hem.w("  asm volatile(\"\" ::: \"memory\");")
+            hem.w("}")
+
+        def g_input(f, r):
+            if g_park:
+                return f"(MODE == kExchange ? ACC({r * NF + fidx[f]}) : {gvals[(r, f)]})"
+            return gvals[(r, f)]
+
         xvals = {}
         for r in range(NRB):
-            cart = emit_hrr_column(hem, lc, ld, lambda f, r=r: gvals[(r, f)], f"k{r}_",
+            cart = emit_hrr_column(hem, lc, ld, lambda f, r=r: g_input(f, r), f"k{r}_",
                                    ["Q.CD[0]", "Q.CD[1]", "Q.CD[2]"])
             outs = emit_sph_pair(hem, lc, ld, cart, f"u{r}_")
             if not sph_fusion:
@@ -593,19 +640,19 @@ def emit_class(cls, spherical_out=True, rule=None, schedule=None, sph_fusion=Tru
     else:
         # bra: loop over ket columns
         bem = Emitter()
-        bem.w(f"const double* __restrict__ Hc = S + (long long)fi * nt;")
-        cart = emit_hrr_column(bem, la, lb, lambda e: f"Hc[{eidx[e] * NF} * nt]", "b", ["Q.AB[0]", "Q.AB[1]", "Q.AB[2]"])
+        bem.w(f"const double* __restrict__ Hc = S + fi * kThreads;")
+        cart = emit_hrr_column(bem, la, lb, lambda e: f"Hc[{eidx[e] * NF} * kThreads]", "b", ["Q.AB[0]", "Q.AB[1]", "Q.AB[2]"])
         rows = bra_rows(bem, cart, "t")
-        bem.w(f"double* __restrict__ Gc = S + (long long)({NE * NF} + fi) * nt;")
+        bem.w(f"double* __restrict__ Gc = S + ({NE * NF} + fi) * kThreads;")
         for r, var in enumerate(rows):
-            bem.w(f"Gc[{r * NF} * nt] = {var};")
+            bem.w(f"Gc[{r * NF} * kThreads] = {var};")
         w(f"    for (int fi = 0; fi < {NF}; ++fi) {{")
         for ln in bem.lines:
             w("      " + ln)
         w("    }")
         kem = Emitter()
-        kem.w(f"const double* __restrict__ Gr = S + (long long)({NE * NF} + r * {NF}) * nt;")
-        cart = emit_hrr_column(kem, lc, ld, lambda f: f"Gr[{fidx[f]} * nt]", "k", ["Q.CD[0]", "Q.CD[1]", "Q.CD[2]"])
+        kem.w(f"const double* __restrict__ Gr = S + ({NE * NF} + r * {NF}) * kThreads;")
+        cart = emit_hrr_column(kem, lc, ld, lambda f: f"Gr[{fidx[f]} * kThreads]", "k", ["Q.CD[0]", "Q.CD[1]", "Q.CD[2]"])
         outs = emit_sph_pair(kem, lc, ld, cart, "u")
         # sph_fusion off: the ket-transformed Cartesian rows X[r][c'd'] reuse the
         # H area when it is large enough (H is dead after the bra loop)
@@ -619,9 +666,9 @@ def emit_class(cls, spherical_out=True, rule=None, schedule=None, sph_fusion=Tru
                 kem.w(f"OUTPUT_VAL(r / {nsb}, r % {nsb}, {cdi // nsd}, {cdi % nsd}, {sv});")
             kem.w("OUTPUT_ROW_END();")
         else:
-            kem.w(f"double* __restrict__ Xr = S + (long long)({xbase} + r * {NSCD}) * nt;")
+            kem.w(f"double* __restrict__ Xr = S + ({xbase} + r * {NSCD}) * kThreads;")
             for cdi, var in enumerate(outs):
-                kem.w(f"Xr[{cdi} * nt] = {var};")
+                kem.w(f"Xr[{cdi} * kThreads] = {var};")
         w(f"    for (int r = 0; r < {NRB}; ++r) {{")
         for ln in kem.lines:
             w("      " + ln)
@@ -630,13 +677,13 @@ def emit_class(cls, spherical_out=True, rule=None, schedule=None, sph_fusion=Tru
         hem.flops = bem.flops * NF + kem.flops * NRB
         if not sph_fusion:
             fem = Emitter()
-            fem.w(f"const double* __restrict__ X = S + (long long){xbase} * nt;")
+            fem.w(f"const double* __restrict__ X = S + {xbase} * kThreads;")
             for r in range(NR):
                 ia, ib = r // nsb, r % nsb
                 terms = final_bra_terms(ia, ib)
                 fem.w(f"OUTPUT_ROW({r}, {ia}, {ib});")
                 for cdi in range(NSCD):
-                    var = lin_comb(fem, [(c, f"X[{rc * NSCD + cdi} * nt]") for c, rc in terms], f"z{r}_{cdi}")
+                    var = lin_comb(fem, [(c, f"X[{rc * NSCD + cdi} * kThreads]") for c, rc in terms], f"z{r}_{cdi}")
                     if not var.isidentifier():
                         fem.w(f"const double z{r}_{cdi} = {var};")
                         var = f"z{r}_{cdi}"
@@ -657,6 +704,8 @@ def emit_class(cls, spherical_out=True, rule=None, schedule=None, sph_fusion=Tru
         w("#undef SMEM")
     if shape == "staged" and gsl_slots:
         w("#undef GSL")
+    if acc_smem:
+        w("#undef ACC")
     w("}")
 
     scratch_slots += gsl_slots
@@ -671,10 +720,12 @@ def emit_class(cls, spherical_out=True, rule=None, schedule=None, sph_fusion=Tru
     vops, vflops = vops_all, vflops_all
     hflops = hem.flops
     smem_slots = meta["smem_slots"]
+    acc_slots = len(g.targets) if acc_smem else 0
+    meta["acc_smem_slots"] = acc_slots
     tail = f"""
 }}  // namespace gen
 
-ERI_DEFINE_CLASS_LAUNCHER({la}, {lb}, {lc}, {ld}, gen::k_{cname}, {scratch_slots}, {vops}LL, {vflops}LL, {hops}LL, {hflops}LL, {smem_slots})
+ERI_DEFINE_CLASS_LAUNCHER({la}, {lb}, {lc}, {ld}, gen::k_{cname}, {scratch_slots}, {vops}LL, {vflops}LL, {hops}LL, {hflops}LL, {smem_slots}, {acc_slots})
 
 }}  // namespace eri
 """

@@ -43,6 +43,8 @@ def translate(src):
         ln = raw.strip()
         if not ln or ln.startswith("//") or ln.startswith("(void)"):
             continue
+        # J+K-mode reads of the parked block: the emulation runs the store mode
+        ln = re.sub(r"\(MODE == kExchange \? ACC\(\d+\) : (\w+)\)", r"\1", ln)
         pad = "    " * ind
         if ln == "PRIM_LOOP_BEGIN(P, Q)":
             out.append(pad + "for prim in prims:")
@@ -57,16 +59,32 @@ def translate(src):
             out.append(pad + f"for {m.group(1)} in range({m.group(2)}):")
             ind += 1
             continue
-        if ln == "if (CONTRACTED) {":
+        if ln in ("if (CONTRACTED) {", "if constexpr (CONTRACTED) {"):
             out.append(pad + "if CONTRACTED:")
             ind += 1
+            continue
+        if ln == "if constexpr (MODE == kExchange) {":  # the emulation runs the store mode
+            out.append(pad + "if False:")
+            ind += 1
+            continue
+        if ln.startswith("if constexpr (MODE >= kCoulomb) load_quartet_digest("):
+            continue
+        if ln.startswith("asm volatile("):
+            out.append(pad + "pass")
+            continue
+        m = re.match(r"if constexpr \(CONTRACTED\) \{ ACC\((\d+)\) \+= (\w+); \} else \{ h(\d+) = \2; \}$", ln)
+        if m:
+            out.append(pad + "if CONTRACTED:")
+            out.append(pad + f"    ACC[{m.group(1)}] = ACC[{m.group(1)}] + {m.group(2)}")
+            out.append(pad + "else:")
+            out.append(pad + f"    h[{m.group(3)}] = {m.group(2)}")
             continue
         if ln == "}":
             ind -= 1
             continue
         m = re.match(r"if \(CONTRACTED\) \{ (.+?) \+= (\w+); \} else \{ \1 = \2; \}$", ln)
         if m:
-            tgt = re.sub(r"\bS\[(\d+) \* nt\]", r"S[\1]", re.sub(r"\bh(\d+)\b", r"h[\1]", m.group(1)))
+            tgt = re.sub(r"\bS\[(\d+) \* kThreads\]", r"S[\1]", re.sub(r"\bh(\d+)\b", r"h[\1]", m.group(1)))
             out.append(pad + f"{tgt} = ({tgt} + {m.group(2)}) if CONTRACTED else {m.group(2)}")
             continue
         if ln.startswith("double F[") or ln.startswith("quartet_setup<") or ln.startswith("double h["):
@@ -75,15 +93,15 @@ def translate(src):
             continue
         if re.match(r"double& h\d+ = h\[\d+\];", ln):
             continue
-        m = re.match(r"for \(int s = 0; s < (\d+); \+\+s\) S\[s \* nt\] = 0\.0;$", ln)
+        m = re.match(r"for \(int s = 0; s < (\d+); \+\+s\) (S|ACC)[\[(]s(?: \* kThreads)?[\])] = 0\.0;$", ln)
         if m:
-            out.append(pad + f"for s in range({m.group(1)}): S[s] = 0.0")
+            out.append(pad + f"for s in range({m.group(1)}): {m.group(2)}[s] = 0.0")
             continue
         m = re.match(r"const double\* __restrict__ osc_ = kOutScale_\w+ \+ r \* (\d+);$", ln)
         if m:
             out.append(pad + f"osc_ = r * {m.group(1)}")
             continue
-        m = re.match(r"(?:const )?double\* __restrict__ (\w+) = S \+ \(long long\)(.+) \* nt;$", ln)
+        m = re.match(r"(?:const )?double\* __restrict__ (\w+) = S \+ (.+) \* kThreads;$", ln)
         if m:
             out.append(pad + f"{m.group(1)} = {m.group(2)}")
             continue
@@ -97,8 +115,9 @@ def translate(src):
             continue
         ln = ln.rstrip(";")
         ln = re.sub(r"^(const )?double ", "", ln)
-        ln = re.sub(r"\b(Hc|Gc|Gr|Xr|X)\[(\d+) \* nt\]", r"S[\1 + \2]", ln)
-        ln = re.sub(r"\bS\[(\d+) \* nt\]", r"S[\1]", ln)
+        ln = re.sub(r"\bACC\((\d+)\)", r"ACC[\1]", ln)
+        ln = re.sub(r"\b(Hc|Gc|Gr|Xr|X)\[(\d+) \* kThreads\]", r"S[\1 + \2]", ln)
+        ln = re.sub(r"\bS\[(\d+) \* kThreads\]", r"S[\1]", ln)
         ln = re.sub(r"\bh(\d+)\b", r"h[\1]", ln)
         ln = re.sub(r"__ldg\(osc_ \+ (\d+)\)", r"OSC[osc_ + \1]", ln)
         ln = re.sub(r"\bSMEM\((\d+)\)", r"SM[\1]", ln)
@@ -156,7 +175,7 @@ def osc_table(cls):
 def run_generated(src, cls, prims, Qns, contracted, shape, meta):
     code = translate(src)
     ns = {"fma": fma, "prims": prims, "Q": Qns, "CONTRACTED": contracted, "OUT": {},
-          "h": [0.0] * meta["ntargets"], "S": {}, "OSC": osc_table(cls), "SM": {}}
+          "h": [0.0] * meta["ntargets"], "S": {}, "OSC": osc_table(cls), "SM": {}, "ACC": {}}
     exec(compile(code, f"<gen {cls}>", "exec"), ns)
     nf = meta["nfunc"]
     blk = np.zeros(nf)
@@ -265,7 +284,7 @@ def test_coop_plan_reproduces_vrr_targets(cls):
     code = translate(src)
     # run only the primitive loop of the straight-line kernel to get h
     ns = {"fma": fma, "prims": prims, "Q": Qns, "CONTRACTED": True, "OUT": {}, "h": [0.0] * meta["ntargets"], "S": {},
-          "OSC": osc_table(cls), "SM": {}}
+          "OSC": osc_table(cls), "SM": {}, "ACC": {}}
     exec(compile(code, "<vrr>", "exec"), ns)
     from electron_repulsion_integrals_gb300.gen.graph import best_vrr
     g, _, _ = best_vrr(cls)
@@ -285,7 +304,7 @@ def test_coop_plan_reproduces_vrr_targets(cls):
         assert abs(got - ref) <= 1e-12 * max(1.0, abs(ref)), (e, f, got, ref)
 
 
-ABLATIONS = [dict(rule="alg1_literal"), dict(rule="bra_first_xyz"), dict(schedule="topo"), dict(sph_fusion=False),
+ABLATIONS = [dict(rule="axis_major"), dict(rule="bra_first_xyz"), dict(schedule="topo"), dict(sph_fusion=False),
              dict(sph_fusion=False, tier="staged"), dict(tier="staged"), dict(tier="reg")]
 
 
