@@ -32,7 +32,9 @@ static __device__ __align__(256) double g_noalloc_scratch[kNoallocDoubles];
 std::mutex g_mu;
 double* g_addr[64] = {nullptr};
 
-// Once per device, with that device current: the array's device address.
+// Once per device: the array's device address.  cudaGetSymbolAddress answers
+// for the current device, so `dev` must be the current device (the caller
+// checks this) and the address is kept under that device's index.
 int scratch_address(int dev, double** out) {
   if (dev < 0 || dev >= 64) return ERI_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lk(g_mu);
@@ -64,6 +66,14 @@ extern "C" int eri_compute_class_noalloc(eri_plan* p, int la, int lb, int lc, in
     if (!sph && l[k] >= 2) return ERI_ERR_UNSUPPORTED_L;
   }
   if (reinterpret_cast<uintptr_t>(quartets_dev) % 16 != 0) return ERI_ERR_INVALID_ARG;
+  // the kernels run on the current device with the plan's device pointers, and
+  // the scratch address below belongs to the current device: both must agree
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return ERI_ERR_CUDA;
+  }
+  if (cur != eri::host::plan_device(p)) return ERI_ERR_INVALID_ARG;
   int canon[4];
   eri::host::canonical_order(l, canon);
   const int cl[4] = {l[canon[0]], l[canon[1]], l[canon[2]], l[canon[3]]};
@@ -93,7 +103,7 @@ extern "C" int eri_compute_class_noalloc(eri_plan* p, int la, int lb, int lc, in
   (void)slots;
   if (n == 0) return ERI_OK;
   if (need > 0) {
-    rc = scratch_address(eri::host::plan_device(p), &scratch);
+    rc = scratch_address(cur, &scratch);
     if (rc) return rc;
   }
   EriLaunch P;
