@@ -1,7 +1,7 @@
 """Benchmark: ERI quartets/s and FP64 GFLOP/s per angular class on one GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload homogeneous|high_l|g_shells|deriv|cluster64|cluster200|cluster64_jk|cluster200_jk]
+                    [--workload homogeneous|high_l|g_shells|deriv|classes|cluster64|cluster200|cluster64_jk|cluster200_jk]
                     [--scale S] [--ablation all|NAME,...]
 
 A step is one pass of the hot path over the workload's batch: for every class
@@ -44,8 +44,9 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "ERI quartets/s and FP64 GFLOP/s per angular class (fraction of GB300 FP64 peak)"
-# FP64 pipe peak from unit counts and clock: 152 SMs x 2 DFMA/clk x 2 flop x 2.070 GHz
-FP64_PEAK_TFLOPS = 152 * 2 * 2 * 2.070e9 / 1e12
+# FP64 pipe rate from unit counts and clock (152 SMs x 2 DFMA/clk x 2 flop x
+# 2.070 GHz): used only when the measured probe is unavailable
+FP64_PEAK_NOMINAL_TFLOPS = 152 * 2 * 2 * 2.070e9 / 1e12
 E2E_CHUNK_BYTES = 0.75e9  # output bytes per e2e chunk: readback of one overlaps compute of the next
 
 WORKLOADS = {
@@ -60,6 +61,9 @@ WORKLOADS = {
     "deriv": {"desc": "first derivatives (12 blocks per quartet): (pp|pp) x 524,288 + (dd|dd) x 131,072 quartets, "
                       "degree 1, centers U[0,10]^3 bohr, exponents log-U[0.05,100], spherical",
               "classes": [((1, 1, 1, 1), 1 << 19, 1, 4), ((2, 2, 2, 2), 1 << 17, 1, 104)], "deriv": True},
+    "classes": {"desc": "every canonical class of s, p, d, f shells through (ff|ff) (55 classes), contraction "
+                        "degree 1 and 2, centers U[0,10]^3 bohr, exponents log-U[0.05,100], spherical; quartets per "
+                        "class sized to about 8 GFLOP per launch"},
     "cluster64": {"desc": "64-atom synthetic cluster (radius 12 bohr, 32 heavy 3s2p1d + 32 light 2s1p, 1-6 "
                           "primitives, exponents log-U[0.1,5000]): Coulomb J over all unique quartets surviving "
                           "Schwarz 1e-10, spherical, D = C C^T", "cluster": (64, 3)},
@@ -180,6 +184,51 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def measure_fp64_peak(dev, stream, gpu_index, target_s=1.0):
+    """FP64 pipe rate on this GPU: eri_fp64_fma_probe (independent FMA chains,
+    8 blocks of 256 threads per SM) timed with CUDA events on `stream`, SM clock
+    sampled meanwhile.  Returns TFLOP/s (2 flops per FMA) and the median clock."""
+    import torch
+    import electron_repulsion_integrals_gb300 as eri
+    nsm = torch.cuda.get_device_properties(dev).multi_processor_count
+    blocks, threads = nsm * 8, 256
+    sink = torch.empty(blocks * threads, dtype=torch.float64, device=dev)
+
+    def timed(iters, reps=1):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fmas = 0
+        for _ in range(reps):
+            fmas += eri.eri_fp64_fma_probe(blocks, threads, iters, sink, stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return fmas, e0.elapsed_time(e1)
+
+    timed(2000)
+    fmas, ms = timed(2000)
+    iters = int(min(4e6, max(2000, 2000 * (target_s / 4) / max(ms / 1e3, 1e-6))))
+    clocks = ClockSampler(gpu_index)
+    clocks.start()
+    time.sleep(0.3)
+    fmas, ms = timed(iters, 4)
+    clk = clocks.stop()
+    return {"tflops": 2 * fmas / (ms / 1e3) / 1e12, "sm_mhz": clk.get("sm_mhz"), "reasons": clk.get("reasons"),
+            "ms": ms, "fmas": fmas, "grid": f"{blocks} x {threads} threads, 8 FMA chains each"}
+
+
+def roofline_peak(probe, timed_mhz):
+    """The FP64 peak for a timed region: the probe's measured rate scaled from
+    its median SM clock to the region's, or the nominal figure without a probe."""
+    if not probe or not probe.get("tflops"):
+        return FP64_PEAK_NOMINAL_TFLOPS, "nominal FP64 pipe: 152 SMs x 2 DFMA/clk x 2 flop x 2.07 GHz"
+    p = probe["tflops"]
+    src = f"measured: eri_fp64_fma_probe {p:.4g} TFLOP/s"
+    if probe.get("sm_mhz") and timed_mhz:
+        p *= timed_mhz / probe["sm_mhz"]
+        src += f" at {probe['sm_mhz']:.0f} MHz, scaled to the timed region's {timed_mhz:.0f} MHz"
+    return p, src
+
+
 def cpu_oracle_rate(wl, budget_s=20.0, nthreads=None):
     """Oracle time per quartet for each class of the workload from a bounded
     sample; returns (quartets/s for the whole step mix, description, cores)."""
@@ -277,6 +326,7 @@ def run_coulomb(a, rank, world, local_rank):
         else:
             plan.build_J(Dd, J, stream)
 
+    probe = measure_fp64_peak(dev, stream, local_rank)
     for _ in range(a.warmup):
         digest()
     torch.cuda.synchronize()
@@ -313,6 +363,7 @@ def run_coulomb(a, rank, world, local_rank):
         flops += pq * st["vrr_flops"] + n * (st["hrr_flops"] + (12 if jk else 4) * eri.block_size(c))
         per_class["({}{}|{}{})".format(*c)] = {"quartets": n, "primitive_quartets": pq}
     ach = flops / (ms / a.steps / 1e3) / 1e12
+    peak, peak_src = roofline_peak(probe, clk.get("sm_mhz"))
     e2e = None
     if a.e2e:
         hD = torch.from_numpy(D).pin_memory()
@@ -345,9 +396,9 @@ def run_coulomb(a, rank, world, local_rank):
                        "plan_create_s": plan_s, "l2": "no flush: J digestion re-reads D; kernels are FP64-bound",
                        "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "alu", "kernel": "all class kernels of " + ("eri_build_JK" if jk else "eri_build_J"), "achieved": ach,
-                         "peak": FP64_PEAK_TFLOPS, "unit": "TFLOP/s", "frac": ach / FP64_PEAK_TFLOPS,
-                         "traffic": None, "peak_source": "FP64 pipe: 152 SMs x 2 DFMA/clk x 2 flop x 2.07 GHz"},
-            "clocks": clk, "e2e": e2e, "cpu_baseline": cpu,
+                         "peak": peak, "unit": "TFLOP/s", "frac": ach / peak,
+                         "traffic": None, "peak_source": peak_src},
+            "fp64_probe": probe, "clocks": clk, "e2e": e2e, "cpu_baseline": cpu,
             "gpu_launches": a.steps * (sum(1 for n in counts.values() if n) + (2 if jk else 1))}
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -436,6 +487,7 @@ def run_ours(a, rank, world, local_rank):
             if record is not None:
                 record[b["cls"]][1].record(stream)
 
+    probe = measure_fp64_peak(dev, stream, local_rank)
     for _ in range(max(a.warmup, 0)):
         step()
     torch.cuda.synchronize()
@@ -463,6 +515,7 @@ def run_ours(a, rank, world, local_rank):
     ms = t0.elapsed_time(t1)
     ms = max_over_ranks(ms, dist, dev)
     value = replica_rate(sum(b["n"] for b in batches), world, a.steps, ms)
+    peak, peak_src = roofline_peak(probe, clk.get("sm_mhz"))
 
     per_class = {}
     for b in batches:
@@ -470,7 +523,7 @@ def run_ours(a, rank, world, local_rank):
         tf = b["flops"] * b["n"] / (kms / 1e3) / 1e12
         per_class["({}{}|{}{})".format(*b["cls"])] = {
             "quartets_per_s": b["n"] / (kms / 1e3), "primitive_quartets_per_s": b["n"] * b["deg"] ** 4 / (kms / 1e3),
-            "ms_per_launch": kms, "fp64_gflops": tf * 1e3, "frac_fp64_peak": tf / FP64_PEAK_TFLOPS,
+            "ms_per_launch": kms, "fp64_gflops": tf * 1e3, "frac_fp64_peak": tf / peak,
             "flops_per_quartet": b["flops"], "tier": ["reg", "staged", "coop"][b["stats"]["staged"]]}
     dom = max(batches, key=lambda b: b["flops"] * b["n"])
     dname = "({}{}|{}{})".format(*dom["cls"])
@@ -558,11 +611,11 @@ def run_ours(a, rank, world, local_rank):
                        "l2": "no flush: inputs and outputs of a step exceed the 126 MB L2",
                        "parallelism": f"replicas x{world}"},
             "per_class": per_class,
-            "roofline": {"bound": "alu", "kernel": dname, "achieved": ach, "peak": FP64_PEAK_TFLOPS,
-                         "unit": "TFLOP/s", "frac": ach / FP64_PEAK_TFLOPS,
+            "roofline": {"bound": "alu", "kernel": dname, "achieved": ach, "peak": peak,
+                         "unit": "TFLOP/s", "frac": ach / peak,
                          "traffic": dram_traffic(dom["cls"], dom["n"], bool(wl.get("deriv"))),
-                         "peak_source": "FP64 pipe: 152 SMs x 2 DFMA/clk x 2 flop x 2.07 GHz"},
-            "clocks": clk, "e2e": e2e, "cpu_baseline": cpu,
+                         "peak_source": peak_src},
+            "fp64_probe": probe, "clocks": clk, "e2e": e2e, "cpu_baseline": cpu,
             "gpu_launches": len(batches) * a.steps}
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -570,6 +623,81 @@ def run_ours(a, rank, world, local_rank):
         b["plan"].close()
     if dist:
         dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------- every class
+def classes_n(fq, deg):
+    """Quartets per launch of a class in the per-class table: about 8 GFLOP of
+    algorithmic work, between 2,048 and 2^21 quartets."""
+    return int(min(1 << 21, max(2048, 8e9 / fq)))
+
+
+def run_classes(a, local_rank):
+    """Every canonical class through (ff|ff) at contraction degree 1 and 2: one
+    JSON line with quartets/s, FP64 GFLOP/s, fraction of the measured FP64
+    peak, tier, registers and ptxas spill bytes per class, each class checked
+    against the oracle on a sample."""
+    import torch
+    import oracle
+    import electron_repulsion_integrals_gb300 as eri
+    from electron_repulsion_integrals_gb300 import workloads as W
+    from electron_repulsion_integrals_gb300.gen.eri_gen import canonical_classes
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    eri.lib()
+    stream = torch.cuda.current_stream()
+    ptx = json.load(open(os.path.join(os.path.dirname(eri.LIB_PATH), "ptxas.json")))
+    probe = measure_fp64_peak(dev, stream, local_rank)
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    rows = {}
+    for cls in canonical_classes(3):
+        st = eri.eri_class_info(cls)
+        for deg in (1, 2):
+            fq = st["vrr_flops"] * deg ** 4 + st["hrr_flops"]
+            n = classes_n(fq, deg)
+            s, q = W.homogeneous(cls, n, deg, seed_index=300 + 10 * sum(cls) + deg)
+            plan = eri.Plan(s, spherical=True)
+            qd = torch.as_tensor(q, device=dev)
+            out = torch.empty(n * eri.block_size(cls), dtype=torch.float64, device=dev)
+            for _ in range(max(a.warmup, 1)):
+                eri.eri_compute_class(plan.handle, cls, qd, out, stream)
+            evs = []
+            for _ in range(a.steps):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                eri.eri_compute_class(plan.handle, cls, qd, out, stream)
+                e1.record(stream)
+                evs.append((e0, e1))
+            torch.cuda.synchronize()
+            ms = statistics.median(e0.elapsed_time(e1) for e0, e1 in evs)
+            idx = np.sort(np.random.default_rng(11).choice(n, 8, replace=False))
+            got = out.view(n, -1)[torch.as_tensor(idx, device=dev)].cpu().numpy().ravel()
+            ref = oracle.eri_blocks(oracle.ShellSet(s.centers, s.L, s.nprim, s.exps, s.coefs), q[idx],
+                                    spherical=True)
+            ok = bool(np.all(np.abs(got - ref) <= np.maximum(1e-12, 1e-10 * np.abs(ref))))
+            kern = [k for k in ptx if "k_c{}{}{}{}I".format(*cls) in k and "ILi0E" in k
+                    and ("Lb1E" in k) == (deg > 1)]
+            tf = fq * n / (ms / 1e3) / 1e12
+            rows["({}{}|{}{}) degree {}".format(*cls, deg)] = {
+                "quartets": n, "ms_per_launch": ms, "quartets_per_s": n / (ms / 1e3),
+                "primitive_quartets_per_s": n * deg ** 4 / (ms / 1e3), "fp64_gflops": tf * 1e3,
+                "flops_per_quartet": fq, "tier": ["reg", "staged", "coop"][st["staged"]], "parity_ok": ok,
+                "registers": max((ptx[k].get("registers", 0) for k in kern), default=None),
+                "spill_bytes": max((ptx[k].get("spill_stores", 0) + ptx[k].get("spill_loads", 0) for k in kern),
+                                   default=None)}
+            plan.close()
+            del out, qd
+            torch.cuda.empty_cache()
+    clk = clocks.stop()
+    peak, peak_src = roofline_peak(probe, clk.get("sm_mhz"))
+    for v in rows.values():
+        v["frac_fp64_peak"] = v["fp64_gflops"] / 1e3 / peak
+    line = {"metric": METRIC, "unit": "quartets/s", "workload": "classes", "steps": a.steps, "warmup": a.warmup,
+            "dtype": "f64", "data": "synthetic", "config": {"workload": WORKLOADS["classes"]["desc"]},
+            "peak": {"tflops": peak, "source": peak_src}, "fp64_probe": probe, "clocks": clk,
+            "all_parity_ok": all(v["parity_ok"] for v in rows.values()), "classes": rows}
+    print(json.dumps(line), flush=True)
 
 
 # ---------------------------------------------------------------- ablations
@@ -710,6 +838,9 @@ def main():
     local_rank = env_int("LOCAL_RANK", 0)
     if a.impl == "reference":
         run_reference(a, rank, world)
+    elif a.workload == "classes":
+        if rank == 0:
+            run_classes(a, local_rank)
     elif "cluster" in WORKLOADS[a.workload]:
         run_coulomb(a, rank, world, local_rank)
     else:

@@ -79,6 +79,8 @@ def lib():
         L.eri_plan_class_work.argtypes = [vp] + [ctypes.c_int] * 4 + [ctypes.POINTER(ctypes.c_longlong),
                                                                      ctypes.POINTER(ctypes.c_double)]
         L.eri_class_info.argtypes = [ctypes.c_int] * 4 + [ctypes.POINTER(ClassStats)]
+        L.eri_fp64_fma_probe.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_longlong, dp,
+                                         ctypes.POINTER(ctypes.c_longlong), vp]
         L.eri_status_string.argtypes = [ctypes.c_int]
         L.eri_status_string.restype = ctypes.c_char_p
         _lib = L
@@ -219,6 +221,14 @@ def eri_class_info(cls):
     s = ClassStats()
     _check("eri_class_info", lib().eri_class_info(*[int(x) for x in cls], ctypes.byref(s)))
     return {f: getattr(s, f) for f, _ in ClassStats._fields_}
+
+
+def eri_fp64_fma_probe(blocks, threads, iters, sink, stream=None):
+    """Launch the FP64 FMA-rate probe (see include/eri.h); returns the FMAs launched."""
+    fmas = ctypes.c_longlong()
+    _check("eri_fp64_fma_probe", lib().eri_fp64_fma_probe(int(blocks), int(threads), int(iters), _ptr(sink),
+                                                          ctypes.byref(fmas), ctypes.c_void_p(_stream_handle(stream))))
+    return fmas.value
 
 
 def nfunc(l, spherical=True):

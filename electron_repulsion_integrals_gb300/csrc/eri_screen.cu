@@ -44,9 +44,10 @@ namespace {
 // path (one FP64 instruction per dependent-latency interval, ~64 cycles) long
 // after the other threads are done.  Digestion is linear in the integrals, so
 // a quartet may be cut into parts that are transformed and scattered on their
-// own.  kThreadsPerClass: threads of one class launch (152 SMs x 256).
+// own.  kThreadsPerSM: resident threads of one class launch per SM (two
+// blocks of 128); a launch covers the plan's device, nsm of them.
 constexpr long long kMinPrimPerItem = 8;
-constexpr double kThreadsPerClass = 152.0 * 256.0;
+constexpr double kThreadsPerSM = 256.0;
 
 #define CUDA_TRY(x)                                                        \
   do {                                                                     \
@@ -440,7 +441,7 @@ int build(eri_plan* p, cudaStream_t st) {
           // class's average primitive quartets per thread, whichever is larger:
           // a class with work enough for every thread keeps its quartets whole
           // (each cut repeats the HRR, transform and scatter of the quartet).
-          const double per_thread = W.prim_total / (double)kThreadsPerClass;
+          const double per_thread = W.prim_total / (kThreadsPerSM * eri::host::plan_nsm(p));
           const long long pmax = std::max<long long>(kMinPrimPerItem, (long long)(0.5 * per_thread));
           for (size_t k = 0; k < segs.size(); ++k) {
             const long long Kb = kb_of[k], Kk = kk_of[k];

@@ -118,6 +118,13 @@ int eri_plan_nbf(const eri_plan* plan, int* nbf);
 int eri_plan_shell_info(const eri_plan* plan, int s, int* nfunc, int* first);
 
 /* Evaluate `n` shell quartets of class (la lb|lc ld) and store their blocks.
+ * Per quartet this is the body of FusionRCG Algorithm 2 (section III-C): over
+ * its primitive quartets the Gaussian products, the Boys base values
+ * [00|00]^(m) of section II-A and the vertical recurrence Eq. (2) (with its
+ * ket twin) into the accumulated [e0|f0] targets; then the horizontal
+ * recurrence Eq. (3) on the bra, the spherical transform of a and b, Eq. (13)
+ * on the ket and the transform of c and d -- the stepwise form Eq. (16) of the
+ * four-index transform Eq. (17) (section III-B).
  *   quartets_dev: device int32 array [n][4] of shell indices in the caller's
  *                 order; shell quartets[i][k] must have angular momentum
  *                 (la, lb, lc, ld)[k] (not checked on the device).
@@ -149,9 +156,11 @@ int eri_compute_class(eri_plan* plan, int la, int lb, int lc, int ld, const int*
  * eri_compute_class uses for the same class, hence lower throughput).
  *   - No cudaMalloc, cudaFree or allocating library routine is called.
  *     The plan must already exist (eri_plan_create allocates).
- *   - The first call on a device (with that device current) looks up the
- *     array's device address with cudaGetSymbolAddress; make that first call
- *     before any stream capture.
+ *   - Call it with the plan's device current (the device that was current
+ *     at eri_plan_create); another current device returns
+ *     ERI_ERR_INVALID_ARG.  The first call on a device looks up the array's
+ *     device address with cudaGetSymbolAddress; make that first call before
+ *     any stream capture.
  *   - Every call shares the one array per device and leaves its last contents
  *     in it; the kernels initialise every scratch slot they read within a
  *     call, so nothing needs clearing between calls.  Calls whose kernels
@@ -187,6 +196,8 @@ int eri_compute_class_deriv(eri_plan* plan, int la, int lb, int lc, int ld, cons
 int eri_schwarz(eri_plan* plan, int la, int lb, const int* pairs_dev, long long n, double* q_out_dev, void* stream);
 
 /* Coulomb matrix J_{mu nu} = sum_{lambda sigma} (mu nu|lambda sigma) D_{lambda sigma}
+ * (the scatter of each finished block into J with the density that ends
+ * FusionRCG Algorithm 2; section V-C builds J this way from the class batches)
  * over every unique shell quartet that passes Q_ab Q_cd >= schwarz_tau
  * (all of them when tau <= 0).  D_dev and J_dev are device nbf x nbf row-major
  * double matrices; D must be symmetric; J is overwritten (not accumulated) and
@@ -214,7 +225,10 @@ int eri_build_J(eri_plan* plan, const double* D_dev, double* J_dev, void* stream
 int eri_build_JK(eri_plan* plan, const double* D_dev, double* J_dev, double* K_dev, void* stream);
 
 /* Number of unique shell quartets of canonical class (la lb|lc ld) that
- * eri_build_J evaluates (after screening). */
+ * eri_build_J evaluates (after screening).  The Schwarz screen
+ * Q_ab Q_cd >= schwarz_tau and the primitive-pair pruning are this library's
+ * own: the page batches quartets by class (section V-C) but states no
+ * screening rule. */
 int eri_plan_quartet_count(const eri_plan* plan, int la, int lb, int lc, int ld, long long* n);
 
 /* Work of canonical class (la lb|lc ld) in eri_build_J: the number of unique
@@ -234,6 +248,17 @@ typedef struct {
   int staged;
 } eri_class_stats;
 int eri_class_info(int la, int lb, int lc, int ld, eri_class_stats* out);
+
+/* Measurement helper (not part of the method): launches `blocks` x `threads`
+ * threads that each run 8 independent chains of `iters` FP64 fused
+ * multiply-adds, and writes one double per thread to sink_dev (device memory
+ * of blocks*threads doubles, owned by the caller).  *fmas receives the number
+ * of FMAs launched (2 flops each).  Timing the launch on `stream` gives the
+ * FP64 pipe's rate, which bounds every class kernel: FusionRCG section II-B
+ * sizes its tiers by the GPU's FP64 and register resources, and this is the
+ * denominator of the library's fraction-of-peak figures.  threads must be a
+ * multiple of 32 and at most 256.  Errors: INVALID_ARG, CUDA. */
+int eri_fp64_fma_probe(int blocks, int threads, long long iters, double* sink_dev, long long* fmas, void* stream);
 
 /* Human-readable text for a status code (static storage). */
 const char* eri_status_string(int status);
