@@ -57,16 +57,17 @@ def axis_ket_first_zyx(e, f):
     return None
 
 
-def axis_alg1_literal(e, f):
-    """Algorithm 1 as printed: loop i = 0..2, the last matching axis wins,
-    ket beats bra only within one axis (axis-major)."""
-    axis = None
-    for i in range(3):
-        if f[i] > 0:
-            axis = ("ket", i)
-        elif e[i] > 0:
-            axis = ("bra", i)
-    return axis
+def axis_axis_major(e, f):
+    """The reading of section III-A's Algorithm 1 that puts the axis first:
+    the step goes along the highest axis (z over y over x) on which either
+    side still carries angular momentum, and only on that axis is the ket side
+    preferred to the bra.  (The section's text instead puts the ket side first
+    for every axis: axis_ket_first_zyx.)"""
+    live = [i for i in range(3) if e[i] > 0 or f[i] > 0]
+    if not live:
+        return None
+    i = max(live)
+    return ("ket", i) if f[i] > 0 else ("bra", i)
 
 
 def axis_bra_first_zyx(e, f):
@@ -91,7 +92,7 @@ def axis_bra_first_xyz(e, f):
     return None
 
 
-AXIS_RULES = {"ket_first_zyx": axis_ket_first_zyx, "alg1_literal": axis_alg1_literal,
+AXIS_RULES = {"ket_first_zyx": axis_ket_first_zyx, "axis_major": axis_axis_major,
               "bra_first_zyx": axis_bra_first_zyx, "bra_first_xyz": axis_bra_first_xyz}
 
 
