@@ -1,9 +1,12 @@
 """GPU Coulomb matrix and Schwarz screen against the CPU oracle.
 
 J must match within 1e-10 relative Frobenius error.  Small clusters are checked
-against the oracle's full J; the 64-atom cluster (the benchmark's cluster
-workload) against oracle J blocks computed one by one from the definition.
+against the oracle's full J computed in the test; the 64-atom cluster against
+the oracle's whole J and K and the 200-atom cluster against oracle blocks of J
+and K, both stored under tests/golden by make_cluster_goldens.py.
 """
+
+import os
 
 import numpy as np
 import pytest
@@ -66,52 +69,95 @@ def test_J_unscreened_equals_full_sum(dev):
     plan.close()
 
 
-def test_J_64_atom_cluster_sampled_blocks(dev):
+def _golden(name, s, D):
+    """Stored oracle values (tests/golden/make_cluster_goldens.py) after a check
+    that they were made from these inputs."""
+    import importlib.util
+    import json
+    gdir = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+    spec = importlib.util.spec_from_file_location("make_cluster_goldens", os.path.join(gdir, "make_cluster_goldens.py"))
+    mk = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mk)
+    z = np.load(os.path.join(gdir, name), allow_pickle=False)
+    meta = json.loads(str(z["meta"]))
+    want, have = meta["fingerprint"], mk.fingerprint(s, D)
+    for k, v in want.items():
+        if isinstance(v, int):
+            assert have[k] == v, (name, k, have[k], v)
+        else:
+            assert abs(have[k] - v) <= 1e-12 * max(1.0, abs(v)), (name, k, have[k], v)
+    return z, meta
+
+
+def _symmetric_from_upper(u, n):
+    M = np.zeros((n, n))
+    iu = np.triu_indices(n)
+    M[iu] = u
+    M.T[iu] = u
+    return M
+
+
+def test_J_and_K_64_atom_cluster_whole_matrix(dev):
+    """The 64-atom workload: eri_build_J's J and eri_build_JK's J and K against
+    the oracle's whole matrices, 1e-10 relative Frobenius."""
     s = W.cluster64()
     nbf = W.nbf(s)
     D = W.density(nbf, 3)
+    z, meta = _golden("cluster64_JK.npz", s, D)
+    Jref = _symmetric_from_upper(z["J_upper"], nbf)
+    Kref = _symmetric_from_upper(z["K_upper"], nbf)
     plan, J = gpu_J(s, D, 1e-10, dev)
-    S = oshells(s)
-    nf = np.array([eri.nfunc(l) for l in s.L])
-    fo = np.concatenate([[0], np.cumsum(nf)])
-    rng = np.random.default_rng(11)
-    heavy_d = [i for i in range(s.n) if s.L[i] == 2]
-    pairs = [(heavy_d[0], heavy_d[0]), (int(rng.integers(s.n)), int(rng.integers(s.n))),
-             (heavy_d[-1], 0)]
-    Q = oracle.schwarz(S, True)
-    blocks = oracle.J_blocks(S, D, pairs, spherical=True, tau=1e-10, Q=Q)
-    for (a, b), B in zip(pairs, blocks):
-        G = J[fo[a]:fo[a + 1], fo[b]:fo[b + 1]]
-        assert np.linalg.norm(G - B) <= 1e-10 * max(np.linalg.norm(B), 1e-3), (a, b, np.abs(G - B).max())
+    assert rel_frob(J, Jref) <= 1e-10, rel_frob(J, Jref)
     assert np.allclose(J, J.T, rtol=0, atol=1e-12 * np.abs(J).max())
-    # Tr(D J) = vec(D)^T ERI vec(D) >= 0 for the PSD density
-    assert np.sum(D * J) > 0
+    assert np.sum(D * J) > 0  # Tr(D J) = vec(D)^T ERI vec(D) >= 0 for the PSD density
+    Jd, Kd = plan.build_JK(torch.as_tensor(D, device=dev))
+    torch.cuda.synchronize()
+    J2, K = Jd.cpu().numpy(), Kd.cpu().numpy()
+    assert rel_frob(J2, Jref) <= 1e-10, rel_frob(J2, Jref)
+    assert rel_frob(K, Kref) <= 1e-10, rel_frob(K, Kref)
     plan.close()
 
 
-def test_JK_200_atom_cluster_sampled_blocks(dev):
-    """The 200-atom workload at full size through the fused J+K pass: sampled J
-    and K blocks against the oracle (the fused J equals eri_build_J's, checked
-    on small clusters in test_gpu_exchange.py)."""
+def _blocks_of(M, pairs, fo):
+    return [M[fo[a]:fo[a + 1], fo[b]:fo[b + 1]] for a, b in pairs]
+
+
+def _split(values, pairs, nf):
+    out, o = [], 0
+    for a, b in pairs:
+        k = nf[a] * nf[b]
+        out.append(values[o:o + k].reshape(nf[a], nf[b]))
+        o += k
+    return out
+
+
+def test_J_and_K_200_atom_cluster_sampled_blocks(dev):
+    """The 200-atom workload at full size: eri_build_J and eri_build_JK, each
+    over all 3.6e9 screened quartets, against oracle blocks stratified over the
+    six (l_a, l_b) pair classes and over distance (120 J blocks, 60 K blocks).
+    The sampled blocks together must match within 1e-10 relative Frobenius, and
+    each block within 1e-10 of its own norm (floored at 1e-6 of the sample's)."""
     s = W.cluster200()
     nbf = W.nbf(s)
     D = W.density(nbf, 4)
-    plan = eri.Plan(s, spherical=True, schwarz_tau=1e-10)
-    Jd, Kd = plan.build_JK(torch.as_tensor(D, device=dev))
-    torch.cuda.synchronize()
-    J, K = Jd.cpu().numpy(), Kd.cpu().numpy()
-    S = oshells(s)
+    z, meta = _golden("cluster200_blocks.npz", s, D)
     nf = np.array([eri.nfunc(l) for l in s.L])
     fo = np.concatenate([[0], np.cumsum(nf)])
-    d_shells = [i for i in range(s.n) if s.L[i] == 2]
-    dsh = d_shells[len(d_shells) // 2]
-    pairs = [(dsh, dsh - 5)]  # a d shell and an s shell of the same atom
-    Q = oracle.schwarz(S, True)
-    for M, blocks in ((J, oracle.J_blocks(S, D, pairs, spherical=True, tau=1e-10, Q=Q)),
-                      (K, oracle.K_blocks(S, D, pairs, spherical=True, tau=1e-10, Q=Q))):
-        for (a, b), B in zip(pairs, blocks):
-            G = M[fo[a]:fo[a + 1], fo[b]:fo[b + 1]]
-            assert np.linalg.norm(G - B) <= 1e-10 * max(np.linalg.norm(B), 1e-3), (a, b, np.abs(G - B).max())
+    plan = eri.Plan(s, spherical=True, schwarz_tau=1e-10)
+    Dd = torch.as_tensor(D, device=dev)
+    J = plan.build_J(Dd).cpu().numpy()
+    Jd, Kd = plan.build_JK(Dd)
+    torch.cuda.synchronize()
+    J2, K = Jd.cpu().numpy(), Kd.cpu().numpy()
+    plan.close()
+    jp, kp = z["J_pairs"], z["K_pairs"]
+    Jb, Kb = _split(z["J_values"], jp, nf), _split(z["K_values"], kp, nf)
+    for name, M, pairs, ref in (("J", J, jp, Jb), ("J of J+K", J2, jp, Jb), ("K", K, kp, Kb)):
+        got = _blocks_of(M, pairs, fo)
+        err = np.sqrt(sum(np.sum((g - r) ** 2) for g, r in zip(got, ref)))
+        norm = np.sqrt(sum(np.sum(r ** 2) for r in ref))
+        assert err <= 1e-10 * norm, (name, err / norm)
+        for (a, b), g, r in zip(pairs, got, ref):
+            assert np.linalg.norm(g - r) <= 1e-10 * max(np.linalg.norm(r), 1e-6 * norm), (name, a, b)
         assert np.allclose(M, M.T, rtol=0, atol=1e-12 * np.abs(M).max())
         assert np.sum(D * M) > 0
-    plan.close()
