@@ -214,28 +214,29 @@ def test_both_tiers_agree(shape, monkeypatch):
     assert np.allclose(got, ref, rtol=1e-10, atol=1e-13)
 
 
-def emulate_coop(cls, prims):
+def emulate_coop(cls, prims, dtype=np.float64):
     """Run the cooperative tier's VRR plan (tables as the kernel reads them) on
     the CPU; returns the accumulators H[target column][e - e_la]."""
     from electron_repulsion_integrals_gb300.gen import coop
     P = coop.plan(cls)
-    return emulate_coop_plan(P, prims)[0], P
+    return emulate_coop_plan(P, prims, dtype=dtype)[0], P
 
 
-def emulate_coop_plan(P, prims, weights=None):
+def emulate_coop_plan(P, prims, weights=None, dtype=np.float64):
     """The column-step VRR of plan P over the primitive quartets; returns the
     accumulator sets [set][target column][e - e_lo]: set 0 plain, set w the
-    targets weighted by weights(prim)[w - 1]."""
+    targets weighted by weights(prim)[w - 1].  dtype: the arithmetic's type
+    (np.longdouble to run the same steps in extended precision)."""
     NE, L, La, Lc = P.NE, P.L, P.La, P.Lc
     NET = NE - P.ie_lo
     nw = 0 if weights is None else len(weights(prims[0]))
-    Hs = np.zeros((1 + nw, len(P.f_targets), NET))
+    Hs = np.zeros((1 + nw, len(P.f_targets), NET), dtype=dtype)
     col0_target = tuple(P.f_targets[0]) == (0, 0, 0)
     for prim in prims:
         pb, pk, qs, F = prim
         wts = [1.0] + (list(weights(prim)) if nw else [])
-        H = np.zeros((len(P.f_targets), NET))
-        A = np.zeros(max(P.arena, 1) + 4 * NE)
+        H = np.zeros((len(P.f_targets), NET), dtype=dtype)
+        A = np.zeros(max(P.arena, 1) + 4 * NE, dtype=dtype)
         PA, QC = pb.PA, pk.PA
         WP = [qs.roz * x for x in qs.PQ]
         WQ = [-qs.roe * x for x in qs.PQ]
@@ -455,14 +456,14 @@ def test_generated_derivative_class_matches_oracle(cls):
         assert worst <= 0, (cls, nprim, float(np.max(np.abs(got - ref))), float(m))
 
 
-def emulate_coop_hrr(cls, prims, Qns, rb, rk):
+def emulate_coop_hrr(cls, prims, Qns, rb, rk, dtype=np.float64):
     """The cooperative kernel's HRR stage on the CPU: the generated bra (one
     call per ket column) and ket (one call per bra row) functions, normal or
     reversed, over the emulated VRR accumulators; returns the spherical block
-    in canonical order."""
+    in canonical order (arithmetic in dtype)."""
     from electron_repulsion_integrals_gb300.gen import coop as CP
     src, meta = CP.emit_coop_class(cls)
-    H, P = emulate_coop(cls, prims)
+    H, P = emulate_coop(cls, prims, dtype)
     cname = E.class_name(cls)
     bra = f"bra_hrr_rev_{cname}" if rb else f"bra_hrr_{cname}"
     ket = f"ket_hrr_rev_{cname}" if rk else f"ket_hrr_{cname}"
@@ -473,14 +474,14 @@ def emulate_coop_hrr(cls, prims, Qns, rb, rk):
     fi_lc = int(re.search(r"FI_LC = (\d+)", src).group(1))
     nr = int(re.search(r"NR = (\d+)", src).group(1))
     NF = H.shape[0]
-    G = _Ptr(np.zeros(int(re.search(r"ARENA = (\d+)", src).group(1))))
+    G = _Ptr(np.zeros(int(re.search(r"ARENA = (\d+)", src).group(1)), dtype=dtype))
     Q = types.SimpleNamespace(AB=Qns.AB, CD=Qns.CD)
     for fi in range(0 if rk else fi_lc, NF):
         ns[bra](Q, _Ptr(H.reshape(-1)), fi, G)
     for r in range(nr):
         ns[ket](None, Q, 0, r, G)
     nf = [2 * l + 1 if l >= 2 else (l + 1) * (l + 2) // 2 for l in cls]
-    blk = np.zeros(nf)
+    blk = np.zeros(nf, dtype=dtype)
     for k, v in out.items():
         blk[k] = v
     return blk, len(out)
