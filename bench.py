@@ -184,8 +184,8 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def measure_fp64_peak(dev, stream, gpu_index, target_s=1.0):
-    """FP64 pipe rate on this GPU: eri_fp64_fma_probe (independent FMA chains,
+def measure_fp64_peak(dev, stream, gpu_index, target_s=0.4):
+    """FP64 pipe rate on this GPU: eri_fp64_probe (independent FMA chains,
     8 blocks of 256 threads per SM) timed with CUDA events on `stream`, SM clock
     sampled meanwhile.  Returns TFLOP/s (2 flops per FMA) and the median clock."""
     import torch
@@ -199,7 +199,7 @@ def measure_fp64_peak(dev, stream, gpu_index, target_s=1.0):
         e0.record(stream)
         fmas = 0
         for _ in range(reps):
-            fmas += eri.eri_fp64_fma_probe(blocks, threads, iters, sink, stream)
+            fmas += eri.eri_fp64_probe("fma", blocks, threads, iters, sink, stream)
         e1.record(stream)
         torch.cuda.synchronize()
         return fmas, e0.elapsed_time(e1)
@@ -216,13 +216,53 @@ def measure_fp64_peak(dev, stream, gpu_index, target_s=1.0):
             "ms": ms, "fmas": fmas, "grid": f"{blocks} x {threads} threads, 8 FMA chains each"}
 
 
+def run_fp64_peak(a, local_rank):
+    """The FP64 probe over launch shapes (threads per block x blocks per SM,
+    8 independent chains per thread) and, at one shape, FMA vs MUL vs ADD:
+    one JSON line with the rates (G operations/s) and the SM clock."""
+    import torch
+    import electron_repulsion_integrals_gb300 as eri
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    eri.lib()
+    stream = torch.cuda.current_stream()
+    nsm = torch.cuda.get_device_properties(dev).multi_processor_count
+    sink = torch.empty(nsm * 2048, dtype=torch.float64, device=dev)
+
+    def rate(op, threads, bps, target_ops=1.5e11):
+        blocks = nsm * bps
+        iters = int(target_ops / (blocks * threads * 8))
+        eri.eri_fp64_probe(op, blocks, threads, 100, sink, stream)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        n = eri.eri_fp64_probe(op, blocks, threads, iters, sink, stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return n / (e0.elapsed_time(e1) / 1e3) / 1e9
+
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    shapes = {}
+    for threads in (64, 128, 256, 512):
+        for bps in (1, 2, 4, 8):
+            if threads * bps <= 2048:
+                shapes[f"{threads}x{bps}"] = rate("fma", threads, bps)
+    ops = {op: rate(op, 256, 4) for op in ("fma", "mul", "add")}
+    clk = clocks.stop()
+    best = max(shapes.values())
+    print(json.dumps({"metric": "FP64 pipe rate (eri_fp64_probe)", "unit": "G operations/s", "nsm": nsm,
+                      "fma_by_shape_threads_x_blocks_per_sm": shapes, "by_op_256x4": ops,
+                      "peak_tflops": 2 * best / 1e3, "clocks": clk}), flush=True)
+
+
 def roofline_peak(probe, timed_mhz):
     """The FP64 peak for a timed region: the probe's measured rate scaled from
     its median SM clock to the region's, or the nominal figure without a probe."""
     if not probe or not probe.get("tflops"):
         return FP64_PEAK_NOMINAL_TFLOPS, "nominal FP64 pipe: 152 SMs x 2 DFMA/clk x 2 flop x 2.07 GHz"
     p = probe["tflops"]
-    src = f"measured: eri_fp64_fma_probe {p:.4g} TFLOP/s"
+    src = f"measured: eri_fp64_probe (FMA chains) {p:.4g} TFLOP/s"
     if probe.get("sm_mhz") and timed_mhz:
         p *= timed_mhz / probe["sm_mhz"]
         src += f" at {probe['sm_mhz']:.0f} MHz, scaled to the timed region's {timed_mhz:.0f} MHz"
@@ -676,8 +716,10 @@ def run_classes(a, local_rank):
             ref = oracle.eri_blocks(oracle.ShellSet(s.centers, s.L, s.nprim, s.exps, s.coefs), q[idx],
                                     spherical=True)
             ok = bool(np.all(np.abs(got - ref) <= np.maximum(1e-12, 1e-10 * np.abs(ref))))
+            # the cooperative tier is built only as its contracted instantiation
+            contracted = deg > 1 or st["staged"] == 2
             kern = [k for k in ptx if "k_c{}{}{}{}I".format(*cls) in k and "ILi0E" in k
-                    and ("Lb1E" in k) == (deg > 1)]
+                    and ("Lb1E" in k) == contracted]
             tf = fq * n / (ms / 1e3) / 1e12
             rows["({}{}|{}{}) degree {}".format(*cls, deg)] = {
                 "quartets": n, "ms_per_launch": ms, "quartets_per_s": n / (ms / 1e3),
@@ -826,12 +868,17 @@ def main():
     ap.add_argument("--ref-budget", type=float, default=12.0, help="seconds of oracle work per sample")
     ap.add_argument("--ablation", default=None, help="'all' or comma-separated ablation libraries to time")
     ap.add_argument("--ablation-worker", default=None, help=argparse.SUPPRESS)
+    ap.add_argument("--fp64-peak", action="store_true", help="sweep the FP64 rate probe and print its rates")
     a = ap.parse_args()
     if a.ablation_worker:
         run_ablation_worker(a)
         return
     if a.ablation:
         run_ablation(a)
+        return
+    if a.fp64_peak:
+        if env_int("RANK", 0) == 0:
+            run_fp64_peak(a, env_int("LOCAL_RANK", 0))
         return
     rank = env_int("RANK", 0)
     world = env_int("WORLD_SIZE", 1)

@@ -79,8 +79,8 @@ def lib():
         L.eri_plan_class_work.argtypes = [vp] + [ctypes.c_int] * 4 + [ctypes.POINTER(ctypes.c_longlong),
                                                                      ctypes.POINTER(ctypes.c_double)]
         L.eri_class_info.argtypes = [ctypes.c_int] * 4 + [ctypes.POINTER(ClassStats)]
-        L.eri_fp64_fma_probe.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_longlong, dp,
-                                         ctypes.POINTER(ctypes.c_longlong), vp]
+        L.eri_fp64_probe.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_longlong, dp,
+                                     ctypes.POINTER(ctypes.c_longlong), vp]
         L.eri_status_string.argtypes = [ctypes.c_int]
         L.eri_status_string.restype = ctypes.c_char_p
         _lib = L
@@ -223,12 +223,16 @@ def eri_class_info(cls):
     return {f: getattr(s, f) for f, _ in ClassStats._fields_}
 
 
-def eri_fp64_fma_probe(blocks, threads, iters, sink, stream=None):
-    """Launch the FP64 FMA-rate probe (see include/eri.h); returns the FMAs launched."""
-    fmas = ctypes.c_longlong()
-    _check("eri_fp64_fma_probe", lib().eri_fp64_fma_probe(int(blocks), int(threads), int(iters), _ptr(sink),
-                                                          ctypes.byref(fmas), ctypes.c_void_p(_stream_handle(stream))))
-    return fmas.value
+FP64_PROBE_OPS = {"fma": 0, "mul": 1, "add": 2}
+
+
+def eri_fp64_probe(op, blocks, threads, iters, sink, stream=None):
+    """Launch the FP64 rate probe (see include/eri.h) for op "fma", "mul" or
+    "add"; returns the number of operations launched."""
+    n = ctypes.c_longlong()
+    _check("eri_fp64_probe", lib().eri_fp64_probe(FP64_PROBE_OPS[op], int(blocks), int(threads), int(iters),
+                                                  _ptr(sink), ctypes.byref(n), ctypes.c_void_p(_stream_handle(stream))))
+    return n.value
 
 
 def nfunc(l, spherical=True):

@@ -1,12 +1,13 @@
-// eri_fp64_fma_probe: a kernel that only issues independent FP64 fused
-// multiply-adds, to measure the rate of the FP64 pipe that bounds every class
-// kernel of this library (the roofline denominator of its throughput figures).
+// eri_fp64_probe: a kernel that only issues independent FP64 operations, to
+// measure the rate of the FP64 pipe that bounds every class kernel of this
+// library (the roofline denominator of its throughput figures).
 //
-// Each thread runs kChains independent recurrences x <- x * a + b with |a| < 1,
-// so the values stay bounded and no chain waits on another: with enough warps
-// per SM the pipe, not latency, sets the time.  One FMA counts 2 flops; a
-// launch performs blocks x threads x iters x kChains FMAs.  The chains' sum is
-// written to sink (one double per thread) so that the compiler keeps the work.
+// Each thread runs kChains independent recurrences -- x <- x * a + b (fused
+// multiply-add), x <- x * a or x <- x + b -- with |a| < 1 and b small, so the
+// values stay bounded and no chain waits on another: with enough warps per SM
+// the pipe, not latency, sets the time.  A launch performs
+// blocks x threads x iters x kChains operations.  The chains' sum is written to
+// sink (one double per thread) so that the compiler keeps the work.
 #include <cuda_runtime.h>
 
 #include "../../include/eri.h"
@@ -15,13 +16,18 @@ namespace {
 
 constexpr int kChains = 8;
 
-__global__ void __launch_bounds__(256) fp64_fma_chains(long long iters, double a, double b, double* __restrict__ sink) {
+template <int OP>
+__global__ void __launch_bounds__(512) fp64_chains(long long iters, double a, double b, double* __restrict__ sink) {
   double x[kChains];
 #pragma unroll
   for (int c = 0; c < kChains; ++c) x[c] = 1.0 + 0.125 * c + 1e-3 * (threadIdx.x & 7);
   for (long long i = 0; i < iters; ++i) {
 #pragma unroll
-    for (int c = 0; c < kChains; ++c) x[c] = fma(x[c], a, b);
+    for (int c = 0; c < kChains; ++c) {
+      if constexpr (OP == 0) x[c] = fma(x[c], a, b);
+      if constexpr (OP == 1) x[c] = x[c] * a;
+      if constexpr (OP == 2) x[c] = x[c] + b;
+    }
   }
   double s = 0.0;
 #pragma unroll
@@ -31,11 +37,15 @@ __global__ void __launch_bounds__(256) fp64_fma_chains(long long iters, double a
 
 }  // namespace
 
-extern "C" int eri_fp64_fma_probe(int blocks, int threads, long long iters, double* sink_dev, long long* fmas,
-                                  void* stream) {
-  if (blocks <= 0 || threads <= 0 || threads > 256 || threads % 32 != 0 || iters <= 0 || !sink_dev || !fmas)
+extern "C" int eri_fp64_probe(int op, int blocks, int threads, long long iters, double* sink_dev, long long* ops,
+                              void* stream) {
+  if (op < 0 || op > 2 || blocks <= 0 || threads <= 0 || threads > 512 || threads % 32 != 0 || iters <= 0 ||
+      !sink_dev || !ops)
     return ERI_ERR_INVALID_ARG;
-  *fmas = (long long)blocks * threads * iters * kChains;
-  fp64_fma_chains<<<blocks, threads, 0, (cudaStream_t)stream>>>(iters, 0.9999999, 1e-7, sink_dev);
+  *ops = (long long)blocks * threads * iters * kChains;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (op == 0) fp64_chains<0><<<blocks, threads, 0, st>>>(iters, 0.9999999, 1e-7, sink_dev);
+  if (op == 1) fp64_chains<1><<<blocks, threads, 0, st>>>(iters, 0.9999999, 1e-7, sink_dev);
+  if (op == 2) fp64_chains<2><<<blocks, threads, 0, st>>>(iters, 0.9999999, 1e-7, sink_dev);
   return cudaGetLastError() == cudaSuccess ? ERI_OK : ERI_ERR_CUDA;
 }

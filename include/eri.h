@@ -250,15 +250,16 @@ typedef struct {
 int eri_class_info(int la, int lb, int lc, int ld, eri_class_stats* out);
 
 /* Measurement helper (not part of the method): launches `blocks` x `threads`
- * threads that each run 8 independent chains of `iters` FP64 fused
- * multiply-adds, and writes one double per thread to sink_dev (device memory
- * of blocks*threads doubles, owned by the caller).  *fmas receives the number
- * of FMAs launched (2 flops each).  Timing the launch on `stream` gives the
- * FP64 pipe's rate, which bounds every class kernel: FusionRCG section II-B
- * sizes its tiers by the GPU's FP64 and register resources, and this is the
+ * threads that each run 8 independent chains of `iters` FP64 operations --
+ * op 0: fused multiply-adds (2 flops each), 1: multiplies, 2: additions --
+ * and writes one double per thread to sink_dev (device memory of
+ * blocks*threads doubles, owned by the caller).  *ops receives the number of
+ * operations launched.  Timing the launch on `stream` gives the FP64 pipe's
+ * rate, which bounds every class kernel: FusionRCG section II-B sizes its
+ * tiers by the GPU's FP64 and register resources, and this rate is the
  * denominator of the library's fraction-of-peak figures.  threads must be a
- * multiple of 32 and at most 256.  Errors: INVALID_ARG, CUDA. */
-int eri_fp64_fma_probe(int blocks, int threads, long long iters, double* sink_dev, long long* fmas, void* stream);
+ * multiple of 32 and at most 512.  Errors: INVALID_ARG, CUDA. */
+int eri_fp64_probe(int op, int blocks, int threads, long long iters, double* sink_dev, long long* ops, void* stream);
 
 /* Human-readable text for a status code (static storage). */
 const char* eri_status_string(int status);
