@@ -30,7 +30,8 @@ constexpr int kCoopBatch = 4;                 // primitive quartets set up at on
 //   14.. k/(2 zeta) for k = 1..La, then k/(2 eta) for k = 1..Lc, then
 //   k/(2(zeta+eta)) for k = 0..max(La, Lc), then F'_0..F'_L.
 //   With NW > 0 (derivative classes) NW accumulation weights follow:
-//   2 alpha, 2 beta, 2 gamma of the primitive quartet's A, B, C primitives.
+//   2 alpha, 2 beta, 2 gamma, 2 delta of the primitive quartet's A, B, C, D
+//   primitives.
 template <int La, int Lc, int NW = 0>
 struct CoopSetup {
   static constexpr int L = La + Lc;
@@ -84,6 +85,7 @@ __device__ __forceinline__ void coop_setup_one(const EriLaunch& P, const Quartet
       s[S::WGT + 1] = 2.0 * __ldg(P.sh.exps + Q.pb + j);
       s[S::WGT + 2] = 2.0 * __ldg(P.sh.exps + Q.pc + k);
     }
+    if constexpr (NW > 3) s[S::WGT + 3] = 2.0 * __ldg(P.sh.exps + Q.pd + l);
   }
   QuartetSetup qs;
   double F[S::L + 1];

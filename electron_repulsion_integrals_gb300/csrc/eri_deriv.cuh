@@ -3,15 +3,17 @@
 // For a primitive Cartesian Gaussian, d/dA_i [x_A^{a_i} ... e^{-alpha r_A^2}]
 // = 2 alpha (a + 1_i) - a_i (a - 1_i).  The derivative kernels therefore run
 // the cooperative tier's VRR for the class extended by one on the bra and on
-// the ket, and accumulate four sets of targets per contracted quartet: plain,
-// and weighted by 2 alpha, 2 beta, 2 gamma (exponents of the A, B, C
-// primitives).  The generated HRR functions then form, per ket column,
+// the ket, and accumulate five sets of targets per contracted quartet: plain,
+// and weighted by 2 alpha, 2 beta, 2 gamma, 2 delta (exponents of the A, B, C,
+// D primitives).  The generated HRR functions then form, per ket column,
 //   d/dA_i: (a+1_i b| from the 2 alpha set minus a_i (a-1_i b| from the plain set,
 //   d/dB_i: (a b+1_i| from the 2 beta set  minus b_i (a b-1_i| from the plain set,
 // transform them to spherical form, and run the ket HRR + transform; d/dC_i
-// combines (c+1_i d) from the 2 gamma set with c_i (c-1_i d) in the ket step.
-// d/dD = -(d/dA + d/dB + d/dC) (translation invariance).  Output per quartet:
-// 12 blocks, [requested position of the shell 0..3][axis x, y, z][block].
+// combines (c+1_i d) from the 2 gamma set with c_i (c-1_i d), and d/dD_i
+// (c d+1_i) from the 2 delta set with d_i (c d-1_i), in the ket step.  Each
+// block is formed on its own (no block is the difference of the others).
+// Output per quartet: 12 blocks, [requested position of the shell 0..3]
+// [axis x, y, z][block].
 #pragma once
 
 #include "eri_coop.cuh"
@@ -26,14 +28,15 @@ __device__ __forceinline__ double* deriv_out(const EriLaunch& P, const Quartet& 
 
 }  // namespace eri
 
-// Kernel of one derivative class.  C: traits (NW = 3; LANES lanes per
+// Kernel of one derivative class.  C: traits (NW = 4; LANES lanes per
 // quartet, GROUPS quartets per block); BRA_A / BRA_B fill the three axis sets
-// of d/dA / d/dB rows, BRA_0G the plain and 2-gamma rows;
+// of d/dA / d/dB rows, BRA_0G the plain, 2-gamma and 2-delta rows;
 // KET_AB(P, Q, q, r, x, G, k) writes row r of d/d(slot k) along axis x from
-// row set x, KET_C(P, Q, q, r, G) writes row r of d/dC for the three axes.
-#define ERI_DERIV_KERNEL(NAME, C, BRA_A, BRA_B, BRA_0G, KET_AB, KET_C)                                   \
+// row set x, KET_C(P, Q, q, r, G) / KET_D(P, Q, q, r, G) write row r of d/dC /
+// d/dD for the three axes.
+#define ERI_DERIV_KERNEL(NAME, C, BRA_A, BRA_B, BRA_0G, KET_AB, KET_C, KET_D)                            \
   template <bool CONTRACTED>                                                                              \
-  __global__ void __launch_bounds__(C::THREADS) NAME(const EriLaunch P) {                                 \
+  __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS) NAME(const EriLaunch P) {                                 \
     extern __shared__ double smem_[];                                                                     \
     using S_ = CoopSetup<C::La, C::Lc, C::NW>;                                                            \
     constexpr int LN_ = C::LANES;                                                                         \
@@ -74,14 +77,17 @@ __device__ __forceinline__ double* deriv_out(const EriLaunch& P, const Quartet& 
       coop_sync<LN_>();                                                                                   \
       for (int fi = lane; fi < C::NF; fi += LN_) BRA_0G(Q, H, fi, G);                                     \
       coop_sync<LN_>();                                                                                   \
-      for (int r = lane; r < C::NR; r += LN_) KET_C(P, Q, q, r, G);                                       \
+      for (int r = lane; r < C::NR; r += LN_) {                                                           \
+        KET_C(P, Q, q, r, G);                                                                             \
+        KET_D(P, Q, q, r, G);                                                                             \
+      }                                                                                                   \
       coop_sync<LN_>();                                                                                   \
     }                                                                                                     \
   }
 
 #define ERI_DERIV_SMEM_(T) ((size_t)(T::GROUPS) * (T::WARP_SMEM) * sizeof(double))
 // Per-class entry points: launch (store mode, contracted or not), grid and
-// scratch sizing (four accumulator sets per group of lanes).
+// scratch sizing (NW + 1 accumulator sets per group of lanes).
 #define ERI_DEFINE_DERIV_LAUNCHER(LA, LB, LC, LD, KERNEL, T)                                             \
   extern "C" int eri_dlaunch_c##LA##LB##LC##LD(const EriLaunch* P, int contracted, int blocks, cudaStream_t st) { \
     if (contracted) {                                                                                    \

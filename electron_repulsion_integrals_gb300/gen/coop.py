@@ -98,10 +98,34 @@ def plan(cls, e_lo=None, f_lo=None):
     la, lb, lc, ld = cls
     La, Lc = la + lb, lc + ld
     L = La + Lc
-    e_list = [e for k in range(La + 1) for e in cart_list(k)]
+    elo = min(la, lb) if e_lo is None else e_lo
+    # Position of bra component e in an arena row.  A ket step along axis i
+    # has its lanes take the components with e_i > 0 (then those with
+    # e_i = 0) in position order, so the positions of each such set should
+    # form few contiguous runs: consecutive lanes then read consecutive
+    # doubles, free of shared-memory bank conflicts.  The row is cut into
+    # segments -- non-targets (|e| < elo) with e_z = 0, non-targets with
+    # e_z > 0, targets with e_z > 0, targets with e_z = 0 -- so that the
+    # e_z > 0 components (z steps are the most frequent: the ket axis rule
+    # prefers z) form one run and the targets the contiguous tail; inside the
+    # segments the e_y > 0 components sit at alternate ends so that adjacent
+    # segments join their runs.  (0,0,0) stays at position 0, where the kernel
+    # writes the Boys values.
+    std = [e for k in range(La + 1) for e in cart_list(k)]
+
+    def row_key(e):
+        t, z, y = sum(e) >= elo, e[2] > 0, e[1] > 0
+        seg = (2 if z else 3) if t else (1 if z else 0)
+        if elo == 0:                      # no non-targets: z = 0 segment first
+            seg = 1 if z else 0
+        y_first = seg in (1, 3) if elo > 0 else seg == 1
+        return (seg, sum(e) > 0, y != y_first, e[0] == 0, std.index(e))
+
+    e_list = sorted(std, key=row_key)
+    assert e_list[0] == (0, 0, 0)
     eidx = {e: i for i, e in enumerate(e_list)}
     NE = len(e_list)
-    ie_lo = sum(ncart(k) for k in range(min(la, lb) if e_lo is None else e_lo))
+    ie_lo = sum(ncart(k) for k in range(elo))
     lcmin = min(lc, ld) if f_lo is None else f_lo
     f_targets = [f for j in range(lcmin, Lc + 1) for f in cart_list(j)]
     fidx = {f: i for i, f in enumerate(f_targets)}
@@ -252,6 +276,17 @@ def lanes_for(arena, La, Lc, batch=4):
     return 32 if groups > MAX_GROUPS_FOR_WIDE else 128
 
 
+def resident_blocks(block_smem_bytes, cap=32):
+    """Launch-bounds hint of the derivative kernels: the blocks of one kernel
+    that fit on an SM by shared memory (1 KB of it reserved per block), at most
+    cap.  Without a hint the compiler chose 72-168 registers for their one-warp
+    blocks and spilled 28-468 B; with it the register budget is what the
+    occupancy that shared memory allows leaves.  (The cooperative class kernels
+    take no hint: measured over every f class, the hint left them no faster and
+    some of them, cut to 128 registers, spilled more and ran up to 5 % slower.)"""
+    return max(1, min(cap, SMEM_PER_SM // (block_smem_bytes + 1024 + 32)))
+
+
 def plan_tables(P, cname):
     """Device tables of a column schedule (bra nodes, per-axis e lists, ket
     column steps) and the trait accessors that expose them; returns
@@ -340,7 +375,7 @@ def emit_coop_class(cls):
     w("};")
     # bra HRR + sph for one ket column (and, for la != lb, the reversed form:
     # VRR on the lb shell, HRR for (lb, la), rows written in canonical order)
-    E_targets = [e for k in range(min(la, lb), La + 1) for e in cart_list(k)]
+    E_targets = P.e_list[P.ie_lo:]   # accumulator order: arena positions of the targets
     eidx = {e: i for i, e in enumerate(E_targets)}
     fidx = {f: i for i, f in enumerate(P.f_targets)}
 

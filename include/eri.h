@@ -179,8 +179,9 @@ int eri_compute_class_noalloc(eri_plan* plan, int la, int lb, int lc, int ld, co
  * d/dA_i [x_A^{a_i} ... e^{-alpha r_A^2}] = 2 alpha (a + 1_i) - a_i (a - 1_i),
  * applied inside the HRR of Eq. (3) to a VRR of the class extended by one on
  * the bra and the ket (the first-derivative kernel variants of FusionRCG
- * section IV, "Build system"); d/dD = -(d/dA + d/dB + d/dC) by translation
- * invariance.
+ * section IV, "Build system"), with the targets accumulated plain and
+ * weighted by 2 alpha, 2 beta, 2 gamma, 2 delta; each of the four centres'
+ * blocks is formed directly.
  * Classes of s, p and d shells (la, lb, lc, ld <= 2).
  * Layout: per quartet 12 consecutive blocks, [position k][axis i][block], each
  * block row-major [a][b][c][d] as in eri_compute_class; out_len (doubles) must
