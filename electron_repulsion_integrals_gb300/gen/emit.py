@@ -93,9 +93,18 @@ def lin_comb(em, terms, name, decl="const double"):
 # ----------------------------------------------------------------------------- VRR
 
 
-def emit_vrr(em, g, order, sink):
+def leaf_targets(g):
+    """Targets that no other node of the graph reads (the highest levels)."""
+    used = {p for nd in g.nodes for p in (nd.x0, nd.x1, nd.y0, nd.y1, nd.z1) if p >= 0}
+    return {k for k, t in enumerate(g.targets) if t not in used}
+
+
+def emit_vrr(em, g, order, sink, acc=None):
     """Straight-line VRR over the scheduled order.  sink(target_index, var)
-    is called right after a target value is produced."""
+    is called right after a target value is produced.  acc(target_index): for
+    a leaf target, the expression of its contracted accumulator; the node then
+    starts from it in the contracted instantiation (its first product an FMA
+    onto the accumulator), which saves the separate addition."""
     L = g.L
     tpos = {t: k for k, t in enumerate(g.targets)}
     name = {}
@@ -113,6 +122,8 @@ def emit_vrr(em, g, order, sink):
             else:
                 c0, c1, cy, cr = f"QC{ax}", f"WQ{ax}", f"k{nd.ky}_o2e", "roe"
             expr = em.mul(c0, name[nd.x0])
+            if acc is not None and v in tpos and acc(tpos[v]) is not None:
+                expr = f"(CONTRACTED ? fma({c0}, {name[nd.x0]}, {acc(tpos[v])}) : {expr})"
             em.w(f"double {var} = {expr};")
             em.w(f"{var} = {em.fma(c1, name[nd.x1], var)};")
             if nd.y0 >= 0:
@@ -124,7 +135,7 @@ def emit_vrr(em, g, order, sink):
     return name
 
 
-def emit_vrr_staged_regs(em, g, order, sink, R):
+def emit_vrr_staged_regs(em, g, order, sink, R, acc=None):
     """Straight-line VRR like emit_vrr, but with at most R VRR values live in
     registers: when a new value would exceed R, the live value whose next use
     is farthest away (Belady) moves to a per-thread shared-memory slot
@@ -211,7 +222,10 @@ def emit_vrr_staged_regs(em, g, order, sink, R):
                 c0, c1, cy, cr = f"PA{ax}", f"WP{ax}", f"k{nd.ky}_o2z", "roz"
             else:
                 c0, c1, cy, cr = f"QC{ax}", f"WQ{ax}", f"k{nd.ky}_o2e", "roe"
-            em.w(f"double {var} = {em.mul(c0, reg[nd.x0])};")
+            expr = em.mul(c0, reg[nd.x0])
+            if acc is not None and v in tpos and acc(tpos[v]) is not None:
+                expr = f"(CONTRACTED ? fma({c0}, {reg[nd.x0]}, {acc(tpos[v])}) : {expr})"
+            em.w(f"double {var} = {expr};")
             em.w(f"{var} = {em.fma(c1, reg[nd.x1], var)};")
             if nd.y0 >= 0:
                 em.w(f"{var} = {em.fma(cy, em.fma('-' + cr, reg[nd.y1], reg[nd.y0]), var)};")
@@ -445,25 +459,45 @@ def emit_class(cls, spherical_out=True, rule=None, schedule=None, sph_fusion=Tru
     tvars = [None] * len(g.targets)
 
     acc_smem = shape == "reg" and len(g.targets) > REG_ACC_MAX
+    # leaf targets: accumulated inside their own first FMA in the contracted
+    # instantiation (emit_vrr's acc); the node's value is then the new sum
+    leaves = leaf_targets(g)
+    base_targets = {k for k, t in enumerate(g.targets) if g.nodes[t].side == "base"}
+    fused = leaves - base_targets
+
+    def acc_expr(ti):
+        if ti not in fused:
+            return None
+        if shape == "reg":
+            return f"ACC({ti})" if acc_smem else f"h{ti}"
+        e, f = g.target_ef[ti]
+        return f"S[{eidx[e] * NF + fidx[f]} * kThreads]"
+
     if shape == "reg":
         def sink(ti, var):
             tvars[ti] = var
             if acc_smem:
-                vem.w(f"if constexpr (CONTRACTED) {{ ACC({ti}) += {var}; }} else {{ h{ti} = {var}; }}")
+                op = "=" if ti in fused else "+="
+                vem.w(f"if constexpr (CONTRACTED) {{ ACC({ti}) {op} {var}; }} else {{ h{ti} = {var}; }}")
+            elif ti in fused:
+                vem.w(f"h{ti} = {var};")
             else:
                 vem.w(f"if (CONTRACTED) {{ h{ti} += {var}; }} else {{ h{ti} = {var}; }}")
     else:
         def sink(ti, var):
             e, f = g.target_ef[ti]
             slot = eidx[e] * NF + fidx[f]
-            vem.w(f"if (CONTRACTED) {{ S[{slot} * kThreads] += {var}; }} else {{ S[{slot} * kThreads] = {var}; }}")
+            if ti in fused:
+                vem.w(f"S[{slot} * kThreads] = {var};")
+            else:
+                vem.w(f"if (CONTRACTED) {{ S[{slot} * kThreads] += {var}; }} else {{ S[{slot} * kThreads] = {var}; }}")
     smem_slots = gsl_slots = 0
     if shape == "staged":
-        nsl = emit_vrr_staged_regs(vem, g, order, sink, STAGED_VRR_REGS)
+        nsl = emit_vrr_staged_regs(vem, g, order, sink, STAGED_VRR_REGS, acc=acc_expr)
         smem_slots = min(nsl, STAGED_SMEM_SLOTS_MAX)
         gsl_slots = nsl - smem_slots
     else:
-        emit_vrr(vem, g, order, sink)
+        emit_vrr(vem, g, order, sink, acc=acc_expr)
     vops, vflops = vem.ops, vem.flops
 
     scratch_slots = 0

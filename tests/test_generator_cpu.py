@@ -72,12 +72,13 @@ def translate(src):
         if ln.startswith("asm volatile("):
             out.append(pad + "pass")
             continue
-        m = re.match(r"if constexpr \(CONTRACTED\) \{ ACC\((\d+)\) \+= (\w+); \} else \{ h(\d+) = \2; \}$", ln)
+        m = re.match(r"if constexpr \(CONTRACTED\) \{ ACC\((\d+)\) (\+?=) (\w+); \} else \{ h(\d+) = \3; \}$", ln)
         if m:
             out.append(pad + "if CONTRACTED:")
-            out.append(pad + f"    ACC[{m.group(1)}] = ACC[{m.group(1)}] + {m.group(2)}")
+            add = f"ACC[{m.group(1)}] + " if m.group(2) == "+=" else ""
+            out.append(pad + f"    ACC[{m.group(1)}] = {add}{m.group(3)}")
             out.append(pad + "else:")
-            out.append(pad + f"    h[{m.group(3)}] = {m.group(2)}")
+            out.append(pad + f"    h[{m.group(4)}] = {m.group(3)}")
             continue
         if ln == "}":
             ind -= 1
@@ -118,6 +119,8 @@ def translate(src):
         ln = re.sub(r"\bACC\((\d+)\)", r"ACC[\1]", ln)
         ln = re.sub(r"\b(Hc|Gc|Gr|Xr|X)\[(\d+) \* kThreads\]", r"S[\1 + \2]", ln)
         ln = re.sub(r"\bS\[(\d+) \* kThreads\]", r"S[\1]", ln)
+        # a leaf target's first product: onto its accumulator when contracted
+        ln = re.sub(r"\(CONTRACTED \? (fma\([^()]*\)) : ([^()]*)\)", r"(\1 if CONTRACTED else \2)", ln)
         ln = re.sub(r"\bh(\d+)\b", r"h[\1]", ln)
         ln = re.sub(r"__ldg\(osc_ \+ (\d+)\)", r"OSC[osc_ + \1]", ln)
         ln = re.sub(r"\bSMEM\((\d+)\)", r"SM[\1]", ln)

@@ -44,7 +44,7 @@ def test_derivative_lanes_are_the_narrowest_that_keep_enough_warps():
     for cls in canonical_classes(D.DERIV_LMAX):
         src, meta = D.emit_deriv_class(cls)
         la, lb, lc, ld = cls
-        per_quartet = meta["arena"] + 4 * CP.setup_stride(la + lb + 1, lc + ld + 1, 3)
+        per_quartet = meta["arena"] + 4 * CP.setup_stride(la + lb + 1, lc + ld + 1, 4)  # weights 2 alpha .. 2 delta
         lanes = _lanes(src)
         assert lanes in (8, 16, 32) and "GROUPS = 32 / LANES, THREADS = 32" in src
         seen[cls] = lanes
