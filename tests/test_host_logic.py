@@ -24,15 +24,24 @@ def test_e2e_chunks_cover_the_batch_in_order(n, out_bytes):
     assert ch[0][0] == 0 and ch[-1][1] == n
     assert all(a[1] == b[0] for a, b in zip(ch, ch[1:]))       # contiguous, in order
     sizes = [hi - lo for lo, hi in ch]
-    assert min(sizes) >= 1 and max(sizes) - min(sizes) <= 1
-    if out_bytes / bench.E2E_CHUNK_BYTES >= 8.5 and n >= 8:
+    assert min(sizes) >= 1
+    per = out_bytes / n
+    if out_bytes > 4 * bench.E2E_TAIL_BYTES and n >= 2:   # a small last chunk, the others even
+        assert sizes[-1] * per <= 1.01 * bench.E2E_TAIL_BYTES + per
+        body = sizes[:-1]
+    else:
+        body = sizes
+    assert max(body) - min(body) <= 1
+    if out_bytes / bench.E2E_CHUNK_BYTES >= 8.5 and n >= 16:
         assert len(ch) == 8
 
 
 def test_e2e_chunks_of_the_homogeneous_batch():
     bench = pytest.importorskip("bench")
-    assert len(bench.e2e_chunks(1 << 20, (1 << 20) * 625 * 8)) == 7      # (dd|dd): 5.24 GB
-    assert len(bench.e2e_chunks(1 << 20, (1 << 20) * 81 * 8)) == 1       # (pp|pp): 0.68 GB
+    dd = bench.e2e_chunks(1 << 20, (1 << 20) * 625 * 8)                  # (dd|dd): 5.24 GB
+    assert len(dd) == 8 and (dd[-1][1] - dd[-1][0]) * 625 * 8 <= 0.1e9 + 5000
+    pp = bench.e2e_chunks(1 << 20, (1 << 20) * 81 * 8)                   # (pp|pp): 0.68 GB
+    assert len(pp) == 2 and (pp[-1][1] - pp[-1][0]) * 81 * 8 <= 0.1e9 + 648
 
 
 def _lanes(src):
