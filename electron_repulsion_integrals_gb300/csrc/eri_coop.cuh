@@ -110,6 +110,27 @@ __device__ __forceinline__ void coop_setup_one(const EriLaunch& P, const Quartet
   for (int m = 0; m <= S::L; ++m) s[S::F + m] = F[m];
 }
 
+// Derivative classes: target column `col`, element k, value v into every
+// accumulator set that holds the column -- set 0 plain, set w weighted by
+// s[WGT + w - 1] -- at H + soff(w) + (col - sc0(w)) NET.
+template <class C>
+__device__ __forceinline__ void coop_acc_sets(double* __restrict__ H, const double* __restrict__ s, int col, int k,
+                                              double v, bool first) {
+  using S = CoopSetup<C::La, C::Lc, C::NW>;
+#pragma unroll
+  for (int w = 0; w <= C::NW; ++w) {
+    if (col >= C::sc0(w) && col < C::sc1(w)) {
+      double* Hw = H + C::soff(w) + (size_t)(col - C::sc0(w)) * C::NET;
+      if (w == 0) {
+        Hw[k] = first ? v : Hw[k] + v;
+      } else {
+        const double wt = s[S::WGT + w - 1];
+        Hw[k] = first ? wt * v : fma(wt, v, Hw[k]);
+      }
+    }
+  }
+}
+
 // VRR of one primitive quartet with parameters s[] into the arena; targets
 // accumulated into H (global, [target column][e - e_lo], e_lo the first
 // component with |e| = min(la, lb)).
@@ -179,12 +200,10 @@ __device__ __forceinline__ void coop_vrr(double* __restrict__ arena, const doubl
     // column 0 is a target column (ket component (0,0,0))
     for (int k = lane; k < C::NET; k += LN) {
       const double v = bra[C::IE_LO + k];
-      H[k] = first ? v : H[k] + v;
-#pragma unroll
-      for (int w = 1; w <= C::NW; ++w) {
-        const double wt = s[S::WGT + w - 1];
-        double* Hw = H + (size_t)w * C::NH;
-        Hw[k] = first ? wt * v : fma(wt, v, Hw[k]);
+      if constexpr (C::NW == 0) {
+        H[k] = first ? v : H[k] + v;
+      } else {
+        coop_acc_sets<C>(H, s, 0, k, v, first);
       }
     }
   }
@@ -204,7 +223,7 @@ __device__ __forceinline__ void coop_vrr(double* __restrict__ arena, const doubl
     constexpr int kHT = (C::NET + LN - 1) / LN;
     double hold[kHT];
     double* Ht = H + (size_t)(st.target >= 0 ? st.target : 0) * C::NET;
-    if (st.target >= 0 && !first) {
+    if (C::NW == 0 && st.target >= 0 && !first) {
 #pragma unroll
       for (int j = 0; j < kHT; ++j) {
         const int k = lane + LN * j;
@@ -319,12 +338,10 @@ __device__ __forceinline__ void coop_vrr(double* __restrict__ arena, const doubl
         const int k = lane + LN * j;
         if (k < C::NET) {
           const double v = O[C::IE_LO + k];
-          Ht[k] = first ? v : hold[j] + v;
-#pragma unroll
-          for (int w = 1; w <= C::NW; ++w) {
-            const double wt = s[S::WGT + w - 1];
-            double* Hw = Ht + (size_t)w * C::NH;
-            Hw[k] = first ? wt * v : fma(wt, v, Hw[k]);
+          if constexpr (C::NW == 0) {
+            Ht[k] = first ? v : hold[j] + v;
+          } else {
+            coop_acc_sets<C>(H, s, st.target, k, v, first);
           }
         }
       }

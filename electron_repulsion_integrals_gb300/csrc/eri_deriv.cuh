@@ -29,12 +29,14 @@ __device__ __forceinline__ double* deriv_out(const EriLaunch& P, const Quartet& 
 }  // namespace eri
 
 // Kernel of one derivative class.  C: traits (NW = 4; LANES lanes per
-// quartet, GROUPS quartets per block); BRA_A / BRA_B fill the three axis sets
-// of d/dA / d/dB rows, BRA_0G the plain, 2-gamma and 2-delta rows;
-// KET_AB(P, Q, q, r, x, G, k) writes row r of d/d(slot k) along axis x from
-// row set x, KET_C(P, Q, q, r, G) / KET_D(P, Q, q, r, G) write row r of d/dC /
-// d/dD for the three axes.
-#define ERI_DERIV_KERNEL(NAME, C, BRA_A, BRA_B, BRA_0G, KET_AB, KET_C, KET_D)                            \
+// quartet, GROUPS quartets per block; accumulator set w holds ket columns
+// [sc0(w), sc1(w)) at offset soff(w)); BRA_A / BRA_B fill the three axis sets
+// of d/dA / d/dB rows, BRA_0 / BRA_G / BRA_D the plain, 2-gamma and 2-delta
+// rows, each over the ket columns its set holds; KET_AB(P, Q, q, r, x, G, k)
+// writes row r of d/d(slot k) along axis x from row set x,
+// KET_C(P, Q, q, r, G) / KET_D(P, Q, q, r, G) write row r of d/dC / d/dD for
+// the three axes.
+#define ERI_DERIV_KERNEL(NAME, C, BRA_A, BRA_B, BRA_0, BRA_G, BRA_D, KET_AB, KET_C, KET_D)               \
   template <bool CONTRACTED>                                                                              \
   __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS) NAME(const EriLaunch P) {                                 \
     extern __shared__ double smem_[];                                                                     \
@@ -45,7 +47,7 @@ __device__ __forceinline__ double* deriv_out(const EriLaunch& P, const Quartet& 
     double* setup = arena + C::ARENA;                                                                     \
     const long long nw = (long long)gridDim.x * C::GROUPS;                                                \
     const long long wid = (long long)blockIdx.x * C::GROUPS + wib;                                        \
-    double* H = P.scratch + (size_t)wid * C::NH * (C::NW + 1);                                            \
+    double* H = P.scratch + (size_t)wid * C::NHT;                                                         \
     for (long long q = wid; q < P.n; q += nw) {                                                           \
       Quartet Q;                                                                                          \
       load_quartet<C::la == C::lb ? 1 : 0, C::lc == C::ld ? 1 : 0, C::la + C::lb, C::lc + C::ld>(P, q, Q); \
@@ -61,21 +63,23 @@ __device__ __forceinline__ double* deriv_out(const EriLaunch& P, const Quartet& 
         coop_sync<LN_>();                                                                                 \
       }                                                                                                   \
       double* G = arena;                                                                                  \
-      for (int fi = lane; fi < C::NF; fi += LN_) BRA_A(Q, H, fi, G);                                      \
+      for (int fi = C::sc0(1) + lane; fi < C::sc1(1); fi += LN_) BRA_A(Q, H, fi, G);                     \
       coop_sync<LN_>();                                                                                   \
       for (int it = lane; it < 3 * C::NR; it += LN_) {                                                    \
         const int x_ = it / C::NR;                                                                        \
         KET_AB(P, Q, q, it - x_ * C::NR, x_, G, 0);                                                       \
       }                                                                                                   \
       coop_sync<LN_>();                                                                                   \
-      for (int fi = lane; fi < C::NF; fi += LN_) BRA_B(Q, H, fi, G);                                      \
+      for (int fi = C::sc0(2) + lane; fi < C::sc1(2); fi += LN_) BRA_B(Q, H, fi, G);                     \
       coop_sync<LN_>();                                                                                   \
       for (int it = lane; it < 3 * C::NR; it += LN_) {                                                    \
         const int x_ = it / C::NR;                                                                        \
         KET_AB(P, Q, q, it - x_ * C::NR, x_, G, 1);                                                       \
       }                                                                                                   \
       coop_sync<LN_>();                                                                                   \
-      for (int fi = lane; fi < C::NF; fi += LN_) BRA_0G(Q, H, fi, G);                                     \
+      for (int fi = C::sc0(0) + lane; fi < C::sc1(0); fi += LN_) BRA_0(Q, H, fi, G);                     \
+      for (int fi = C::sc0(3) + lane; fi < C::sc1(3); fi += LN_) BRA_G(Q, H, fi, G);                     \
+      for (int fi = C::sc0(4) + lane; fi < C::sc1(4); fi += LN_) BRA_D(Q, H, fi, G);                     \
       coop_sync<LN_>();                                                                                   \
       for (int r = lane; r < C::NR; r += LN_) {                                                           \
         KET_C(P, Q, q, r, G);                                                                             \
@@ -87,7 +91,7 @@ __device__ __forceinline__ double* deriv_out(const EriLaunch& P, const Quartet& 
 
 #define ERI_DERIV_SMEM_(T) ((size_t)(T::GROUPS) * (T::WARP_SMEM) * sizeof(double))
 // Per-class entry points: launch (store mode, contracted or not), grid and
-// scratch sizing (NW + 1 accumulator sets per group of lanes).
+// scratch sizing (the accumulator sets of one group of lanes, NHT doubles).
 #define ERI_DEFINE_DERIV_LAUNCHER(LA, LB, LC, LD, KERNEL, T)                                             \
   extern "C" int eri_dlaunch_c##LA##LB##LC##LD(const EriLaunch* P, int contracted, int blocks, cudaStream_t st) { \
     if (contracted) {                                                                                    \
@@ -112,6 +116,6 @@ __device__ __forceinline__ double* deriv_out(const EriLaunch& P, const Quartet& 
     if (b > need) b = need;                                                                              \
     if (b < 1) b = 1;                                                                                    \
     *blocks = b;                                                                                         \
-    *scratch = b * T::GROUPS * (long long)T::NH * (T::NW + 1);                                          \
+    *scratch = b * T::GROUPS * (long long)T::NHT;                                                        \
     return 0;                                                                                            \
   }

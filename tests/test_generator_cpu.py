@@ -416,7 +416,7 @@ def emulate_deriv(cls, prims, Qns):
     Hs = emulate_coop_plan(P, prims, lambda pr: (2 * pr[0].alpha, 2 * pr[0].beta, 2 * pr[1].gamma, 2 * pr[1].delta))
     cname = "d" + E.class_name(cls)[1:]
     ns = {"fma": fma}
-    for fn in ("bra_dA", "bra_dB", "bra_0g", "ket_ab", "ket_c", "ket_d"):
+    for fn in ("bra_dA", "bra_dB", "bra_0", "bra_g", "bra_d", "ket_ab", "ket_c", "ket_d"):
         exec(compile(_translate_function(src, f"{fn}_{cname}"), f"<{fn} {cls}>", "exec"), ns)
     nf = [2 * l + 1 if l >= 2 else (l + 1) * (l + 2) // 2 for l in cls]
     bs = nf[0] * nf[1] * nf[2] * nf[3]
@@ -426,15 +426,19 @@ def emulate_deriv(cls, prims, Qns):
                               ost=[nf[1] * nf[2] * nf[3], nf[2] * nf[3], nf[3], 1])
     ns["deriv_out"] = lambda P_, Q_, q_, k_, x_: _Ptr(out, (Q_.pos[k_] * 3 + x_) * bs)
     ns[f"kOutScale_{cname}"] = _Ptr(np.asarray(osc_table(cls)))
-    H = _Ptr(Hs.reshape(-1))
+    # the kernel's layout: set w holds only its ket columns [c0, c1)
+    sets = meta["set_cols"]
+    H = _Ptr(np.concatenate([Hs[w][c0:c1].reshape(-1) for w, (c0, c1) in enumerate(sets)]))
+    assert len(H.a) == meta["nht"]
     G = _Ptr(np.zeros(meta["arena"]))
-    for bra, k in (("bra_dA", 0), ("bra_dB", 1)):
-        for fi in range(NF):
+    for bra, k, w in (("bra_dA", 0, 1), ("bra_dB", 1, 2)):
+        for fi in range(*sets[w]):
             ns[f"{bra}_{cname}"](Q, H, fi, G)
         for it in range(3 * NR):
             ns[f"ket_ab_{cname}"](None, Q, 0, it % NR, it // NR, G, k)
-    for fi in range(NF):
-        ns[f"bra_0g_{cname}"](Q, H, fi, G)
+    for bra, w in (("bra_0", 0), ("bra_g", 3), ("bra_d", 4)):
+        for fi in range(*sets[w]):
+            ns[f"{bra}_{cname}"](Q, H, fi, G)
     for r in range(NR):
         ns[f"ket_c_{cname}"](None, Q, 0, r, G)
         ns[f"ket_d_{cname}"](None, Q, 0, r, G)
