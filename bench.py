@@ -1,7 +1,8 @@
 """Benchmark: ERI quartets/s and FP64 GFLOP/s per angular class on one GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload homogeneous|high_l|g_shells|deriv|classes|cluster64|cluster200|cluster64_jk|cluster200_jk]
+                    [--workload homogeneous|high_l|g_shells|deriv|classes|cluster64|cluster200|cluster64_jk|
+                                cluster200_jk|cluster64_store|ladder_f_jk]
                     [--scale S] [--ablation all|NAME,...]
 
 A step is one pass of the hot path over the workload's batch: for every class
@@ -76,6 +77,13 @@ WORKLOADS = {
     "cluster200_jk": {"desc": "200-atom synthetic cluster as cluster200: Coulomb J and exchange K together in one "
                               "pass over all unique quartets surviving Schwarz 1e-10", "cluster": (200, 4),
                       "jk": True},
+    "ladder_f_jk": {"desc": "16-atom synthetic cluster (radius 6 bohr, atoms >= 2 bohr apart) with one s, p, d and f "
+                            "shell per atom (1-3 primitives, exponents log-U[0.1,50]): Coulomb J and exchange K in one "
+                            "pass over all unique quartets surviving Schwarz 1e-10, spherical, D = C C^T; the "
+                            "cooperative tier's digestion", "cluster": (16, 842), "ladder": (3, 6.0, 2.0), "jk": True},
+    "cluster64_store": {"desc": "64-atom synthetic cluster as cluster64: every unique quartet surviving Schwarz 1e-10 "
+                                "computed and stored, spherical, one eri_compute_screened launch per class",
+                        "cluster": (64, 3), "store": True},
 }
 
 
@@ -316,6 +324,31 @@ def cpu_oracle_rate(wl, budget_s=20.0, nthreads=None):
     return total_q / total_time, "oracle on " + " + ".join(parts), nthreads, per_class
 
 
+def oracle_cluster_counts(s, tau=1e-10):
+    """Unique shell quartets per canonical class that pass Q_ab Q_cd >= tau
+    with the oracle's Schwarz factors (counted from the sorted pair factors,
+    not listed)."""
+    import oracle
+    Q = oracle.schwarz(oracle.ShellSet(s.centers, s.L, s.nprim, s.exps, s.coefs), spherical=True)
+    L = np.asarray(s.L)
+    a, b = np.tril_indices(s.n)
+    hi, lo = np.maximum(L[a], L[b]), np.minimum(L[a], L[b])
+    pc = hi * (hi + 1) // 2 + lo
+    groups = {int(k): (int(hi[pc == k][0]), int(lo[pc == k][0]), np.sort(Q[a, b][pc == k])) for k in np.unique(pc)}
+    counts = {}
+    with np.errstate(divide="ignore"):
+        for cb, (la, lb, qb) in groups.items():
+            for ck, (lc, ld, qk) in groups.items():
+                if ck > cb:
+                    continue
+                ge = len(qk) - np.searchsorted(qk, tau / qb, side="left")  # ket factors >= tau / Q_bra
+                n = int(ge.sum())
+                if ck == cb:
+                    n = (n + int(np.count_nonzero(qb * qb >= tau))) // 2
+                counts[(la, lb, lc, ld)] = n
+    return counts
+
+
 def run_reference(a, rank, world):
     wl = WORKLOADS[a.workload]
     if rank != 0:
@@ -323,11 +356,17 @@ def run_reference(a, rank, world):
     rates = []
     desc = ""
     cores = 0
+    if "cluster" in wl:
+        cs = cluster_shells(wl)
+        counts = oracle_cluster_counts(cs)
+        rate_fn = lambda budget: cpu_oracle_rate_cluster(cs, counts, budget_s=budget) + (None,)  # noqa: E731
+    else:
+        rate_fn = lambda budget: cpu_oracle_rate(wl, budget_s=budget)  # noqa: E731
     for _ in range(a.warmup):
-        cpu_oracle_rate(wl, budget_s=2.0)
+        rate_fn(2.0)
     t_all = time.perf_counter()
     for _ in range(a.steps):
-        r, desc, cores, _ = cpu_oracle_rate(wl, budget_s=a.ref_budget)
+        r, desc, cores, _ = rate_fn(a.ref_budget)
         rates.append(r)
     elapsed = time.perf_counter() - t_all
     value = statistics.median(rates)
@@ -339,6 +378,16 @@ def run_reference(a, rank, world):
                              "sample": desc + " per step, projected to the full step mix"},
             "e2e": {"value": value, "unit": "quartets/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def cluster_shells(wl):
+    """Shells of a cluster workload."""
+    from electron_repulsion_integrals_gb300 import workloads as W
+    natom, idx = wl["cluster"]
+    if "ladder" in wl:
+        lmax, radius, dmin = wl["ladder"]
+        return W.shell_ladder_cluster(natom, lmax, seed_index=idx, radius=radius, dmin=dmin)
+    return W.cluster(natom, seed_index=idx)
 
 
 def run_coulomb(a, rank, world, local_rank):
@@ -356,8 +405,8 @@ def run_coulomb(a, rank, world, local_rank):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
     wl = WORKLOADS[a.workload]
-    natom, idx = wl["cluster"]
-    s = W.cluster(natom, seed_index=idx)
+    idx = wl["cluster"][1]
+    s = cluster_shells(wl)
     nbf = W.nbf(s)
     D = W.density(nbf, idx)
     stream = torch.cuda.current_stream()
@@ -451,6 +500,134 @@ def run_coulomb(a, rank, world, local_rank):
                          "traffic": None, "peak_source": peak_src},
             "fp64_probe": probe, "clocks": clk, "e2e": e2e, "cpu_baseline": cpu,
             "gpu_launches": a.steps * (sum(1 for n in counts.values() if n) + (2 if jk else 1))}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    plan.close()
+    if dist:
+        dist.destroy_process_group()
+
+
+def run_store(a, rank, world, local_rank):
+    """Cluster store workload: one step = eri_compute_screened over every
+    class's screened unique quartets, blocks stored into per-class device
+    buffers (eri_plan_class_quartets gives the shells of each block)."""
+    import torch
+    import electron_repulsion_integrals_gb300 as eri
+    from electron_repulsion_integrals_gb300.gen.eri_gen import canonical_classes
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    eri.lib()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    wl = WORKLOADS[a.workload]
+    s = cluster_shells(wl)
+    stream = torch.cuda.current_stream()
+    t = time.perf_counter()
+    plan = eri.Plan(s, spherical=True, schwarz_tau=1e-10, stream=stream)
+    plan_s = time.perf_counter() - t
+    counts = {c: plan.quartet_count(c) for c in canonical_classes(int(s.L.max()))}
+    classes = [c for c, n in counts.items() if n]
+    outs = {}
+    prim_q = {}
+    for c in classes:
+        outs[c] = torch.empty(counts[c] * eri.block_size(c), dtype=torch.float64, device=dev)
+        prim_q[c] = eri.eri_plan_class_work(plan.handle, c)[1]
+    nq = sum(counts[c] for c in classes)
+    out_bytes = sum(o.numel() * 8 for o in outs.values())
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(classes) + 1)]
+
+    def step(record=False):
+        if record:
+            ev[0].record(stream)
+        for i, c in enumerate(classes):
+            eri.eri_compute_screened(plan.handle, c, 0, counts[c], outs[c], stream)
+            if record:
+                ev[i + 1].record(stream)
+
+    probe = measure_fp64_peak(dev, stream, local_rank)
+    for _ in range(a.warmup):
+        step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for k in range(a.steps):
+        step(record=(k == a.steps - 1))
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    ms = t0.elapsed_time(t1)
+    ms = max_over_ranks(ms, dist, dev)
+    value = replica_rate(nq, world, a.steps, ms)
+    flops = 0.0
+    per_class = {}
+    for i, c in enumerate(classes):
+        st = eri.eri_class_info(c)
+        f = prim_q[c] * st["vrr_flops"] + counts[c] * st["hrr_flops"]
+        flops += f
+        cms = ev[i].elapsed_time(ev[i + 1])
+        per_class["({}{}|{}{})".format(*c)] = {"quartets": counts[c], "primitive_quartets": prim_q[c],
+                                               "ms_per_launch": cms, "quartets_per_s": counts[c] / (cms / 1e3),
+                                               "fp64_gflops": f / (cms / 1e3) / 1e9,
+                                               "tier": "staged" if st["staged"] else "register"}
+    ach = flops / (ms / a.steps / 1e3) / 1e12
+    peak, peak_src = roofline_peak(probe, clk.get("sm_mhz"))
+    e2e = None
+    if a.e2e:
+        # public API end to end: plan from host shells, every class's blocks
+        # and its quartet list (the shells of each block) computed and read
+        # back into pinned host memory (each class's readback on a copy
+        # stream overlaps the next class's compute)
+        host = {c: torch.empty(o.numel(), dtype=torch.float64, pin_memory=True) for c, o in outs.items()}
+        hlist = {c: torch.empty((counts[c], 4), dtype=torch.int32, pin_memory=True) for c in classes}
+        lists = {c: torch.empty((counts[c], 4), dtype=torch.int32, device=dev) for c in classes}
+        copy = torch.cuda.Stream(device=dev)
+        torch.cuda.synchronize()
+        te = time.perf_counter()
+        p2 = eri.Plan(s, spherical=True, schwarz_tau=1e-10, stream=stream)
+        for c in classes:
+            eri.eri_plan_class_quartets(p2.handle, c, 0, counts[c], lists[c], stream)
+            eri.eri_compute_screened(p2.handle, c, 0, counts[c], outs[c], stream)
+            done = torch.cuda.Event()
+            done.record(stream)
+            copy.wait_event(done)
+            with torch.cuda.stream(copy):
+                host[c].copy_(outs[c], non_blocking=True)
+                hlist[c].copy_(lists[c], non_blocking=True)
+        torch.cuda.synchronize()
+        te = time.perf_counter() - te
+        p2.close()
+        e2e = {"value": nq * world / te, "unit": "quartets/s",
+               "h2d_bytes_per_step": s.n * 48 + s.exps.size * 16, "d2h_bytes_per_step": out_bytes + nq * 16,
+               "wall_s": te, "includes": "plan creation (Schwarz screen), compute, quartet lists, readback"}
+        del host, hlist, lists
+    cpu = None
+    if rank == 0 and a.cpu_baseline:
+        rate, desc, cores = cpu_oracle_rate_cluster(s, counts, budget_s=a.ref_budget)
+        cpu = {"value": rate, "unit": "quartets/s", "cores": cores, "kind": "oracle", "sample": desc}
+    line = {"metric": METRIC, "value": value, "unit": "quartets/s", "n_gpus": world, "steps": a.steps,
+            "warmup": a.warmup, "ms_per_step": ms / a.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "per_class": per_class,
+            "config": {"workload": wl["desc"], "unique_quartets": nq, "stored_values": out_bytes // 8,
+                       "stored_bytes": out_bytes, "primitive_quartets": sum(prim_q.values()),
+                       "plan_create_s": plan_s, "l2": "no flush: stored output (GBs) far exceeds L2",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "alu", "kernel": "all class kernels of the store step", "achieved": ach,
+                         "peak": peak, "unit": "TFLOP/s", "frac": ach / peak, "traffic": None,
+                         "peak_source": peak_src},
+            "fp64_probe": probe, "clocks": clk, "e2e": e2e, "cpu_baseline": cpu,
+            "gpu_launches": a.steps * len(classes)}
     if rank == 0:
         print(json.dumps(line), flush=True)
     plan.close()
@@ -899,6 +1076,8 @@ def main():
     elif a.workload == "classes":
         if rank == 0:
             run_classes(a, local_rank)
+    elif WORKLOADS[a.workload].get("store"):
+        run_store(a, rank, world, local_rank)
     elif "cluster" in WORKLOADS[a.workload]:
         run_coulomb(a, rank, world, local_rank)
     else:

@@ -23,6 +23,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "_build", "liberi.so")
 
 ERI_OK = 0
+ERI_ERR_INVALID_ARG = -1
+ERI_ERR_UNSUPPORTED_L = -2
 STATUS = {0: "ok", -1: "invalid argument", -2: "unsupported angular momentum or basis", -3: "output buffer too small",
           -4: "CUDA error", -5: "out of memory", -6: "non-finite or non-positive shell data", -7: "not implemented",
           -8: "class needs more scratch than the static no-allocation array holds"}
@@ -78,6 +80,10 @@ def lib():
         L.eri_plan_quartet_count.argtypes = [vp] + [ctypes.c_int] * 4 + [ctypes.POINTER(ctypes.c_longlong)]
         L.eri_plan_class_work.argtypes = [vp] + [ctypes.c_int] * 4 + [ctypes.POINTER(ctypes.c_longlong),
                                                                      ctypes.POINTER(ctypes.c_double)]
+        L.eri_plan_class_quartets.argtypes = [vp] + [ctypes.c_int] * 4 + [ctypes.c_longlong, ctypes.c_longlong, vp,
+                                                                         vp]
+        L.eri_compute_screened.argtypes = [vp] + [ctypes.c_int] * 4 + [ctypes.c_longlong, ctypes.c_longlong, dp,
+                                                                      ctypes.c_longlong, vp]
         L.eri_class_info.argtypes = [ctypes.c_int] * 4 + [ctypes.POINTER(ClassStats)]
         L.eri_fp64_probe.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_longlong, dp,
                                      ctypes.POINTER(ctypes.c_longlong), vp]
@@ -217,6 +223,24 @@ def eri_plan_class_work(plan, cls):
     return n.value, pq.value
 
 
+def eri_plan_class_quartets(plan, cls, first, count, quartets, stream=None):
+    """Write quartets [first, first + count) of a class's screened list into
+    the device int32 tensor `quartets` ([count, 4])."""
+    if count and (quartets.dtype.itemsize != 4 or not quartets.is_contiguous() or quartets.numel() < 4 * count):
+        raise ValueError("quartets must be a contiguous int32 tensor of at least 4 x count elements")
+    _check("eri_plan_class_quartets", lib().eri_plan_class_quartets(
+        plan, *[int(x) for x in cls], int(first), int(count), _ptr(quartets) if count else None,
+        ctypes.c_void_p(_stream_handle(stream))))
+
+
+def eri_compute_screened(plan, cls, first, count, out, stream=None):
+    """Blocks of quartets [first, first + count) of a class's screened list
+    into the device float64 tensor `out`."""
+    _check("eri_compute_screened", lib().eri_compute_screened(
+        plan, *[int(x) for x in cls], int(first), int(count), _ptr(out), int(out.numel()) if out is not None else 0,
+        ctypes.c_void_p(_stream_handle(stream))))
+
+
 def eri_class_info(cls):
     s = ClassStats()
     _check("eri_class_info", lib().eri_class_info(*[int(x) for x in cls], ctypes.byref(s)))
@@ -291,6 +315,29 @@ class Plan:
 
     def quartet_count(self, cls):
         return eri_plan_quartet_count(self.handle, cls)
+
+    def class_quartets(self, cls, first=0, count=None, out=None, stream=None):
+        """The screened unique quartets of canonical class `cls` (all of them,
+        or [first, first + count)) as a device int32 tensor [count, 4]."""
+        import torch
+        if count is None:
+            count = self.quartet_count(cls) - first
+        if out is None:
+            out = torch.empty((max(count, 1), 4), dtype=torch.int32, device=torch.device("cuda", torch.cuda.current_device()))
+        eri_plan_class_quartets(self.handle, cls, first, count, out, stream)
+        return out[:count]
+
+    def compute_screened(self, cls, first=0, count=None, out=None, stream=None):
+        """Blocks of the screened quartets [first, first + count) of canonical
+        class `cls` (all of them by default), flat float64 on the device."""
+        import torch
+        if count is None:
+            count = self.quartet_count(cls) - first
+        if out is None:
+            out = torch.empty(max(count, 1) * block_size(cls, self.spherical), dtype=torch.float64,
+                              device=torch.device("cuda", torch.cuda.current_device()))
+        eri_compute_screened(self.handle, cls, first, count, out, stream)
+        return out
 
     def close(self):
         if self.handle:

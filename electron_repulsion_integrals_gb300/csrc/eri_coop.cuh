@@ -70,7 +70,7 @@ template <int MODE, int La, int Lc, int NW = 0>
 __device__ __forceinline__ void coop_setup_one(const EriLaunch& P, const Quartet& Q, int iab, int icd, double* s) {
   using S = CoopSetup<La, Lc, NW>;
   PrimPair pb, pk;
-  if constexpr (MODE == kCoulomb) {
+  if constexpr (MODE >= kCoulomb) {
     load_prim(P.prims, Q.pab + iab, pb);
     load_prim(P.prims, Q.pcd + icd, pk);
   } else {
@@ -352,6 +352,127 @@ __device__ __forceinline__ void coop_vrr(double* __restrict__ arena, const doubl
 
 }  // namespace eri
 
+// Output of row r = (ia, ib) of a cooperative class's final block, one value
+// (ic, id) -- position cdi = ic NSD + id in the row -- at a time: the store
+// mode writes it to the caller's buffer in the requested shell order, the
+// Schwarz mode keeps the largest diagonal element, and the Coulomb and
+// exchange modes write the row, row-major, into the lane group's scratch
+// block hb_ (the accumulator region, free once the bra HRR has read it) for
+// coop_digest, and the screened store mode into the caller's buffer
+// (canonical order; cooperative quartets are never split into parts).
+#define COOP_ROW(r, ia, ib)                                                     \
+  {                                                                             \
+    double* __restrict__ orow_ = nullptr;                                       \
+    if constexpr (MODE == kStore)                                               \
+      orow_ = P.out + q * P.out_stride + (ia) * Q.ost[0] + (ib) * Q.ost[1];     \
+    double* __restrict__ hrow_ = hb_ + (size_t)(r) * kNCD_;                     \
+    if constexpr (MODE == kStoreScreen) hrow_ = P.out + (Q.qi - P.q0) * P.out_stride + (size_t)(r) * kNCD_;
+
+#define COOP_VAL(cdi, ia, ib, ic, id, v)                                        \
+  if constexpr (MODE == kStore) {                                               \
+    orow_[(ic) * Q.ost[2] + (id) * Q.ost[3]] = (v);                             \
+  } else if constexpr (MODE == kSchwarz) {                                      \
+    if ((ia) == (ic) && (ib) == (id)) smax_ = fmax(smax_, fabs(v));             \
+  } else if constexpr (MODE >= kCoulomb) {                                      \
+    hrow_[cdi] = (v);                                                           \
+  }
+
+#define COOP_ROW_END() \
+  (void)orow_;         \
+  (void)hrow_;         \
+  }
+
+// Digestion of one finished block I (row-major [ia ib][ic id] in hb, written
+// by the group's lanes) with the density, the scatter that ends FusionRCG
+// Algorithm 2.  For the unique quartet (ab|cd) with pair factors f_ab, f_cd
+// (2 for a pair of two different shells) and weight w (Q.wk):
+//   J_ab += f_cd sum_cd I D_cd      one lane per bra row (ia, ib)
+//   J_cd += f_ab sum_ab I D_ab      one lane per ket column (ic, id), unless
+//                                   the two pairs are the same pair
+// and with K, the one-orientation exchange accumulator T (K = T + T^T):
+//   T_ac += w sum_{b,d} I D_bd,  T_ad += w sum_{b,c} I D_bc,
+//   T_bc += w sum_{a,d} I D_ad,  T_bd += w sum_{a,c} I D_ac,
+// one lane per element of each.  Each lane sums its element in registers and
+// issues one FP64 atomic add to J or K; consecutive lanes read consecutive
+// density elements where the element's index runs over d (or b).
+namespace eri {
+
+template <class C, int MODE, int LN>
+__device__ __forceinline__ void coop_digest(const EriLaunch& P, const Quartet& Q, const double* __restrict__ hb,
+                                            int lane) {
+  constexpr int NSA = C::NSA, NSB = C::NSB, NSC = C::NSC, NSD = C::NSD, NCD = NSC * NSD, NR = NSA * NSB;
+  static_assert(NR * NCD <= C::NH, "the block must fit in the group's accumulator region");
+  const double* __restrict__ D = P.D;
+  const size_t nbf = (size_t)P.nbf;
+  for (int r = lane; r < NR; r += LN) {
+    const int ia = r / NSB, ib = r - (r / NSB) * NSB;
+    const double* __restrict__ row = hb + (size_t)r * NCD;
+    double s = 0.0;
+#pragma unroll
+    for (int ic = 0; ic < NSC; ++ic)
+#pragma unroll
+      for (int id = 0; id < NSD; ++id) s = fma(row[ic * NSD + id], __ldg(D + (Q.fc + ic) * nbf + Q.fd + id), s);
+    atomicAdd(P.J + (Q.fa + ia) * nbf + Q.fb + ib, Q.fcd * s);
+  }
+  if (Q.bra != Q.ket) {
+    for (int k = lane; k < NCD; k += LN) {
+      const int ic = k / NSD, id = k - (k / NSD) * NSD;
+      double s = 0.0;
+#pragma unroll
+      for (int ia = 0; ia < NSA; ++ia)
+#pragma unroll
+        for (int ib = 0; ib < NSB; ++ib)
+          s = fma(hb[(size_t)(ia * NSB + ib) * NCD + k], __ldg(D + (Q.fa + ia) * nbf + Q.fb + ib), s);
+      atomicAdd(P.J + (Q.fc + ic) * nbf + Q.fd + id, Q.fab * s);
+    }
+  }
+  if constexpr (MODE == kExchange) {
+    // T_ac and T_ad (rows of a), then T_bc and T_bd (rows of b)
+    for (int t = lane; t < NSA * (NSC + NSD); t += LN) {
+      const int ia = t / (NSC + NSD), u = t - ia * (NSC + NSD);
+      double s = 0.0;
+      if (u < NSC) {  // T_ac[ia][u]
+#pragma unroll
+        for (int ib = 0; ib < NSB; ++ib)
+#pragma unroll
+          for (int id = 0; id < NSD; ++id)
+            s = fma(hb[(size_t)(ia * NSB + ib) * NCD + u * NSD + id], __ldg(D + (Q.fb + ib) * nbf + Q.fd + id), s);
+        atomicAdd(P.K + (Q.fa + ia) * nbf + Q.fc + u, Q.wk * s);
+      } else {  // T_ad[ia][u - NSC]
+        const int id = u - NSC;
+#pragma unroll
+        for (int ib = 0; ib < NSB; ++ib)
+#pragma unroll
+          for (int ic = 0; ic < NSC; ++ic)
+            s = fma(hb[(size_t)(ia * NSB + ib) * NCD + ic * NSD + id], __ldg(D + (Q.fb + ib) * nbf + Q.fc + ic), s);
+        atomicAdd(P.K + (Q.fa + ia) * nbf + Q.fd + id, Q.wk * s);
+      }
+    }
+    for (int t = lane; t < NSB * (NSC + NSD); t += LN) {
+      const int ib = t / (NSC + NSD), u = t - ib * (NSC + NSD);
+      double s = 0.0;
+      if (u < NSC) {  // T_bc[ib][u]
+#pragma unroll
+        for (int ia = 0; ia < NSA; ++ia)
+#pragma unroll
+          for (int id = 0; id < NSD; ++id)
+            s = fma(hb[(size_t)(ia * NSB + ib) * NCD + u * NSD + id], __ldg(D + (Q.fa + ia) * nbf + Q.fd + id), s);
+        atomicAdd(P.K + (Q.fb + ib) * nbf + Q.fc + u, Q.wk * s);
+      } else {  // T_bd[ib][u - NSC]
+        const int id = u - NSC;
+#pragma unroll
+        for (int ia = 0; ia < NSA; ++ia)
+#pragma unroll
+          for (int ic = 0; ic < NSC; ++ic)
+            s = fma(hb[(size_t)(ia * NSB + ib) * NCD + ic * NSD + id], __ldg(D + (Q.fa + ia) * nbf + Q.fc + ic), s);
+        atomicAdd(P.K + (Q.fb + ib) * nbf + Q.fd + id, Q.wk * s);
+      }
+    }
+  }
+}
+
+}  // namespace eri
+
 // Kernel body shared by every cooperative class.  C: traits; BRA_FN / KET_FN
 // are the generated per-column / per-row HRR functions and BRA_REV_FN /
 // KET_REV_FN their reversed forms (pair evaluated with the VRR on its
@@ -371,13 +492,13 @@ __device__ __forceinline__ void coop_vrr(double* __restrict__ arena, const doubl
     double* H = P.scratch + (size_t)wid * C::NH;                                                          \
     for (long long q = wid; q < P.n; q += nw) {                                                           \
       Quartet Q;                                                                                          \
-      if constexpr (MODE == kCoulomb) {                                                                   \
+      if constexpr (MODE >= kCoulomb) {                                                                   \
         load_quartet_coulomb(P, q, Q);                                                                    \
       } else {                                                                                            \
         load_quartet<C::la == C::lb ? 1 : 2, C::lc == C::ld ? 1 : 2, C::La, C::Lc>(P, q, Q);                \
       }                                                                                                   \
-      const int nab = MODE == kCoulomb ? Q.nab : Q.na * Q.nb;                                             \
-      const int ncd = MODE == kCoulomb ? Q.ncd : Q.nc * Q.nd;                                             \
+      const int nab = MODE >= kCoulomb ? Q.nab : Q.na * Q.nb;                                             \
+      const int ncd = MODE >= kCoulomb ? Q.ncd : Q.nc * Q.nd;                                             \
       const int nprim = nab * ncd;                                                                        \
       for (int base = 0; base < nprim; base += kCoopBatch) {                                              \
         const int p = base + lane;                                                                        \
@@ -399,8 +520,13 @@ __device__ __forceinline__ void coop_vrr(double* __restrict__ arena, const doubl
       coop_sync<LN_>();                                                                                   \
       double smax_ = 0.0;                                                                                 \
       for (int r = lane; r < C::NR; r += LN_) {                                                           \
-        if (Q.rk) KET_REV_FN<MODE>(P, Q, q, r, G, smax_);                                                 \
-        else KET_FN<MODE>(P, Q, q, r, G, smax_);                                                          \
+        if (Q.rk) KET_REV_FN<MODE>(P, Q, q, r, G, smax_, H);                                              \
+        else KET_FN<MODE>(P, Q, q, r, G, smax_, H);                                                       \
+      }                                                                                                   \
+      if constexpr (digest_mode(MODE)) {                                                                  \
+        coop_sync<LN_>();                                                                                 \
+        load_quartet_digest(P, Q);                                                                        \
+        coop_digest<C, MODE, LN_>(P, Q, H, lane);                                                         \
       }                                                                                                   \
       if constexpr (MODE == kSchwarz) {                                                                   \
         _Pragma("unroll") for (int o = 16; o > 0; o >>= 1) smax_ = fmax(smax_, __shfl_xor_sync(0xffffffffu, smax_, o)); \
@@ -435,6 +561,9 @@ __device__ __forceinline__ void coop_vrr(double* __restrict__ arena, const doubl
     (void)contracted;                                                                                    \
     if (mode == kStore) ERI_COOP_LAUNCH_(KERNEL, T, kStore, true)                                        \
     else if (mode == kSchwarz) ERI_COOP_LAUNCH_(KERNEL, T, kSchwarz, true)                               \
+    else if (mode == kCoulomb) ERI_COOP_LAUNCH_(KERNEL, T, kCoulomb, true)                               \
+    else if (mode == kExchange) ERI_COOP_LAUNCH_(KERNEL, T, kExchange, true)                             \
+    else if (mode == kStoreScreen) ERI_COOP_LAUNCH_(KERNEL, T, kStoreScreen, true)                       \
     else return -1;                                                                                      \
     return (int)cudaGetLastError();                                                                      \
   }                                                                                                      \

@@ -87,8 +87,11 @@ __device__ __forceinline__ void boys_scaled(double T, double pref, const double*
 // kSchwarz reduces each diagonal block (ab|ab) to sqrt(max |diagonal|);
 // kSchwarzPart adds one part of the primitive sum of the diagonal elements to
 // a buffer (work item = quartet x part, see schwarz_part); kCoulomb digests
-// every block into J; kExchange into J and K together.
-enum OutputMode { kStore = 0, kSchwarz = 1, kSchwarzPart = 2, kCoulomb = 3, kExchange = 4 };
+// every block into J; kExchange into J and K together; kStoreScreen stores
+// the blocks of a range of a class's screened quartets.  The last three take
+// their work items from the plan's screened segment list.
+enum OutputMode { kStore = 0, kSchwarz = 1, kSchwarzPart = 2, kCoulomb = 3, kExchange = 4, kStoreScreen = 5 };
+__host__ __device__ constexpr bool digest_mode(int m) { return m == kCoulomb || m == kExchange; }
 
 struct ShellsDev {
   const double* cen;    // [nshell][3]
@@ -131,6 +134,11 @@ struct EriLaunch {
   const int4* segs;
   const long long* seg_start;
   int nseg;
+  // screened store mode: seg_qstart[k] = quartets before segment k; the
+  // launch covers work items item0 .. item0 + n - 1, and the block of the
+  // class's quartet g goes to out + (g - q0) out_stride
+  const long long* seg_qstart;
+  long long item0, q0;
   // scratch for staged classes: slot s of thread t at scratch[s * nthreads + t]
   double* scratch;
   const double* boys;
@@ -155,7 +163,8 @@ struct Quartet {
   int bra, ket;       // pair ids
   int pab, nab, pcd, ncd;
   int iab0, iab1, icd0, icd1;  // primitive pairs of this work item: [iab0, iab1) x [icd0, icd1)
-  long long qi;                // Schwarz-part mode: quartet of the work item
+  long long qi;                // Schwarz-part / screened store mode: quartet of the work item
+  int whole;                   // screened store mode: the item is the whole quartet
   int fa, fb, fc, fd;  // first basis functions of the four shells
   double fab, fcd;     // 2 for a pair of distinct shells, else 1
   double wk;           // 1 / (number of the 8 index permutations that leave the quartet unchanged)
@@ -302,7 +311,8 @@ __device__ __forceinline__ void schwarz_part(const EriLaunch& P, long long t, Qu
 
 // Coulomb mode: work item t -> (bra pair, ket pair) by binary search over the
 // segment starts, then the pair records.
-__device__ __forceinline__ void load_quartet_coulomb(const EriLaunch& P, long long t, Quartet& Q) {
+__device__ __forceinline__ void load_quartet_coulomb(const EriLaunch& P, long long tl, Quartet& Q) {
+  const long long t = tl + P.item0;
   int lo = 0, hi = P.nseg - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -317,6 +327,8 @@ __device__ __forceinline__ void load_quartet_coulomb(const EriLaunch& P, long lo
   const int cb = ch / sk, ck = ch - cb * sk;
   Q.bra = sg.x;
   Q.ket = sg.y + (int)qo;
+  Q.qi = (P.seg_qstart ? __ldg(P.seg_qstart + lo) : 0) + qo;
+  Q.whole = sb * sk == 1;
   const PairMeta* mb = P.pairs + Q.bra;
   const PairMeta* mk = P.pairs + Q.ket;
   Q.pab = __ldg(&mb->poff);
@@ -500,7 +512,9 @@ __device__ __forceinline__ void quartet_setup(const PrimPair& pb, const PrimPair
     const int ia_ = (ia), ib_ = (ib);                                       \
     if constexpr (MODE == kStore) {                                         \
       orow_ = P.out + q * P.out_stride + (ia) * Q.ost[0] + (ib) * Q.ost[1]; \
-    } else if constexpr (MODE >= kCoulomb) {                                \
+    } else if constexpr (MODE == kStoreScreen) {                            \
+      orow_ = P.out + (Q.qi - P.q0) * P.out_stride + ((ia) * kNSB_ + (ib)) * kNCD_; \
+    } else if constexpr (digest_mode(MODE)) {                               \
       const size_t rowoff_ = (size_t)(Q.fa + (ia)) * P.nbf + Q.fb + (ib);   \
       dab_ = Q.fab * __ldg(P.D + rowoff_);                                  \
       jdst_ = P.J + rowoff_;                                                \
@@ -521,6 +535,11 @@ __device__ __forceinline__ void quartet_setup(const PrimPair& pb, const PrimPair
   } else if constexpr (MODE == kSchwarzPart) {                                 \
     if ((ia) == (ic) && (ib) == (id))                                          \
       atomicAdd(P.q_out + Q.qi * P.q_stride + (ia) * kNSB_ + (ib), (v));       \
+  } else if constexpr (MODE == kStoreScreen) {                                 \
+    if (Q.whole)                                                               \
+      orow_[(ic) * kNSD_ + (id)] = (v);                                        \
+    else                                                                       \
+      atomicAdd(orow_ + (ic) * kNSD_ + (id), (v));                             \
   } else {                                                                     \
     jrow_ = fma((v), __ldg(dcd_ + (size_t)(ic) * P.nbf + (id)), jrow_);     \
     jcd_[(ic) * kNSD_ + (id)] = fma((v), dab_, jcd_[(ic) * kNSD_ + (id)]);   \
@@ -533,7 +552,7 @@ __device__ __forceinline__ void quartet_setup(const PrimPair& pb, const PrimPair
   }
 
 #define OUTPUT_ROW_END()                                                            \
-  if constexpr (MODE >= kCoulomb) {                                                 \
+  if constexpr (digest_mode(MODE)) {                                                \
     atomicAdd(jdst_, Q.fcd * jrow_);                                                \
   }                                                                                 \
   if constexpr (MODE == kExchange) {                                                \
@@ -568,7 +587,7 @@ __device__ __forceinline__ void quartet_setup(const PrimPair& pb, const PrimPair
 #define OUTPUT_QUARTET_END()                                                             \
   if constexpr (MODE == kSchwarz) {                                                      \
     P.q_out[q] = sqrt(smax_);                                                            \
-  } else if constexpr (MODE >= kCoulomb) {                                               \
+  } else if constexpr (digest_mode(MODE)) {                                              \
     if (Q.bra != Q.ket) {                                                                \
       _Pragma("unroll") for (int k_ = 0; k_ < kNCD_; ++k_) {                             \
         atomicAdd(P.J + (size_t)(Q.fc + k_ / kNSD_) * P.nbf + Q.fd + k_ % kNSD_, jcd_[k_]); \
@@ -611,6 +630,8 @@ __device__ __forceinline__ void quartet_setup(const PrimPair& pb, const PrimPair
       ERI_LAUNCH_ONE_(KERNEL, kCoulomb, true, csmemb_)                                                    \
     } else if (mode == kExchange) {                                                                       \
       ERI_LAUNCH_ONE_(KERNEL, kExchange, true, csmemb_)                                                   \
+    } else if (mode == kStoreScreen) {                                                                    \
+      ERI_LAUNCH_ONE_(KERNEL, kStoreScreen, true, csmemb_)                                                \
     } else {                                                                                              \
       return -1;                                                                                          \
     }                                                                                                     \

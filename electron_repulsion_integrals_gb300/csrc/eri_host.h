@@ -44,5 +44,7 @@ double plan_tau(const eri_plan* p);
 size_t plan_nprim_total(const eri_plan* p);
 const double* plan_dcoef(const eri_plan* p);
 int class_grid(const int l[4], int nsm, long long n, long long* blocks, long long* scratch);
+// tier of the class's kernel: 0 register, 1 staged, 2 cooperative; -1 if not built
+int class_tier(const int l[4]);
 }  // namespace host
 }  // namespace eri

@@ -621,6 +621,13 @@ int eri::host::class_launcher(const int l[4], int (**launch)(const EriLaunch*, i
   *slots = ce->slots();
   return ERI_OK;
 }
+int eri::host::class_tier(const int l[4]) {
+  const ClassEntry* ce = find_class(l[0], l[1], l[2], l[3]);
+  if (!ce) return -1;
+  long long v[6] = {0, 0, 0, 0, 0, 0};
+  ce->stats(v);
+  return (int)v[5];
+}
 int eri::host::class_grid(const int l[4], int nsm, long long n, long long* blocks, long long* scratch) {
   const ClassEntry* ce = find_class(l[0], l[1], l[2], l[3]);
   if (!ce) return ERI_ERR_UNSUPPORTED_L;

@@ -99,6 +99,25 @@ __global__ void build_prim_pairs(int npairs, const PairMeta* __restrict__ pairs,
   }
 }
 
+// One thread per listed quartet: quartet first + i of a class's screened list
+// (segment order) as the shells of its bra and ket pairs.
+__global__ void list_quartets(long long first, long long count, int nseg, const int4* __restrict__ segs,
+                              const long long* __restrict__ qstart, const PairMeta* __restrict__ pairs,
+                              int4* __restrict__ out) {
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= count) return;
+  const long long g = first + i;
+  int lo = 0, hi = nseg - 1;  // last segment with qstart <= g
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) / 2;
+    if (qstart[mid] <= g) lo = mid;
+    else hi = mid - 1;
+  }
+  const int4 sg = segs[lo];
+  const PairMeta bra = pairs[sg.x], ket = pairs[sg.y + (int)(g - qstart[lo])];
+  out[i] = make_int4(bra.a, bra.b, ket.a, ket.b);
+}
+
 // q[i] = sqrt(max_k |diag[i][k]|): Schwarz factors from summed diagonal parts.
 __global__ void schwarz_reduce(long long n, int nd, const double* __restrict__ diag, double* __restrict__ q) {
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -142,6 +161,10 @@ struct ClassWork {
   double prim_total = 0;  // primitive quartets evaluated (after pruning)
   int4* dsegs = nullptr;
   long long* dstart = nullptr;
+  long long* dqstart = nullptr;  // quartets before each segment (nseg + 1)
+  // host copies: segments (w = parts) and the item / quartet starts
+  std::vector<int4> hsegs;
+  std::vector<long long> hstart, hqstart;
 };
 
 }  // namespace
@@ -166,6 +189,7 @@ struct Screen {
     for (auto& c : classes) {
       cudaFree(c.dsegs);
       cudaFree(c.dstart);
+      cudaFree(c.dqstart);
     }
   }
 };
@@ -441,9 +465,12 @@ int build(eri_plan* p, cudaStream_t st) {
           // class's average primitive quartets per thread, whichever is larger:
           // a class with work enough for every thread keeps its quartets whole
           // (each cut repeats the HRR, transform and scatter of the quartet).
+          // (The cooperative tier spreads each quartet over a group of lanes
+          // already and keeps its quartets whole.)
           const double per_thread = W.prim_total / (kThreadsPerSM * eri::host::plan_nsm(p));
           const long long pmax = std::max<long long>(kMinPrimPerItem, (long long)(0.5 * per_thread));
-          for (size_t k = 0; k < segs.size(); ++k) {
+          const bool whole = eri::host::class_tier(W.l) == 2;
+          for (size_t k = 0; k < segs.size() && !whole; ++k) {
             const long long Kb = kb_of[k], Kk = kk_of[k];
             int sb = 1, sk = 1;
             if (Kb * Kk > pmax) {
@@ -463,16 +490,18 @@ int build(eri_plan* p, cudaStream_t st) {
             return kk_of[x] > kk_of[y];
           });
           std::vector<int4> so(segs.size());
-          std::vector<long long> start(segs.size() + 1);
+          std::vector<long long> start(segs.size() + 1), qstart(segs.size() + 1);
           long long t = 0;
           long long nq = 0;
           for (size_t k = 0; k < ord.size(); ++k) {
             so[k] = segs[ord[k]];
             start[k] = t;
+            qstart[k] = nq;
             t += (long long)so[k].z * (so[k].w & 0xffff) * (so[k].w >> 16);
             nq += so[k].z;
           }
           start[segs.size()] = t;
+          qstart[segs.size()] = nq;
           W.nseg = (int)segs.size();
           W.total = nq;
           W.items = t;
@@ -481,6 +510,12 @@ int build(eri_plan* p, cudaStream_t st) {
           CUDA_TRY(cudaMemcpyAsync(W.dsegs, so.data(), so.size() * sizeof(int4), cudaMemcpyHostToDevice, st));
           CUDA_TRY(cudaMemcpyAsync(W.dstart, start.data(), start.size() * sizeof(long long), cudaMemcpyHostToDevice,
                                    st));
+          W.hsegs = so;
+          W.hstart = start;
+          W.hqstart = qstart;
+          CUDA_TRY(cudaMalloc(&W.dqstart, qstart.size() * sizeof(long long)));
+          CUDA_TRY(cudaMemcpyAsync(W.dqstart, qstart.data(), qstart.size() * sizeof(long long),
+                                   cudaMemcpyHostToDevice, st));
           CUDA_TRY(cudaStreamSynchronize(st));
           S->classes.push_back(W);
         }
@@ -581,6 +616,80 @@ int eri_plan_class_work(const eri_plan* p, int la, int lb, int lc, int ld, long 
       return ERI_OK;
     }
   return ERI_ERR_UNSUPPORTED_L;
+}
+
+int eri_plan_class_quartets(const eri_plan* p, int la, int lb, int lc, int ld, long long first, long long count,
+                            int* quartets_dev, void* stream) {
+  if (!p || first < 0 || count < 0 || (count > 0 && !quartets_dev)) return ERI_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(quartets_dev) % 16 != 0) return ERI_ERR_INVALID_ARG;
+  eri::screen::Screen* S = eri::host::plan_screen(const_cast<eri_plan*>(p));
+  if (!S) return ERI_ERR_INVALID_ARG;
+  for (const ClassWork& W : S->classes)
+    if (W.l[0] == la && W.l[1] == lb && W.l[2] == lc && W.l[3] == ld) {
+      if (first + count > W.total) return ERI_ERR_INVALID_ARG;
+      if (count == 0) return ERI_OK;
+      int dev = -1;
+      CUDA_TRY(cudaGetDevice(&dev));
+      if (dev != eri::host::plan_device(p)) return ERI_ERR_INVALID_ARG;
+      list_quartets<<<(unsigned)((count + 255) / 256), 256, 0, (cudaStream_t)stream>>>(
+          first, count, W.nseg, W.dsegs, W.dqstart, S->dpairs, reinterpret_cast<int4*>(quartets_dev));
+      CUDA_TRY(cudaGetLastError());
+      return ERI_OK;
+    }
+  return ERI_ERR_UNSUPPORTED_L;
+}
+
+int eri_compute_screened(eri_plan* p, int la, int lb, int lc, int ld, long long first, long long count,
+                         double* out_dev, long long out_len, void* stream) {
+  if (!p || first < 0 || count < 0 || (count > 0 && !out_dev)) return ERI_ERR_INVALID_ARG;
+  eri::screen::Screen* S = eri::host::plan_screen(p);
+  if (!S) return ERI_ERR_INVALID_ARG;
+  const ClassWork* W = nullptr;
+  for (const ClassWork& c : S->classes)
+    if (c.l[0] == la && c.l[1] == lb && c.l[2] == lc && c.l[3] == ld) W = &c;
+  if (!W) return ERI_ERR_UNSUPPORTED_L;
+  if (first + count > W->total) return ERI_ERR_INVALID_ARG;
+  const bool sph = eri::host::plan_spherical(p);
+  long long blk = 1;
+  for (int k = 0; k < 4; ++k) {
+    if (!sph && W->l[k] >= 2) return ERI_ERR_UNSUPPORTED_L;
+    blk *= (sph && W->l[k] >= 2) ? 2 * W->l[k] + 1 : (W->l[k] + 1) * (W->l[k] + 2) / 2;
+  }
+  if (count > 0 && out_len / blk < count) return ERI_ERR_BUFFER_TOO_SMALL;
+  if (count == 0) return ERI_OK;
+  int dev = -1;
+  CUDA_TRY(cudaGetDevice(&dev));
+  if (dev != eri::host::plan_device(p)) return ERI_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  // work items of quartets [first, first + count): segment k holds quartets
+  // [hqstart[k], hqstart[k+1]), each cut into parts(k) items
+  auto parts = [&](size_t k) { return (long long)(W->hsegs[k].w & 0xffff) * (W->hsegs[k].w >> 16); };
+  auto seg_of = [&](long long g) {
+    return (size_t)(std::upper_bound(W->hqstart.begin(), W->hqstart.end() - 1, g) - W->hqstart.begin()) - 1;
+  };
+  auto item_of = [&](long long g) {
+    if (g >= W->total) return W->items;
+    const size_t k = seg_of(g);
+    return W->hstart[k] + (g - W->hqstart[k]) * parts(k);
+  };
+  const size_t k0 = seg_of(first), k1 = seg_of(first + count - 1);
+  bool split = false;
+  for (size_t k = k0; k <= k1; ++k) split = split || parts(k) > 1;
+  if (split) CUDA_TRY(cudaMemsetAsync(out_dev, 0, (size_t)count * blk * sizeof(double), st));
+  EriLaunch P;
+  std::memset(&P, 0, sizeof(P));
+  P.item0 = item_of(first);
+  P.n = item_of(first + count) - P.item0;
+  P.q0 = first;
+  P.out = out_dev;
+  P.out_stride = blk;
+  P.pairs = S->dpairs;
+  P.prims = S->dprims;
+  P.segs = W->dsegs;
+  P.seg_start = W->dstart;
+  P.seg_qstart = W->dqstart;
+  P.nseg = W->nseg;
+  return eri::host::launch_class(p, W->l, P, kStoreScreen, st);
 }
 
 int eri_plan_quartet_count(const eri_plan* p, int la, int lb, int lc, int ld, long long* n) {

@@ -365,6 +365,7 @@ def emit_coop_class(cls):
     fi_lc = sum(1 for f in P.f_targets if sum(f) < lc)
     w(f"  static constexpr int NE = {NE}, NET = {NET}, IE_LO = {P.ie_lo}, NF = {NF}, NR = {NR}, GS = {GS};")
     w(f"  static constexpr int LCMIN = {min(lc, ld)}, FI_LC = {fi_lc};")
+    w(f"  static constexpr int NSA = {nsa}, NSB = {nsb}, NSC = {nsc}, NSD = {nsd};")
     w("  static constexpr int NW = 0;")
     lanes = lanes_for(arena, La, Lc)
     w(f"  static constexpr int LANES = {lanes}, GROUPS = LANES == 32 ? kCoopWarps : 1, THREADS = LANES * GROUPS;")
@@ -408,16 +409,12 @@ def emit_coop_class(cls):
         outs = E.emit_sph_pair(kem, l1, l2, cart, "u")
         w("template <int MODE>")
         w(f"__device__ __forceinline__ void {name}(const EriLaunch& P, const Quartet& Q, long long q, int r, "
-          f"const double* __restrict__ G, double& smax_) {{")
+          f"const double* __restrict__ G, double& smax_, double* __restrict__ hb_) {{")
         w(f"  const double* __restrict__ Gr = G + r * {GS};")
-        w("  constexpr int kNSB_ = 1, kNSC_ = 1, kNSD_ = 1;")
-        w("  double jcd_[1], kac_[1], kad_[1];")
-        w("  (void)jcd_;")
-        w("  (void)kac_;")
-        w("  (void)kad_;")
+        w(f"  constexpr int kNCD_ = {nsc * nsd};")
         for ln in kem.lines:
             w("  " + ln)
-        w(f"  OUTPUT_ROW(r, r / {nsb}, r % {nsb});")
+        w(f"  COOP_ROW(r, r / {nsb}, r % {nsb});")
         w(f"  const double* __restrict__ osc_ = kOutScale_{cname} + r * {nsc * nsd};")
         n2 = len(cart2sph(l2))
         for k, var in enumerate(outs):
@@ -425,8 +422,8 @@ def emit_coop_class(cls):
             ic, idd = (i2, i1) if rev else (i1, i2)
             cdi = ic * nsd + idd
             w(f"  const double o{k} = {kem.mul(var, f'__ldg(osc_ + {cdi})')};")
-            w(f"  OUTPUT_VAL(r / {nsb}, r % {nsb}, {ic}, {idd}, o{k});")
-        w("  OUTPUT_ROW_END();")
+            w(f"  COOP_VAL({cdi}, r / {nsb}, r % {nsb}, {ic}, {idd}, o{k});")
+        w("  COOP_ROW_END();")
         w("}")
         return kem
 

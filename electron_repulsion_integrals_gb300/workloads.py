@@ -138,6 +138,24 @@ def cluster(natom: int, seed_index: int, radius: float = 12.0, dmin: float = 2.0
     return Shells(centers, L, nprim, np.concatenate(exps), np.concatenate(coefs))
 
 
+def shell_ladder_cluster(natom: int, lmax: int, seed_index: int, radius: float = 3.0, dmin: float = 1.5) -> Shells:
+    """Small cluster whose every atom carries one shell of each l = 0..lmax
+    (1-3 primitives, exponents log-U[0.1,50], coefficients U[0.1,1]): J and K
+    over classes with f and g shells, the cooperative tier's digestion."""
+    rng = np.random.default_rng(SEED_BASE + seed_index)
+    pos = _ball_positions(rng, natom, radius, dmin)
+    centers, L, nprim, exps, coefs = [], [], [], [], []
+    for a in range(natom):
+        for l in range(lmax + 1):
+            k = int(rng.integers(1, 4))
+            centers.append(pos[a])
+            L.append(l)
+            nprim.append(k)
+            exps.append(_log_uniform(rng, 0.1, 50.0, k))
+            coefs.append(rng.uniform(0.1, 1.0, size=k))
+    return Shells(centers, L, nprim, np.concatenate(exps), np.concatenate(coefs))
+
+
 def cluster64() -> Shells:
     return cluster(64, seed_index=3)
 

@@ -204,10 +204,12 @@ int eri_schwarz(eri_plan* plan, int la, int lb, const int* pairs_dev, long long 
  * double matrices; D must be symmetric; J is overwritten (not accumulated) and
  * comes out symmetric.  The class kernels digest each block as soon as it is
  * formed (no integral is written to memory); J is accumulated with FP64
- * atomics, so its last bits depend on scheduling.  The digestion is built for
- * the register and staged tiers (total angular momentum la+lb+lc+ld <= 8, e.g.
- * every class of s, p, d shells): a screened class above that returns
- * ERI_ERR_NOT_IMPLEMENTED.  Errors: INVALID_ARG, NOT_IMPLEMENTED, CUDA, OOM. */
+ * atomics, so its last bits depend on scheduling.  Every class the library
+ * builds (s through g shells) is digested: the register and staged tiers
+ * (total angular momentum la+lb+lc+ld <= 8) per thread as each value is
+ * formed, the cooperative tier (9 and above) by the group of lanes that
+ * formed the block, one lane per element of J it adds to.  Errors:
+ * INVALID_ARG, CUDA, OOM. */
 int eri_build_J(eri_plan* plan, const double* D_dev, double* J_dev, void* stream);
 
 /* Coulomb and exchange matrices from one pass over the screened quartets (the
@@ -220,9 +222,8 @@ int eri_build_J(eri_plan* plan, const double* D_dev, double* J_dev, void* stream
  * be symmetric; J and K are overwritten and come out symmetric.  J equals what
  * eri_build_J returns up to the order of its atomic additions.  The first call
  * on a plan allocates an nbf x nbf device accumulator for K that the plan keeps
- * until eri_plan_destroy.  Same class limit as eri_build_J.  Errors:
- * INVALID_ARG (NULL argument, plan without a screen), NOT_IMPLEMENTED, OOM,
- * CUDA. */
+ * until eri_plan_destroy.  Every class is digested, as in eri_build_J.
+ * Errors: INVALID_ARG (NULL argument, plan without a screen), OOM, CUDA. */
 int eri_build_JK(eri_plan* plan, const double* D_dev, double* J_dev, double* K_dev, void* stream);
 
 /* Number of unique shell quartets of canonical class (la lb|lc ld) that
@@ -231,6 +232,52 @@ int eri_build_JK(eri_plan* plan, const double* D_dev, double* J_dev, double* K_d
  * own: the page batches quartets by class (section V-C) but states no
  * screening rule. */
 int eri_plan_quartet_count(const eri_plan* plan, int la, int lb, int lc, int ld, long long* n);
+
+/* The screened unique quartets of canonical class (la lb|lc ld) themselves:
+ * writes quartets [first, first + count) of the plan's list for the class --
+ * the eri_plan_quartet_count(...) quartets that eri_build_J evaluates -- to
+ * quartets_dev as int32 [count][4] shell indices (a, b, c, d), ready to pass to
+ * eri_compute_class for the same class.  This is how a caller computes and
+ * stores every surviving integral block class by class and in chunks (the
+ * page's class batches of section V-C, with this library's Schwarz screen).
+ *   - Each unordered quartet of the screen appears once, as one of its eight
+ *     permutation images: L(a) = la, L(b) = lb, L(c) = lc, L(d) = ld, and for
+ *     (la, lb) = (lc, ld) the ket pair comes at or before the bra pair in the
+ *     plan's pair order.
+ *   - The order is the plan's (quartets with equal primitive-loop shapes
+ *     adjacent, heaviest first); it is fixed for the plan's lifetime, so
+ *     consecutive chunks tile the list.
+ *   - quartets_dev: device memory, 16-byte aligned, >= 4 count ints, owned by
+ *     the caller; the kernel is launched on `stream` and the call returns
+ *     without waiting for it.  The plan's device must be current.
+ * Errors: INVALID_ARG (NULL or misaligned buffer, plan without a screen,
+ * first + count above the class's quartet count, another device current),
+ * UNSUPPORTED_L (class not canonical or above the plan's shells), CUDA. */
+int eri_plan_class_quartets(const eri_plan* plan, int la, int lb, int lc, int ld, long long first, long long count,
+                            int* quartets_dev, void* stream);
+
+/* Blocks of the screened unique quartets [first, first + count) of canonical
+ * class (la lb|lc ld): the quartets eri_plan_class_quartets lists, in the same
+ * order, block i (quartet first + i) at out_dev + i B in canonical order
+ * [a][b][c][d] of the listed shells (B = nf(la) nf(lb) nf(lc) nf(ld)).  The
+ * arithmetic is that of eri_compute_class -- FusionRCG Algorithm 2 per
+ * quartet, Eqs. (2), (3), (13), (16) -- on the plan's screened work: the
+ * primitive-pair data precomputed once per shell pair, primitive quartets
+ * whose Schwarz estimate is below 1e-18 skipped (as in eri_build_J), and a
+ * quartet with many primitive quartets split into parts run by different
+ * threads and summed into its block with FP64 atomic adds (the block's last
+ * bits then depend on scheduling; out_dev is cleared first).  This is how the
+ * library computes and stores every surviving integral class by class and in
+ * chunks (section V-C's class batches with this library's screen).
+ *   out_dev: device memory owned by the caller, out_len >= count B doubles.
+ *   The plan's device must be current; the kernels are launched on `stream`
+ *   and the call returns without waiting for them.
+ * Errors: INVALID_ARG (NULL buffer, plan without a screen, first + count above
+ * the class's quartet count, another device current), UNSUPPORTED_L (class
+ * not canonical or above the plan's shells; Cartesian d, f, g output),
+ * BUFFER_TOO_SMALL, OOM (scratch of large classes), CUDA. */
+int eri_compute_screened(eri_plan* plan, int la, int lb, int lc, int ld, long long first, long long count,
+                         double* out_dev, long long out_len, void* stream);
 
 /* Work of canonical class (la lb|lc ld) in eri_build_J: the number of unique
  * shell quartets and of primitive quartets evaluated (after the Schwarz screen

@@ -19,7 +19,12 @@ the oracle in extended precision:
 * in extended precision the same schedule lands at least 100 times closer, so
   the loss is FP64 rounding, not an error in the recurrences;
 * the double result is within the 1e-6 bound that the GPU tests use for
-  classes with a g shell.
+  classes with a g shell;
+* extended precision in one stage only -- the VRR with its [e0|f0] targets
+  rounded to double before a double HRR, or a double VRR followed by an
+  extended HRR -- does not recover the digits: the loss is the FP64 rounding
+  of the [e0|f0] intermediates themselves, which the HRR's cancellation
+  amplifies, so no compensated summation in the HRR alone can remove it.
 """
 
 import types
@@ -79,13 +84,16 @@ def primitive_inputs(s, idx, dtype):
     return prims, types.SimpleNamespace(AB=list(A - B), CD=list(C - D))
 
 
-def block_error(s, idx, dtype):
+def block_error(s, idx, dtype, hrr_dtype=None):
+    """Largest error of the emulated block relative to the block maximum:
+    VRR in dtype, HRR and transforms in hrr_dtype (default dtype), the VRR
+    targets converted between them."""
     S = oracle.ShellSet([s.centers[i] for i in idx], [int(s.L[i]) for i in idx], [int(s.nprim[i]) for i in idx],
                         np.concatenate([s.exps[s.off[i]:s.off[i] + s.nprim[i]] for i in idx]),
                         np.concatenate([s.coefs[s.off[i]:s.off[i] + s.nprim[i]] for i in idx]))
     ref = oracle.eri_block(S, 0, 1, 2, 3, spherical=True, extended=True)
     prims, Qns = primitive_inputs(s, idx, dtype)
-    got, n = emulate_coop_hrr(CLS, prims, Qns, 0, 0, dtype=dtype)
+    got, n = emulate_coop_hrr(CLS, prims, Qns, 0, 0, dtype=dtype, hrr_dtype=hrr_dtype)
     assert n == ref.size
     return float(np.max(np.abs(got.astype(np.float64) - ref)) / np.max(np.abs(ref)))
 
@@ -108,3 +116,6 @@ def test_fp64_hgp_loss_on_a_g_shell_quartet_is_rounding():
     assert err64 <= 1e-6, choices
     err_ext = block_error(s, idx, np.longdouble)
     assert err_ext <= err64 / 100, (err_ext, err64)
+    vrr_ext = block_error(s, idx, np.longdouble, hrr_dtype=np.float64)
+    hrr_ext = block_error(s, idx, np.float64, hrr_dtype=np.longdouble)
+    assert min(vrr_ext, hrr_ext) >= err64 / 4, (vrr_ext, hrr_ext, err64)

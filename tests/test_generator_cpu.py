@@ -366,8 +366,9 @@ def _translate_function(src, name):
     start = next(i for i, ln in enumerate(lines) if re.search(rf"void {name}\(", ln))
     sig = lines[start]
     args = [a.split()[-1].lstrip("&*") for a in sig[sig.index("(") + 1:sig.index(")")].split(",")]
-    if "smax_" in args:
-        args[args.index("smax_")] = "smax_=None"
+    for opt in ("smax_", "hb_"):
+        if opt in args:
+            args[args.index(opt)] = opt + "=None"
     out = [f"def {name}({', '.join(args)}):"]
     for raw in lines[start + 1:]:
         if raw.startswith("}"):
@@ -381,12 +382,12 @@ def _translate_function(src, name):
         if m:
             out.append(f"    {m.group(1)}, {m.group(4)} = {m.group(2)} // {m.group(3)}, {m.group(2)} % {m.group(3)}")
             continue
-        if ln.startswith(("constexpr ", "(void)", "double jcd_[", "OUTPUT_ROW_END")):
+        if ln.startswith(("constexpr ", "(void)", "COOP_ROW_END")):
             continue
-        m = re.match(r"OUTPUT_ROW\(r, .*\);$", ln)
+        m = re.match(r"COOP_ROW\(r, .*\);$", ln)
         if m:
             continue
-        m = re.match(r"OUTPUT_VAL\((\w+) / (\d+), \1 % \2, (\d+), (\d+), (\w+)\);$", ln)
+        m = re.match(r"COOP_VAL\(\d+, (\w+) / (\d+), \1 % \2, (\d+), (\d+), (\w+)\);$", ln)
         if m:
             out.append(f"    OUT[({m.group(1)} // {m.group(2)}, {m.group(1)} % {m.group(2)}, {m.group(3)}, {m.group(4)})]"
                        f" = {m.group(5)}")
@@ -463,14 +464,19 @@ def test_generated_derivative_class_matches_oracle(cls):
         assert worst <= 0, (cls, nprim, float(np.max(np.abs(got - ref) / np.maximum(np.abs(ref), 1e-300))))
 
 
-def emulate_coop_hrr(cls, prims, Qns, rb, rk, dtype=np.float64):
+def emulate_coop_hrr(cls, prims, Qns, rb, rk, dtype=np.float64, hrr_dtype=None):
     """The cooperative kernel's HRR stage on the CPU: the generated bra (one
     call per ket column) and ket (one call per bra row) functions, normal or
     reversed, over the emulated VRR accumulators; returns the spherical block
-    in canonical order (arithmetic in dtype)."""
+    in canonical order (VRR arithmetic in dtype, HRR and transforms in
+    hrr_dtype, by default the same)."""
     from electron_repulsion_integrals_gb300.gen import coop as CP
     src, meta = CP.emit_coop_class(cls)
     H, P = emulate_coop(cls, prims, dtype)
+    if hrr_dtype is not None and hrr_dtype != dtype:
+        dtype = hrr_dtype
+        H = H.astype(dtype)
+        Qns = types.SimpleNamespace(AB=[dtype(x) for x in Qns.AB], CD=[dtype(x) for x in Qns.CD])
     cname = E.class_name(cls)
     bra = f"bra_hrr_rev_{cname}" if rb else f"bra_hrr_{cname}"
     ket = f"ket_hrr_rev_{cname}" if rk else f"ket_hrr_{cname}"

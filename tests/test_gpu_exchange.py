@@ -123,15 +123,29 @@ def test_K_64_atom_cluster_sampled_blocks(dev):
     plan.close()
 
 
-def test_J_and_K_report_classes_above_d_as_not_implemented(dev):
-    """The J/K digestion covers the register and staged tiers (every class of
-    s, p, d shells); a screened class of the cooperative tier is reported, not
-    skipped."""
-    s, _ = W.homogeneous((3, 3, 3, 3), 2, 1, seed_index=830, box=2.0)
+@pytest.mark.parametrize("natom,lmax,seed", [(3, 3, 840), (3, 4, 841)])
+def test_J_and_K_with_f_and_g_shells(dev, natom, lmax, seed):
+    """Classes of the cooperative tier (total angular momentum 9 and above)
+    digested by their own kernels: a 3-atom cluster with s..f or s..g shells
+    on every atom, eri_build_J's J and eri_build_JK's J and K against the
+    oracle's, 1e-10 relative Frobenius."""
+    s = W.shell_ladder_cluster(natom, lmax, seed_index=seed)
+    nbf = W.nbf(s)
+    D = W.density(nbf, seed)
+    Jref, Kref = oracle.build_JK(oshells(s), D, spherical=True, tau=1e-10)[:2]
     plan = eri.Plan(s, spherical=True, schwarz_tau=1e-10)
-    D = torch.zeros((W.nbf(s), W.nbf(s)), dtype=torch.float64, device=dev)
-    for call in (lambda: plan.build_J(D), lambda: plan.build_JK(D)):
-        with pytest.raises(eri.EriError) as ei:
-            call()
-        assert ei.value.code == -7
+    coop = [c for c in plan_classes(lmax) if sum(c) >= 9 and plan.quartet_count(c)]
+    assert len(coop) >= (9 if lmax == 3 else 40), coop
+    Dd = torch.as_tensor(D, device=dev)
+    J1 = plan.build_J(Dd).cpu().numpy()
+    J2, K = (m.cpu().numpy() for m in plan.build_JK(Dd))
+    errs = rel_frob(J1, Jref), rel_frob(J2, Jref), rel_frob(K, Kref)
+    print(f"s..{'fg'[lmax - 3]} cluster: J {errs[0]:.3g}, J (JK) {errs[1]:.3g}, K {errs[2]:.3g}")
+    assert max(errs) <= 1e-10, errs
+    assert np.allclose(K, K.T, rtol=0, atol=1e-12 * np.abs(K).max())
     plan.close()
+
+
+def plan_classes(lmax):
+    from electron_repulsion_integrals_gb300.gen.eri_gen import canonical_classes
+    return canonical_classes(lmax)

@@ -68,3 +68,28 @@ def test_derivative_lanes_are_the_narrowest_that_keep_enough_warps():
             if narrower < lanes:
                 assert warps(narrower) < D.MIN_WARPS_PER_SM
     assert seen[(1, 1, 1, 1)] == 8 and seen[(2, 1, 2, 1)] == 16 and seen[(2, 2, 2, 2)] == 32
+
+
+def test_reference_arm_cluster_counts_match_brute_force():
+    """The reference arm's per-class quartet counts for the cluster workloads
+    (oracle Schwarz factors, counted from sorted pair factors) against an
+    enumeration of every unique quartet of a 4-atom cluster."""
+    bench = pytest.importorskip("bench")
+    import numpy as np
+    import oracle
+    from electron_repulsion_integrals_gb300 import workloads as W
+    s = W.cluster(4, seed_index=800, radius=4.0)
+    L = np.asarray(s.L)
+    Q = oracle.schwarz(oracle.ShellSet(s.centers, s.L, s.nprim, s.exps, s.coefs), spherical=True)
+    pc = lambda x, y: max(L[x], L[y]) * (max(L[x], L[y]) + 1) // 2 + min(L[x], L[y])  # noqa: E731
+    pairs = [(a, b) for a in range(s.n) for b in range(a + 1)]
+    want = {}
+    for i, (a, b) in enumerate(pairs):
+        for c, d in pairs[:i + 1]:
+            if Q[a, b] * Q[c, d] >= 1e-10:
+                hi, lo = ((a, b), (c, d)) if pc(a, b) >= pc(c, d) else ((c, d), (a, b))
+                cls = tuple(sorted((int(L[hi[0]]), int(L[hi[1]])), reverse=True) +
+                            sorted((int(L[lo[0]]), int(L[lo[1]])), reverse=True))
+                want[cls] = want.get(cls, 0) + 1
+    got = {c: n for c, n in bench.oracle_cluster_counts(s).items() if n}
+    assert got == want
