@@ -168,9 +168,12 @@ def eri_plan_shell_info(plan, s):
     return nf.value, first.value
 
 
-def eri_compute_class(plan, cls, quartets, out, stream=None):
-    """quartets: int32 CUDA tensor (n,4); out: float64 CUDA tensor with >= n*B elements."""
-    n = quartets.shape[0] if quartets is not None else 0
+def eri_compute_class(plan, cls, quartets, out, stream=None, n=None):
+    """quartets: int32 CUDA tensor (n,4); out: float64 CUDA tensor with >= n*B elements.
+    quartets None with n = the class's screened quartet count: every screened quartet."""
+    if quartets is not None:
+        n = quartets.shape[0]
+    n = n or 0
     rc = lib().eri_compute_class(plan, *[int(x) for x in cls], _ptr(quartets), int(n), _ptr(out), int(out.numel()),
                                  ctypes.c_void_p(_stream_handle(stream)))
     _check("eri_compute_class", rc)

@@ -828,6 +828,14 @@ int eri_plan_shell_info(const eri_plan* p, int s, int* nf, int* first) {
 
 int eri_compute_class(eri_plan* p, int la, int lb, int lc, int ld, const int* quartets_dev, long long n,
                       double* out_dev, long long out_len, void* stream) {
+  if (p && n > 0 && !quartets_dev && out_dev) {
+    // every screened quartet of the (canonical) class, in the plan's order
+    long long total = 0;
+    const int rc = eri_plan_quartet_count(p, la, lb, lc, ld, &total);
+    if (rc) return rc;
+    if (n != total) return ERI_ERR_INVALID_ARG;
+    return eri_compute_screened(p, la, lb, lc, ld, 0, n, out_dev, out_len, stream);
+  }
   if (!p || n < 0 || (n > 0 && (!quartets_dev || !out_dev))) return ERI_ERR_INVALID_ARG;
   const int l[4] = {la, lb, lc, ld};
   for (int k = 0; k < 4; ++k) {

@@ -127,7 +127,11 @@ int eri_plan_shell_info(const eri_plan* plan, int s, int* nfunc, int* first);
  * four-index transform Eq. (17) (section III-B).
  *   quartets_dev: device int32 array [n][4] of shell indices in the caller's
  *                 order; shell quartets[i][k] must have angular momentum
- *                 (la, lb, lc, ld)[k] (not checked on the device).
+ *                 (la, lb, lc, ld)[k] (not checked on the device).  NULL
+ *                 with n equal to eri_plan_quartet_count for a canonical
+ *                 class selects every screened quartet of the class: the
+ *                 call is then eri_compute_screened(plan, la, lb, lc, ld, 0,
+ *                 n, ...), in eri_plan_class_quartets order.
  *   out_dev:      device double array; block i starts at out_dev + i*B where
  *                 B = nf(la) nf(lb) nf(lc) nf(ld) and is row-major [a][b][c][d];
  *   out_len:      number of doubles available at out_dev (>= n*B).
@@ -166,8 +170,10 @@ int eri_compute_class(eri_plan* plan, int la, int lb, int lc, int ld, const int*
  *     call, so nothing needs clearing between calls.  Calls whose kernels
  *     overlap on the GPU (different streams, or different host threads) race
  *     on the array and give wrong results: serialise them.
- * Errors: those of eri_compute_class, plus ERI_ERR_SCRATCH_LIMIT when one
- * thread block's scratch for the class exceeds the array. */
+ * quartets_dev must not be NULL here (eri_compute_class's selection of every
+ * screened quartet is not offered).  Errors: those of eri_compute_class, plus
+ * ERI_ERR_SCRATCH_LIMIT when one thread block's scratch for the class exceeds
+ * the array. */
 #define ERI_NOALLOC_SCRATCH_BYTES (64ull << 20)
 int eri_compute_class_noalloc(eri_plan* plan, int la, int lb, int lc, int ld, const int* quartets_dev, long long n,
                               double* out_dev, long long out_len, void* stream);

@@ -392,6 +392,7 @@ def _translate_function(src, name):
             out.append(f"    OUT[({m.group(1)} // {m.group(2)}, {m.group(1)} % {m.group(2)}, {m.group(3)}, {m.group(4)})]"
                        f" = {m.group(5)}")
             continue
+        ln = re.sub(r"^__stcs\((\w+) \+ (.+?), (.+)\);$", r"\1[\2] = \3;", ln)
         m = re.match(r"if \(k == 0\) (.+?) = (.+?); else \1 -= (.+?);$", ln)
         if m:
             out.append(f"    {m.group(1)} = {m.group(2)} if k == 0 else {m.group(1)} - {m.group(3)}")

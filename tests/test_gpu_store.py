@@ -164,6 +164,16 @@ def test_screened_blocks_of_a_small_cluster(dev):
     with pytest.raises(eri.EriError) as e:
         eri.eri_compute_screened(plan.handle, (1, 1, 0, 0), 0, 2, small)
     assert e.value.code == -3
+    # eri_compute_class with no quartet list: every screened quartet of the class
+    cls = (2, 1, 1, 0)
+    n = plan.quartet_count(cls)
+    out = torch.empty(n * eri.block_size(cls), dtype=torch.float64, device=dev)
+    eri.eri_compute_class(plan.handle, cls, None, out, n=n)
+    assert np.allclose(out.cpu().numpy(), plan.compute_screened(cls)[:out.numel()].cpu().numpy(), rtol=1e-13,
+                       atol=1e-15)
+    with pytest.raises(eri.EriError) as e:
+        eri.eri_compute_class(plan.handle, cls, None, out, n=n - 1)
+    assert e.value.code == eri.ERI_ERR_INVALID_ARG
     plan.close()
 
 
