@@ -131,6 +131,122 @@ __device__ __forceinline__ void coop_acc_sets(double* __restrict__ H, const doub
   }
 }
 
+// Ket column step, nodes with a cross term: for node u = m nz + k of the
+// rows x nz rectangle (list entry zl[k] = {e, e - 1_i, e_i}),
+//   O[m][e] = qc X[m][e] + wq X[m+1][e] + kyo2e (Y[m][e] - roe Y[m+1][e])
+//             + e_i / (2 (zeta + eta)) X[m+1][e - 1_i]
+// (the Y term when the step has one).  Lane l takes u = u0 + l and
+// u0 + l + LN in iteration u0 (steps of 2 LN, integer stepping of (m, k)
+// only), so that two dependent FMA chains overlap; when at most LN nodes
+// remain (a group-uniform test) one node per lane.  A lane without a second
+// node in a two-node iteration repeats its first and does not store it.
+template <class C>
+__device__ __forceinline__ void coop_cross_nodes(const int4* __restrict__ zl, int nz, int rows,
+                                                 const double* __restrict__ X, const double* __restrict__ Y,
+                                                 double* __restrict__ O, const double* __restrict__ s, double qc,
+                                                 double wq, double kyo2e, double roe, bool hy, int lane) {
+  using S = CoopSetup<C::La, C::Lc, C::NW>;
+  constexpr int NE = C::NE;
+  constexpr int LN = C::LANES;
+  const int total = nz > 0 ? rows * nz : 0;  // (no e_i > 0 only when la + lb = 0)
+  int m = 0, k = nz > 0 ? lane : 0;
+  while (nz > 0 && k >= nz) {
+    k -= nz;
+    ++m;
+  }
+  for (int u0 = 0; u0 < total; u0 += 2 * LN) {
+    if (u0 + LN < total) {
+      int m2 = m, k2 = k + LN;
+      while (k2 >= nz) {
+        k2 -= nz;
+        ++m2;
+      }
+      const bool two = m2 < rows;
+      const int mb = two ? m2 : m, kb = two ? k2 : k;
+      const int4 za = __ldg(zl + k);
+      const int4 zb = __ldg(zl + kb);
+      const int oa = m * NE + za.x, ob = mb * NE + zb.x;
+      double va = qc * X[oa];
+      double vb = qc * X[ob];
+      va = fma(wq, X[oa + NE], va);
+      vb = fma(wq, X[ob + NE], vb);
+      if (hy) {
+        va = fma(kyo2e, fma(-roe, Y[oa + NE], Y[oa]), va);
+        vb = fma(kyo2e, fma(-roe, Y[ob + NE], Y[ob]), vb);
+      }
+      va = fma(s[S::KO2ZE + za.z], X[(m + 1) * NE + za.y], va);
+      vb = fma(s[S::KO2ZE + zb.z], X[(mb + 1) * NE + zb.y], vb);
+      O[oa] = va;
+      if (two) O[ob] = vb;
+      m = m2;
+      k = k2 + LN;
+      while (k >= nz) {
+        k -= nz;
+        ++m;
+      }
+    } else if (m < rows) {
+      const int4 za = __ldg(zl + k);
+      const int oa = m * NE + za.x;
+      double va = qc * X[oa];
+      va = fma(wq, X[oa + NE], va);
+      if (hy) va = fma(kyo2e, fma(-roe, Y[oa + NE], Y[oa]), va);
+      va = fma(s[S::KO2ZE + za.z], X[(m + 1) * NE + za.y], va);
+      O[oa] = va;
+    }
+  }
+}
+
+// Ket column step, nodes without a cross term (e_i = 0), in the same lane
+// pattern: O[m][e] = qc X[m][e] + wq X[m+1][e] (+ the Y term).
+template <class C>
+__device__ __forceinline__ void coop_plain_nodes(const int* __restrict__ nl, int nn, int rows,
+                                                 const double* __restrict__ X, const double* __restrict__ Y,
+                                                 double* __restrict__ O, double qc, double wq, double kyo2e,
+                                                 double roe, bool hy, int lane) {
+  constexpr int NE = C::NE;
+  constexpr int LN = C::LANES;
+  const int total = rows * nn;
+  int m = 0, k = lane;
+  while (k >= nn) {
+    k -= nn;
+    ++m;
+  }
+  for (int u0 = 0; u0 < total; u0 += 2 * LN) {
+    if (u0 + LN < total) {
+      int m2 = m, k2 = k + LN;
+      while (k2 >= nn) {
+        k2 -= nn;
+        ++m2;
+      }
+      const bool two = m2 < rows;
+      const int mb = two ? m2 : m, kb = two ? k2 : k;
+      const int oa = m * NE + __ldg(nl + k), ob = mb * NE + __ldg(nl + kb);
+      double va = qc * X[oa];
+      double vb = qc * X[ob];
+      va = fma(wq, X[oa + NE], va);
+      vb = fma(wq, X[ob + NE], vb);
+      if (hy) {
+        va = fma(kyo2e, fma(-roe, Y[oa + NE], Y[oa]), va);
+        vb = fma(kyo2e, fma(-roe, Y[ob + NE], Y[ob]), vb);
+      }
+      O[oa] = va;
+      if (two) O[ob] = vb;
+      m = m2;
+      k = k2 + LN;
+      while (k >= nn) {
+        k -= nn;
+        ++m;
+      }
+    } else if (m < rows) {
+      const int oa = m * NE + __ldg(nl + k);
+      double va = qc * X[oa];
+      va = fma(wq, X[oa + NE], va);
+      if (hy) va = fma(kyo2e, fma(-roe, Y[oa + NE], Y[oa]), va);
+      O[oa] = va;
+    }
+  }
+}
+
 // VRR of one primitive quartet with parameters s[] into the arena; targets
 // accumulated into H (global, [target column][e - e_lo], e_lo the first
 // component with |e| = min(la, lb)).
@@ -230,106 +346,18 @@ __device__ __forceinline__ void coop_vrr(double* __restrict__ arena, const doubl
         hold[j] = k < C::NET ? Ht[k] : 0.0;
       }
     }
-    // nodes with e_i > 0 (cross term [e - 1_i | f]^(m+1)).  Node u = m nz + k
-    // of the rows x list rectangle; lane l takes u = u0 + l and u0 + l + LN in
-    // iteration u0 (steps of 2 LN, integer stepping of (m, k) only), so that two
-    // dependent FMA chains overlap; when at most LN nodes remain (a
-    // group-uniform test) one node per lane.  A lane without a second node in a
-    // two-node iteration repeats its first and does not store it.
-    {
-      const int nz = C::nz(st.axis);
-      const int4* zl = C::zlist(st.axis);
-      const int total = nz > 0 ? rows * nz : 0;  // (no e_i > 0 only when la + lb = 0)
-      int m = 0, k = nz > 0 ? lane : 0;
-      while (nz > 0 && k >= nz) {
-        k -= nz;
-        ++m;
-      }
-      for (int u0 = 0; u0 < total; u0 += 2 * LN) {
-       if (u0 + LN < total) {
-        int m2 = m, k2 = k + LN;
-        while (k2 >= nz) {
-          k2 -= nz;
-          ++m2;
-        }
-        const bool two = m2 < rows;
-        const int mb = two ? m2 : m, kb = two ? k2 : k;
-        const int4 za = __ldg(zl + k);
-        const int4 zb = __ldg(zl + kb);
-        const int oa = m * NE + za.x, ob = mb * NE + zb.x;
-        double va = qc * X[oa];
-        double vb = qc * X[ob];
-        va = fma(wq, X[oa + NE], va);
-        vb = fma(wq, X[ob + NE], vb);
-        if (hy) {
-          va = fma(kyo2e, fma(-roe, Y[oa + NE], Y[oa]), va);
-          vb = fma(kyo2e, fma(-roe, Y[ob + NE], Y[ob]), vb);
-        }
-        va = fma(s[S::KO2ZE + za.z], X[(m + 1) * NE + za.y], va);
-        vb = fma(s[S::KO2ZE + zb.z], X[(mb + 1) * NE + zb.y], vb);
-        O[oa] = va;
-        if (two) O[ob] = vb;
-        m = m2;
-        k = k2 + LN;
-        while (k >= nz) {
-          k -= nz;
-          ++m;
-        }
-       } else if (m < rows) {
-        const int4 za = __ldg(zl + k);
-        const int oa = m * NE + za.x;
-        double va = qc * X[oa];
-        va = fma(wq, X[oa + NE], va);
-        if (hy) va = fma(kyo2e, fma(-roe, Y[oa + NE], Y[oa]), va);
-        va = fma(s[S::KO2ZE + za.z], X[(m + 1) * NE + za.y], va);
-        O[oa] = va;
-       }
-      }
-    }
-    // nodes with e_i = 0
-    {
-      const int nn = C::nn(st.axis);
-      const int* nl = C::nlist(st.axis);
-      const int total = rows * nn;
-      int m = 0, k = lane;
-      while (k >= nn) {
-        k -= nn;
-        ++m;
-      }
-      for (int u0 = 0; u0 < total; u0 += 2 * LN) {
-       if (u0 + LN < total) {
-        int m2 = m, k2 = k + LN;
-        while (k2 >= nn) {
-          k2 -= nn;
-          ++m2;
-        }
-        const bool two = m2 < rows;
-        const int mb = two ? m2 : m, kb = two ? k2 : k;
-        const int oa = m * NE + __ldg(nl + k), ob = mb * NE + __ldg(nl + kb);
-        double va = qc * X[oa];
-        double vb = qc * X[ob];
-        va = fma(wq, X[oa + NE], va);
-        vb = fma(wq, X[ob + NE], vb);
-        if (hy) {
-          va = fma(kyo2e, fma(-roe, Y[oa + NE], Y[oa]), va);
-          vb = fma(kyo2e, fma(-roe, Y[ob + NE], Y[ob]), vb);
-        }
-        O[oa] = va;
-        if (two) O[ob] = vb;
-        m = m2;
-        k = k2 + LN;
-        while (k >= nn) {
-          k -= nn;
-          ++m;
-        }
-       } else if (m < rows) {
-        const int oa = m * NE + __ldg(nl + k);
-        double va = qc * X[oa];
-        va = fma(wq, X[oa + NE], va);
-        if (hy) va = fma(kyo2e, fma(-roe, Y[oa + NE], Y[oa]), va);
-        O[oa] = va;
-       }
-      }
+    // nodes with e_i > 0 (cross term [e - 1_i | f]^(m+1)), then those with
+    // e_i = 0; a merged step (classes whose column steps gain from it, see
+    // merged_step in gen/coop.py) runs both in one list, the e_i = 0 nodes with
+    // a zero cross-term coefficient
+    bool merged = false;
+    if constexpr (C::MERGED) merged = st.pad != 0;
+    if (merged) {
+      coop_cross_nodes<C>(C::mlist(st.axis), C::nz(st.axis) + C::nn(st.axis), rows, X, Y, O, s, qc, wq, kyo2e, roe, hy,
+                          lane);
+    } else {
+      coop_cross_nodes<C>(C::zlist(st.axis), C::nz(st.axis), rows, X, Y, O, s, qc, wq, kyo2e, roe, hy, lane);
+      coop_plain_nodes<C>(C::nlist(st.axis), C::nn(st.axis), rows, X, Y, O, qc, wq, kyo2e, roe, hy, lane);
     }
     coop_sync<LN>();
     if (st.target >= 0) {

@@ -287,10 +287,63 @@ def resident_blocks(block_smem_bytes, cap=32):
     return max(1, min(cap, SMEM_PER_SM // (block_smem_bytes + 1024 + 32)))
 
 
-def plan_tables(P, cname):
+def _loop_instructions(total, per_node, lanes):
+    """FP64 warp instructions of one node loop of the kernel's column step:
+    iterations of two nodes per lane while more than `lanes` nodes remain,
+    then one (coop_vrr in eri_coop.cuh)."""
+    n, u0 = 0, 0
+    while u0 < total:
+        n += (2 if u0 + lanes < total else 1) * per_node
+        u0 += 2 * lanes
+    return n
+
+
+def merged_step(P, c, lanes):
+    """Whether ket column step c runs its nodes as one list (the e_i > 0
+    components and then the e_i = 0 ones, whose cross term gets a zero
+    coefficient) rather than as two loops.  One list fills the lanes better
+    when the step has few nodes (a high ket level has few m rows) and costs an
+    FMA per e_i = 0 node; the generator takes whichever issues fewer FP64 warp
+    instructions."""
+    rows = P.Lc - c.level + 1
+    nz, nn = len(P.zlist[c.axis]), len(P.nlist[c.axis])
+    per = 2 + (2 if c.y >= 0 else 0)
+    two = _loop_instructions(rows * nz, per + 1, lanes) + _loop_instructions(rows * nn, per, lanes)
+    one = _loop_instructions(rows * (nz + nn), per + 1, lanes)
+    return one < two
+
+
+MERGED_MIN_GAIN = 0.08  # merged steps only where they save at least this share of the ket steps' instructions
+
+
+def merged_flags(P, lanes):
+    """Per ket column step: run it as one merged list (merged_step).  Only
+    for classes where that saves at least MERGED_MIN_GAIN of the column
+    steps' FP64 warp instructions: measured on GB300, (fd|fd) (model: -10.9 %)
+    ran 6.9 % faster with merged steps, while (ff|ff), (gd|gd) and (gg|gg)
+    (model: -0.9 to -2.7 %) ran 4-6 % slower -- a merged e_i = 0 node also
+    loads its cross-term operand and a wider table entry, which the model does
+    not count."""
+    flags, two, best = [], 0, 0
+    for c in P.cols:
+        rows = P.Lc - c.level + 1
+        nz, nn = len(P.zlist[c.axis]), len(P.nlist[c.axis])
+        per = 2 + (2 if c.y >= 0 else 0)
+        t = _loop_instructions(rows * nz, per + 1, lanes) + _loop_instructions(rows * nn, per, lanes)
+        o = _loop_instructions(rows * (nz + nn), per + 1, lanes)
+        flags.append(o < t)
+        two += t
+        best += min(o, t)
+    if two == 0 or best > (1.0 - MERGED_MIN_GAIN) * two:
+        return [False] * len(P.cols)
+    return flags
+
+
+def plan_tables(P, cname, lanes):
     """Device tables of a column schedule (bra nodes, per-axis e lists, ket
-    column steps) and the trait accessors that expose them; returns
-    (table lines, accessor lines, number of bra nodes)."""
+    column steps) and the trait accessors that expose them, for a group of
+    `lanes` lanes per quartet; returns (table lines, accessor lines, number of
+    bra nodes)."""
     by = [x for lev in P.bra_nodes_y for x in lev]
     bys = [0]
     for lev in P.bra_nodes_y:
@@ -310,11 +363,20 @@ def plan_tables(P, cname):
     t.append(_arr(f"kZ_{cname}", "int4", [(a, b, c, 0) for a, b, c in zall], i4))
     nall = [z for ax in range(3) for z in P.nlist[ax]]
     t.append(_arr(f"kN_{cname}", "int", nall, lambda v: "0" if v is None else str(v)))
-    t.append(_arr(f"kCols_{cname}", "CoopCol", [(c.out, c.x, c.y, c.axis, c.ky, c.level, c.target, 0) for c in P.cols],
+    # one list per axis for the merged steps: the e_i > 0 entries, then the
+    # e_i = 0 ones with cross-term coefficient index 0 (k/(2(zeta+eta)) at
+    # k = 0 is 0) and any valid component as its source
+    mall = [z for ax in range(3) for z in P.zlist[ax] + [(n, n, 0) for n in P.nlist[ax]]]
+    t.append(_arr(f"kM_{cname}", "int4", [(a, b, c, 0) for a, b, c in mall], i4))
+    flags = merged_flags(P, lanes)
+    t.append(_arr(f"kCols_{cname}", "CoopCol", [(c.out, c.x, c.y, c.axis, c.ky, c.level, c.target, int(f))
+                                                 for c, f in zip(P.cols, flags)],
                   lambda v: "{0,0,0,0,0,0,0,0}" if v is None else "{%d,%d,%d,%d,%d,%d,%d,%d}" % v))
     nz = [len(P.zlist[a]) for a in range(3)]
     nn = [len(P.nlist[a]) for a in range(3)]
+    nm = [nz[a] + nn[a] for a in range(3)]
     a = []
+    a.append(f"  static constexpr bool MERGED = {'true' if any(flags) else 'false'};")
     a.append(f"  static __device__ __forceinline__ const int4* bra_y() {{ return kBraY_{cname}; }}")
     a.append(f"  static __device__ __forceinline__ const int* bra_y_start() {{ return kBraYS_{cname}; }}")
     a.append(f"  static __device__ __forceinline__ const int4* bra_n() {{ return kBraN_{cname}; }}")
@@ -326,6 +388,8 @@ def plan_tables(P, cname):
              f"{nz[0]} : {nz[0] + nz[1]}); }}")
     a.append(f"  static __device__ __forceinline__ const int* nlist(int a) {{ return kN_{cname} + (a == 0 ? 0 : a == 1 ? "
              f"{nn[0]} : {nn[0] + nn[1]}); }}")
+    a.append(f"  static __device__ __forceinline__ const int4* mlist(int a) {{ return kM_{cname} + (a == 0 ? 0 : a == 1 ? "
+             f"{nm[0]} : {nm[0] + nm[1]}); }}")
     return t, a, len(by) + len(bn)
 
 
@@ -344,7 +408,8 @@ def emit_coop_class(cls):
     NR = nsa * nsb
     GS = NF | 1
     arena = max(P.arena, NR * GS)
-    tables, accessors, nbra = plan_tables(P, cname)
+    lanes = lanes_for(arena, La, Lc)
+    tables, accessors, nbra = plan_tables(P, cname, lanes)
     bc = P.bra_col
     lines = []
     w = lines.append
@@ -367,7 +432,6 @@ def emit_coop_class(cls):
     w(f"  static constexpr int LCMIN = {min(lc, ld)}, FI_LC = {fi_lc};")
     w(f"  static constexpr int NSA = {nsa}, NSB = {nsb}, NSC = {nsc}, NSD = {nsd};")
     w("  static constexpr int NW = 0;")
-    lanes = lanes_for(arena, La, Lc)
     w(f"  static constexpr int LANES = {lanes}, GROUPS = LANES == 32 ? kCoopWarps : 1, THREADS = LANES * GROUPS;")
     w(f"  static constexpr int NCOL = {len(P.cols)}, BRA_COL = {bc}, ARENA = {arena}, NH = {NF * NET};")
     w(f"  static constexpr int WARP_SMEM = ARENA + kCoopBatch * CoopSetup<La, Lc>::STRIDE;")

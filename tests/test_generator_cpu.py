@@ -523,3 +523,43 @@ def test_coop_hrr_functions_match_oracle(cls, rb, rk):
     tol = np.maximum(1e-10 * np.abs(ref), 1e-12 * m)
     worst = np.max(np.abs(got - ref) - tol)
     assert worst <= 0, (cls, rb, rk, float(np.max(np.abs(got - ref)) / m))
+
+
+@pytest.mark.parametrize("cls", [(3, 2, 3, 2), (3, 3, 3, 3), (4, 4, 4, 4), (3, 3, 2, 2)],
+                         ids=lambda c: "".join(map(str, c)))
+def test_merged_column_step_tables(cls):
+    """The cooperative kernel's merged column steps: the emitted per-axis
+    merged list is the e_i > 0 list followed by the e_i = 0 components with
+    cross-term coefficient index 0 (k / (2 (zeta + eta)) at k = 0 is zero); in
+    a class above the gain threshold a step is flagged merged exactly when
+    that issues fewer FP64 warp instructions than two loops, and a class
+    below it has no merged step."""
+    from electron_repulsion_integrals_gb300.gen import coop as CP
+    src, _ = CP.emit_coop_class(cls)
+    P = CP.plan(cls)
+    lanes = int(re.search(r"LANES = (\d+)", src).group(1))
+    body = src[src.index("kM_"):]
+    body = body[body.index("{") + 1:body.index("};")]
+    got = [tuple(int(v) for v in t.split(",")) for t in re.findall(r"\{([-\d,]+)\}", body)]
+    want = [(a, b, c, 0) for ax in range(3) for a, b, c in P.zlist[ax] + [(n, n, 0) for n in P.nlist[ax]]]
+    assert got == want
+    cols = src[src.index("kCols_"):]
+    cols = cols[cols.index("{") + 1:cols.index("};")]
+    flags = [int(t.split(",")[-1]) for t in re.findall(r"\{([-\d,]+)\}", cols)]
+    assert flags == [int(f) for f in CP.merged_flags(P, lanes)]
+    if cls == (3, 2, 3, 2):   # merged where one list is cheaper
+        assert flags == [int(CP.merged_step(P, c, lanes)) for c in P.cols] and 0 < sum(flags) < len(flags)
+        assert "MERGED = true" in src
+    else:                     # below the gain threshold: no merged steps at all
+        assert sum(flags) == 0 and "MERGED = false" in src
+    # the model: (fd|fd) saves about a tenth of its ket-step instructions
+    if cls == (3, 2, 3, 2):
+        def cost(c, merged):
+            rows, nz, nn = P.Lc - c.level + 1, len(P.zlist[c.axis]), len(P.nlist[c.axis])
+            per = 2 + (2 if c.y >= 0 else 0)
+            if merged:
+                return CP._loop_instructions(rows * (nz + nn), per + 1, lanes)
+            return CP._loop_instructions(rows * nz, per + 1, lanes) + CP._loop_instructions(rows * nn, per, lanes)
+        two = sum(cost(c, False) for c in P.cols)
+        best = sum(cost(c, f) for c, f in zip(P.cols, flags))
+        assert best <= 0.92 * two, (best, two)
