@@ -139,6 +139,9 @@ struct EriLaunch {
   // class's quartet g goes to out + (g - q0) out_stride
   const long long* seg_qstart;
   long long item0, q0;
+  // screened modes: work counter (zeroed before the launch) from which each
+  // warp takes its next 32 consecutive work items
+  unsigned long long* work;
   // scratch for staged classes: slot s of thread t at scratch[s * nthreads + t]
   double* scratch;
   const double* boys;
@@ -346,6 +349,42 @@ __device__ __forceinline__ void load_quartet_coulomb(const EriLaunch& P, long lo
   }
   Q.rb = 0;
   Q.rk = 0;
+}
+
+// Work distribution of the thread-per-quartet kernels.  Stored batches take
+// their quartets in grid-stride order.  The screened modes' work items are
+// sorted by primitive-loop size, heaviest first, and vary in cost; there each
+// warp takes the next 32 consecutive items from a counter when it is ready for
+// them (all lanes call item_loop_next together: the shuffle waits for the
+// warp), so the items are spread over the GPU in order of their cost and
+// a lane with a light item is not left waiting for its stride's heavy ones.
+// The loop runs over the warp's first item q_; the lane's item is
+// item_of(q_); lanes past the end take part in the next grab.
+template <int MODE>
+__device__ __forceinline__ long long item_loop_first(const EriLaunch& P, long long gid) {
+  if constexpr (MODE >= kCoulomb) {
+    unsigned long long v = 0;
+    if ((threadIdx.x & 31) == 0) v = atomicAdd(P.work, 32ull);
+    return (long long)__shfl_sync(0xffffffffu, v, 0);
+  } else {
+    return gid;
+  }
+}
+template <int MODE>
+__device__ __forceinline__ long long item_loop_next(const EriLaunch& P, long long q_, long long nt) {
+  if constexpr (MODE >= kCoulomb) {
+    return item_loop_first<MODE>(P, 0);
+  } else {
+    return q_ + nt;
+  }
+}
+template <int MODE>
+__device__ __forceinline__ long long item_of(long long q_) {
+  if constexpr (MODE >= kCoulomb) {
+    return q_ + (threadIdx.x & 31);
+  } else {
+    return q_;
+  }
 }
 
 // Coulomb mode, after the primitive loop: what the digestion of the finished

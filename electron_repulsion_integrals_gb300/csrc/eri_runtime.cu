@@ -581,6 +581,8 @@ int eri::host::launch_class(eri_plan* p, const int l[4], EriLaunch& P, int mode,
   const ClassEntry* ce = find_class(l[0], l[1], l[2], l[3]);
   if (!ce) return ERI_ERR_UNSUPPORTED_L;
   if (P.n <= 0) return ERI_OK;
+  // the screened modes hand out their work items through P.work
+  if (mode >= kCoulomb && !P.work) return ERI_ERR_INVALID_ARG;
   fill_shells(p, P.sh);
   P.boys = p->dboys;
   long long blocks = 0, scratch = 0;

@@ -179,6 +179,7 @@ struct Screen {
   int* dshell_of = nullptr;
   double* Jacc = nullptr;
   double* Kacc = nullptr;  // allocated by the first eri_build_JK
+  unsigned long long* dwork = nullptr;  // work counter of the screened launches
   std::vector<ClassWork> classes;
   ~Screen() {
     cudaFree(dpairs);
@@ -186,6 +187,7 @@ struct Screen {
     cudaFree(dshell_of);
     cudaFree(Jacc);
     cudaFree(Kacc);
+    cudaFree(dwork);
     for (auto& c : classes) {
       cudaFree(c.dsegs);
       cudaFree(c.dstart);
@@ -527,6 +529,7 @@ int build(eri_plan* p, cudaStream_t st) {
   CUDA_TRY(cudaMalloc(&S->dshell_of, std::max(nbf, 1) * sizeof(int)));
   CUDA_TRY(cudaMemcpyAsync(S->dshell_of, shell_of.data(), nbf * sizeof(int), cudaMemcpyHostToDevice, st));
   CUDA_TRY(cudaMalloc(&S->Jacc, std::max<size_t>((size_t)nbf * nbf, 1) * sizeof(double)));
+  CUDA_TRY(cudaMalloc(&S->dwork, sizeof(unsigned long long)));
   CUDA_TRY(cudaStreamSynchronize(st));
   return ERI_OK;
 }
@@ -567,6 +570,8 @@ int build_digest(eri_plan* p, const double* D, double* J, double* K, cudaStream_
     P.segs = W.dsegs;
     P.seg_start = W.dstart;
     P.nseg = W.nseg;
+    P.work = S->dwork;
+    CUDA_TRY(cudaMemsetAsync(S->dwork, 0, sizeof(unsigned long long), st));
     int rc = eri::host::launch_class(p, W.l, P, K ? kExchange : kCoulomb, st);
     if (rc) return rc;
   }
@@ -689,6 +694,8 @@ int eri_compute_screened(eri_plan* p, int la, int lb, int lc, int ld, long long 
   P.seg_start = W->dstart;
   P.seg_qstart = W->dqstart;
   P.nseg = W->nseg;
+  P.work = S->dwork;
+  CUDA_TRY(cudaMemsetAsync(S->dwork, 0, sizeof(unsigned long long), st));
   return eri::host::launch_class(p, W->l, P, kStoreScreen, st);
 }
 
