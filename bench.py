@@ -2,7 +2,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload homogeneous|high_l|g_shells|deriv|classes|cluster64|cluster200|cluster64_jk|
-                                cluster200_jk|cluster64_store|ladder_f_jk]
+                                cluster200_jk|cluster64_store|ladder_f_jk|deriv_f]
                     [--scale S] [--ablation all|NAME,...]
 
 A step is one pass of the hot path over the workload's batch: for every class
@@ -63,6 +63,9 @@ WORKLOADS = {
     "deriv": {"desc": "first derivatives (12 blocks per quartet): (pp|pp) x 524,288 + (dd|dd) x 131,072 quartets, "
                       "degree 1, centers U[0,10]^3 bohr, exponents log-U[0.05,100], spherical",
               "classes": [((1, 1, 1, 1), 1 << 19, 1, 4), ((2, 2, 2, 2), 1 << 17, 1, 104)], "deriv": True},
+    "deriv_f": {"desc": "first derivatives of f-shell classes (12 blocks per quartet): (fd|fd) x 16,384 + (ff|ff) x "
+                        "4,096 quartets, degree 1, centers U[0,10]^3 bohr, exponents log-U[0.05,100], spherical",
+                "classes": [((3, 2, 3, 2), 1 << 14, 1, 105), ((3, 3, 3, 3), 1 << 12, 1, 106)], "deriv": True},
     "classes": {"desc": "every canonical class of s, p, d, f shells through (ff|ff) (55 classes), contraction "
                         "degree 1 and 2, centers U[0,10]^3 bohr, exponents log-U[0.05,100], spherical; quartets per "
                         "class sized to about 8 GFLOP per launch"},

@@ -188,10 +188,10 @@ int eri_compute_class_noalloc(eri_plan* plan, int la, int lb, int lc, int ld, co
  * section IV, "Build system"), with the targets accumulated plain and
  * weighted by 2 alpha, 2 beta, 2 gamma, 2 delta; each of the four centres'
  * blocks is formed directly.
- * Classes of s, p and d shells (la, lb, lc, ld <= 2).
+ * Classes of s, p, d and f shells (la, lb, lc, ld <= 3).
  * Layout: per quartet 12 consecutive blocks, [position k][axis i][block], each
  * block row-major [a][b][c][d] as in eri_compute_class; out_len (doubles) must
- * be >= 12 n x block size.  Errors: as eri_compute_class; UNSUPPORTED_L above d. */
+ * be >= 12 n x block size.  Errors: as eri_compute_class; UNSUPPORTED_L above f. */
 int eri_compute_class_deriv(eri_plan* plan, int la, int lb, int lc, int ld, const int* quartets_dev, long long n,
                             double* out_dev, long long out_len, void* stream);
 

@@ -35,14 +35,14 @@ import pytest
 import oracle
 from electron_repulsion_integrals_gb300 import workloads as W
 
-from test_generator_cpu import emulate_coop_hrr
+from test_generator_cpu import emulate_coop_hrr, emulate_deriv
 
 mpmath = pytest.importorskip("mpmath")
 
 CLS = (4, 4, 4, 4)
 
 
-def primitive_inputs(s, idx, dtype):
+def primitive_inputs(s, idx, dtype, L=None):
     """Per primitive quartet the inputs the kernel's setup provides (pair and
     quartet parameters, prefactor times F_m(T)), computed in dtype from the
     shells' centres, exponents and the oracle's normalised coefficients."""
@@ -52,7 +52,7 @@ def primitive_inputs(s, idx, dtype):
     ex = [X(s.exps[s.off[i]:s.off[i] + s.nprim[i]]) for i in idx]
     d = [X(oracle.norm_coefs(int(s.L[i]), s.exps[s.off[i]:s.off[i] + s.nprim[i]],
                              s.coefs[s.off[i]:s.off[i] + s.nprim[i]])) for i in idx]
-    L = sum(int(s.L[i]) for i in idx)
+    L = sum(int(s.L[i]) for i in idx) if L is None else L
     A, B, C, D = cen
     one = dtype(1)
     two_pi52 = dtype(mpmath.nstr(2 * mpmath.pi ** mpmath.mpf(2.5), 35))
@@ -62,14 +62,15 @@ def primitive_inputs(s, idx, dtype):
             a, b = ex[0][i], ex[1][j]
             z = a + b
             P = (a * A + b * B) / z
-            pb = types.SimpleNamespace(zeta=z, o2z=one / (2 * z), P=list(P), PA=list(P - A))
+            pb = types.SimpleNamespace(zeta=z, o2z=one / (2 * z), P=list(P), PA=list(P - A), alpha=a, beta=b)
             Kab = np.exp(-a * b / z * np.sum((A - B) ** 2)) * d[0][i] * d[1][j]
             for k in range(len(ex[2])):
                 for m in range(len(ex[3])):
                     c, e_ = ex[2][k], ex[3][m]
                     eta = c + e_
                     Q = (c * C + e_ * D) / eta
-                    pk = types.SimpleNamespace(zeta=eta, o2z=one / (2 * eta), P=list(Q), PA=list(Q - C))
+                    pk = types.SimpleNamespace(zeta=eta, o2z=one / (2 * eta), P=list(Q), PA=list(Q - C), gamma=c,
+                                               delta=e_)
                     Kcd = np.exp(-c * e_ / eta * np.sum((C - D) ** 2)) * d[2][k] * d[3][m]
                     PQ = Q - P
                     rho = z * eta / (z + eta)
@@ -119,3 +120,29 @@ def test_fp64_hgp_loss_on_a_g_shell_quartet_is_rounding():
     vrr_ext = block_error(s, idx, np.longdouble, hrr_dtype=np.float64)
     hrr_ext = block_error(s, idx, np.float64, hrr_dtype=np.longdouble)
     assert min(vrr_ext, hrr_ext) >= err64 / 4, (vrr_ext, hrr_ext, err64)
+
+
+def test_fp64_loss_of_an_f_shell_derivative_quartet_is_rounding():
+    """First derivatives of a (fd|fp) quartet of the derivative tests' workload
+    (degree 1, exponents log-uniform in [0.05, 100], centres in a 10 bohr
+    cube): the derivative kernel's schedule -- the VRR raised to (gd|dp) with
+    its five accumulator sets and the generated derivative HRR functions --
+    on the CPU misses the oracle by more than 1e-6 of the quartet's largest
+    derivative element in double, as the GPU does, and by at least 1,000 times
+    less in extended precision: FP64 rounding of the g-level recurrences, for
+    which the GPU tests hold f-shell derivative classes to 1e-5 of that
+    maximum."""
+    if np.finfo(np.longdouble).eps > 1e-18:
+        pytest.skip("np.longdouble is not wider than double on this host")
+    cls = (3, 2, 3, 1)
+    s, q = W.homogeneous(cls, 12, 1, seed_index=760 + sum(cls) + 10)
+    idx = [int(x) for x in q[8]]
+    S = oracle.ShellSet(s.centers, s.L, s.nprim, s.exps, s.coefs)
+    ref = np.asarray(oracle.eri_deriv_blocks(S, np.array([idx], dtype=np.int32), spherical=True)).reshape(-1)
+    err = {}
+    for dt in (np.float64, np.longdouble):
+        prims, Qns = primitive_inputs(s, idx, dt, L=sum(cls) + 2)
+        got = emulate_deriv(cls, prims, Qns, dtype=dt).astype(np.float64).reshape(-1)
+        err[dt] = float(np.max(np.abs(got - ref)) / np.max(np.abs(ref)))
+    assert 1e-6 < err[np.float64] <= 1e-5, err
+    assert err[np.longdouble] <= err[np.float64] / 1000, err

@@ -405,17 +405,19 @@ def _translate_function(src, name):
     return "\n".join(out)
 
 
-def emulate_deriv(cls, prims, Qns):
+def emulate_deriv(cls, prims, Qns, dtype=np.float64):
     """The derivative kernel of class cls on the CPU: the cooperative VRR of the
     raised class with the plain, 2 alpha, 2 beta, 2 gamma and 2 delta accumulator sets,
     then the generated bra and ket functions in the kernel's order.  Returns the
-    12 blocks [position][axis][block] of one quartet in canonical order."""
+    12 blocks [position][axis][block] of one quartet in canonical order
+    (arithmetic in dtype)."""
     from electron_repulsion_integrals_gb300.gen import coop as CP
     from electron_repulsion_integrals_gb300.gen import deriv as D
     la, lb, lc, ld = cls
     src, meta = D.emit_deriv_class(cls)
     P = CP.plan((la + 1, lb, lc + 1, ld), e_lo=max(0, la - 1), f_lo=max(0, lc - 1))
-    Hs = emulate_coop_plan(P, prims, lambda pr: (2 * pr[0].alpha, 2 * pr[0].beta, 2 * pr[1].gamma, 2 * pr[1].delta))
+    Hs = emulate_coop_plan(P, prims, lambda pr: (2 * pr[0].alpha, 2 * pr[0].beta, 2 * pr[1].gamma, 2 * pr[1].delta),
+                           dtype=dtype)
     cname = "d" + E.class_name(cls)[1:]
     ns = {"fma": fma}
     for fn in ("bra_dA", "bra_dB", "bra_0", "bra_g", "bra_d", "ket_ab", "ket_c", "ket_d"):
@@ -423,7 +425,7 @@ def emulate_deriv(cls, prims, Qns):
     nf = [2 * l + 1 if l >= 2 else (l + 1) * (l + 2) // 2 for l in cls]
     bs = nf[0] * nf[1] * nf[2] * nf[3]
     NF, NR = Hs.shape[1], nf[0] * nf[1]
-    out = np.zeros(12 * bs)
+    out = np.zeros(12 * bs, dtype=dtype)
     Q = types.SimpleNamespace(AB=Qns.AB, CD=Qns.CD, pos=[0, 1, 2, 3],
                               ost=[nf[1] * nf[2] * nf[3], nf[2] * nf[3], nf[3], 1])
     ns["deriv_out"] = lambda P_, Q_, q_, k_, x_: _Ptr(out, (Q_.pos[k_] * 3 + x_) * bs)
@@ -432,7 +434,7 @@ def emulate_deriv(cls, prims, Qns):
     sets = meta["set_cols"]
     H = _Ptr(np.concatenate([Hs[w][c0:c1].reshape(-1) for w, (c0, c1) in enumerate(sets)]))
     assert len(H.a) == meta["nht"]
-    G = _Ptr(np.zeros(meta["arena"]))
+    G = _Ptr(np.zeros(meta["arena"], dtype=dtype))
     for bra, k, w in (("bra_dA", 0, 1), ("bra_dB", 1, 2)):
         for fi in range(*sets[w]):
             ns[f"{bra}_{cname}"](Q, H, fi, G)
@@ -447,7 +449,8 @@ def emulate_deriv(cls, prims, Qns):
     return out.reshape(4, 3, bs)
 
 
-DERIV_CLASSES = [(0, 0, 0, 0), (1, 0, 1, 0), (1, 1, 1, 1), (2, 0, 1, 1), (2, 1, 2, 1), (2, 2, 1, 0), (2, 2, 2, 2)]
+DERIV_CLASSES = [(0, 0, 0, 0), (1, 0, 1, 0), (1, 1, 1, 1), (2, 0, 1, 1), (2, 1, 2, 1), (2, 2, 1, 0), (2, 2, 2, 2),
+                 (3, 1, 2, 0), (3, 2, 3, 1)]
 
 
 @pytest.mark.parametrize("cls", DERIV_CLASSES, ids=lambda c: "".join(map(str, c)))

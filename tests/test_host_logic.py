@@ -55,7 +55,9 @@ def test_derivative_lanes_are_the_narrowest_that_keep_enough_warps():
         la, lb, lc, ld = cls
         per_quartet = meta["arena"] + 4 * CP.setup_stride(la + lb + 1, lc + ld + 1, 4)  # weights 2 alpha .. 2 delta
         lanes = _lanes(src)
-        assert lanes in (8, 16, 32) and "GROUPS = 32 / LANES, THREADS = 32" in src
+        assert lanes in (8, 16, 32, 128)
+        groups = 32 // lanes if lanes <= 32 else 1
+        assert f"GROUPS = {groups}, THREADS = {lanes * groups}" in src
         seen[cls] = lanes
 
         def warps(w):  # resident warps per SM with w lanes per quartet (one warp per block)
@@ -67,7 +69,12 @@ def test_derivative_lanes_are_the_narrowest_that_keep_enough_warps():
         for narrower in (8, 16):
             if narrower < lanes:
                 assert warps(narrower) < D.MIN_WARPS_PER_SM
+        # four warps share a quartet exactly when shared memory leaves at most
+        # MAX_GROUPS_FOR_WIDE one-warp quartets on an SM
+        wide = CP.SMEM_PER_SM // (per_quartet * 8 + 1024) <= CP.MAX_GROUPS_FOR_WIDE
+        assert (lanes == 128) == wide, (cls, lanes)
     assert seen[(1, 1, 1, 1)] == 8 and seen[(2, 1, 2, 1)] == 16 and seen[(2, 2, 2, 2)] == 32
+    assert seen[(3, 3, 3, 3)] == 128
 
 
 def test_reference_arm_cluster_counts_match_brute_force():
