@@ -1,6 +1,6 @@
 // eri_compute_class_deriv: first derivatives of contracted ERI blocks with
 // respect to the four shell centres (kernels: eri_deriv.cuh and the generated
-// generated/d*.cu, one per canonical class of s, p and d shells).
+// generated/d*.cu, one per canonical class of s, p, d and f shells).
 #include <cuda_runtime.h>
 
 #include <cstdint>
