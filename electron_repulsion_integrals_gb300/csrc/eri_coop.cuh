@@ -149,23 +149,38 @@ __device__ __forceinline__ void coop_cross_nodes(const int4* __restrict__ zl, in
   constexpr int NE = C::NE;
   constexpr int LN = C::LANES;
   const int total = nz > 0 ? rows * nz : 0;  // (no e_i > 0 only when la + lb = 0)
-  int m = 0, k = nz > 0 ? lane : 0;
-  while (nz > 0 && k >= nz) {
+  if (total == 0) return;
+  // (m, k) of this lane's first node u0 + lane, (m2, k2) of its second node
+  // u0 + lane + LN; the list entries of the next iteration are fetched one
+  // iteration ahead (every k stays in [0, nz), so each fetch is in bounds)
+  int m = 0, k = lane;
+  while (k >= nz) {
     k -= nz;
     ++m;
   }
+  int m2 = m, k2 = k + LN;
+  while (k2 >= nz) {
+    k2 -= nz;
+    ++m2;
+  }
+  int4 za = __ldg(zl + k), zb = __ldg(zl + k2);
   for (int u0 = 0; u0 < total; u0 += 2 * LN) {
+    int mn = m2, kn = k2 + LN;
+    while (kn >= nz) {
+      kn -= nz;
+      ++mn;
+    }
+    int mn2 = mn, kn2 = kn + LN;
+    while (kn2 >= nz) {
+      kn2 -= nz;
+      ++mn2;
+    }
+    const int4 zan = __ldg(zl + kn), zbn = __ldg(zl + kn2);
     if (u0 + LN < total) {
-      int m2 = m, k2 = k + LN;
-      while (k2 >= nz) {
-        k2 -= nz;
-        ++m2;
-      }
       const bool two = m2 < rows;
-      const int mb = two ? m2 : m, kb = two ? k2 : k;
-      const int4 za = __ldg(zl + k);
-      const int4 zb = __ldg(zl + kb);
-      const int oa = m * NE + za.x, ob = mb * NE + zb.x;
+      const int mb = two ? m2 : m;
+      const int4 zbb = two ? zb : za;
+      const int oa = m * NE + za.x, ob = mb * NE + zbb.x;
       double va = qc * X[oa];
       double vb = qc * X[ob];
       va = fma(wq, X[oa + NE], va);
@@ -175,17 +190,10 @@ __device__ __forceinline__ void coop_cross_nodes(const int4* __restrict__ zl, in
         vb = fma(kyo2e, fma(-roe, Y[ob + NE], Y[ob]), vb);
       }
       va = fma(s[S::KO2ZE + za.z], X[(m + 1) * NE + za.y], va);
-      vb = fma(s[S::KO2ZE + zb.z], X[(mb + 1) * NE + zb.y], vb);
+      vb = fma(s[S::KO2ZE + zbb.z], X[(mb + 1) * NE + zbb.y], vb);
       O[oa] = va;
       if (two) O[ob] = vb;
-      m = m2;
-      k = k2 + LN;
-      while (k >= nz) {
-        k -= nz;
-        ++m;
-      }
     } else if (m < rows) {
-      const int4 za = __ldg(zl + k);
       const int oa = m * NE + za.x;
       double va = qc * X[oa];
       va = fma(wq, X[oa + NE], va);
@@ -193,6 +201,12 @@ __device__ __forceinline__ void coop_cross_nodes(const int4* __restrict__ zl, in
       va = fma(s[S::KO2ZE + za.z], X[(m + 1) * NE + za.y], va);
       O[oa] = va;
     }
+    m = mn;
+    k = kn;
+    m2 = mn2;
+    k2 = kn2;
+    za = zan;
+    zb = zbn;
   }
 }
 
@@ -206,21 +220,33 @@ __device__ __forceinline__ void coop_plain_nodes(const int* __restrict__ nl, int
   constexpr int NE = C::NE;
   constexpr int LN = C::LANES;
   const int total = rows * nn;
+  if (total == 0) return;
   int m = 0, k = lane;
   while (k >= nn) {
     k -= nn;
     ++m;
   }
+  int m2 = m, k2 = k + LN;
+  while (k2 >= nn) {
+    k2 -= nn;
+    ++m2;
+  }
+  int ea = __ldg(nl + k), eb = __ldg(nl + k2);
   for (int u0 = 0; u0 < total; u0 += 2 * LN) {
+    int mn = m2, kn = k2 + LN;
+    while (kn >= nn) {
+      kn -= nn;
+      ++mn;
+    }
+    int mn2 = mn, kn2 = kn + LN;
+    while (kn2 >= nn) {
+      kn2 -= nn;
+      ++mn2;
+    }
+    const int ean = __ldg(nl + kn), ebn = __ldg(nl + kn2);
     if (u0 + LN < total) {
-      int m2 = m, k2 = k + LN;
-      while (k2 >= nn) {
-        k2 -= nn;
-        ++m2;
-      }
       const bool two = m2 < rows;
-      const int mb = two ? m2 : m, kb = two ? k2 : k;
-      const int oa = m * NE + __ldg(nl + k), ob = mb * NE + __ldg(nl + kb);
+      const int oa = m * NE + ea, ob = two ? m2 * NE + eb : oa;
       double va = qc * X[oa];
       double vb = qc * X[ob];
       va = fma(wq, X[oa + NE], va);
@@ -231,19 +257,19 @@ __device__ __forceinline__ void coop_plain_nodes(const int* __restrict__ nl, int
       }
       O[oa] = va;
       if (two) O[ob] = vb;
-      m = m2;
-      k = k2 + LN;
-      while (k >= nn) {
-        k -= nn;
-        ++m;
-      }
     } else if (m < rows) {
-      const int oa = m * NE + __ldg(nl + k);
+      const int oa = m * NE + ea;
       double va = qc * X[oa];
       va = fma(wq, X[oa + NE], va);
       if (hy) va = fma(kyo2e, fma(-roe, Y[oa + NE], Y[oa]), va);
       O[oa] = va;
     }
+    m = mn;
+    k = kn;
+    m2 = mn2;
+    k2 = kn2;
+    ea = ean;
+    eb = ebn;
   }
 }
 
