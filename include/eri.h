@@ -71,7 +71,8 @@ typedef struct {
 
 typedef struct {
   int spherical;      /* 1: spherical functions for l >= 2 (required for d, f and g shells); 0: Cartesian */
-  double schwarz_tau; /* Schwarz threshold for eri_build_J / eri_plan_quartet_count; <= 0 keeps every quartet */
+  double schwarz_tau; /* Schwarz threshold of the plan's screen (eri_build_J, eri_build_JK, eri_plan_quartet_count,
+                         eri_plan_class_quartets, eri_compute_screened); <= 0: no screen is built */
   int flags;          /* reserved, must be 0 */
 } eri_options;
 
@@ -205,17 +206,20 @@ int eri_schwarz(eri_plan* plan, int la, int lb, const int* pairs_dev, long long 
 /* Coulomb matrix J_{mu nu} = sum_{lambda sigma} (mu nu|lambda sigma) D_{lambda sigma}
  * (the scatter of each finished block into J with the density that ends
  * FusionRCG Algorithm 2; section V-C builds J this way from the class batches)
- * over every unique shell quartet that passes Q_ab Q_cd >= schwarz_tau
- * (all of them when tau <= 0).  D_dev and J_dev are device nbf x nbf row-major
+ * over every unique shell quartet that passes Q_ab Q_cd >= schwarz_tau.  The
+ * plan needs a screen (schwarz_tau > 0 at eri_plan_create; a tiny tau such as
+ * 1e-300 keeps every quartet whose bound is not zero); without one the call
+ * returns INVALID_ARG.  D_dev and J_dev are device nbf x nbf row-major
  * double matrices; D must be symmetric; J is overwritten (not accumulated) and
  * comes out symmetric.  The class kernels digest each block as soon as it is
- * formed (no integral is written to memory); J is accumulated with FP64
- * atomics, so its last bits depend on scheduling.  Every class the library
- * builds (s through g shells) is digested: the register and staged tiers
- * (total angular momentum la+lb+lc+ld <= 8) per thread as each value is
- * formed, the cooperative tier (9 and above) by the group of lanes that
- * formed the block, one lane per element of J it adds to.  Errors:
- * INVALID_ARG, CUDA, OOM. */
+ * formed; J is accumulated with FP64 atomics, so its last bits depend on
+ * scheduling.  Every class the library builds (s through g shells) is
+ * digested: the register and staged tiers (total angular momentum
+ * la+lb+lc+ld <= 8) per thread as each value is formed, with no integral
+ * written to memory; the cooperative tier (9 and above) writes each finished
+ * block once to its lane group's scratch region, from which the group adds it
+ * to J with one lane per element.  Errors: INVALID_ARG (NULL argument, plan
+ * without a screen), CUDA, OOM. */
 int eri_build_J(eri_plan* plan, const double* D_dev, double* J_dev, void* stream);
 
 /* Coulomb and exchange matrices from one pass over the screened quartets (the
