@@ -73,6 +73,16 @@ __device__ __forceinline__ void coop_setup_one(const EriLaunch& P, const Quartet
   if constexpr (MODE >= kCoulomb) {
     load_prim(P.prims, Q.pab + iab, pb);
     load_prim(P.prims, Q.pcd + icd, pk);
+    // a reversed pair runs its VRR on its second shell: P - B = (P - A) + (A - B),
+    // with Q.AB already turned into B - A for the reversed HRR
+    if (Q.rb) {
+#pragma unroll
+      for (int x = 0; x < 3; ++x) pb.PA[x] -= Q.AB[x];
+    }
+    if (Q.rk) {
+#pragma unroll
+      for (int x = 0; x < 3; ++x) pk.PA[x] -= Q.CD[x];
+    }
   } else {
     const int i = iab / Q.nb, j = iab - i * Q.nb;
     const int k = icd / Q.nd, l = icd - k * Q.nd;
@@ -548,6 +558,19 @@ __device__ __forceinline__ void coop_digest(const EriLaunch& P, const Quartet& Q
       Quartet Q;                                                                                          \
       if constexpr (MODE >= kCoulomb) {                                                                   \
         load_quartet_coulomb(P, q, Q);                                                                    \
+        /* pairs of unequal l whose VRR is better on the lower-l shell: reversed HRR */                   \
+        if constexpr (C::la != C::lb) {                                                                   \
+          if (__ldg(&P.pairs[Q.bra].rev)) {                                                               \
+            Q.rb = 1;                                                                                     \
+            _Pragma("unroll") for (int x_ = 0; x_ < 3; ++x_) Q.AB[x_] = -Q.AB[x_];                       \
+          }                                                                                               \
+        }                                                                                                 \
+        if constexpr (C::lc != C::ld) {                                                                   \
+          if (__ldg(&P.pairs[Q.ket].rev)) {                                                               \
+            Q.rk = 1;                                                                                     \
+            _Pragma("unroll") for (int x_ = 0; x_ < 3; ++x_) Q.CD[x_] = -Q.CD[x_];                       \
+          }                                                                                               \
+        }                                                                                                 \
       } else {                                                                                            \
         load_quartet<C::la == C::lb ? 1 : 2, C::lc == C::ld ? 1 : 2, C::La, C::Lc>(P, q, Q);                \
       }                                                                                                   \

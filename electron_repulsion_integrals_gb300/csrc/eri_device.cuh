@@ -151,6 +151,7 @@ struct EriLaunch {
 struct PairMeta {
   int a, b;       // shells
   int poff, np;   // primitive-pair records [poff, poff + np)
+  int rev, pad_;  // l_a > l_b and the VRR is better conditioned on b (the cooperative tier's reversed HRR)
   double AB[3];   // A - B
   double rAB2;
 };

@@ -340,6 +340,25 @@ int build(eri_plan* p, cudaStream_t st) {
     std::stable_sort(tmp.begin(), tmp.end(), [](const auto& x, const auto& y) { return x.first > y.first; });
     for (const auto& t : tmp) out.push_back(t.second);
   };
+  // for a pair of unequal angular momenta, whether the VRR on the lower-l
+  // shell b conditions the HRR better than on a: the weighting of
+  // second_is_better_center in eri_device.cuh (power l_a + l_b) with the
+  // device coefficients; the cooperative kernels then run that pair's
+  // reversed HRR, as in store mode
+  auto vrr_on_second = [&](int a, int b) {
+    const int n = L[a] + L[b];
+    double r2 = 0;
+    for (int x = 0; x < 3; ++x) r2 += (cen[3 * a + x] - cen[3 * b + x]) * (cen[3 * a + x] - cen[3 * b + x]);
+    double sa = 0, sb = 0;
+    for (int i = 0; i < np[a]; ++i)
+      for (int j = 0; j < np[b]; ++j) {
+        const double al = ex[po[a] + i], be = ex[po[b] + j], iz = 1.0 / (al + be);
+        const double w = std::fabs(coef[po[a] + i] * coef[po[b] + j]) * std::exp(-al * be * iz * r2) * iz * std::sqrt(iz);
+        sa += w * std::pow(be * iz, n);
+        sb += w * std::pow(al * iz, n);
+      }
+    return sb < sa;
+  };
   // 3. survivors, grouped by K (descending) then Q (descending); global pair order
   std::vector<PairMeta> meta;
   std::vector<int2> uvglob;
@@ -381,6 +400,8 @@ int build(eri_plan* p, cudaStream_t st) {
       m.b = pr.y;
       m.poff = prim_total;
       m.np = K;
+      m.rev = L[pr.x] != L[pr.y] && vrr_on_second(pr.x, pr.y) ? 1 : 0;
+      m.pad_ = 0;
       double r2 = 0;
       for (int x = 0; x < 3; ++x) {
         m.AB[x] = cen[3 * (size_t)pr.x + x] - cen[3 * (size_t)pr.y + x];

@@ -177,6 +177,33 @@ def test_screened_blocks_of_a_small_cluster(dev):
     plan.close()
 
 
+@pytest.mark.parametrize("lmax,seed", [(3, 840), (4, 841)])
+def test_screened_blocks_with_f_and_g_shells(dev, lmax, seed):
+    """3-atom clusters with s..f and s..g shells on every atom: every block
+    eri_compute_screened stores, in every class -- the cooperative tier's
+    screened store included -- against the oracle's block of the listed
+    quartet (per integral max(1e-12, 1e-10 |o|); classes with a g shell also
+    within 1e-6 of the block maximum, the g-shell bound of the parity tests)."""
+    s = W.shell_ladder_cluster(3, lmax, seed_index=seed)
+    plan = eri.Plan(s, spherical=True, schwarz_tau=TAU)
+    S = oshells(s)
+    coop = 0
+    for cls, lst in listed(plan, lmax).items():
+        n = len(lst)
+        if n == 0:
+            continue
+        coop += sum(cls) >= 9
+        bs = eri.block_size(cls)
+        got = plan.compute_screened(cls).cpu().numpy()[:n * bs].reshape(n, bs)
+        ref = oracle.eri_blocks(S, lst, spherical=True).reshape(n, bs)
+        tol = np.maximum(1e-12, 1e-10 * np.abs(ref))
+        if max(cls) == 4:
+            tol = np.maximum(tol, 1e-6 * np.abs(ref).max(axis=1, keepdims=True))
+        assert np.all(np.abs(got - ref) <= tol), (cls, float(np.max(np.abs(got - ref) - tol)))
+    assert coop >= (9 if lmax == 3 else 40)
+    plan.close()
+
+
 def oracle_counts(s):
     """Quartets per canonical class passing the screen with the oracle's
     Schwarz factors, counted from the sorted pair factors."""
