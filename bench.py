@@ -365,11 +365,13 @@ def run_reference(a, rank, world):
         rate_fn = lambda budget: cpu_oracle_rate_cluster(cs, counts, budget_s=budget) + (None,)  # noqa: E731
     else:
         rate_fn = lambda budget: cpu_oracle_rate(wl, budget_s=budget)  # noqa: E731
+    # each step a bounded sample: about two minutes for the whole timed run
+    budget = max(2.0, min(a.ref_budget, 120.0 / max(a.steps, 1)))
     for _ in range(a.warmup):
         rate_fn(2.0)
     t_all = time.perf_counter()
     for _ in range(a.steps):
-        r, desc, cores, _ = rate_fn(a.ref_budget)
+        r, desc, cores, _ = rate_fn(budget)
         rates.append(r)
     elapsed = time.perf_counter() - t_all
     value = statistics.median(rates)
